@@ -1,0 +1,411 @@
+#!/usr/bin/env python3
+"""Benchmark of the W4 MoE expert layer on GB300.
+
+One step = one whole MoE layer (router logits, top-k + gates, histogram,
+scan, scatter, block map, gate/up grouped GEMM with fused dequant + SwiGLU,
+down grouped GEMM with fused dequant + gated combine, bf16 output) over one
+batch of T tokens, through the library's C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the FP64 CPU oracle, timed
+
+Prints ONE JSON line (rank 0).  Multi-GPU runs (torchrun) are token data
+parallel with replicated weights and no exchange: every rank runs its own
+batch (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "MoE-layer tokens/s"
+UNIT = "tokens/s"
+
+WORKLOADS = {
+    # name: (T, d, E, k, F, zipf)
+    "prefill512": (512, 2048, 256, 8, 512, None),
+    "prefill2048_zipf": (2048, 2048, 256, 8, 512, 1.1),
+    "prefill2048": (2048, 2048, 256, 8, 512, None),
+    "decode1": (1, 2048, 256, 8, 512, None),
+    "decode5": (5, 2048, 256, 8, 512, None),
+    "small": (32, 512, 32, 4, 128, None),
+}
+DEFAULT_WORKLOAD = "prefill512"
+
+# ncu DRAM traffic (read + write bytes per launch) of the dominant kernel, keyed
+# by workload and by a hash of the kernel's source files: a changed kernel
+# reports null until it is profiled again.
+KERNEL_SOURCES = ["w4_grouped_gemm_gb300/csrc/gemm.cu", "w4_grouped_gemm_gb300/csrc/common.cuh"]
+NCU_TRAFFIC = {}  # {(workload, kernel, source_hash): bytes}
+
+
+def source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update((ROOT / f).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 50):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        rows = []
+        for ts, line in self.lines:
+            if t0 is not None and not (t0 - 0.25 <= ts <= t1 + 0.25):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- helpers
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def algorithmic_bytes(T, d, E, k, F, counts):
+    """Touched experts' W4 bytes (packed + bf16 scale/bias) + router W + x + y."""
+    per_expert = 3 * (F * d // 2 + F * d // 64 * 4)
+    touched = int((np.asarray(counts) > 0).sum()) + 1  # + shared expert
+    return touched * per_expert + E * d * 4 + T * d * 2 * 2, touched
+
+
+def gateup_bytes(T, d, F, touched):
+    """Gate/up kernel: touched experts' gate+up W4 bytes + x read."""
+    return touched * 2 * (F * d // 2 + F * d // 64 * 4) + T * d * 2
+
+
+def layer_flops(T, d, E, k, F):
+    return 2 * T * d * E + T * (k + 1) * 6 * d * F
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(shape_args, seed, n_rows, rows_offset=0):
+    """Time the FP64 oracle on a bounded sample of the workload: router logits,
+    routing and the layer output of n_rows tokens (host inputs)."""
+    import oracle
+    from w4_grouped_gemm_gb300 import synth
+    T, d, E, k, F, zipf = shape_args
+    shape = synth.LayerShape(T, d, E, k, F)
+    inp = synth.make_layer(shape, seed, device="cpu", zipf_s=zipf)
+    x = synth.bf16_bits(inp["x"])
+    wr = inp["router_w"].numpy()
+    br = None if inp["router_b"] is None else inp["router_b"].numpy()
+    w = synth.experts_to_numpy(inp["experts"])
+    rows = (np.arange(n_rows) + rows_offset) % T
+    oracle.build()
+    t0 = time.perf_counter()
+    L, _ = oracle.router_logits(x[rows], wr, br)
+    ro = oracle.route(L.astype(np.float32), k, 128)
+    oracle.moe_rows(x[rows], w, ro["ids"], ro["gates"], np.arange(n_rows))
+    return time.perf_counter() - t0
+
+
+def run_reference(args, ws, rank):
+    """--impl reference: the oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    wl = WORKLOADS[args.workload]
+    T, d, E, k, F, zipf = wl
+    # one step = one token row of the workload through the oracle layer
+    n_rows = 1
+    for i in range(args.warmup):
+        oracle_sample(wl, 1000, n_rows, i)
+    t = 0.0
+    for i in range(args.steps):
+        t += oracle_sample(wl, 1000, n_rows, args.warmup + i)
+    value = args.steps * n_rows / t
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "T": T, "d_model": d, "n_experts": E, "top_k": k,
+                   "d_ff": F, "zipf_s": zipf, "step_sample": f"{n_rows} token row(s) per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{n_rows} token row per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_lily(args, world, rank, local):
+    import w4_grouped_gemm_gb300 as lily
+    from w4_grouped_gemm_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lily.lib()
+    T, d, E, k, F, zipf = WORKLOADS[args.workload]
+    decode = T <= 8
+    shape = synth.LayerShape(T, d, E, k, F)
+    dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
+    # several layers of weights, rotated per step, so no step finds the
+    # previous step's weights in L2 (each layer's weights are 455 MB)
+    nl = args.layers
+    layers = []
+    for l in range(nl):
+        inp = synth.make_layer(shape, 1000 * 2 + 17 * l + 101 * rank, device=dev, zipf_s=zipf)
+        layers.append((inp["x"], lily.LayerWeights(inp["router_w"], inp["router_b"], inp["experts"])))
+    r = lily.RoutingBuffers(dims, dev)
+    wsb = lily.alloc_workspace(lily.lily_moe_workspace_bytes(dims), dev)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lily.lily_moe_decode if decode else lily.lily_moe_forward
+
+    def step(i):
+        x, w = layers[i % nl]
+        call(dims, x, w, r, y, wsb, stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if lily.lily_moe_status(wsb) != 0:
+        raise RuntimeError("device status bits set during warm-up")
+    counts_by_layer = []
+    for l in range(nl):
+        step(l)
+        torch.cuda.synchronize()
+        counts_by_layer.append(r.counts.cpu().numpy().copy())
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    lily.lily_moe_profile_enable(True)
+    lily.lily_moe_profile_read()  # reset
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.perf_counter()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
+    if world > 1:
+        torch.distributed.barrier()
+    lily.lily_moe_profile_enable(False)
+    prof = lily.lily_moe_profile_read()
+    ms = e0.elapsed_time(e1)
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = lily.lily_moe_status(wsb)
+    if status:
+        raise RuntimeError(f"device status bits set: {status}")
+
+    # end to end through the host-buffer entry point (pinned host x and y)
+    e2e_steps = max(3, min(args.steps, 200))
+    xh = [layers[l][0].cpu().pin_memory() for l in range(nl)]
+    yh = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    for i in range(3):
+        lily.lily_moe_forward_host(dims, xh[i % nl], xd, layers[i % nl][1], r, y, yh, wsb, stream)
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        lily.lily_moe_forward_host(dims, xh[i % nl], xd, layers[i % nl][1], r, y, yh, wsb, stream)
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    if rank != 0:
+        return
+    hbm, tf_burst, tf_sus, peak_src = measured_peaks()
+    value = world * T * args.steps / (ms / 1000.0)
+    e2e_value = world * T * e2e_steps / e2e_s
+    alg_bytes = []
+    touched_l = []
+    for c in counts_by_layer:
+        b, tch = algorithmic_bytes(T, d, E, k, F, c)
+        alg_bytes.append(b)
+        touched_l.append(tch)
+    step_bytes = float(np.mean(alg_bytes))
+    flops = layer_flops(T, d, E, k, F)
+    step_s = ms / 1000.0 / args.steps
+    layer_t_hbm = step_bytes / (hbm * 1e9)
+    layer_t_tc = flops / (tf_sus * 1e12)
+    # dominant kernel of the step by device time
+    kernels = {n: {"ms_per_launch": v["ms"] / v["launches"], "launches": v["launches"],
+                   "share": v["ms"] / sum(u["ms"] for u in prof.values())}
+               for n, v in prof.items()}
+    dom = max(prof, key=lambda n: prof[n]["ms"]) if prof else None
+    roofline = None
+    if dom:
+        dur = prof[dom]["ms"] / prof[dom]["launches"] / 1000.0
+        touched = float(np.mean(touched_l))
+        if dom == "gateup_gemm":
+            dbytes = gateup_bytes(T, d, F, touched)
+        elif dom == "down_gemm":
+            dbytes = touched * (F * d // 2 + F * d // 64 * 4) + T * d * 2
+        elif dom in ("dec_gateup",):
+            dbytes = gateup_bytes(T, d, F, touched)
+        elif dom in ("dec_down",):
+            dbytes = touched * (F * d // 2 + F * d // 64 * 4)
+        else:
+            dbytes = step_bytes
+        achieved = dbytes / dur / 1e9
+        key = (args.workload, dom, source_hash(KERNEL_SOURCES))
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved / hbm, "traffic": NCU_TRAFFIC.get(key),
+                    "kernel": dom, "algorithmic_bytes_per_launch": dbytes,
+                    "peak_source": f"hbm_gbs of {peak_src} peaks (copy bandwidth)"}
+    launches = sum(v["launches"] for n, v in prof.items() if n != "memset_acc")
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+
+    # CPU baseline: the oracle, bounded sample of the same workload
+    cpu = None
+    if not args.no_cpu_baseline:
+        n_rows = 1 if decode else args.cpu_rows
+        t_cpu = oracle_sample(WORKLOADS[args.workload], 1000, n_rows)
+        cpu = {"value": n_rows / t_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{n_rows} token rows of the {args.workload} layer (router logits, "
+                         f"routing, explicit dequant of every touched expert, FP64 layer)"}
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (W4 weights, fp32 accumulate)",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {
+            "workload": args.workload, "T": T, "d_model": d, "n_experts": E, "top_k": k,
+            "d_ff": F, "zipf_s": zipf, "tile_rows": args.tile_rows,
+            "path": "decode GEMV" if decode else "prefill grouped GEMM",
+            "l2": f"inputs larger than L2: {nl} layers of weights rotated per step",
+            "parallelism": f"token data parallel x{world} (replicated weights, no exchange)",
+            "experts_touched_per_step": float(np.mean(touched_l)),
+            "layer_algorithmic_bytes": step_bytes, "layer_flops": flops,
+            "layer_roofline_us": 1e6 * max(layer_t_hbm, layer_t_tc),
+            "layer_frac_of_roofline": max(layer_t_hbm, layer_t_tc) / step_s,
+            "kernels": kernels,
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * d * 2,
+                "d2h_bytes_per_step": T * d * 2},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["lily", "reference"], default="lily")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--tile-rows", type=int, default=128)
+    ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_info()
+    if world > 1:
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "lily" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_lily(args, world, rank, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

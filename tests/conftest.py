@@ -3,9 +3,11 @@ import sys
 
 import pytest
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-if ROOT not in sys.path:
-    sys.path.insert(0, ROOT)
+ROOT = os.path.dirname(os.path.abspath(__file__))
+REPO = os.path.dirname(ROOT)
+for p in (REPO, ROOT):
+    if p not in sys.path:
+        sys.path.insert(0, p)
 
 
 def pytest_configure(config):
@@ -18,3 +20,15 @@ def oracle():
     import oracle as orc
     orc.build()
     return orc
+
+
+@pytest.fixture(scope="session")
+def oracle_lib(oracle):
+    """Oracle built and the CUDA library built and loaded (GPU tests)."""
+    import torch
+    from w4_grouped_gemm_gb300 import build
+    build.build()
+    import w4_grouped_gemm_gb300 as lily
+    lily.lib()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return oracle

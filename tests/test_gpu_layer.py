@@ -1,0 +1,150 @@
+"""Whole-layer parity, CUDA path vs the FP64 oracle.
+
+The oracle routes from the GPU's own fp32 logits (routing parity is tested
+bit-exact separately), so a near-tie can never make the two sides pick
+different experts.  Outputs must meet max|err|/rms <= 2e-2 and
+mean|err|/mean|ref| <= 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4_grouped_gemm_gb300 as lily
+from w4_grouped_gemm_gb300 import synth
+
+from gpu_util import Layer, assert_layer_close, assert_routing_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_forward(L, rows=None, decode=False):
+    (L.decode if decode else L.forward)()
+    assert L.status() == 0
+    gpu = L.r.host()
+    ro = oracle.route(gpu["logits"], L.shape.k, L.dims.tile_rows)
+    assert_routing_equal(gpu, ro, L.shape.T, L.shape.k)
+    rows = np.arange(L.shape.T) if rows is None else np.asarray(rows)
+    ref = L.oracle_rows(rows, ro)
+    got = L.y.float().cpu().numpy()[rows]
+    return assert_layer_close(got, ref, f"T={L.shape.T} BM={L.dims.tile_rows}")
+
+
+# ------------------------------------------------------------ full-layer, small
+
+@pytest.mark.parametrize("bm", [32, 64, 128, 256])
+def test_small_layer_all_tile_rows(oracle_lib, bm):
+    _check_forward(Layer(synth.SHAPES["small"], seed=1000, tile_rows=bm))
+
+
+@pytest.mark.parametrize("shape,bm", [
+    (synth.LayerShape(37, 256, 16, 3, 128), 32),      # ragged tiles everywhere
+    (synth.LayerShape(130, 384, 24, 5, 256), 64),     # 2 F slices, 3 d slices
+    (synth.LayerShape(9, 512, 32, 4, 128), 32),       # smallest prefill T
+    (synth.LayerShape(257, 128, 8, 8, 128), 128),     # E == k: every expert chosen
+])
+def test_ragged_layers(oracle_lib, shape, bm):
+    _check_forward(Layer(shape, seed=shape.T * 7, tile_rows=bm))
+
+
+def test_all_tokens_one_expert(oracle_lib):
+    """A huge router bias sends every token to expert 5 first: one expert with
+    T rows spans many tiles; most experts are empty."""
+    shape = synth.LayerShape(300, 512, 32, 2, 128)
+    b = torch.zeros(32, dtype=torch.float32, device="cuda")
+    b[5] = 100.0
+    b[9] = 50.0
+    L = Layer(shape, seed=55, tile_rows=64, router_b=b)
+    _check_forward(L)
+    counts = L.r.counts.cpu().numpy()
+    assert counts[5] == 300 and counts[9] == 300 and counts.sum() == 600
+
+
+def test_identical_experts_closed_form(oracle_lib):
+    """Every routed expert and the shared expert identical: y = 2 FFN(x) on
+    the GPU too (gates sum to 1), checked against the oracle's closed form."""
+    shape = synth.LayerShape(64, 512, 16, 4, 128)
+    one = synth.make_experts(0, shape.d, shape.F, seed=77, device="cuda")
+    experts = {n: t.expand(shape.E + 1, *t.shape[1:]).contiguous() for n, t in one.items()}
+    L = Layer(shape, seed=78, tile_rows=32, experts=experts)
+    L.forward()
+    npone = synth.experts_to_numpy(one)
+    ref = 2.0 * _dense_ffn(npone, synth.bf16_bits(L.x))
+    assert_layer_close(L.y.float().cpu().numpy(), ref, "identical experts")
+
+
+def _dense_ffn(npw, xbits):
+    x = (xbits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Wg = oracle.dequant(npw["gate_q"][0], npw["gate_s"][0], npw["gate_b"][0])
+    Wu = oracle.dequant(npw["up_q"][0], npw["up_s"][0], npw["up_b"][0])
+    Wd = oracle.dequant(npw["down_q"][0], npw["down_s"][0], npw["down_b"][0])
+    g = x @ Wg.T
+    h = g / (1.0 + np.exp(-g)) * (x @ Wu.T)
+    return h @ Wd.T
+
+
+# ------------------------------------------------------------ full-size configs
+
+def test_prefill512_sampled_rows(oracle_lib):
+    L = Layer(synth.SHAPES["prefill512"], seed=2000, tile_rows=128)
+    rows = np.random.default_rng(1).choice(512, 40, replace=False)
+    _check_forward(L, rows)
+
+
+def test_prefill2048_zipf_sampled_rows(oracle_lib):
+    L = Layer(synth.SHAPES["prefill2048_zipf"], seed=3000, tile_rows=128, zipf_s=1.1)
+    rows = np.random.default_rng(2).choice(2048, 32, replace=False)
+    _check_forward(L, rows)
+    counts = L.r.counts.cpu().numpy()
+    assert (counts == 0).any() and counts.max() > 256
+
+
+def test_prefill2048_uniform_sampled_rows_bm256(oracle_lib):
+    L = Layer(synth.SHAPES["prefill2048_zipf"], seed=3100, tile_rows=256)
+    rows = np.random.default_rng(3).choice(2048, 24, replace=False)
+    _check_forward(L, rows)
+
+
+def test_forward_repeat_is_stable(oracle_lib):
+    """Two calls on the same workspace give the same routing and outputs that
+    agree to fp32 atomic-order noise."""
+    L = Layer(synth.LayerShape(256, 1024, 64, 8, 256), seed=91, tile_rows=64)
+    y1 = L.forward().float().clone()
+    y2 = L.forward().float()
+    rel = (y1 - y2).abs().max().item() / y1.pow(2).mean().sqrt().item()
+    assert rel < 1e-2
+
+
+# ------------------------------------------------------------ decode path
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 8])
+def test_decode_full_size(oracle_lib, T):
+    _check_forward(Layer(synth.LayerShape(T, 2048, 256, 8, 512), seed=4000 + T, tile_rows=128),
+                   decode=True)
+
+
+def test_decode_small_shape(oracle_lib):
+    _check_forward(Layer(synth.LayerShape(3, 512, 32, 4, 128), seed=4100, tile_rows=32),
+                   decode=True)
+
+
+def test_decode_matches_forward(oracle_lib):
+    """Decode (GEMV) and prefill (grouped GEMM) paths agree on T = 8."""
+    L = Layer(synth.LayerShape(8, 1024, 64, 8, 256), seed=4200, tile_rows=32)
+    yd = L.decode().float().clone()
+    yf = L.forward().float()
+    rel = (yd - yf).abs().max().item() / yf.pow(2).mean().sqrt().item()
+    assert rel < 2e-2
+
+
+def test_forward_host_entry(oracle_lib):
+    """The host-buffer entry point gives the same result as the device one."""
+    L = Layer(synth.LayerShape(64, 512, 32, 4, 128), seed=4300, tile_rows=32)
+    ydev = L.forward().clone()
+    xh = L.x.cpu().pin_memory()
+    yh = torch.empty(64, 512, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(L.x)
+    yd = torch.empty_like(L.y)
+    lily.lily_moe_forward_host(L.dims, xh, xd, L.w, L.r, yd, yh, L.ws)
+    rel = (yh.float() - ydev.cpu().float()).abs().max().item() / ydev.float().pow(2).mean().sqrt().item()
+    assert rel < 1e-2

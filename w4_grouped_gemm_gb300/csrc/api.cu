@@ -1,0 +1,509 @@
+// api.cu -- the C ABI (include/lily_moe.h): argument validation, workspace
+// layout and the launch sequence of each call.  No call allocates device
+// memory; every launch goes to the caller's stream.
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace lily {
+
+// ---------------------------------------------------------------- profiling
+namespace {
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_open;  // recorded, not yet read
+std::vector<cudaEvent_t> g_prof_pool;
+int g_prof_kind = -1;
+cudaEvent_t g_prof_start = nullptr;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+void prof_begin(int kind, cudaStream_t s) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_kind = kind;
+  g_prof_start = prof_event();
+  cudaEventRecord(g_prof_start, s);
+}
+
+void prof_end(int kind, cudaStream_t s) {
+  if (!g_prof_on) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (g_prof_kind != kind || !g_prof_start) return;
+  cudaEvent_t e = prof_event();
+  cudaEventRecord(e, s);
+  g_prof_open.push_back({kind, g_prof_start, e});
+  g_prof_start = nullptr;
+  g_prof_kind = -1;
+}
+
+// ---------------------------------------------------------------- workspace
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+struct Layout {
+  size_t ctrl, hist, x16, H, acc, total;
+};
+
+// ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
+Layout layout(const lily_moe_dims& d) {
+  const size_t T = d.T, E = d.n_experts, k = d.top_k, F = d.d_ff, D = d.d_model;
+  const size_t P = T * k;
+  const size_t nblk = (T + kRouteTok - 1) / kRouteTok;
+  Layout L;
+  size_t off = 0;
+  L.ctrl = off; off += up(256);
+  L.hist = off; off += up(nblk * E * 4);
+  L.x16 = off;  off += up(T * D * 2);
+  L.H = off;    off += up((P + T) * F * 2);
+  L.acc = off;
+  size_t acc = T * D * 4;                         // prefill: fp32 y accumulator
+  if (d.T <= 8) acc = std::max(acc, (P + T) * D * 4);  // decode: per-row outputs
+  off += up(acc);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int check_arch() {
+  int dev = 0, maj = 0, min = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LILY_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return LILY_ERR_CUDA;
+  return (maj == 10 && min == 3) ? LILY_OK : LILY_ERR_ARCH;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LILY_OK : LILY_ERR_CUDA; }
+
+int check_routing(const lily_moe_routing* r) {
+  if (!r) return LILY_ERR_INVALID_ARG;
+  const void* ptrs[] = {r->logits, r->topk_ids, r->topk_gates, r->counts, r->offsets,
+                        r->perm,   r->inv_perm, r->block_map,  r->n_tiles};
+  for (const void* p : ptrs) {
+    if (!p) return LILY_ERR_INVALID_ARG;
+    if (!aligned16(p)) return LILY_ERR_MISALIGNED;
+  }
+  return LILY_OK;
+}
+
+int check_weights(const lily_moe_weights* w, bool need_router, bool need_experts) {
+  if (!w) return LILY_ERR_INVALID_ARG;
+  if (need_router) {
+    if (!w->router_w) return LILY_ERR_INVALID_ARG;
+    if (!aligned16(w->router_w) || (w->router_bias && !aligned16(w->router_bias)))
+      return LILY_ERR_MISALIGNED;
+  }
+  if (need_experts) {
+    const void* ptrs[] = {w->gate_q, w->gate_s, w->gate_b, w->up_q,  w->up_s,
+                          w->up_b,   w->down_q, w->down_s, w->down_b};
+    for (const void* p : ptrs) {
+      if (!p) return LILY_ERR_INVALID_ARG;
+      if (!aligned16(p)) return LILY_ERR_MISALIGNED;
+    }
+  }
+  return LILY_OK;
+}
+
+int check_ws(const lily_moe_dims* d, void* ws, size_t bytes) {
+  if (!ws) return LILY_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return LILY_ERR_MISALIGNED;
+  if (bytes < layout(*d).total) return LILY_ERR_WORKSPACE_TOO_SMALL;
+  return LILY_OK;
+}
+
+uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws)); }
+
+// Routing on `s` (logits computed unless logits_in is given).
+int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
+             const lily_moe_weights* w, const lily_moe_routing& r, void* ws, cudaStream_t s) {
+  const Layout L = layout(d);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const float* src = logits_in;
+  if (!src) {
+    cudaError_t e = launch_router_logits(x, w->router_w, w->router_bias, r.logits, d.T, d.d_model,
+                                         d.n_experts, base + L.x16, ws_status(ws), s);
+    if (e != cudaSuccess) return LILY_ERR_CUDA;
+    src = r.logits;
+  }
+  RouteArgs a;
+  a.logits_src = src;
+  a.logits_dst = r.logits;
+  a.T = d.T;
+  a.E = d.n_experts;
+  a.k = d.top_k;
+  a.BM = d.tile_rows;
+  a.cap = (int)lily_moe_block_map_cap(&d);
+  a.ids = r.topk_ids;
+  a.gates = r.topk_gates;
+  a.counts = r.counts;
+  a.offsets = r.offsets;
+  a.perm = r.perm;
+  a.inv = r.inv_perm;
+  a.block_map = r.block_map;
+  a.n_tiles = r.n_tiles;
+  a.hist = reinterpret_cast<int32_t*>(base + L.hist);
+  a.bar = reinterpret_cast<uint32_t*>(base + L.ctrl) + 1;
+  a.status = ws_status(ws);
+  return cuda_rc(launch_route(a, s));
+}
+
+GemmArgs gemm_args(const lily_moe_dims& d, const lily_moe_weights* w, const lily_moe_routing& r,
+                   void* ws) {
+  const Layout L = layout(d);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  GemmArgs a;
+  a.T = d.T;
+  a.E = d.n_experts;
+  a.k = d.top_k;
+  a.d = d.d_model;
+  a.F = d.d_ff;
+  a.BM = d.tile_rows;
+  a.block_map = r.block_map;
+  a.n_tiles = r.n_tiles;
+  a.offsets = r.offsets;
+  a.perm = r.perm;
+  a.gates = r.topk_gates;
+  a.s0 = w->gate_s;
+  a.b0 = w->gate_b;
+  a.s1 = w->up_s;
+  a.b1 = w->up_b;
+  a.H = base + L.H;
+  a.yacc = reinterpret_cast<float*>(base + L.acc);
+  a.status = ws_status(ws);
+  return a;
+}
+
+// Routing + grouped GEMMs; the layer output stays in the fp32 accumulator.
+int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
+                   const lily_moe_routing& r, void* ws, cudaStream_t s) {
+  int rc = do_route(d, x, nullptr, w, r, ws, s);
+  if (rc) return rc;
+  GemmArgs a = gemm_args(d, w, r, ws);
+  prof_begin(K_MEMSET, s);
+  cudaError_t e = cudaMemsetAsync(a.yacc, 0, (size_t)d.T * d.d_model * 4, s);
+  prof_end(K_MEMSET, s);
+  if (e != cudaSuccess) return LILY_ERR_CUDA;
+  const Layout L = layout(d);
+  if (launch_gateup(a, static_cast<uint8_t*>(ws) + L.x16, w->gate_q, w->up_q, s) != cudaSuccess)
+    return LILY_ERR_CUDA;
+  a.s0 = w->down_s;
+  a.b0 = w->down_b;
+  a.s1 = nullptr;
+  a.b1 = nullptr;
+  if (launch_down(a, w->down_q, s) != cudaSuccess) return LILY_ERR_CUDA;
+  return LILY_OK;
+}
+
+int common_checks(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
+                  const lily_moe_routing* r, const void* y, void* ws, size_t ws_bytes,
+                  bool experts) {
+  if (!dims) return LILY_ERR_INVALID_ARG;
+  int rc = lily_moe_check_dims(dims);
+  if (rc) return rc;
+  if (!x || (experts && !y)) return LILY_ERR_INVALID_ARG;
+  if (!aligned16(x) || (y && !aligned16(y))) return LILY_ERR_MISALIGNED;
+  if ((rc = check_weights(w, true, experts))) return rc;
+  if ((rc = check_routing(r))) return rc;
+  if ((rc = check_ws(dims, ws, ws_bytes))) return rc;
+  return check_arch();
+}
+
+}  // namespace
+}  // namespace lily
+
+using namespace lily;
+
+extern "C" {
+
+int lily_moe_check_dims(const lily_moe_dims* d) {
+  if (!d) return LILY_ERR_INVALID_ARG;
+  if (d->T < 1 || d->d_model < 1 || d->n_experts < 1 || d->top_k < 1 || d->d_ff < 1)
+    return LILY_ERR_INVALID_ARG;
+  if (d->T > 16384) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (d->d_model % 128 || d->d_model > 4096) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (d->d_ff % 128 || d->d_ff > 4096) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (d->n_experts > 256) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (d->top_k > 8 || d->top_k > d->n_experts) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (d->group != 64) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (d->tile_rows != 32 && d->tile_rows != 64 && d->tile_rows != 128 && d->tile_rows != 256)
+    return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (gemm_stages(true, d->tile_rows, d->d_model) < 2 || gemm_stages(false, d->tile_rows, d->d_ff) < 2)
+    return LILY_ERR_UNSUPPORTED_SHAPE;
+  return LILY_OK;
+}
+
+size_t lily_moe_workspace_bytes(const lily_moe_dims* d) {
+  if (lily_moe_check_dims(d) != LILY_OK) return 0;
+  return layout(*d).total;
+}
+
+int64_t lily_moe_block_map_cap(const lily_moe_dims* d) {
+  if (!d || d->tile_rows < 1 || d->T < 0 || d->top_k < 1) return 0;
+  const int64_t P = (int64_t)d->T * d->top_k;
+  return (P + d->tile_rows - 1) / d->tile_rows + (d->n_experts < P ? d->n_experts : P);
+}
+
+int lily_moe_route(const lily_moe_dims* dims, const void* x, const float* logits_in,
+                   const lily_moe_weights* w, lily_moe_routing* r, void* ws, size_t ws_bytes,
+                   void* stream) {
+  if (!dims) return LILY_ERR_INVALID_ARG;
+  int rc = lily_moe_check_dims(dims);
+  if (rc) return rc;
+  if (logits_in) {
+    if (!aligned16(logits_in)) return LILY_ERR_MISALIGNED;
+  } else {
+    if (!x) return LILY_ERR_INVALID_ARG;
+    if (!aligned16(x)) return LILY_ERR_MISALIGNED;
+    if ((rc = check_weights(w, true, false))) return rc;
+  }
+  if ((rc = check_routing(r))) return rc;
+  if ((rc = check_ws(dims, ws, ws_bytes))) return rc;
+  if ((rc = check_arch())) return rc;
+  const int maxb = route_max_blocks();
+  if (maxb > 0 && (dims->T + kRouteTok - 1) / kRouteTok > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
+  return do_route(*dims, x, logits_in, w, *r, ws, (cudaStream_t)stream);
+}
+
+int lily_moe_forward(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
+                     lily_moe_routing* r, void* y, void* ws, size_t ws_bytes, void* stream) {
+  int rc = common_checks(dims, x, w, r, y, ws, ws_bytes, true);
+  if (rc) return rc;
+  const int maxb = route_max_blocks();
+  if (maxb > 0 && (dims->T + kRouteTok - 1) / kRouteTok > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((rc = do_forward_acc(*dims, x, w, *r, ws, s))) return rc;
+  const Layout L = layout(*dims);
+  return cuda_rc(launch_finalize(reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.acc), y,
+                                 (int64_t)dims->T * dims->d_model, s));
+}
+
+int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
+                    lily_moe_routing* r, void* y, void* ws, size_t ws_bytes, void* stream) {
+  int rc = common_checks(dims, x, w, r, y, ws, ws_bytes, true);
+  if (rc) return rc;
+  if (dims->T > 8) return LILY_ERR_UNSUPPORTED_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if ((rc = do_route(*dims, x, nullptr, w, *r, ws, s))) return rc;
+  const Layout L = layout(*dims);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  DecodeArgs a;
+  a.T = dims->T;
+  a.E = dims->n_experts;
+  a.k = dims->top_k;
+  a.d = dims->d_model;
+  a.F = dims->d_ff;
+  a.cap = (int)lily_moe_block_map_cap(dims);
+  a.block_map = r->block_map;
+  a.n_tiles = r->n_tiles;
+  a.offsets = r->offsets;
+  a.perm = r->perm;
+  a.inv = r->inv_perm;
+  a.gates = r->topk_gates;
+  a.gq = w->gate_q; a.gs = w->gate_s; a.gb = w->gate_b;
+  a.uq = w->up_q;   a.us = w->up_s;   a.ub = w->up_b;
+  a.dq = w->down_q; a.ds = w->down_s; a.db = w->down_b;
+  a.x = x;
+  a.H = base + L.H;
+  a.O = reinterpret_cast<float*>(base + L.acc);
+  a.y = y;
+  a.status = ws_status(ws);
+  return cuda_rc(launch_decode(a, s));
+}
+
+int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x_dev,
+                          const lily_moe_weights* w, lily_moe_routing* r, void* y_dev,
+                          void* y_host, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims || !x_host || !y_host) return LILY_ERR_INVALID_ARG;
+  int rc = common_checks(dims, x_dev, w, r, y_dev, ws, ws_bytes, true);
+  if (rc) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t bytes = (size_t)dims->T * dims->d_model * 2;
+  if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return LILY_ERR_CUDA;
+  rc = dims->T <= 8 ? lily_moe_decode(dims, x_dev, w, r, y_dev, ws, ws_bytes, stream)
+                    : lily_moe_forward(dims, x_dev, w, r, y_dev, ws, ws_bytes, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return LILY_ERR_CUDA;
+  return cuda_rc(cudaStreamSynchronize(s));
+}
+
+int lily_moe_rmsnorm(int32_t T, int32_t d, const float* x, float eps, void* out, void* stream) {
+  if (T < 1 || d < 1 || !x || !out) return LILY_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out)) return LILY_ERR_MISALIGNED;
+  int rc = check_arch();
+  if (rc) return rc;
+  return cuda_rc(launch_rmsnorm(x, out, T, d, eps, (cudaStream_t)stream));
+}
+
+// Stack workspace: [layer workspace][routing buffers][xn bf16]
+namespace {
+struct StackLayout {
+  size_t ws, logits, ids, gates, counts, offsets, perm, inv, bmap, ntiles, xn, total;
+};
+StackLayout stack_layout(const lily_moe_dims& d) {
+  StackLayout S;
+  const size_t T = d.T, E = d.n_experts, k = d.top_k, P = T * k;
+  const size_t cap = (size_t)lily_moe_block_map_cap(&d);
+  size_t off = 0;
+  S.ws = off; off += up(layout(d).total);
+  S.logits = off; off += up(T * E * 4);
+  S.ids = off; off += up(P * 4);
+  S.gates = off; off += up(P * 4);
+  S.counts = off; off += up(E * 4);
+  S.offsets = off; off += up((E + 1) * 4);
+  S.perm = off; off += up(P * 4);
+  S.inv = off; off += up(P * 4);
+  S.bmap = off; off += up(cap * 8);
+  S.ntiles = off; off += up(4);
+  S.xn = off; off += up(T * d.d_model * 2);
+  S.total = off;
+  return S;
+}
+}  // namespace
+
+size_t lily_moe_stack_workspace_bytes(const lily_moe_dims* d) {
+  if (lily_moe_check_dims(d) != LILY_OK) return 0;
+  return stack_layout(*d).total;
+}
+
+int lily_moe_stack_prefill(const lily_moe_dims* dims, int32_t T_total, int32_t n_layers,
+                           const lily_moe_weights* layers, float* x, float eps,
+                           float* layer_inputs, float* layer_logits, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!dims || !layers || !x || !ws || n_layers < 1 || T_total < 1) return LILY_ERR_INVALID_ARG;
+  int rc = lily_moe_check_dims(dims);
+  if (rc) return rc;
+  if (T_total % dims->T) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(ws) || (layer_inputs && !aligned16(layer_inputs)) ||
+      (layer_logits && !aligned16(layer_logits)))
+    return LILY_ERR_MISALIGNED;
+  for (int l = 0; l < n_layers; ++l)
+    if ((rc = check_weights(&layers[l], true, true))) return rc;
+  const StackLayout S = stack_layout(*dims);
+  if (ws_bytes < S.total) return LILY_ERR_WORKSPACE_TOO_SMALL;
+  if ((rc = check_arch())) return rc;
+  const int T = dims->T, D = dims->d_model, E = dims->n_experts;
+  if (layer_logits && ((size_t)T * E) % 4) return LILY_ERR_MISALIGNED;  // per-chunk slices
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* lws = base + S.ws;
+  lily_moe_routing r;
+  r.logits = reinterpret_cast<float*>(base + S.logits);
+  r.topk_ids = reinterpret_cast<int32_t*>(base + S.ids);
+  r.topk_gates = reinterpret_cast<float*>(base + S.gates);
+  r.counts = reinterpret_cast<int32_t*>(base + S.counts);
+  r.offsets = reinterpret_cast<int32_t*>(base + S.offsets);
+  r.perm = reinterpret_cast<int32_t*>(base + S.perm);
+  r.inv_perm = reinterpret_cast<int32_t*>(base + S.inv);
+  r.block_map = reinterpret_cast<int32_t*>(base + S.bmap);
+  r.n_tiles = reinterpret_cast<int32_t*>(base + S.ntiles);
+  void* xn = base + S.xn;
+  const Layout L = layout(*dims);
+  float* yacc = reinterpret_cast<float*>(static_cast<uint8_t*>(lws) + L.acc);
+  const int nchunks = T_total / T;
+  for (int c = 0; c < nchunks; ++c) {
+    float* xc = x + (size_t)c * T * D;
+    if (launch_rmsnorm(xc, xn, T, D, eps, s) != cudaSuccess) return LILY_ERR_CUDA;
+    for (int l = 0; l < n_layers; ++l) {
+      if (layer_inputs &&
+          cudaMemcpyAsync(layer_inputs + ((size_t)l * T_total + (size_t)c * T) * D, xc,
+                          (size_t)T * D * 4, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return LILY_ERR_CUDA;
+      lily_moe_routing rl = r;
+      if (layer_logits) rl.logits = layer_logits + ((size_t)l * T_total + (size_t)c * T) * E;
+      if ((rc = do_forward_acc(*dims, xn, &layers[l], rl, lws, s))) return rc;
+      if (launch_stack_boundary(yacc, xc, l + 1 < n_layers ? xn : nullptr, T, D, eps, s) !=
+          cudaSuccess)
+        return LILY_ERR_CUDA;
+    }
+  }
+  return LILY_OK;
+}
+
+int lily_moe_status(void* ws, void* stream) {
+  if (!ws) return LILY_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws_status(ws), 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return LILY_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
+  if (v && cudaMemsetAsync(ws_status(ws), 0, 4, s) != cudaSuccess) return LILY_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
+  return (int)v;
+}
+
+const char* lily_moe_strerror(int code) {
+  switch (code) {
+    case LILY_OK: return "ok";
+    case LILY_ERR_INVALID_ARG: return "invalid argument";
+    case LILY_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case LILY_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case LILY_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case LILY_ERR_ARCH: return "device is not compute capability 10.3 (sm_103a)";
+    case LILY_ERR_CUDA: return "CUDA runtime error";
+    case LILY_ERR_DEVICE: return "device status bits set";
+    default: return "unknown error";
+  }
+}
+
+int lily_moe_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = enable != 0;
+  return LILY_OK;
+}
+
+int lily_moe_profile_read(double* total_ms, int64_t* launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (total_ms)
+    for (int i = 0; i < LILY_KERNEL_KINDS; ++i) total_ms[i] = 0.0;
+  if (launches)
+    for (int i = 0; i < LILY_KERNEL_KINDS; ++i) launches[i] = 0;
+  int rc = LILY_OK;
+  for (auto& rec : g_prof_open) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(rec.b) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, rec.a, rec.b) != cudaSuccess)
+      rc = LILY_ERR_CUDA;
+    if (rec.kind >= 0 && rec.kind < LILY_KERNEL_KINDS) {
+      if (total_ms) total_ms[rec.kind] += ms;
+      if (launches) launches[rec.kind] += 1;
+    }
+    g_prof_pool.push_back(rec.a);
+    g_prof_pool.push_back(rec.b);
+  }
+  g_prof_open.clear();
+  return rc;
+}
+
+const char* lily_moe_kernel_name(int kind) {
+  static const char* names[] = {"router_gemm", "router_gemv", "route", "gateup_gemm",
+                                "down_gemm",   "finalize",    "dec_gateup", "dec_down",
+                                "dec_combine", "rmsnorm",     "stack_boundary", "memset_acc"};
+  if (kind < 0 || kind >= (int)(sizeof(names) / sizeof(names[0]))) return "unused";
+  return names[kind];
+}
+
+const char* lily_moe_version(void) { return "lily_moe 0.1 sm_103a"; }
+
+}  // extern "C"

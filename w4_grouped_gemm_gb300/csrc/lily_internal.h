@@ -1,0 +1,118 @@
+// lily_internal.h -- host-side launchers shared by the library's translation
+// units (not part of the public ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/lily_moe.h"
+
+namespace lily {
+
+// Kernel kinds for the optional per-kernel event timing.
+enum KernelKind : int {
+  K_ROUTER_GEMM = 0,
+  K_ROUTER_GEMV = 1,
+  K_ROUTE = 2,
+  K_GATEUP = 3,
+  K_DOWN = 4,
+  K_FINALIZE = 5,
+  K_DEC_GATEUP = 6,
+  K_DEC_DOWN = 7,
+  K_DEC_COMBINE = 8,
+  K_RMSNORM = 9,
+  K_STACK_BOUNDARY = 10,
+  K_MEMSET = 11,
+  K_NUM = 12
+};
+
+// Profiling hooks (api.cu): bracket one launch with events when enabled.
+void prof_begin(int kind, cudaStream_t s);
+void prof_end(int kind, cudaStream_t s);
+
+// Tokens handled by one block of the routing kernel.
+constexpr int kRouteTok = 32;
+constexpr int kRouteThreads = 256;
+
+// ---------------------------------------------------------------- routing
+struct RouteArgs {
+  const float* logits_src;  // fp32 [T][E]
+  float* logits_dst;        // fp32 [T][E] (may equal logits_src)
+  int T, E, k, BM, cap;
+  int32_t* ids;
+  float* gates;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* block_map;
+  int32_t* n_tiles;
+  int32_t* hist;       // workspace [nblk][E]
+  uint32_t* bar;       // workspace: grid barrier {count, generation}
+  uint32_t* status;    // workspace status word
+};
+// Also writes x16 (fp16 copy of x, for the grouped GEMM) when x16 != NULL.
+cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
+                                 int T, int d, int E, void* x16, uint32_t* status,
+                                 cudaStream_t s);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+int route_max_blocks();  // co-resident blocks of the routing kernel (0 = unknown)
+
+// ---------------------------------------------------------------- prefill GEMMs
+struct GemmArgs {
+  int T, E, k, d, F, BM;
+  const int32_t* block_map;
+  const int32_t* n_tiles;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const float* gates;
+  const uint16_t* s0;  // gate (or down) scales
+  const uint16_t* b0;
+  const uint16_t* s1;  // up scales (gate/up only)
+  const uint16_t* b1;
+  void* H;             // fp16 [P+T][F]
+  float* yacc;         // fp32 [T][d]
+  uint32_t* status;
+};
+// Tensor maps are built by the launcher from the raw pointers; x16 is the
+// fp16 copy of x written by the router kernel.
+cudaError_t launch_gateup(const GemmArgs& a, const void* x16, const uint8_t* gq, const uint8_t* uq,
+                          cudaStream_t s);
+cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s);
+cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s);
+size_t gemm_smem_bytes(bool gateup, int BM, int K);
+int gemm_stages(bool gateup, int BM, int K);
+
+// ---------------------------------------------------------------- decode
+struct DecodeArgs {
+  int T, E, k, d, F, cap;
+  const int32_t* block_map;
+  const int32_t* n_tiles;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* inv;
+  const float* gates;
+  const uint8_t* gq; const uint16_t* gs; const uint16_t* gb;
+  const uint8_t* uq; const uint16_t* us; const uint16_t* ub;
+  const uint8_t* dq; const uint16_t* ds; const uint16_t* db;
+  const void* x;   // bf16 [T][d]
+  void* H;         // fp16 [P+T][F]
+  float* O;        // fp32 [P+T][d]
+  void* y;         // bf16 [T][d]
+  uint32_t* status;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- misc
+cudaError_t launch_rmsnorm(const float* x, void* out, int T, int d, float eps, cudaStream_t s);
+// y = bf16(yacc); x += float(y); xn = bf16(rmsnorm(x)) (xn may be NULL)
+cudaError_t launch_stack_boundary(const float* yacc, float* x, void* xn, int T, int d, float eps,
+                                  cudaStream_t s);
+
+// Driver entry point for cuTensorMapEncodeTiled (resolved through the runtime).
+CUresult encode_tiled(CUtensorMap* tm, CUtensorMapDataType dt, uint32_t rank, void* base,
+                      const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                      CUtensorMapSwizzle swz);
+
+}  // namespace lily
