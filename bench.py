@@ -141,11 +141,11 @@ def dist_info():
     return ws, rank, local
 
 
-def algorithmic_bytes(T, d, E, k, F, counts):
+def algorithmic_bytes(T, d, E, k, F, counts, y_bytes=4):
     """Touched experts' W4 bytes (packed + bf16 scale/bias) + router W + x + y."""
     per_expert = 3 * (F * d // 2 + F * d // 64 * 4)
     touched = int((np.asarray(counts) > 0).sum()) + 1  # + shared expert
-    return touched * per_expert + E * d * 4 + T * d * 2 * 2, touched
+    return touched * per_expert + E * d * 4 + T * d * (2 + y_bytes), touched
 
 
 def gateup_bytes(T, d, F, touched):
@@ -228,7 +228,7 @@ def run_lily(args, world, rank, local):
         layers.append((inp["x"], lily.LayerWeights(inp["router_w"], inp["router_b"], inp["experts"])))
     r = lily.RoutingBuffers(dims, dev)
     wsb = lily.alloc_workspace(lily.lily_moe_workspace_bytes(dims), dev)
-    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(T, d, dtype=lily.out_torch_dtype(dims), device=dev)
     stream = torch.cuda.current_stream(dev)
     call = lily.lily_moe_decode if decode else lily.lily_moe_forward
 
@@ -284,7 +284,7 @@ def run_lily(args, world, rank, local):
     # end to end through the host-buffer entry point (pinned host x and y)
     e2e_steps = max(3, min(args.steps, 200))
     xh = [layers[l][0].cpu().pin_memory() for l in range(nl)]
-    yh = torch.empty(T, d, dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty(T, d, dtype=y.dtype).pin_memory()
     xd = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
     for i in range(3):
         lily.lily_moe_forward_host(dims, xh[i % nl], xd, layers[i % nl][1], r, y, yh, wsb, stream)
@@ -354,7 +354,7 @@ def run_lily(args, world, rank, local):
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (W4 weights, fp32 accumulate)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 tensor-core operands (W4 weights, bf16 x), fp32 accumulate, fp32 out",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
         "config": {
             "workload": args.workload, "T": T, "d_model": d, "n_experts": E, "top_k": k,
@@ -371,7 +371,7 @@ def run_lily(args, world, rank, local):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * d * 2,
-                "d2h_bytes_per_step": T * d * 2},
+                "d2h_bytes_per_step": T * d * y.element_size()},
         "gpu_launches": launches,
         "clocks": clocks,
     }

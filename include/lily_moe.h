@@ -67,9 +67,13 @@ extern "C" {
  * group      quantisation group; must be 64
  * tile_rows  BM, rows of one block-map tile (the grouped GEMM's N tile);
  *            one of 32, 64, 128, 256
+ * out_dtype  element type of the layer output y: LILY_DTYPE_F32 (the fp32
+ *            accumulator itself) or LILY_DTYPE_BF16 (rounded once)
  */
+#define LILY_DTYPE_BF16 0
+#define LILY_DTYPE_F32 1
 typedef struct {
-  int32_t T, d_model, n_experts, top_k, d_ff, group, tile_rows;
+  int32_t T, d_model, n_experts, top_k, d_ff, group, tile_rows, out_dtype;
 } lily_moe_dims;
 
 /* Weights of one layer.  Expert index E (the (E+1)-th) is the shared expert.
@@ -146,7 +150,8 @@ int lily_moe_route(const lily_moe_dims* dims, const void* x, const float* logits
 /* The whole layer for prefill-sized T: routing as in lily_moe_route, then the
  * gate/up grouped GEMM (fused 4-bit dequant + SwiGLU) and the down grouped GEMM
  * (fused dequant + gated scatter-add back to token order).
- *   x  bf16 [T][d] device in, y  bf16 [T][d] device out. */
+ *   x  bf16 [T][d] device in; y [T][d] device out, fp32 or bf16 per
+ *   dims->out_dtype. */
 int lily_moe_forward(const lily_moe_dims* dims, const void* x,
                      const lily_moe_weights* weights, lily_moe_routing* routing,
                      void* y, void* workspace, size_t workspace_bytes, void* stream);
@@ -162,7 +167,7 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x,
  * callers holding activations in HOST memory: copies x_host (bf16 [T][d],
  * pinned for best speed) to x_dev, runs the layer, copies y_dev back into
  * y_host and synchronises `stream` before returning.  x_dev/y_dev are device
- * staging buffers of T*d bf16 each. */
+ * staging buffers of T*d elements (bf16 for x, out_dtype for y). */
 int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x_dev,
                           const lily_moe_weights* weights, lily_moe_routing* routing,
                           void* y_dev, void* y_host, void* workspace,
@@ -176,7 +181,7 @@ int lily_moe_rmsnorm(int32_t T, int32_t d, const float* x, float eps, void* out_
 /* Stacked prefill: n_layers MoE layers with residual, in chunks of `chunk`
  * tokens (dims->T is the chunk size; T_total a multiple of it):
  *   for each chunk, for l in 0..n_layers-1:
- *     x <- x + float(MoE_l(bf16(rmsnorm(x))))
+ *     x <- x + MoE_l(bf16(rmsnorm(x)))      (MoE output added in fp32)
  * x fp32 [T_total][d] device, updated in place.  layers[l] are the weights of
  * layer l.  layer_inputs (fp32 [n_layers][T_total][d]) and layer_logits
  * (fp32 [n_layers][T_total][E]) are optional device traces (NULL to skip).

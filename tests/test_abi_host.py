@@ -53,6 +53,7 @@ def test_check_dims():
         lily.make_dims(512, 2048, 256, 8, 512, 48),
         lily.make_dims(512, 2048, 256, 8, 512, 128, group=32),
         lily.make_dims(20000, 2048, 256, 8, 512, 128),
+        lily.make_dims(512, 2048, 256, 8, 512, 128, out_dtype=7),
     ]
     for d in bad:
         assert lily.lily_moe_check_dims(d) < 0

@@ -2,8 +2,8 @@
 
 The oracle routes from the GPU's own fp32 logits (routing parity is tested
 bit-exact separately), so a near-tie can never make the two sides pick
-different experts.  Outputs must meet max|err|/rms <= 2e-2 and
-mean|err|/mean|ref| <= 5e-3.
+different experts.  The fp32 layer output must meet max|err|/rms <= 2e-2 and
+mean|err|/mean|ref| <= 5e-3; the bf16 output is that fp32 output rounded once.
 """
 import numpy as np
 import pytest
@@ -134,7 +134,7 @@ def test_decode_matches_forward(oracle_lib):
     yd = L.decode().float().clone()
     yf = L.forward().float()
     rel = (yd - yf).abs().max().item() / yf.pow(2).mean().sqrt().item()
-    assert rel < 2e-2
+    assert rel < 5e-3
 
 
 def test_forward_host_entry(oracle_lib):
@@ -142,9 +142,23 @@ def test_forward_host_entry(oracle_lib):
     L = Layer(synth.LayerShape(64, 512, 32, 4, 128), seed=4300, tile_rows=32)
     ydev = L.forward().clone()
     xh = L.x.cpu().pin_memory()
-    yh = torch.empty(64, 512, dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty(64, 512, dtype=L.y.dtype).pin_memory()
     xd = torch.empty_like(L.x)
     yd = torch.empty_like(L.y)
     lily.lily_moe_forward_host(L.dims, xh, xd, L.w, L.r, yd, yh, L.ws)
     rel = (yh.float() - ydev.cpu().float()).abs().max().item() / ydev.float().pow(2).mean().sqrt().item()
     assert rel < 1e-2
+
+
+@pytest.mark.parametrize("decode", [False, True])
+def test_bf16_output_is_rounded_fp32_output(oracle_lib, decode):
+    """out_dtype = bf16 gives the fp32 output rounded once (to within the fp32
+    atomic-order noise between two runs), for both paths."""
+    shape = synth.LayerShape(8 if decode else 96, 512, 32, 4, 128)
+    Lf = Layer(shape, seed=4400, tile_rows=32)
+    Lb = Layer(shape, seed=4400, tile_rows=32, out_dtype=lily.LILY_DTYPE_BF16)
+    yf = (Lf.decode() if decode else Lf.forward()).double()
+    yb = (Lb.decode() if decode else Lb.forward()).double()
+    assert Lb.y.dtype == torch.bfloat16
+    bound = yf.abs() * 2.0 ** -8 + 1e-6 * yf.pow(2).mean().sqrt()
+    assert bool(((yb - yf).abs() <= bound).all())

@@ -26,6 +26,7 @@ LILY_ERR_DEVICE = -7
 LILY_STATUS_NAN_LOGIT = 0x1
 LILY_STATUS_TIMEOUT = 0x2
 LILY_STATUS_BAD_TILE = 0x4
+LILY_STATUS_F16_RANGE = 0x8
 LILY_KERNEL_KINDS = 16
 
 # Every symbol include/lily_moe.h declares.
@@ -44,10 +45,14 @@ class LilyError(RuntimeError):
         self.code = code
 
 
+LILY_DTYPE_BF16 = 0
+LILY_DTYPE_F32 = 1
+
+
 class Dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
                 ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("tile_rows", ctypes.c_int32)]
+                ("tile_rows", ctypes.c_int32), ("out_dtype", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -127,8 +132,12 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def make_dims(T, d, E, k, F, tile_rows=128, group=64) -> Dims:
-    return Dims(T, d, E, k, F, group, tile_rows)
+def make_dims(T, d, E, k, F, tile_rows=128, group=64, out_dtype=LILY_DTYPE_F32) -> Dims:
+    return Dims(T, d, E, k, F, group, tile_rows, out_dtype)
+
+
+def out_torch_dtype(dims: Dims):
+    return torch.float32 if dims.out_dtype == LILY_DTYPE_F32 else torch.bfloat16
 
 
 def lily_moe_check_dims(dims: Dims) -> int:

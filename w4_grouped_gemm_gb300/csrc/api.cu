@@ -193,12 +193,14 @@ GemmArgs gemm_args(const lily_moe_dims& d, const lily_moe_weights* w, const lily
   return a;
 }
 
-// Routing + grouped GEMMs; the layer output stays in the fp32 accumulator.
+// Routing + grouped GEMMs.  The layer output is accumulated in fp32 into
+// yacc (the workspace accumulator when NULL).
 int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
-                   const lily_moe_routing& r, void* ws, cudaStream_t s) {
+                   const lily_moe_routing& r, void* ws, cudaStream_t s, float* yacc = nullptr) {
   int rc = do_route(d, x, nullptr, w, r, ws, s);
   if (rc) return rc;
   GemmArgs a = gemm_args(d, w, r, ws);
+  if (yacc) a.yacc = yacc;
   prof_begin(K_MEMSET, s);
   cudaError_t e = cudaMemsetAsync(a.yacc, 0, (size_t)d.T * d.d_model * 4, s);
   prof_end(K_MEMSET, s);
@@ -245,6 +247,8 @@ int lily_moe_check_dims(const lily_moe_dims* d) {
   if (d->n_experts > 256) return LILY_ERR_UNSUPPORTED_SHAPE;
   if (d->top_k > 8 || d->top_k > d->n_experts) return LILY_ERR_UNSUPPORTED_SHAPE;
   if (d->group != 64) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (d->out_dtype != LILY_DTYPE_BF16 && d->out_dtype != LILY_DTYPE_F32)
+    return LILY_ERR_UNSUPPORTED_SHAPE;
   if (d->tile_rows != 32 && d->tile_rows != 64 && d->tile_rows != 128 && d->tile_rows != 256)
     return LILY_ERR_UNSUPPORTED_SHAPE;
   if (gemm_stages(true, d->tile_rows, d->d_model) < 2 || gemm_stages(false, d->tile_rows, d->d_ff) < 2)
@@ -291,6 +295,8 @@ int lily_moe_forward(const lily_moe_dims* dims, const void* x, const lily_moe_we
   const int maxb = route_max_blocks();
   if (maxb > 0 && (dims->T + kRouteTok - 1) / kRouteTok > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
+  if (dims->out_dtype == LILY_DTYPE_F32)  // accumulate straight into the caller's y
+    return do_forward_acc(*dims, x, w, *r, ws, s, static_cast<float*>(y));
   if ((rc = do_forward_acc(*dims, x, w, *r, ws, s))) return rc;
   const Layout L = layout(*dims);
   return cuda_rc(launch_finalize(reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.acc), y,
@@ -326,6 +332,7 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_wei
   a.H = base + L.H;
   a.O = reinterpret_cast<float*>(base + L.acc);
   a.y = y;
+  a.y_f32 = dims->out_dtype == LILY_DTYPE_F32;
   a.status = ws_status(ws);
   return cuda_rc(launch_decode(a, s));
 }
@@ -337,13 +344,14 @@ int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x
   int rc = common_checks(dims, x_dev, w, r, y_dev, ws, ws_bytes, true);
   if (rc) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t bytes = (size_t)dims->T * dims->d_model * 2;
-  if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  const size_t n = (size_t)dims->T * dims->d_model;
+  if (cudaMemcpyAsync(x_dev, x_host, n * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
     return LILY_ERR_CUDA;
   rc = dims->T <= 8 ? lily_moe_decode(dims, x_dev, w, r, y_dev, ws, ws_bytes, stream)
                     : lily_moe_forward(dims, x_dev, w, r, y_dev, ws, ws_bytes, stream);
   if (rc) return rc;
-  if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  const size_t ybytes = n * (dims->out_dtype == LILY_DTYPE_F32 ? 4 : 2);
+  if (cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return LILY_ERR_CUDA;
   return cuda_rc(cudaStreamSynchronize(s));
 }

@@ -246,11 +246,11 @@ __global__ void __launch_bounds__(kDecThreads) dec_down_kernel(const DecodeArgs 
   }
 }
 
-// y[t] = bf16( sum_j gate[t][j] * O[inv[t*k+j]] + O[P + t] ), slot order.
+// y[t] = sum_j gate[t][j] * O[inv[t*k+j]] + O[P + t], in slot order (fp32,
+// or rounded once to bf16).
 __global__ void __launch_bounds__(256) dec_combine_kernel(const DecodeArgs a) {
   const int t = blockIdx.x;
   const int P = a.T * a.k;
-  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(a.y);
   for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
     float acc = 0.f;
     for (int j = 0; j < a.k; ++j) {
@@ -258,7 +258,10 @@ __global__ void __launch_bounds__(256) dec_combine_kernel(const DecodeArgs a) {
       acc += a.gates[p] * a.O[(size_t)a.inv[p] * a.d + i];
     }
     acc += a.O[(size_t)(P + t) * a.d + i];
-    y[(size_t)t * a.d + i] = __float2bfloat16_rn(acc);
+    if (a.y_f32)
+      static_cast<float*>(a.y)[(size_t)t * a.d + i] = acc;
+    else
+      static_cast<__nv_bfloat16*>(a.y)[(size_t)t * a.d + i] = __float2bfloat16_rn(acc);
   }
 }
 

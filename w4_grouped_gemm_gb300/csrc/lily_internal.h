@@ -99,14 +99,15 @@ struct DecodeArgs {
   const void* x;   // bf16 [T][d]
   void* H;         // fp16 [P+T][F]
   float* O;        // fp32 [P+T][d]
-  void* y;         // bf16 [T][d]
+  void* y;         // [T][d], fp32 if y_f32 else bf16
+  bool y_f32;
   uint32_t* status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- misc
 cudaError_t launch_rmsnorm(const float* x, void* out, int T, int d, float eps, cudaStream_t s);
-// y = bf16(yacc); x += float(y); xn = bf16(rmsnorm(x)) (xn may be NULL)
+// x += yacc; xn = bf16(rmsnorm(x)) (xn may be NULL)
 cudaError_t launch_stack_boundary(const float* yacc, float* x, void* xn, int T, int d, float eps,
                                   cudaStream_t s);
 

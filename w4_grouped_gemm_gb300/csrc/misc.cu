@@ -4,7 +4,7 @@
 // The pages name no normalisation around the MoE block; a bare residual stack
 // x <- x + MoE(x) of SwiGLU experts grows without bound, so the stack uses the
 // standard pre-norm block x <- x + MoE(bf16(rmsnorm(x))) with an fp32
-// residual.  Long prompts run in bounded chunks (page "Lily Beats MLX-LM
+// residual to which the layer's fp32 output is added.  Long prompts run in bounded chunks (page "Lily Beats MLX-LM
 // 1.35x on Decode: Perplexity's Rust+Metal Engine for Apple Silicon", section
 // "Prefill: fusing dequantisation and keeping routing GPU-resident").
 #include "common.cuh"
@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __res
   rms_row(x + row * d, out + row * d, d, eps, tmp);
 }
 
-// y = bf16(yacc); x += float(y); then (optionally) xn = bf16(rmsnorm(x)).
+// x += yacc (the layer's fp32 output); then (optionally) xn = bf16(rmsnorm(x)).
 __global__ void __launch_bounds__(kRowThreads) stack_boundary_kernel(const float* __restrict__ yacc,
                                                                      float* __restrict__ x,
                                                                      __nv_bfloat16* __restrict__ xn,
@@ -50,10 +50,7 @@ __global__ void __launch_bounds__(kRowThreads) stack_boundary_kernel(const float
   const size_t row = blockIdx.x;
   float* xr = x + row * d;
   const float* yr = yacc + row * d;
-  for (int i = threadIdx.x; i < d; i += kRowThreads) {
-    const float y = __bfloat162float(__float2bfloat16_rn(yr[i]));
-    xr[i] = xr[i] + y;
-  }
+  for (int i = threadIdx.x; i < d; i += kRowThreads) xr[i] = xr[i] + yr[i];
   __syncthreads();
   if (xn) rms_row(xr, xn + row * d, d, eps, tmp);
 }
