@@ -163,6 +163,30 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x,
                     const lily_moe_weights* weights, lily_moe_routing* routing,
                     void* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/* lily_moe_decode without a caller workspace.  The Lily pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory: a host application that passes this library only its activation
+ * and weight buffers while keeping all other device memory under its own
+ * accounting, or a token loop that must not enter the CUDA allocator between
+ * tokens.  Same arguments and result as lily_moe_decode minus the workspace.
+ *   - Scratch comes from one array of 1 MiB declared at file scope in the
+ *     library; every device that loads the library holds it until the
+ *     process exits.  Dims whose workspace (lily_moe_workspace_bytes) exceeds
+ *     1 MiB are refused with LILY_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - Every call shares the one array, which keeps the previous call's
+ *     contents; each call clears the part that must start at zero (the status
+ *     and barrier words).  Calls that overlap on the GPU (other streams, other
+ *     host threads) race on the array and must be ordered by the caller.
+ *   - Device status bits are cleared at the start of each call and cannot be
+ *     read back through this entry point. */
+int lily_moe_decode_static(const lily_moe_dims* dims, const void* x,
+                           const lily_moe_weights* weights, lily_moe_routing* routing,
+                           void* y, void* stream);
+
 /* End-to-end form of lily_moe_forward (T >= 9) / lily_moe_decode (T <= 8) for
  * callers holding activations in HOST memory: copies x_host (bf16 [T][d],
  * pinned for best speed) to x_dev, runs the layer, copies y_dev back into

@@ -32,7 +32,8 @@ LILY_KERNEL_KINDS = 16
 # Every symbol include/lily_moe.h declares.
 EXPORTS = (
     "lily_moe_workspace_bytes", "lily_moe_block_map_cap", "lily_moe_check_dims",
-    "lily_moe_route", "lily_moe_forward", "lily_moe_decode", "lily_moe_forward_host",
+    "lily_moe_route", "lily_moe_forward", "lily_moe_decode", "lily_moe_decode_static",
+    "lily_moe_forward_host",
     "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_workspace_bytes",
     "lily_moe_status", "lily_moe_strerror", "lily_moe_profile_enable", "lily_moe_profile_read",
     "lily_moe_kernel_name", "lily_moe_version",
@@ -88,6 +89,7 @@ def lib():
             "lily_moe_route": (I, [DP, P, P, WP, RP, P, SZ, P]),
             "lily_moe_forward": (I, [DP, P, WP, RP, P, P, SZ, P]),
             "lily_moe_decode": (I, [DP, P, WP, RP, P, P, SZ, P]),
+            "lily_moe_decode_static": (I, [DP, P, WP, RP, P, P]),
             "lily_moe_forward_host": (I, [DP, P, P, WP, RP, P, P, P, SZ, P]),
             "lily_moe_rmsnorm": (I, [ctypes.c_int32, ctypes.c_int32, P, ctypes.c_float, P, P]),
             "lily_moe_stack_prefill": (I, [DP, ctypes.c_int32, ctypes.c_int32, WP, P,

@@ -17,7 +17,7 @@ CSRC = PKG / "csrc"
 INCLUDE = PKG.parent / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "liblily_moe.so"
-SOURCES = ["api.cu", "route.cu", "gemm.cu", "decode.cu", "misc.cu"]
+SOURCES = ["api.cu", "route.cu", "gemm.cu", "decode.cu", "misc.cu", "static_ws.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]
