@@ -141,6 +141,20 @@ def dist_info():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_rank: int, steps: int, seconds: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / seconds
+
+
 def algorithmic_bytes(T, d, E, k, F, counts, y_bytes=4):
     """Touched experts' W4 bytes (packed + bf16 scale/bias) + router W + x + y."""
     per_expert = 3 * (F * d // 2 + F * d // 64 * 4)
@@ -273,10 +287,7 @@ def run_lily(args, world, rank, local):
     if sampler:
         time.sleep(0.2)
         sampler.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     status = lily.lily_moe_status(wsb)
     if status:
         raise RuntimeError(f"device status bits set: {status}")
@@ -294,16 +305,13 @@ def run_lily(args, world, rank, local):
     for i in range(e2e_steps):
         lily.lily_moe_forward_host(dims, xh[i % nl], xd, layers[i % nl][1], r, y, yh, wsb, stream)
     e2e_s = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(e2e_s, world, dev)
 
     if rank != 0:
         return
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
-    value = world * T * args.steps / (ms / 1000.0)
-    e2e_value = world * T * e2e_steps / e2e_s
+    value = job_throughput(world, T, args.steps, ms / 1000.0)
+    e2e_value = job_throughput(world, T, e2e_steps, e2e_s)
     alg_bytes = []
     touched_l = []
     for c in counts_by_layer:

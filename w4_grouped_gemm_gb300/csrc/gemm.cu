@@ -26,34 +26,47 @@
 // Epilogues: gate/up writes H = silu(gate) * up (fp16) in expert-sorted row
 // order; down adds gate * out into the fp32 token-order accumulator.
 //
-// Warp roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
-// MMA issuer (one thread), warps 2..9 = dequant, then epilogue.
-// Every wait is bounded (2 s) and sets LILY_STATUS_TIMEOUT when it runs out.
+// Persistent: one CTA per SM walks the (tile, slice) work items; warp roles
+// are listed below.  Every wait is bounded (2 s) and sets
+// LILY_STATUS_TIMEOUT when it runs out.
 #include "common.cuh"
 
 namespace lily {
 
-constexpr int kGemmThreads = 320;
+// Warp roles.  Warp 0: TMA producer.  Warp 1: TMEM owner + MMA issuer (one
+// thread).  Warps 2..9: dequant (one 128-row weight slice per K-step).
+// Warps 10..13: epilogue (TMEM -> global), overlapped with the next item's
+// main loop through double-buffered accumulators; the epilogue warps also
+// fill the next item's scale/bias table ahead of the dequant warps.
+constexpr int kNumDequantWarps = 8;
+constexpr int kNumEpiWarps = 4;
+constexpr int kEpiWarp0 = 2 + kNumDequantWarps;
+constexpr int kGemmThreads = 32 * (2 + kNumDequantWarps + kNumEpiWarps);  // 448
+constexpr int kDequantThreads = 32 * kNumDequantWarps;
+constexpr int kEpiThreads = 32 * kNumEpiWarps;
 constexpr int kMaxStages = 8;
 constexpr int kPackedBytes = 128 * 32;  // 128 rows x 64 4-bit codes
 constexpr int kABytes = 128 * 128;      // 128 rows x 64 fp16
+constexpr int kNumBars = 2 * kMaxStages + 13;
 
 template <bool GATEUP, int BM>
 struct GemmLayout {
   static constexpr int kMats = GATEUP ? 2 : 1;
   static constexpr int kBBytes = BM * 128;
   static constexpr int kStage = kBBytes + kMats * kPackedBytes;
-  static constexpr uint32_t kTmemCols = GATEUP ? 2 * BM : BM;
+  static constexpr int kAccCols = GATEUP ? 2 * BM : BM;         // one accumulator set
+  static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;  // TMEM double buffer
+  static constexpr uint32_t kTmemCols =
+      (kAccCols * kNumAcc <= 32) ? 32 : (uint32_t)(kAccCols * kNumAcc);
 };
 
-__host__ __device__ inline size_t gemm_fixed_bytes(int mats, int BM, int K) {
+__host__ __device__ inline size_t gemm_fixed_bytes(int mats, int BM, int K, int nsb) {
   const int G = K / 64;
-  return 1024                               // alignment slack
-         + (size_t)2 * mats * kABytes       // dequantised A, double-buffered
-         + (size_t)mats * G * 128 * 4       // scale/bias pairs
-         + (size_t)BM * 8                   // row -> token, row -> gate
-         + (2 * kMaxStages + 5) * 8         // mbarriers
-         + 16;                              // abort flag, TMEM address
+  return 1024                                  // alignment slack
+         + (size_t)2 * mats * kABytes          // dequantised A, double-buffered
+         + (size_t)nsb * mats * G * 128 * 4    // scale/bias tables (one per item in flight)
+         + kNumBars * 8                        // mbarriers
+         + 16;                                 // abort flag, TMEM address
 }
 
 size_t gemm_stage_bytes(bool gateup, int BM) {
@@ -62,22 +75,42 @@ size_t gemm_stage_bytes(bool gateup, int BM) {
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
 
-int gemm_stages(bool gateup, int BM, int K) {
-  const size_t fixed = gemm_fixed_bytes(gateup ? 2 : 1, BM, K);
+// Pipeline depth and scale-table buffering that fit in shared memory: two
+// scale tables (the next item's is filled while the current one is in use)
+// when that still leaves >= 3 stages, else one table.
+static int stages_for(bool gateup, int BM, int K, int nsb) {
+  const size_t fixed = gemm_fixed_bytes(gateup ? 2 : 1, BM, K, nsb);
   if (fixed >= kSmemLimit) return 0;
   int s = (int)((kSmemLimit - fixed) / gemm_stage_bytes(gateup, BM));
-  if (s > kMaxStages) s = kMaxStages;
-  if (s > K / 64) s = (K / 64 < 2) ? 2 : K / 64;
-  return s < 2 ? 0 : s;
+  return s > kMaxStages ? kMaxStages : s;
+}
+
+void gemm_config(bool gateup, int BM, int K, int* stages, int* nsb) {
+  const int s2 = stages_for(gateup, BM, K, 2);
+  if (s2 >= 3) {
+    *stages = s2;
+    *nsb = 2;
+    return;
+  }
+  const int s1 = stages_for(gateup, BM, K, 1);
+  *stages = s1 >= 2 ? s1 : 0;
+  *nsb = 1;
+}
+
+int gemm_stages(bool gateup, int BM, int K) {
+  int s, n;
+  gemm_config(gateup, BM, K, &s, &n);
+  return s;
 }
 
 size_t gemm_smem_bytes(bool gateup, int BM, int K) {
-  int s = gemm_stages(gateup, BM, K);
-  return gemm_fixed_bytes(gateup ? 2 : 1, BM, K) + (size_t)s * gemm_stage_bytes(gateup, BM);
+  int s, n;
+  gemm_config(gateup, BM, K, &s, &n);
+  return gemm_fixed_bytes(gateup ? 2 : 1, BM, K, n) + (size_t)s * gemm_stage_bytes(gateup, BM);
 }
 
 // Wait by lane 0 only, result broadcast: keeps every warp-collective op
-// (tcgen05.ld, __syncwarp) convergent even when a wait gives up.
+// (tcgen05.ld, __syncwarp, shuffles) convergent even when a wait gives up.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
   int ok = 1;
@@ -85,63 +118,131 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// One work item = one block-map tile (or shared-expert tile) x one 128-row
+// slice of the weight matrix.  Items are numbered tile-major so the slices of
+// one tile, and the tiles of one expert, run at the same time and share the
+// expert's weights and token rows through L2.  Shared-expert tiles come first.
+struct Item {
+  int expert, row0, rows, slice;
+  bool shared;
+};
+
+template <int BM>
+__device__ __forceinline__ bool get_item(const GemmArgs& a, int w, int nslices, int nsh, int P,
+                                         Item& it) {
+  const int tile = w / nslices;
+  it.slice = w % nslices;
+  it.shared = tile < nsh;
+  if (it.shared) {
+    it.expert = a.E;
+    it.row0 = P + tile * BM;
+    it.rows = min(BM, P + a.T - it.row0);
+    return true;
+  }
+  const int ti = tile - nsh;
+  it.expert = __ldg(a.block_map + 2 * ti);
+  it.row0 = __ldg(a.block_map + 2 * ti + 1);
+  if (it.expert < 0 || it.expert >= a.E || it.row0 < 0 || it.row0 >= P) return false;
+  it.rows = min(BM, __ldg(a.offsets + it.expert + 1) - it.row0);
+  return it.rows > 0;
+}
+
+// Advance w (stepping by gridDim.x) to the next valid item; false at the end.
+template <int BM>
+__device__ __forceinline__ bool next_item(const GemmArgs& a, int& w, int n_items, int nslices,
+                                          int nsh, int P, Item& it) {
+  for (; w < n_items; w += gridDim.x)
+    if (get_item<BM>(a, w, nslices, nsh, P, it)) return true;
+  return false;
+}
+
+// Scale/bias table of one item: sb[mat][g][r] = (fp16 scale | fp16 bias << 16)
+// for the item's 128 weight rows r and every group g.  Filled by the epilogue
+// threads, thread r owning row r.  One 16-byte chunk = 8 groups of one array
+// (scale or bias) of one matrix; chunk q -> (mat, array, 8-group block).
+__device__ __forceinline__ uint4 scale_chunk_load(const GemmArgs& a, size_t row, int G, int q) {
+  const int per = G / 8;
+  const int mat = q / (2 * per), arr = (q / per) & 1, ch = q % per;
+  const uint16_t* src = mat == 0 ? (arr ? a.b0 : a.s0) : (arr ? a.b1 : a.s1);
+  return __ldg(reinterpret_cast<const uint4*>(src + row * G + ch * 8));
+}
+__device__ __forceinline__ void scale_chunk_store(uint16_t* sbh, int G, int q, int r, uint4 v) {
+  const int per = G / 8;
+  const int mat = q / (2 * per), arr = (q / per) & 1, ch = q % per;
+  const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    sbh[2 * ((mat * G + ch * 8 + e) * 128 + r) + arr] = bf16_to_f16_bits(h[e]);
+}
+template <int MATS>
+__device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint16_t* sbh) {
+  if ((G & 7) == 0) {
+    const int nq = MATS * 2 * (G / 8);
+    for (int base = 0; base < nq; base += 8) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (base + j < nq) v[j] = scale_chunk_load(a, row, G, base + j);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (base + j < nq) scale_chunk_store(sbh, G, base + j, r, v[j]);
+    }
+  } else {
+    for (int q = 0; q < MATS * 2 * G; ++q) {
+      const int mat = q / (2 * G), arr = (q / G) & 1, g = q % G;
+      const uint16_t* src = mat == 0 ? (arr ? a.b0 : a.s0) : (arr ? a.b1 : a.s1);
+      sbh[2 * ((mat * G + g) * 128 + r) + arr] = bf16_to_f16_bits(__ldg(src + row * G + g));
+    }
+  }
+}
+
+// Token of expert-sorted row r (the row's pair index / k; shared rows are
+// tokens in order).
+__device__ __forceinline__ int row_token(const GemmArgs& a, int r, int P) {
+  return r >= P ? r - P : __ldg(a.perm + r) / a.k;
+}
+
+// Persistent kernel: one CTA per SM loops over the work items.
 template <bool GATEUP, int BM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     w4_gemm_kernel(const __grid_constant__ CUtensorMap tm_q0,
                    const __grid_constant__ CUtensorMap tm_q1,
-                   const __grid_constant__ CUtensorMap tm_b, const GemmArgs a, const int nstages) {
+                   const __grid_constant__ CUtensorMap tm_b, const GemmArgs a, const int nstages,
+                   const int nsb) {
   using L = GemmLayout<GATEUP, BM>;
   constexpr int MATS = L::kMats;
   constexpr int BBYTES = L::kBBytes;
   constexpr int STAGE = L::kStage;
+  constexpr int NACC = L::kNumAcc;
 
   const int K = GATEUP ? a.d : a.F;     // reduction length
   const int NOUT = GATEUP ? a.F : a.d;  // output features of each matrix
   const int G = K / 64;                 // K-steps = quantisation groups
   const int nslices = NOUT / 128;
   const int P = a.T * a.k;
-  const int nsh = (a.T + BM - 1) / BM;  // shared-expert tiles come first
-
-  // ---- which tile / slice this CTA computes (uniform early exit)
-  const int tile = blockIdx.x / nslices, slice = blockIdx.x % nslices;
-  int expert, row0, rows;
-  const bool shared_tile = tile < nsh;
-  if (shared_tile) {
-    expert = a.E;
-    row0 = P + tile * BM;
-    rows = min(BM, P + a.T - row0);
-  } else {
-    const int ti = tile - nsh;
-    if (ti >= *a.n_tiles) return;
-    expert = a.block_map[2 * ti];
-    row0 = a.block_map[2 * ti + 1];
-    if (expert < 0 || expert >= a.E || row0 < 0 || row0 >= P) {
-      if (threadIdx.x == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
-      return;
-    }
-    rows = min(BM, a.offsets[expert + 1] - row0);
-    if (rows <= 0) {
-      if (threadIdx.x == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
-      return;
-    }
-  }
-  const int N = (rows + 15) & ~15;  // MMA N: multiple of 16, <= BM
+  const int nsh = (a.T + BM - 1) / BM;
+  const int cap = (P + BM - 1) / BM + min(a.E, P);
+  const int ntiles = min(max(*a.n_tiles, 0), cap);
+  const int n_items = (nsh + ntiles) * nslices;
 
   // ---- shared memory carve-up
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
   uint8_t* a_base = smem + (size_t)nstages * STAGE;
-  uint32_t* sb = (uint32_t*)(a_base + 2 * MATS * kABytes);  // [MATS][G][128] (scale | bias<<16)
-  int* rowtok = (int*)(sb + MATS * G * 128);                 // [BM]
-  float* rowgate = (float*)(rowtok + BM);                    // [BM]
-  uint64_t* bars = (uint64_t*)(rowgate + BM);
-  uint64_t* full = bars;                       // [kMaxStages] TMA landed
-  uint64_t* empty = bars + kMaxStages;         // [kMaxStages] stage consumed by MMA
-  uint64_t* afull = bars + 2 * kMaxStages;     // [2] dequantised A ready
-  uint64_t* aempty = afull + 2;                // [2] A consumed by MMA
-  uint64_t* accfull = aempty + 2;              // accumulators final
-  int* misc = (int*)(accfull + 1);
+  uint32_t* sb = (uint32_t*)(a_base + 2 * MATS * kABytes);  // [nsb][MATS][G][128] scale|bias<<16
+  const int sb_words = MATS * G * 128;                       // one table
+  uint64_t* bars = (uint64_t*)(sb + nsb * sb_words);
+  uint64_t* full = bars;                      // [kMaxStages] TMA landed
+  uint64_t* empty = bars + kMaxStages;        // [kMaxStages] stage consumed by the MMAs
+  uint64_t* afull = bars + 2 * kMaxStages;    // [2] dequantised A ready
+  uint64_t* aempty = afull + 2;               // [2] A consumed by the MMAs
+  uint64_t* accfull = aempty + 2;             // [2] accumulator set final
+  uint64_t* accempty = accfull + 2;           // [2] accumulator set drained by the epilogue
+  uint64_t* sbfull = accempty + 2;            // [2] scale table filled (epilogue -> dequant)
+  uint64_t* sbempty = sbfull + 2;             // [2] scale table no longer read (dequant -> epilogue)
+  uint64_t* drain = sbempty + 2;              // every MMA of this CTA finished
+  int* misc = (int*)(drain + 1);
   volatile int* abort = misc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -152,10 +253,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&afull[b]), kGemmThreads - 64);
+      mbar_init(smem_u32(&afull[b]), kDequantThreads);
       mbar_init(smem_u32(&aempty[b]), 1);
+      mbar_init(smem_u32(&accfull[b]), 1);
+      mbar_init(smem_u32(&accempty[b]), kEpiThreads);
+      mbar_init(smem_u32(&sbfull[b]), kEpiThreads);
+      mbar_init(smem_u32(&sbempty[b]), kDequantThreads);
     }
-    mbar_init(smem_u32(accfull), 1);
+    mbar_init(smem_u32(drain), 1);
     misc[0] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_q0);
@@ -166,33 +271,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(smem_u32(&misc[1]), L::kTmemCols);
     tmem_relinquish();
   }
-  for (int n = threadIdx.x; n < BM; n += kGemmThreads) {
-    const int r = row0 + min(n, rows - 1);  // padding rows repeat the last row
-    int tok;
-    float g;
-    if (shared_tile) {
-      tok = r - P;
-      g = 1.f;
-    } else {
-      const int p = a.perm[r];
-      tok = p / a.k;
-      g = a.gates[p];
-    }
-    rowtok[n] = tok;
-    rowgate[n] = g;
-  }
-  if (warp >= 2) {  // scale/bias of this CTA's 128 weight rows, per group
-    const int i = threadIdx.x - 64;
-    int mat, r, g0, gstep;
-    if (GATEUP) { mat = i >> 7; r = i & 127; g0 = 0; gstep = 1; }
-    else        { mat = 0;      r = i >> 1;  g0 = i & 1; gstep = 2; }
-    const size_t row = (size_t)expert * NOUT + (size_t)slice * 128 + r;
-    const uint16_t* sp = (mat == 0 ? a.s0 : a.s1) + row * G;
-    const uint16_t* bp = (mat == 0 ? a.b0 : a.b1) + row * G;
-    for (int g = g0; g < G; g += gstep)
-      sb[(mat * G + g) * 128 + r] = (uint32_t)bf16_to_f16_bits(__ldg(sp + g)) |
-                                    ((uint32_t)bf16_to_f16_bits(__ldg(bp + g)) << 16);
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -200,136 +278,269 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ================================================= TMA producer
-    const int wrow = expert * NOUT + slice * 128;
-    const uint32_t tx_bytes = MATS * kPackedBytes + (GATEUP ? N * 128 : BBYTES);
-    int issued = 0;
-    for (int kk = 0; kk < G; ++kk) {
-      const int s = kk % nstages;
-      if (kk >= nstages && !warp_wait(smem_u32(&empty[s]), ((kk / nstages) + 1) & 1, abort, a.status))
-        break;
-      const uint32_t fb = smem_u32(&full[s]);
-      uint8_t* st = stage_base + (size_t)s * STAGE;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(fb, tx_bytes);
-        tma_load_2d(smem_u32(st + BBYTES), &tm_q0, kk * 32, wrow, fb);
-        if (GATEUP) tma_load_2d(smem_u32(st + BBYTES + kPackedBytes), &tm_q1, kk * 32, wrow, fb);
-        if (!GATEUP) tma_load_2d(smem_u32(st), &tm_b, kk * 64, row0, fb);
+    uint32_t it = 0;  // K-steps issued by this CTA, across items
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      Item itm;
+      if (!get_item<BM>(a, w, nslices, nsh, P, itm)) {
+        if (lane == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
+        continue;
       }
-      if (GATEUP) {
-        for (int q = lane; q < N / 4; q += 32)
-          tma_gather4(smem_u32(st + q * 512), &tm_b, kk * 64, rowtok[4 * q], rowtok[4 * q + 1],
-                      rowtok[4 * q + 2], rowtok[4 * q + 3], fb);
+      const int N = (itm.rows + 15) & ~15;
+      const int wrow = itm.expert * NOUT + itm.slice * 128;
+      // gather rows of this item (gate/up): lane owns gathers q = lane, lane + 32
+      int tok[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int n = 4 * (lane + 32 * (j >> 2)) + (j & 3);
+        tok[j] = GATEUP ? row_token(a, itm.row0 + min(n, itm.rows - 1), P) : 0;
       }
-      __syncwarp();
-      issued = kk + 1;
+      const uint32_t tx_bytes = MATS * kPackedBytes + (GATEUP ? N * 128 : BBYTES);
+      for (int kk = 0; kk < G; ++kk, ++it) {
+        const int s = it % nstages;
+        if (it >= (uint32_t)nstages &&
+            !warp_wait(smem_u32(&empty[s]), ((it / nstages) + 1) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&full[s]);
+        uint8_t* st = stage_base + (size_t)s * STAGE;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, tx_bytes);
+          tma_load_2d(smem_u32(st + BBYTES), &tm_q0, kk * 32, wrow, fb);
+          if (GATEUP) tma_load_2d(smem_u32(st + BBYTES + kPackedBytes), &tm_q1, kk * 32, wrow, fb);
+          if (!GATEUP) tma_load_2d(smem_u32(st), &tm_b, kk * 64, itm.row0, fb);
+        }
+        if (GATEUP) {
+          if (lane < N / 4)
+            tma_gather4(smem_u32(st + lane * 512), &tm_b, kk * 64, tok[0], tok[1], tok[2], tok[3], fb);
+          if (lane + 32 < N / 4)
+            tma_gather4(smem_u32(st + (lane + 32) * 512), &tm_b, kk * 64, tok[4], tok[5], tok[6],
+                        tok[7], fb);
+        }
+        __syncwarp();
+      }
     }
     if (*abort && lane == 0) {  // let copies still in flight land before exit
       int never = 0;
-      for (int kk = (issued > nstages ? issued - nstages : 0); kk < issued; ++kk)
-        mbar_wait(smem_u32(&full[kk % nstages]), (kk / nstages) & 1, &never, a.status);
+      for (uint32_t k2 = (it > (uint32_t)nstages ? it - nstages : 0); k2 < it; ++k2)
+        mbar_wait(smem_u32(&full[k2 % nstages]), (k2 / nstages) & 1, &never, a.status);
     }
   } else if (warp == 1) {
     // ================================================= MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(128, N);
-      for (int kk = 0; kk < G; ++kk) {
-        const int s = kk % nstages, b = kk & 1;
-        if (!mbar_wait(smem_u32(&afull[b]), (kk >> 1) & 1, abort, a.status)) break;
-        if (!mbar_wait(smem_u32(&full[s]), (kk / nstages) & 1, abort, a.status)) break;
+      uint32_t it = 0, titem = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        Item itm;
+        if (!get_item<BM>(a, w, nslices, nsh, P, itm)) continue;
+        const int N = (itm.rows + 15) & ~15;
+        const uint32_t idesc = idesc_f16_f32(128, N);
+        const int ab = titem % NACC;
+        if (titem >= (uint32_t)NACC &&
+            !mbar_wait(smem_u32(&accempty[ab]), ((titem / NACC) + 1) & 1, abort, a.status))
+          break;
         tc_fence_after();
-        const uint32_t bsm = smem_u32(stage_base + (size_t)s * STAGE);
+        const uint32_t dacc = tmem + ab * L::kAccCols;
+        for (int kk = 0; kk < G; ++kk, ++it) {
+          const int s = it % nstages, b = it & 1;
+          if (!mbar_wait(smem_u32(&afull[b]), (it >> 1) & 1, abort, a.status) ||
+              !mbar_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t bsm = smem_u32(stage_base + (size_t)s * STAGE);
 #pragma unroll
-        for (int m = 0; m < MATS; ++m) {
-          const uint32_t asm_ = smem_u32(a_base + (size_t)(b * MATS + m) * kABytes);
+          for (int m = 0; m < MATS; ++m) {
+            const uint32_t asm_ = smem_u32(a_base + (size_t)(b * MATS + m) * kABytes);
 #pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16)
-            mma_f16(tmem + m * BM, sdesc_sw128(asm_ + k16 * 32), sdesc_sw128(bsm + k16 * 32),
-                     idesc, (kk | k16) != 0);
+            for (int k16 = 0; k16 < 4; ++k16)
+              mma_f16(dacc + m * BM, sdesc_sw128(asm_ + k16 * 32), sdesc_sw128(bsm + k16 * 32),
+                      idesc, (kk | k16) != 0);
+          }
+          mma_commit(smem_u32(&empty[s]));
+          mma_commit(smem_u32(&aempty[b]));
         }
-        mma_commit(smem_u32(&empty[s]));
-        mma_commit(smem_u32(&aempty[b]));
+        if (!ok) break;
+        mma_commit(smem_u32(&accfull[ab]));
+        ++titem;
       }
-      mma_commit(smem_u32(accfull));  // also drains MMAs issued before an abort
+      mma_commit(smem_u32(drain));  // arrives once every MMA above has finished
     }
     __syncwarp();
-  } else {
-    // ================================================= dequant, then epilogue
+  } else if (warp < kEpiWarp0) {
+    // ================================================= dequant
     const int i = threadIdx.x - 64;
     int mat, r, c0, nch;
     if (GATEUP) { mat = i >> 7; r = i & 127; c0 = 0; nch = 8; }
     else        { mat = 0;      r = i >> 1;  c0 = (i & 1) * 4; nch = 4; }
     const uint32_t swz = (uint32_t)(r & 7);
-    for (int kk = 0; kk < G; ++kk) {
-      const int s = kk % nstages, b = kk & 1;
-      bool ok = warp_wait(smem_u32(&full[s]), (kk / nstages) & 1, abort, a.status);
-      if (ok && kk >= 2) ok = warp_wait(smem_u32(&aempty[b]), ((kk >> 1) + 1) & 1, abort, a.status);
-      if (!ok) break;
-      const uint8_t* pk =
-          stage_base + (size_t)s * STAGE + BBYTES + mat * kPackedBytes + r * 32 + c0 * 4;
-      const uint32_t sbv = sb[(mat * G + kk) * 128 + r];
-      const uint32_t s2 = prmt(sbv, sbv, 0x1010u), b2 = prmt(sbv, sbv, 0x3232u);
-      const uint32_t arow = smem_u32(a_base + (size_t)(b * MATS + mat) * kABytes) + r * 128;
-      for (int c = 0; c < nch; c += 4) {
-        const uint4 wv = *reinterpret_cast<const uint4*>(pk + c * 4);
-        const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t o[4];
-          dequant8(wd[j], s2, b2, o);
-          const uint32_t chunk = (uint32_t)(c0 + c + j);
-          st_shared_v4(arow + ((chunk ^ swz) << 4), o[0], o[1], o[2], o[3]);
+    uint32_t it = 0, j = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      Item itm;
+      if (!get_item<BM>(a, w, nslices, nsh, P, itm)) continue;
+      const int slot = j % nsb;
+      if (!warp_wait(smem_u32(&sbfull[slot]), (j / nsb) & 1, abort, a.status)) break;
+      const uint32_t* sbs = sb + slot * sb_words;
+      for (int kk = 0; kk < G; ++kk, ++it) {
+        const int s = it % nstages, b = it & 1;
+        bool got = warp_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status);
+        if (got && it >= 2) got = warp_wait(smem_u32(&aempty[b]), ((it >> 1) + 1) & 1, abort, a.status);
+        if (!got) {
+          ok = false;
+          break;
         }
+        const uint8_t* pk =
+            stage_base + (size_t)s * STAGE + BBYTES + mat * kPackedBytes + r * 32 + c0 * 4;
+        const uint32_t sbv = sbs[(mat * G + kk) * 128 + r];
+        const uint32_t s2 = prmt(sbv, sbv, 0x1010u), b2 = prmt(sbv, sbv, 0x3232u);
+        const uint32_t arow = smem_u32(a_base + (size_t)(b * MATS + mat) * kABytes) + r * 128;
+        for (int c = 0; c < nch; c += 4) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(pk + c * 4);
+          const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint32_t o[4];
+            dequant8(wd[jj], s2, b2, o);
+            const uint32_t chunk = (uint32_t)(c0 + c + jj);
+            st_shared_v4(arow + ((chunk ^ swz) << 4), o[0], o[1], o[2], o[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&afull[b]));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&afull[b]));
+      if (!ok) break;
+      mbar_arrive(smem_u32(&sbempty[slot]));
+      ++j;
     }
+  } else {
+    // ================================================= epilogue
+    // Per item j: (1) fill the scale table of item j+1 for the dequant warps,
+    // (2) for short items (down), start loading item j+2's table into
+    // registers, (3) drain item j's accumulators to global memory.
+    const int q = warp & 3;  // TMEM lane quadrant of this warp
+    const int r = threadIdx.x - 32 * kEpiWarp0;
+    uint16_t* sbh = reinterpret_cast<uint16_t*>(sb);
+    auto slot_ptr = [&](int slot) { return sbh + (size_t)slot * sb_words * 2; };
+    auto row_of = [&](const Item& it) {
+      return (size_t)it.expert * NOUT + (size_t)it.slice * 128 + r;
+    };
+    const int nq = (G & 7) == 0 ? MATS * 2 * (G / 8) : 1 << 30;
+    const bool lookahead = !GATEUP && nq <= 4;
+    uint4 la[4];
+    int w = blockIdx.x;
+    Item cur, nxt, nn;
+    bool have = next_item<BM>(a, w, n_items, nslices, nsh, P, cur);
+    if (have) {
+      scale_fill<MATS>(a, row_of(cur), G, r, slot_ptr(0));
+      mbar_arrive(smem_u32(&sbfull[0]));
+    }
+    int wn = w + gridDim.x;
+    bool have_next = have && next_item<BM>(a, wn, n_items, nslices, nsh, P, nxt);
+    if (lookahead && have_next) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (c < nq) la[c] = scale_chunk_load(a, row_of(nxt), G, c);
+    }
+    uint32_t j = 0;
+    while (have) {
+      if (have_next) {
+        const uint32_t jn = j + 1;
+        const int slot = jn % nsb;
+        if (jn >= (uint32_t)nsb &&
+            !warp_wait(smem_u32(&sbempty[slot]), ((jn / nsb) + 1) & 1, abort, a.status))
+          break;
+        if (lookahead) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (c < nq) scale_chunk_store(slot_ptr(slot), G, c, r, la[c]);
+        } else {
+          scale_fill<MATS>(a, row_of(nxt), G, r, slot_ptr(slot));
+        }
+        mbar_arrive(smem_u32(&sbfull[slot]));
+      }
+      int wnn = wn + gridDim.x;
+      const bool have_nn = have_next && next_item<BM>(a, wnn, n_items, nslices, nsh, P, nn);
+      if (lookahead && have_nn) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (c < nq) la[c] = scale_chunk_load(a, row_of(nn), G, c);
+      }
 
-    // ---- epilogue: TMEM -> registers -> global
-    const bool ok = warp_wait(smem_u32(accfull), 0, abort, a.status) && (*abort == 0);
-    if (ok) {
+      const int N = (cur.rows + 15) & ~15;
+      const int ab = j % NACC;
+      if (!warp_wait(smem_u32(&accfull[ab]), (j / NACC) & 1, abort, a.status)) break;
       tc_fence_after();
-      const int q = warp & 3;            // TMEM lane quadrant of this warp
-      const int set = (warp - 2) >> 2;   // two warp sets split the columns
-      const int feat = slice * 128 + q * 32 + lane;
-      const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16);
-      for (int cb = set * 32; cb < N; cb += 64) {
+      const int feat = cur.slice * 128 + q * 32 + lane;
+      const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + ab * L::kAccCols;
+      for (int cb = 0; cb < N; cb += 32) {
+        const bool last = cb + 32 >= N;
         if (GATEUP) {
           uint32_t gr[32], ur[32];
-          tmem_ld32(tlane + cb, gr);
-          tmem_ld32(tlane + BM + cb, ur);
+          tmem_ld32(tl + cb, gr);
+          tmem_ld32(tl + BM + cb, ur);
           tmem_ld_wait();
+          if (last) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(&accempty[ab]));
+          }
           __half* H = static_cast<__half*>(a.H);
           bool range_ok = true;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int n = cb + j;
-            if (n < rows) {
-              const float gv = __uint_as_float(gr[j]), uv = __uint_as_float(ur[j]);
+          for (int jj = 0; jj < 32; ++jj) {
+            const int n = cb + jj;
+            if (n < cur.rows) {
+              const float gv = __uint_as_float(gr[jj]), uv = __uint_as_float(ur[jj]);
               const float h = gv / (1.f + __expf(-gv)) * uv;
               range_ok &= fabsf(h) <= 65504.f;
-              H[(size_t)(row0 + n) * a.F + feat] = __float2half_rn(h);
+              H[(size_t)(cur.row0 + n) * a.F + feat] = __float2half_rn(h);
             }
           }
           if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
         } else {
           uint32_t orr[32];
-          tmem_ld32(tlane + cb, orr);
+          tmem_ld32(tl + cb, orr);
           tmem_ld_wait();
+          if (last) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(&accempty[ab]));
+          }
+          // lane jj looks up row cb + jj: its token and its gate weight
+          const int rj = cur.row0 + min(cb + lane, cur.rows - 1);
+          int tokj;
+          float gj;
+          if (cur.shared) {
+            tokj = rj - P;
+            gj = 1.f;
+          } else {
+            const int p = __ldg(a.perm + rj);
+            tokj = p / a.k;
+            gj = __ldg(a.gates + p);
+          }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int n = cb + j;
-            if (n < rows)
-              red_add_f32(a.yacc + (size_t)rowtok[n] * a.d + feat, rowgate[n] * __uint_as_float(orr[j]));
+          for (int jj = 0; jj < 32; ++jj) {
+            const int tj = __shfl_sync(0xffffffffu, tokj, jj);
+            const float g = __shfl_sync(0xffffffffu, gj, jj);
+            if (cb + jj < cur.rows)
+              red_add_f32(a.yacc + (size_t)tj * a.d + feat, g * __uint_as_float(orr[jj]));
           }
         }
       }
+      cur = nxt;
+      have = have_next;
+      nxt = nn;
+      wn = wnn;
+      have_next = have_nn;
+      ++j;
     }
   }
 
   // ---- teardown: every MMA has finished before TMEM is released
   if (warp == 1 && lane == 0) {
     int never = 0;
-    mbar_wait(smem_u32(accfull), 0, &never, a.status);
+    mbar_wait(smem_u32(drain), 0, &never, a.status);
   }
   tc_fence_before();
   __syncthreads();
@@ -369,7 +580,8 @@ static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, cons
                                   const CUtensorMap& b, cudaStream_t s) {
   const int K = GATEUP ? a.d : a.F;
   const int NOUT = GATEUP ? a.F : a.d;
-  const int nstages = gemm_stages(GATEUP, BM, K);
+  int nstages = 0, nsb = 0;
+  gemm_config(GATEUP, BM, K, &nstages, &nsb);
   if (nstages < 2) return cudaErrorInvalidValue;
   const size_t smem = gemm_smem_bytes(GATEUP, BM, K);
   auto kern = w4_gemm_kernel<GATEUP, BM>;
@@ -378,9 +590,17 @@ static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, cons
   const int P = a.T * a.k;
   const int cap = (P + BM - 1) / BM + (a.E < P ? a.E : P);
   const int nsh = (a.T + BM - 1) / BM;
-  const int grid = (nsh + cap) * (NOUT / 128);
+  const int max_items = (nsh + cap) * (NOUT / 128);
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      num_sms = 148;
+  }
+  const int grid = max_items < num_sms ? max_items : num_sms;  // persistent: one CTA per SM
   prof_begin(GATEUP ? K_GATEUP : K_DOWN, s);
-  kern<<<grid, kGemmThreads, smem, s>>>(q0, q1, b, a, nstages);
+  kern<<<grid, kGemmThreads, smem, s>>>(q0, q1, b, a, nstages, nsb);
   prof_end(GATEUP ? K_GATEUP : K_DOWN, s);
   return cudaGetLastError();
 }
