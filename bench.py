@@ -293,7 +293,7 @@ def run_lily(args, world, rank, local):
         raise RuntimeError(f"device status bits set: {status}")
 
     # end to end through the host-buffer entry point (pinned host x and y)
-    e2e_steps = max(3, min(args.steps, 200))
+    e2e_steps = 3 if args.no_e2e else max(3, min(args.steps, 200))
     xh = [layers[l][0].cpu().pin_memory() for l in range(nl)]
     yh = torch.empty(T, d, dtype=y.dtype).pin_memory()
     xd = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
@@ -397,6 +397,7 @@ def main():
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_info()

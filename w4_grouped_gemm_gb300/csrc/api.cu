@@ -60,7 +60,7 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t ctrl, hist, x16, H, acc, total;
+  size_t ctrl, hist, x16, w3, part, H, acc, total;
 };
 
 // ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
@@ -73,6 +73,9 @@ Layout layout(const lily_moe_dims& d) {
   L.ctrl = off; off += up(256);
   L.hist = off; off += up(nblk * E * 4);
   L.x16 = off;  off += up(T * D * 2);
+  const bool tc_router = d.T > 8;  // tensor-core router: split W + split-K partials
+  L.w3 = off;   off += tc_router ? up(3 * E * D * 2) : 0;
+  L.part = off; off += tc_router ? up((size_t)router_splits(d.T, d.d_model) * T * E * 4) : 0;
   L.H = off;    off += up((P + T) * F * 2);
   L.acc = off;
   size_t acc = T * D * 4;                         // prefill: fp32 y accumulator
@@ -138,15 +141,27 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
              const lily_moe_weights* w, const lily_moe_routing& r, void* ws, cudaStream_t s) {
   const Layout L = layout(d);
   uint8_t* base = static_cast<uint8_t*>(ws);
-  const float* src = logits_in;
-  if (!src) {
-    cudaError_t e = launch_router_logits(x, w->router_w, w->router_bias, r.logits, d.T, d.d_model,
-                                         d.n_experts, base + L.x16, ws_status(ws), s);
-    if (e != cudaSuccess) return LILY_ERR_CUDA;
-    src = r.logits;
-  }
   RouteArgs a;
-  a.logits_src = src;
+  a.logits_src = logits_in;
+  a.partial = nullptr;
+  a.nsplit = 0;
+  a.bias = nullptr;
+  if (!logits_in) {
+    if (d.T > 8) {
+      float* part = reinterpret_cast<float*>(base + L.part);
+      cudaError_t e = launch_router_tc(x, w->router_w, d.T, d.d_model, d.n_experts, base + L.w3,
+                                       part, base + L.x16, ws_status(ws), s);
+      if (e != cudaSuccess) return LILY_ERR_CUDA;
+      a.partial = part;
+      a.nsplit = router_splits(d.T, d.d_model);
+      a.bias = w->router_bias;
+    } else {
+      cudaError_t e = launch_router_logits(x, w->router_w, w->router_bias, r.logits, d.T,
+                                           d.d_model, d.n_experts, base + L.x16, ws_status(ws), s);
+      if (e != cudaSuccess) return LILY_ERR_CUDA;
+      a.logits_src = r.logits;
+    }
+  }
   a.logits_dst = r.logits;
   a.T = d.T;
   a.E = d.n_experts;
@@ -507,7 +522,8 @@ int lily_moe_profile_read(double* total_ms, int64_t* launches) {
 const char* lily_moe_kernel_name(int kind) {
   static const char* names[] = {"router_gemm", "router_gemv", "route", "gateup_gemm",
                                 "down_gemm",   "finalize",    "dec_gateup", "dec_down",
-                                "dec_combine", "rmsnorm",     "stack_boundary", "memset_acc"};
+                                "dec_combine", "rmsnorm",     "stack_boundary", "memset_acc",
+                                "router_prep"};
   if (kind < 0 || kind >= (int)(sizeof(names) / sizeof(names[0]))) return "unused";
   return names[kind];
 }

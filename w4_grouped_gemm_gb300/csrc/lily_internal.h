@@ -24,7 +24,8 @@ enum KernelKind : int {
   K_RMSNORM = 9,
   K_STACK_BOUNDARY = 10,
   K_MEMSET = 11,
-  K_NUM = 12
+  K_ROUTER_PREP = 12,
+  K_NUM = 13
 };
 
 // Profiling hooks (api.cu): bracket one launch with events when enabled.
@@ -37,7 +38,10 @@ constexpr int kRouteThreads = 256;
 
 // ---------------------------------------------------------------- routing
 struct RouteArgs {
-  const float* logits_src;  // fp32 [T][E]
+  const float* logits_src;  // fp32 [T][E], or NULL when partial is used
+  const float* partial;     // fp32 [nsplit][T][E] split-K router partials (or NULL)
+  int nsplit;
+  const float* bias;        // fp32 [E] added to summed partials (or NULL)
   float* logits_dst;        // fp32 [T][E] (may equal logits_src)
   int T, E, k, BM, cap;
   int32_t* ids;
@@ -52,10 +56,18 @@ struct RouteArgs {
   uint32_t* bar;       // workspace: grid barrier {count, generation}
   uint32_t* status;    // workspace status word
 };
-// Also writes x16 (fp16 copy of x, for the grouped GEMM) when x16 != NULL.
+// T <= 8 only.  Also writes x16 (fp16 copy of x, for the grouped GEMM) when
+// x16 != NULL.
 cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
                                  int T, int d, int E, void* x16, uint32_t* status,
                                  cudaStream_t s);
+// Router on tensor cores for larger T: W split exactly into three bf16 terms
+// (w_split, [3][E][d]), fp32 partial logits per K-split into partial
+// ([router_splits(T,d)][T][E]); x16 written as above.
+int router_splits(int T, int d);
+size_t router_tc_smem(int E);
+cudaError_t launch_router_tc(const void* x, const float* w, int T, int d, int E, void* w_split,
+                             float* partial, void* x16, uint32_t* status, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 int route_max_blocks();  // co-resident blocks of the routing kernel (0 = unknown)
 

@@ -9,15 +9,17 @@
 // GPU-resident": histogram, prefix scan, scatter and block map stay on the GPU;
 // section "Model structure and three workload shapes": a router scores 256
 // experts and picks eight).
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace lily {
 
 // ============================================================== router logits
 // logits[t][e] = sum_i x[t][i] * W[e][i] (+ b[e]), fp32 accumulation.
-// Both kernels also write x16, the fp16 copy of x that the grouped GEMM's
-// tensor-core operand uses (exact for |x| in [2^-17, 65504]; larger values
-// set LILY_STATUS_F16_RANGE).
+// The router kernels also write x16, the fp16 copy of x that the grouped
+// GEMM's tensor-core operand uses (exact for |x| in [2^-17, 65504]; larger
+// values set LILY_STATUS_F16_RANGE).
 
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v, bool& ok) {
   const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
@@ -26,7 +28,7 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v, bool& ok) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Small T (decode): one warp per expert row, all tokens at once.
+// Small T (decode, T <= 8): one warp per expert row, all tokens at once.
 constexpr int kGemvMaxT = 8;
 __global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* __restrict__ x,
                                                           const float* __restrict__ w,
@@ -71,97 +73,224 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* _
   }
 }
 
-// Larger T: 64 tokens x 64 experts per block, 4x4 outputs per thread.
-constexpr int RG_BT = 64, RG_BE = 64, RG_BK = 32;
-__global__ void __launch_bounds__(256) router_gemm_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          const float* __restrict__ w,
-                                                          const float* __restrict__ b,
-                                                          float* __restrict__ logits, int T,
-                                                          int d, int E, uint32_t* __restrict__ x16,
-                                                          uint32_t* status) {
-  bool range_ok = true;
-  __shared__ float xs[RG_BK][RG_BT + 4];
-  __shared__ float ws[RG_BK][RG_BE + 4];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int t0 = blockIdx.x * RG_BT, e0 = blockIdx.y * RG_BE;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < d; k0 += RG_BK) {
-    {  // x tile: 64 tokens x 32 k, 8 bf16 per thread
-      int row = threadIdx.x >> 2, kc = (threadIdx.x & 3) * 8;
-      int t = t0 + row;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < T) v = *reinterpret_cast<const uint4*>(x + (size_t)t * d + k0 + kc);
-      if (t < T && blockIdx.y == 0 && x16) {
-        uint4 hv;
-        hv.x = bf2_to_h2(v.x, range_ok);
-        hv.y = bf2_to_h2(v.y, range_ok);
-        hv.z = bf2_to_h2(v.z, range_ok);
-        hv.w = bf2_to_h2(v.w, range_ok);
-        *reinterpret_cast<uint4*>(x16 + ((size_t)t * d + k0 + kc) / 2) = hv;
-      }
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float2 f = __bfloat1622float2(h[j]);
-        xs[kc + 2 * j][row] = f.x;
-        xs[kc + 2 * j + 1][row] = f.y;
-      }
-    }
-    {  // w tile: 64 experts x 32 k, 8 floats per thread
-      int row = threadIdx.x >> 2, kc = (threadIdx.x & 3) * 8;
-      int e = e0 + row;
-      float4 v0 = make_float4(0, 0, 0, 0), v1 = v0;
-      if (e < E) {
-        const float4* p = reinterpret_cast<const float4*>(w + (size_t)e * d + k0 + kc);
-        v0 = __ldg(p);
-        v1 = __ldg(p + 1);
-      }
-      ws[kc + 0][row] = v0.x; ws[kc + 1][row] = v0.y; ws[kc + 2][row] = v0.z; ws[kc + 3][row] = v0.w;
-      ws[kc + 4][row] = v1.x; ws[kc + 5][row] = v1.y; ws[kc + 6][row] = v1.z; ws[kc + 7][row] = v1.w;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < RG_BK; ++kk) {
-      float a[4], c[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = xs[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) c[j] = ws[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], c[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-  if (!range_ok) set_status(status, LILY_STATUS_F16_RANGE);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      int e = e0 + tx * 4 + j;
-      if (e < E) logits[(size_t)t * E + e] = acc[i][j] + (b ? b[e] : 0.f);
-    }
-  }
-}
-
 cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
                                  int T, int d, int E, void* x16, uint32_t* status,
                                  cudaStream_t s) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   uint32_t* x16w = static_cast<uint32_t*>(x16);
-  if (T <= kGemvMaxT) {
-    prof_begin(K_ROUTER_GEMV, s);
-    router_gemv_kernel<<<(E + 7) / 8, 256, 0, s>>>(xb, w, b, logits, T, d, E, x16w, status);
-    prof_end(K_ROUTER_GEMV, s);
-  } else {
-    prof_begin(K_ROUTER_GEMM, s);
-    dim3 grid((T + RG_BT - 1) / RG_BT, (E + RG_BE - 1) / RG_BE);
-    router_gemm_kernel<<<grid, 256, 0, s>>>(xb, w, b, logits, T, d, E, x16w, status);
-    prof_end(K_ROUTER_GEMM, s);
+  if (T > kGemvMaxT) return cudaErrorInvalidValue;  // larger T: launch_router_tc
+  prof_begin(K_ROUTER_GEMV, s);
+  router_gemv_kernel<<<(E + 7) / 8, 256, 0, s>>>(xb, w, b, logits, T, d, E, x16w, status);
+  prof_end(K_ROUTER_GEMV, s);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- tensor cores
+// logits = x * W^T with x (bf16, exact) and W = W_hi + W_mid + W_lo, three
+// bf16 terms that together hold every bit of the fp32 W.  Each bf16 x bf16
+// product is exact in fp32, so the tensor cores give fp32-accumulated logits
+// of the fp32 weights.  Tokens are the M = 128 operand, experts the N operand;
+// the K loop runs over (term, 64-wide block) pairs and is split across CTAs,
+// each writing fp32 partial logits that the routing kernel sums in order.
+
+__global__ void __launch_bounds__(256) router_prep_kernel(const float* __restrict__ w,
+                                                          __nv_bfloat16* __restrict__ w3,
+                                                          int64_t n_w,
+                                                          const uint32_t* __restrict__ x,
+                                                          uint32_t* __restrict__ x16,
+                                                          int64_t n_x2, uint32_t* status) {
+  bool ok = true;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_w; i += stride) {
+    const float v = w[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    w3[i] = hi;
+    w3[n_w + i] = mid;
+    w3[2 * n_w + i] = __float2bfloat16_rn(r2);
   }
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_x2; i += stride)
+    x16[i] = bf2_to_h2(x[i], ok);
+  if (!ok) set_status(status, LILY_STATUS_F16_RANGE);
+}
+
+constexpr int kRtThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kRtStages = 4;
+constexpr int kRtMaxSplits = 8;
+
+int router_splits(int T, int d) {
+  const int mt = (T + 127) / 128;
+  const int ks = 3 * (d / 64);
+  int S = (128 + mt - 1) / mt;
+  if (S > kRtMaxSplits) S = kRtMaxSplits;
+  if (S > ks / 2) S = ks / 2;
+  return S < 1 ? 1 : S;
+}
+
+static int router_ne(int E) { return (E + 15) & ~15; }
+
+size_t router_tc_smem(int E) {
+  return 1024 + (size_t)kRtStages * (128 * 128 + router_ne(E) * 128) + 16 * 8 + 16;
+}
+
+__global__ void __launch_bounds__(kRtThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                     int T, int d, int E, int NE, float* __restrict__ partial, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int ABYTES = 128 * 128, STAGE = ABYTES + NE * 128;
+  uint64_t* full = (uint64_t*)(smem + kRtStages * STAGE);
+  uint64_t* empty = full + kRtStages;
+  uint64_t* accfull = empty + kRtStages;
+  int* misc = (int*)(accfull + 1);
+  volatile int* abort = misc;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * 128, split = blockIdx.y, S = gridDim.y;
+  const int KB = d / 64, KS = 3 * KB;
+  const int ks0 = split * KS / S, nk = (split + 1) * KS / S - ks0;
+  uint32_t tcols = 32;
+  while ((int)tcols < NE) tcols <<= 1;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRtStages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    mbar_init(smem_u32(accfull), 1);
+    misc[0] = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_w);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&misc[1]), tcols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = (uint32_t)misc[1];
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int i = 0;
+      for (; i < nk; ++i) {
+        const int st = i % kRtStages;
+        if (i >= kRtStages &&
+            !mbar_wait(smem_u32(&empty[st]), ((i / kRtStages) + 1) & 1, abort, status))
+          break;
+        const int ks = ks0 + i, term = ks / KB, kb = ks % KB;
+        const uint32_t fb = smem_u32(&full[st]);
+        uint8_t* sp = smem + (size_t)st * STAGE;
+        mbar_arrive_expect_tx(fb, (uint32_t)STAGE);
+        tma_load_2d(smem_u32(sp), &tm_x, kb * 64, m0, fb);
+        tma_load_2d(smem_u32(sp + ABYTES), &tm_w, kb * 64, term * E, fb);
+      }
+      if (*abort) {  // let copies still in flight land before exit
+        int never = 0;
+        for (int k2 = (i > kRtStages ? i - kRtStages : 0); k2 < i; ++k2)
+          mbar_wait(smem_u32(&full[k2 % kRtStages]), (k2 / kRtStages) & 1, &never, status);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, NE);
+      for (int i = 0; i < nk; ++i) {
+        const int st = i % kRtStages;
+        if (!mbar_wait(smem_u32(&full[st]), (i / kRtStages) & 1, abort, status)) break;
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(smem + (size_t)st * STAGE), b0 = a0 + ABYTES;
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16)
+          mma_f16(tmem, sdesc_sw128(a0 + k16 * 32), sdesc_sw128(b0 + k16 * 32), idesc,
+                  (i | k16) != 0);
+        mma_commit(smem_u32(&empty[st]));
+      }
+      mma_commit(smem_u32(accfull));
+    }
+    __syncwarp();
+  } else {
+    int okv = 1;
+    if (lane == 0) okv = mbar_wait(smem_u32(accfull), 0, abort, status) && !*abort;
+    okv = __shfl_sync(0xffffffffu, okv, 0);
+    if (okv) {
+      tc_fence_after();
+      const int q = warp & 3;
+      const int t = m0 + q * 32 + lane;
+      float* dst = partial + ((size_t)split * T + t) * E;
+      for (int cb = 0; cb < NE; cb += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + cb, v);
+        tmem_ld_wait();
+        if (t < T) {
+          if ((E & 3) == 0 && cb + 32 <= E) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(dst + cb + j) =
+                  make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                              __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (cb + j < E) dst[cb + j] = __uint_as_float(v[j]);
+          }
+        }
+      }
+    }
+  }
+
+  if (warp == 1 && lane == 0) {
+    int never = 0;
+    mbar_wait(smem_u32(accfull), 0, &never, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tcols);
+  }
+}
+
+cudaError_t launch_router_tc(const void* x, const float* w, int T, int d, int E, void* w_split,
+                             float* partial, void* x16, uint32_t* status, cudaStream_t s) {
+  const int NE = router_ne(E);
+  CUtensorMap tm_x, tm_w;
+  {
+    uint64_t dims[2] = {(uint64_t)d, (uint64_t)T};
+    uint64_t strides[1] = {(uint64_t)d * 2};
+    uint32_t box[2] = {64, 128};
+    if (encode_tiled(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)x, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    uint64_t dims[2] = {(uint64_t)d, (uint64_t)3 * E};
+    uint64_t strides[1] = {(uint64_t)d * 2};
+    uint32_t box[2] = {64, (uint32_t)NE};
+    if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_split, dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const int64_t n_w = (int64_t)E * d, n_x2 = (int64_t)T * d / 2;
+  int pblocks = (int)((std::max(n_w, n_x2) + 255) / 256);
+  if (pblocks > 152 * 8) pblocks = 152 * 8;
+  prof_begin(K_ROUTER_PREP, s);
+  router_prep_kernel<<<pblocks, 256, 0, s>>>(w, static_cast<__nv_bfloat16*>(w_split), n_w,
+                                             static_cast<const uint32_t*>(x),
+                                             static_cast<uint32_t*>(x16), n_x2, status);
+  prof_end(K_ROUTER_PREP, s);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t smem = router_tc_smem(E);
+  err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  dim3 grid((T + 127) / 128, router_splits(T, d));
+  prof_begin(K_ROUTER_GEMM, s);
+  router_tc_kernel<<<grid, kRtThreads, smem, s>>>(tm_x, tm_w, T, d, E, NE, partial, status);
+  prof_end(K_ROUTER_GEMM, s);
   return cudaGetLastError();
 }
 
@@ -236,7 +365,7 @@ __device__ void grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* status) 
 
 constexpr int kMaxE = 256, kMaxK = 8;
 
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
+__global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
   __shared__ int s_ids[kRouteTok * kMaxK];
   __shared__ int s_rank[kRouteTok * kMaxK];
   __shared__ int s_cnt[kMaxE];
@@ -252,8 +381,48 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
   const int npair = ntok * k;
 
   // ---- phase 1: top-k + gates, one warp per token (4 tokens per warp)
-  for (int i = 0; i < kRouteTok / 8; ++i) {
-    const int tl = warp * (kRouteTok / 8) + i;
+  constexpr int kWarpTok = kRouteTok / 8;
+  // logits of this warp's tokens, lane holding experts lane + 32c; with a
+  // split-K router the partials are summed here in split order (all loads
+  // of one split issued together)
+  float lv[kWarpTok][kMaxE / 32];
+#pragma unroll
+  for (int i = 0; i < kWarpTok; ++i)
+#pragma unroll
+    for (int c = 0; c < kMaxE / 32; ++c) lv[i][c] = 0.f;
+  if (a.partial) {
+    for (int sp = 0; sp < a.nsplit; ++sp) {
+#pragma unroll
+      for (int i = 0; i < kWarpTok; ++i) {
+        const int tl = warp * kWarpTok + i;
+        const float* pp = a.partial + ((size_t)sp * T + t0 + tl) * E;
+#pragma unroll
+        for (int c = 0; c < kMaxE / 32; ++c)
+          if (tl < ntok && lane + 32 * c < E) lv[i][c] += __ldcg(pp + lane + 32 * c);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kWarpTok; ++i) {
+    const int tl = warp * kWarpTok + i;
+    if (tl >= ntok) continue;
+#pragma unroll
+    for (int c = 0; c < kMaxE / 32; ++c) {
+      const int e = lane + 32 * c;
+      if (e >= E) continue;
+      const size_t idx = (size_t)(t0 + tl) * E + e;
+      if (a.partial) {
+        if (a.bias) lv[i][c] += a.bias[e];
+        a.logits_dst[idx] = lv[i][c];
+      } else {
+        lv[i][c] = a.logits_src[idx];
+        if (a.logits_dst != a.logits_src) a.logits_dst[idx] = lv[i][c];
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kWarpTok; ++i) {
+    const int tl = warp * kWarpTok + i;
     if (tl >= ntok) break;
     const int t = t0 + tl;
     uint32_t key[kMaxE / 32];
@@ -264,8 +433,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteArgs a) {
       const int e = lane + 32 * c;
       key[c] = 0;
       if (e < E) {
-        float v = a.logits_src[(size_t)t * E + e];
-        if (a.logits_dst != a.logits_src) a.logits_dst[(size_t)t * E + e] = v;
+        const float v = lv[i][c];
         saw_nan |= (v != v);
         key[c] = logit_key(v);
         avail |= 1u << c;
