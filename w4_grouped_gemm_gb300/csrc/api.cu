@@ -143,18 +143,14 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
   uint8_t* base = static_cast<uint8_t*>(ws);
   RouteArgs a;
   a.logits_src = logits_in;
-  a.partial = nullptr;
-  a.nsplit = 0;
-  a.bias = nullptr;
   if (!logits_in) {
     if (d.T > 8) {
       float* part = reinterpret_cast<float*>(base + L.part);
-      cudaError_t e = launch_router_tc(x, w->router_w, d.T, d.d_model, d.n_experts, base + L.w3,
-                                       part, base + L.x16, ws_status(ws), s);
+      cudaError_t e = launch_router_tc(x, w->router_w, w->router_bias, d.T, d.d_model,
+                                       d.n_experts, base + L.w3, part, r.logits, base + L.x16,
+                                       ws_status(ws), s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
-      a.partial = part;
-      a.nsplit = router_splits(d.T, d.d_model);
-      a.bias = w->router_bias;
+      a.logits_src = r.logits;
     } else {
       cudaError_t e = launch_router_logits(x, w->router_w, w->router_bias, r.logits, d.T,
                                            d.d_model, d.n_experts, base + L.x16, ws_status(ws), s);
@@ -523,7 +519,7 @@ const char* lily_moe_kernel_name(int kind) {
   static const char* names[] = {"router_gemm", "router_gemv", "route", "gateup_gemm",
                                 "down_gemm",   "finalize",    "dec_gateup", "dec_down",
                                 "dec_combine", "rmsnorm",     "stack_boundary", "memset_acc",
-                                "router_prep"};
+                                "router_prep", "router_reduce"};
   if (kind < 0 || kind >= (int)(sizeof(names) / sizeof(names[0]))) return "unused";
   return names[kind];
 }

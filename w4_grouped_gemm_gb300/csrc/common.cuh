@@ -51,24 +51,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity.  Gives up after
+// try_wait that may suspend the thread in hardware for up to hint_ns while
+// the phase is incomplete (no issue slots spent spinning).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  The waiting thread
+// sleeps in try_wait (up to 100 us per attempt); the wait gives up after
 // kWaitLimitNs of wall time, or early when *abort is set by another role of
 // the same CTA; on giving up it sets *abort and the TIMEOUT status bit and
 // returns false.  Never traps, never spins forever.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kSleepHintNs = 100000u;        // 100 us
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        set_status(status, LILY_STATUS_TIMEOUT);
-        return false;
-      }
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      set_status(status, LILY_STATUS_TIMEOUT);
+      return false;
     }
   }
 }
@@ -218,25 +233,22 @@ __device__ __forceinline__ uint16_t bf16_to_f16_bits(uint16_t b) {
 }
 
 // Eight 4-bit codes (one 32-bit word, element i in bits 4i..4i+3) times one
-// fp16 scale plus one fp16 bias, as 8 fp16 in element order (4 words).
-// Each weight is round_fp16(scale * q + bias): 1024 + q is exact in fp16,
+// fp16 scale plus one fp16 bias, as 8 fp16 in the "pair-interleaved" chunk
+// order (q0, q4, q1, q5, q2, q6, q3, q7) -- the order in which one LOP3 per
+// pair extracts them.  The other GEMM operand stores every 8-element K chunk
+// in the same order (kchunk_pos), so the dot products are unchanged.  Each
+// weight is round_fp16(scale * q + bias): 1024 + q is exact in fp16,
 // subtracting 1024 is exact, and the f16x2 FMA rounds once.
 __device__ __forceinline__ void dequant8(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
   const uint32_t kMagic = 0x64006400u;  // fp16 pair (1024, 1024)
   const uint32_t kMask = 0x000F000Fu;
-  uint32_t p04 = lop3_and_or(w, kMask, kMagic);        // (q0, q4) + 1024
-  uint32_t p15 = lop3_and_or(w >> 4, kMask, kMagic);   // (q1, q5)
-  uint32_t p26 = lop3_and_or(w >> 8, kMask, kMagic);   // (q2, q6)
-  uint32_t p37 = lop3_and_or(w >> 12, kMask, kMagic);  // (q3, q7)
-  uint32_t q01 = prmt(p04, p15, 0x5410u);
-  uint32_t q45 = prmt(p04, p15, 0x7632u);
-  uint32_t q23 = prmt(p26, p37, 0x5410u);
-  uint32_t q67 = prmt(p26, p37, 0x7632u);
-  o[0] = h2_fma(s2, h2_sub(q01, kMagic), b2);
-  o[1] = h2_fma(s2, h2_sub(q23, kMagic), b2);
-  o[2] = h2_fma(s2, h2_sub(q45, kMagic), b2);
-  o[3] = h2_fma(s2, h2_sub(q67, kMagic), b2);
+  o[0] = h2_fma(s2, h2_sub(lop3_and_or(w, kMask, kMagic), kMagic), b2);        // (q0, q4)
+  o[1] = h2_fma(s2, h2_sub(lop3_and_or(w >> 4, kMask, kMagic), kMagic), b2);   // (q1, q5)
+  o[2] = h2_fma(s2, h2_sub(lop3_and_or(w >> 8, kMask, kMagic), kMagic), b2);   // (q2, q6)
+  o[3] = h2_fma(s2, h2_sub(lop3_and_or(w >> 12, kMask, kMagic), kMagic), b2);  // (q3, q7)
 }
+// Position of element e (0..7) of an 8-element K chunk in that order.
+__host__ __device__ __forceinline__ int kchunk_pos(int e) { return ((e & 3) << 1) | (e >> 2); }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

@@ -25,6 +25,9 @@
 // [2^-17, 65504] (values beyond 65504 set LILY_STATUS_F16_RANGE).
 // Epilogues: gate/up writes H = silu(gate) * up (fp16) in expert-sorted row
 // order; down adds gate * out into the fp32 token-order accumulator.
+// K order: the rebuilt weights come out of the nibble extraction with each
+// 8-element K chunk in the order (0,4,1,5,2,6,3,7); the K operands x16 and H
+// are stored in that same order, so no shuffle is needed.
 //
 // Persistent: one CTA per SM walks the (tile, slice) work items; warp roles
 // are listed below.  Every wait is bounded (2 s) and sets
@@ -253,12 +256,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&afull[b]), kDequantThreads);
+      mbar_init(smem_u32(&afull[b]), kNumDequantWarps);
       mbar_init(smem_u32(&aempty[b]), 1);
       mbar_init(smem_u32(&accfull[b]), 1);
-      mbar_init(smem_u32(&accempty[b]), kEpiThreads);
-      mbar_init(smem_u32(&sbfull[b]), kEpiThreads);
-      mbar_init(smem_u32(&sbempty[b]), kDequantThreads);
+      mbar_init(smem_u32(&accempty[b]), kNumEpiWarps);
+      mbar_init(smem_u32(&sbfull[b]), kNumEpiWarps);
+      mbar_init(smem_u32(&sbempty[b]), kNumDequantWarps);
     }
     mbar_init(smem_u32(drain), 1);
     misc[0] = 0;
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int n = 4 * (lane + 32 * (j >> 2)) + (j & 3);
         tok[j] = GATEUP ? row_token(a, itm.row0 + min(n, itm.rows - 1), P) : 0;
       }
-      const uint32_t tx_bytes = MATS * kPackedBytes + (GATEUP ? N * 128 : BBYTES);
+      const uint32_t tx_bytes = MATS * kPackedBytes + N * 128;
       for (int kk = 0; kk < G; ++kk, ++it) {
         const int s = it % nstages;
         if (it >= (uint32_t)nstages &&
@@ -309,7 +312,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(fb, tx_bytes);
           tma_load_2d(smem_u32(st + BBYTES), &tm_q0, kk * 32, wrow, fb);
           if (GATEUP) tma_load_2d(smem_u32(st + BBYTES + kPackedBytes), &tm_q1, kk * 32, wrow, fb);
-          if (!GATEUP) tma_load_2d(smem_u32(st), &tm_b, kk * 64, itm.row0, fb);
+          if (!GATEUP)  // the tile's N rows of H, 16 rows per box
+            for (int r16 = 0; r16 < N; r16 += 16)
+              tma_load_2d(smem_u32(st + r16 * 128), &tm_b, kk * 64, itm.row0 + r16, fb);
         }
         if (GATEUP) {
           if (lane < N / 4)
@@ -372,9 +377,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp < kEpiWarp0) {
     // ================================================= dequant
     const int i = threadIdx.x - 64;
-    int mat, r, c0, nch;
-    if (GATEUP) { mat = i >> 7; r = i & 127; c0 = 0; nch = 8; }
-    else        { mat = 0;      r = i >> 1;  c0 = (i & 1) * 4; nch = 4; }
+    int mat, r, c0;
+    if (GATEUP) { mat = i >> 7; r = i & 127; c0 = 0; }
+    else        { mat = 0;      r = i >> 1;  c0 = (i & 1) * 4; }
     const uint32_t swz = (uint32_t)(r & 7);
     uint32_t it = 0, j = 0;
     bool ok = true;
@@ -397,22 +402,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t sbv = sbs[(mat * G + kk) * 128 + r];
         const uint32_t s2 = prmt(sbv, sbv, 0x1010u), b2 = prmt(sbv, sbv, 0x3232u);
         const uint32_t arow = smem_u32(a_base + (size_t)(b * MATS + mat) * kABytes) + r * 128;
-        for (int c = 0; c < nch; c += 4) {
-          const uint4 wv = *reinterpret_cast<const uint4*>(pk + c * 4);
-          const uint32_t wd[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            uint32_t o[4];
-            dequant8(wd[jj], s2, b2, o);
-            const uint32_t chunk = (uint32_t)(c0 + c + jj);
-            st_shared_v4(arow + ((chunk ^ swz) << 4), o[0], o[1], o[2], o[3]);
-          }
+        uint32_t wd[8];
+        if (GATEUP) {
+          // a 32-byte row is read as two 16-byte loads; rows 4..7 of every 8
+          // issue the halves in the other order so that each 8 consecutive
+          // lanes hit all eight 16-byte bank groups, then swap back
+          const int sw = (r >> 2) & 1;
+          const uint4 v0 = *reinterpret_cast<const uint4*>(pk + (sw ? 16 : 0));
+          const uint4 v1 = *reinterpret_cast<const uint4*>(pk + (sw ? 0 : 16));
+          const uint4 lo = sw ? v1 : v0, hi = sw ? v0 : v1;
+          wd[0] = lo.x; wd[1] = lo.y; wd[2] = lo.z; wd[3] = lo.w;
+          wd[4] = hi.x; wd[5] = hi.y; wd[6] = hi.z; wd[7] = hi.w;
+        } else {
+          const uint4 v0 = *reinterpret_cast<const uint4*>(pk);
+          wd[0] = v0.x; wd[1] = v0.y; wd[2] = v0.z; wd[3] = v0.w;
         }
+#pragma unroll
+        for (int jj = 0; jj < (GATEUP ? 8 : 4); ++jj) {  // chunk order uniform across lanes
+          uint32_t o[4];
+          dequant8(wd[jj], s2, b2, o);
+          const uint32_t chunk = (uint32_t)(c0 + jj);
+          st_shared_v4(arow + ((chunk ^ swz) << 4), o[0], o[1], o[2], o[3]);
+        }
+        // every lane makes its stores visible to the tensor core, then one
+        // arrive per warp (256 arrivals on one barrier would serialise)
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&afull[b]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
       }
       if (!ok) break;
-      mbar_arrive(smem_u32(&sbempty[slot]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sbempty[slot]));
       ++j;
     }
   } else {
@@ -435,7 +455,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool have = next_item<BM>(a, w, n_items, nslices, nsh, P, cur);
     if (have) {
       scale_fill<MATS>(a, row_of(cur), G, r, slot_ptr(0));
-      mbar_arrive(smem_u32(&sbfull[0]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sbfull[0]));
     }
     int wn = w + gridDim.x;
     bool have_next = have && next_item<BM>(a, wn, n_items, nslices, nsh, P, nxt);
@@ -459,7 +480,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         } else {
           scale_fill<MATS>(a, row_of(nxt), G, r, slot_ptr(slot));
         }
-        mbar_arrive(smem_u32(&sbfull[slot]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sbfull[slot]));
       }
       int wnn = wn + gridDim.x;
       const bool have_nn = have_next && next_item<BM>(a, wnn, n_items, nslices, nsh, P, nn);
@@ -474,6 +496,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!warp_wait(smem_u32(&accfull[ab]), (j / NACC) & 1, abort, a.status)) break;
       tc_fence_after();
       const int feat = cur.slice * 128 + q * 32 + lane;
+      // H stores each 8-feature chunk in K-chunk order: it is the down GEMM's
+      // K operand against weights rebuilt in that order
+      const int hcol = (feat & ~7) | kchunk_pos(feat & 7);
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + ab * L::kAccCols;
       for (int cb = 0; cb < N; cb += 32) {
         const bool last = cb + 32 >= N;
@@ -484,7 +509,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_wait();
           if (last) {
             tc_fence_before();
-            mbar_arrive(smem_u32(&accempty[ab]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
           __half* H = static_cast<__half*>(a.H);
           bool range_ok = true;
@@ -495,7 +521,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const float gv = __uint_as_float(gr[jj]), uv = __uint_as_float(ur[jj]);
               const float h = gv / (1.f + __expf(-gv)) * uv;
               range_ok &= fabsf(h) <= 65504.f;
-              H[(size_t)(cur.row0 + n) * a.F + feat] = __float2half_rn(h);
+              H[(size_t)(cur.row0 + n) * a.F + hcol] = __float2half_rn(h);
             }
           }
           if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
@@ -505,7 +531,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld_wait();
           if (last) {
             tc_fence_before();
-            mbar_arrive(smem_u32(&accempty[ab]));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
           // lane jj looks up row cb + jj: its token and its gate weight
           const int rj = cur.row0 + min(cb + lane, cur.rows - 1);
@@ -645,7 +672,7 @@ cudaError_t launch_gateup(const GemmArgs& a, const void* x16, const uint8_t* gq,
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
   CUtensorMap q0, b;
   const int P = a.T * a.k;
-  if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d) || !f16_rows_map(&b, a.H, a.F, P + a.T, a.BM))
+  if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d) || !f16_rows_map(&b, a.H, a.F, P + a.T, 16))
     return cudaErrorInvalidValue;
   return launch_gemm<false>(a, q0, q0, b, s);
 }

@@ -25,7 +25,8 @@ enum KernelKind : int {
   K_STACK_BOUNDARY = 10,
   K_MEMSET = 11,
   K_ROUTER_PREP = 12,
-  K_NUM = 13
+  K_ROUTER_REDUCE = 13,
+  K_NUM = 14
 };
 
 // Profiling hooks (api.cu): bracket one launch with events when enabled.
@@ -38,10 +39,7 @@ constexpr int kRouteThreads = 256;
 
 // ---------------------------------------------------------------- routing
 struct RouteArgs {
-  const float* logits_src;  // fp32 [T][E], or NULL when partial is used
-  const float* partial;     // fp32 [nsplit][T][E] split-K router partials (or NULL)
-  int nsplit;
-  const float* bias;        // fp32 [E] added to summed partials (or NULL)
+  const float* logits_src;  // fp32 [T][E]
   float* logits_dst;        // fp32 [T][E] (may equal logits_src)
   int T, E, k, BM, cap;
   int32_t* ids;
@@ -62,12 +60,14 @@ cudaError_t launch_router_logits(const void* x, const float* w, const float* b, 
                                  int T, int d, int E, void* x16, uint32_t* status,
                                  cudaStream_t s);
 // Router on tensor cores for larger T: W split exactly into three bf16 terms
-// (w_split, [3][E][d]), fp32 partial logits per K-split into partial
-// ([router_splits(T,d)][T][E]); x16 written as above.
+// (w_split, [3][E][d]), fp32 partial logits per K-split (partial,
+// [router_splits(T,d)][T][E]) summed in order into logits (+ bias); x16
+// written as above.
 int router_splits(int T, int d);
 size_t router_tc_smem(int E);
-cudaError_t launch_router_tc(const void* x, const float* w, int T, int d, int E, void* w_split,
-                             float* partial, void* x16, uint32_t* status, cudaStream_t s);
+cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, int T, int d,
+                             int E, void* w_split, float* partial, float* logits, void* x16,
+                             uint32_t* status, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 int route_max_blocks();  // co-resident blocks of the routing kernel (0 = unknown)
 
@@ -83,7 +83,7 @@ struct GemmArgs {
   const uint16_t* b0;
   const uint16_t* s1;  // up scales (gate/up only)
   const uint16_t* b1;
-  void* H;             // fp16 [P+T][F]
+  void* H;             // fp16 [P+T][F], 8-element chunks in K-chunk order
   float* yacc;         // fp32 [T][d]
   uint32_t* status;
 };

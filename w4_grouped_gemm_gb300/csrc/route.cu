@@ -19,13 +19,31 @@ namespace lily {
 // logits[t][e] = sum_i x[t][i] * W[e][i] (+ b[e]), fp32 accumulation.
 // The router kernels also write x16, the fp16 copy of x that the grouped
 // GEMM's tensor-core operand uses (exact for |x| in [2^-17, 65504]; larger
-// values set LILY_STATUS_F16_RANGE).
+// values set LILY_STATUS_F16_RANGE), every 8-element chunk stored in the
+// K-chunk order of the rebuilt weights (kchunk_pos).
 
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t v, bool& ok) {
-  const float lo = __uint_as_float(v << 16), hi = __uint_as_float(v & 0xFFFF0000u);
-  ok &= fabsf(lo) <= 65504.f && fabsf(hi) <= 65504.f;
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
+// 8 bf16 (one 16-byte chunk of a row of x) -> 8 fp16 in the grouped GEMM's
+// K-chunk order (element e at position kchunk_pos(e)).
+__device__ __forceinline__ uint4 bf8_to_h8_kchunk(uint4 v, bool& ok) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  uint16_t h[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ok &= fabsf(f[e]) <= 65504.f;
+    h[kchunk_pos(e)] = __half_as_ushort(__float2half_rn(f[e]));
+  }
+  uint4 o;
+  o.x = h[0] | ((uint32_t)h[1] << 16);
+  o.y = h[2] | ((uint32_t)h[3] << 16);
+  o.z = h[4] | ((uint32_t)h[5] << 16);
+  o.w = h[6] | ((uint32_t)h[7] << 16);
+  return o;
 }
 
 // Small T (decode, T <= 8): one warp per expert row, all tokens at once.
@@ -39,8 +57,9 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* _
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (blockIdx.x == 0 && x16) {  // fp16 copy of the (few) rows
     bool ok = true;
-    const uint32_t* xs = reinterpret_cast<const uint32_t*>(x);
-    for (int i = threadIdx.x; i < T * d / 2; i += blockDim.x) x16[i] = bf2_to_h2(xs[i], ok);
+    const uint4* xs = reinterpret_cast<const uint4*>(x);
+    for (int i = threadIdx.x; i < T * d / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(x16)[i] = bf8_to_h8_kchunk(xs[i], ok);
     if (!ok) set_status(status, LILY_STATUS_F16_RANGE);
   }
   const int e = blockIdx.x * 8 + warp;
@@ -91,14 +110,15 @@ cudaError_t launch_router_logits(const void* x, const float* w, const float* b, 
 // product is exact in fp32, so the tensor cores give fp32-accumulated logits
 // of the fp32 weights.  Tokens are the M = 128 operand, experts the N operand;
 // the K loop runs over (term, 64-wide block) pairs and is split across CTAs,
-// each writing fp32 partial logits that the routing kernel sums in order.
+// each writing fp32 partial logits; a wide reduction kernel sums the splits
+// in order (deterministic) and adds the bias.
 
 __global__ void __launch_bounds__(256) router_prep_kernel(const float* __restrict__ w,
                                                           __nv_bfloat16* __restrict__ w3,
                                                           int64_t n_w,
                                                           const uint32_t* __restrict__ x,
                                                           uint32_t* __restrict__ x16,
-                                                          int64_t n_x2, uint32_t* status) {
+                                                          int64_t n_x8, uint32_t* status) {
   bool ok = true;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_w; i += stride) {
@@ -111,8 +131,8 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float* __restric
     w3[n_w + i] = mid;
     w3[2 * n_w + i] = __float2bfloat16_rn(r2);
   }
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_x2; i += stride)
-    x16[i] = bf2_to_h2(x[i], ok);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_x8; i += stride)
+    reinterpret_cast<uint4*>(x16)[i] = bf8_to_h8_kchunk(reinterpret_cast<const uint4*>(x)[i], ok);
   if (!ok) set_status(status, LILY_STATUS_F16_RANGE);
 }
 
@@ -254,8 +274,40 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   }
 }
 
-cudaError_t launch_router_tc(const void* x, const float* w, int T, int d, int E, void* w_split,
-                             float* partial, void* x16, uint32_t* status, cudaStream_t s) {
+// logits[t][e] = sum_s partial[s][t][e] (+ b[e]), splits added in order;
+// four logits per thread (E % 4 == 0) or one.
+__global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restrict__ partial,
+                                                            int S, const float* __restrict__ b,
+                                                            float* __restrict__ logits, int T,
+                                                            int E) {
+  const int64_t n = (int64_t)T * E;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if ((E & 3) == 0) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n / 4; i += stride) {
+      float4 acc = __ldcg(reinterpret_cast<const float4*>(partial) + i);
+      for (int sp = 1; sp < S; ++sp) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(partial + (int64_t)sp * n) + i);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      if (b) {
+        const int e = (int)((4 * i) % E);
+        acc.x += b[e]; acc.y += b[e + 1]; acc.z += b[e + 2]; acc.w += b[e + 3];
+      }
+      reinterpret_cast<float4*>(logits)[i] = acc;
+    }
+  } else {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
+      float acc = __ldcg(partial + i);
+      for (int sp = 1; sp < S; ++sp) acc += __ldcg(partial + (int64_t)sp * n + i);
+      if (b) acc += b[i % E];
+      logits[i] = acc;
+    }
+  }
+}
+
+cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, int T, int d,
+                             int E, void* w_split, float* partial, float* logits, void* x16,
+                             uint32_t* status, cudaStream_t s) {
   const int NE = router_ne(E);
   CUtensorMap tm_x, tm_w;
   {
@@ -274,13 +326,13 @@ cudaError_t launch_router_tc(const void* x, const float* w, int T, int d, int E,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const int64_t n_w = (int64_t)E * d, n_x2 = (int64_t)T * d / 2;
-  int pblocks = (int)((std::max(n_w, n_x2) + 255) / 256);
+  const int64_t n_w = (int64_t)E * d, n_x8 = (int64_t)T * d / 8;
+  int pblocks = (int)((std::max(n_w, n_x8) + 255) / 256);
   if (pblocks > 152 * 8) pblocks = 152 * 8;
   prof_begin(K_ROUTER_PREP, s);
   router_prep_kernel<<<pblocks, 256, 0, s>>>(w, static_cast<__nv_bfloat16*>(w_split), n_w,
                                              static_cast<const uint32_t*>(x),
-                                             static_cast<uint32_t*>(x16), n_x2, status);
+                                             static_cast<uint32_t*>(x16), n_x8, status);
   prof_end(K_ROUTER_PREP, s);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
@@ -291,6 +343,13 @@ cudaError_t launch_router_tc(const void* x, const float* w, int T, int d, int E,
   prof_begin(K_ROUTER_GEMM, s);
   router_tc_kernel<<<grid, kRtThreads, smem, s>>>(tm_x, tm_w, T, d, E, NE, partial, status);
   prof_end(K_ROUTER_GEMM, s);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  const int64_t nr = (E & 3) == 0 ? (int64_t)T * E / 4 : (int64_t)T * E;
+  int rblocks = (int)((nr + 255) / 256);
+  if (rblocks > 152 * 8) rblocks = 152 * 8;
+  prof_begin(K_ROUTER_REDUCE, s);
+  router_reduce_kernel<<<rblocks, 256, 0, s>>>(partial, grid.y, bias, logits, T, E);
+  prof_end(K_ROUTER_REDUCE, s);
   return cudaGetLastError();
 }
 
@@ -382,42 +441,25 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
 
   // ---- phase 1: top-k + gates, one warp per token (4 tokens per warp)
   constexpr int kWarpTok = kRouteTok / 8;
-  // logits of this warp's tokens, lane holding experts lane + 32c; with a
-  // split-K router the partials are summed here in split order (all loads
-  // of one split issued together)
+  // logits of this warp's tokens (lane holds experts lane + 32c), all loads
+  // of the warp issued together
   float lv[kWarpTok][kMaxE / 32];
-#pragma unroll
-  for (int i = 0; i < kWarpTok; ++i)
-#pragma unroll
-    for (int c = 0; c < kMaxE / 32; ++c) lv[i][c] = 0.f;
-  if (a.partial) {
-    for (int sp = 0; sp < a.nsplit; ++sp) {
-#pragma unroll
-      for (int i = 0; i < kWarpTok; ++i) {
-        const int tl = warp * kWarpTok + i;
-        const float* pp = a.partial + ((size_t)sp * T + t0 + tl) * E;
-#pragma unroll
-        for (int c = 0; c < kMaxE / 32; ++c)
-          if (tl < ntok && lane + 32 * c < E) lv[i][c] += __ldcg(pp + lane + 32 * c);
-      }
-    }
-  }
 #pragma unroll
   for (int i = 0; i < kWarpTok; ++i) {
     const int tl = warp * kWarpTok + i;
-    if (tl >= ntok) continue;
 #pragma unroll
     for (int c = 0; c < kMaxE / 32; ++c) {
       const int e = lane + 32 * c;
-      if (e >= E) continue;
-      const size_t idx = (size_t)(t0 + tl) * E + e;
-      if (a.partial) {
-        if (a.bias) lv[i][c] += a.bias[e];
-        a.logits_dst[idx] = lv[i][c];
-      } else {
-        lv[i][c] = a.logits_src[idx];
-        if (a.logits_dst != a.logits_src) a.logits_dst[idx] = lv[i][c];
-      }
+      lv[i][c] = (tl < ntok && e < E) ? a.logits_src[(size_t)(t0 + tl) * E + e] : 0.f;
+    }
+  }
+  if (a.logits_dst != a.logits_src) {
+#pragma unroll
+    for (int i = 0; i < kWarpTok; ++i) {
+      const int tl = warp * kWarpTok + i;
+#pragma unroll
+      for (int c = 0; c < kMaxE / 32; ++c)
+        if (tl < ntok && lane + 32 * c < E) a.logits_dst[(size_t)(t0 + tl) * E + lane + 32 * c] = lv[i][c];
     }
   }
 #pragma unroll
