@@ -2,6 +2,7 @@
 // layout and the launch sequence of each call.  No call allocates device
 // memory; every launch goes to the caller's stream.
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -53,6 +54,25 @@ void prof_end(int kind, cudaStream_t s) {
   g_prof_kind = -1;
 }
 
+// ---------------------------------------------------------------- host caches
+namespace {
+std::mutex g_attr_mu;
+std::map<std::pair<int, const void*>, size_t> g_smem_set;
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* func, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  auto key = std::make_pair(dev, func);
+  auto it = g_smem_set.find(key);
+  if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) g_smem_set[key] = bytes;
+  return e;
+}
+
 // ---------------------------------------------------------------- workspace
 namespace {
 
@@ -60,7 +80,7 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t ctrl, hist, x16, w3, part, H, acc, total;
+  size_t ctrl, hist, x16, xs, w3, part, H, acc, total;
 };
 
 // ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
@@ -73,6 +93,7 @@ Layout layout(const lily_moe_dims& d) {
   L.ctrl = off; off += up(256);
   L.hist = off; off += up(nblk * E * 4);
   L.x16 = off;  off += up(T * D * 2);
+  L.xs = off;   off += up(P * D * 2);
   const bool tc_router = d.T > 8;  // tensor-core router: split W + split-K partials
   L.w3 = off;   off += tc_router ? up(3 * E * D * 2) : 0;
   L.part = off; off += tc_router ? up((size_t)router_splits(d.T, d.d_model) * T * E * 4) : 0;
@@ -87,13 +108,18 @@ Layout layout(const lily_moe_dims& d) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Compute capability 10.3 of the current device, checked once per device.
 int check_arch() {
+  static int verdict[64] = {};  // 0 unknown, 1 sm_103, -1 other
   int dev = 0, maj = 0, min = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LILY_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && verdict[dev]) return verdict[dev] > 0 ? LILY_OK : LILY_ERR_ARCH;
   if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return LILY_ERR_CUDA;
-  return (maj == 10 && min == 3) ? LILY_OK : LILY_ERR_ARCH;
+  const bool ok = maj == 10 && min == 3;
+  if (dev >= 0 && dev < 64) verdict[dev] = ok ? 1 : -1;
+  return ok ? LILY_OK : LILY_ERR_ARCH;
 }
 
 int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LILY_OK : LILY_ERR_CUDA; }
@@ -147,13 +173,12 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
     if (d.T > 8) {
       float* part = reinterpret_cast<float*>(base + L.part);
       cudaError_t e = launch_router_tc(x, w->router_w, w->router_bias, d.T, d.d_model,
-                                       d.n_experts, base + L.w3, part, r.logits, base + L.x16,
-                                       ws_status(ws), s);
+                                       d.n_experts, base + L.w3, part, r.logits, ws_status(ws), s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
       a.logits_src = r.logits;
     } else {
       cudaError_t e = launch_router_logits(x, w->router_w, w->router_bias, r.logits, d.T,
-                                           d.d_model, d.n_experts, base + L.x16, ws_status(ws), s);
+                                           d.d_model, d.n_experts, s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
       a.logits_src = r.logits;
     }
@@ -217,7 +242,9 @@ int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights
   prof_end(K_MEMSET, s);
   if (e != cudaSuccess) return LILY_ERR_CUDA;
   const Layout L = layout(d);
-  if (launch_gateup(a, static_cast<uint8_t*>(ws) + L.x16, w->gate_q, w->up_q, s) != cudaSuccess)
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  if (launch_token_rows(a, x, base + L.xs, base + L.x16, s) != cudaSuccess) return LILY_ERR_CUDA;
+  if (launch_gateup(a, base + L.xs, base + L.x16, w->gate_q, w->up_q, s) != cudaSuccess)
     return LILY_ERR_CUDA;
   a.s0 = w->down_s;
   a.b0 = w->down_b;
@@ -519,7 +546,7 @@ const char* lily_moe_kernel_name(int kind) {
   static const char* names[] = {"router_gemm", "router_gemv", "route", "gateup_gemm",
                                 "down_gemm",   "finalize",    "dec_gateup", "dec_down",
                                 "dec_combine", "rmsnorm",     "stack_boundary", "memset_acc",
-                                "router_prep", "router_reduce"};
+                                "router_prep", "router_reduce", "token_rows"};
   if (kind < 0 || kind >= (int)(sizeof(names) / sizeof(names[0]))) return "unused";
   return names[kind];
 }

@@ -250,6 +250,30 @@ __device__ __forceinline__ void dequant8(uint32_t w, uint32_t s2, uint32_t b2, u
 // Position of element e (0..7) of an 8-element K chunk in that order.
 __host__ __device__ __forceinline__ int kchunk_pos(int e) { return ((e & 3) << 1) | (e >> 2); }
 
+// 8 bf16 (one 16-byte chunk of a row of x) -> 8 fp16 in the grouped GEMM's
+// K-chunk order (element e at position kchunk_pos(e)).
+__device__ __forceinline__ uint4 bf8_to_h8_kchunk(uint4 v, bool& ok) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float f[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  uint16_t h[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ok &= fabsf(f[e]) <= 65504.f;
+    h[kchunk_pos(e)] = __half_as_ushort(__float2half_rn(f[e]));
+  }
+  uint4 o;
+  o.x = h[0] | ((uint32_t)h[1] << 16);
+  o.y = h[2] | ((uint32_t)h[3] << 16);
+  o.z = h[4] | ((uint32_t)h[5] << 16);
+  o.w = h[6] | ((uint32_t)h[7] << 16);
+  return o;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),

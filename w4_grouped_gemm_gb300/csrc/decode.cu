@@ -103,11 +103,19 @@ __device__ void stage_rows(uint32_t* xp, float* xs, int rows, int K, Src src) {
     }
     xp[e] = v;
   }
+  __syncthreads();
+  // group sums from the staged copy (shared memory), not from global memory
   for (int e = threadIdx.x; e < kDecMaxRows * G; e += kDecThreads) {
-    const int n = e / G, g = e % G;
+    const int n = e / G;
     float s = 0.f;
-    if (n < rows)
-      for (int i = 0; i < 64; ++i) s += act_to_float<F16>(src(n, g * 64 + i));
+    if (n < rows) {
+      const uint32_t* p = xp + (size_t)e * 32;
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t v = p[i];
+        s += act_to_float<F16>((uint16_t)(v & 0xFFFFu)) + act_to_float<F16>((uint16_t)(v >> 16));
+      }
+    }
     xs[e] = s;
   }
 }
@@ -247,11 +255,11 @@ __global__ void __launch_bounds__(kDecThreads) dec_down_kernel(const DecodeArgs 
 }
 
 // y[t] = sum_j gate[t][j] * O[inv[t*k+j]] + O[P + t], in slot order (fp32,
-// or rounded once to bf16).
+// or rounded once to bf16).  Grid: (T, d / 256).
 __global__ void __launch_bounds__(256) dec_combine_kernel(const DecodeArgs a) {
   const int t = blockIdx.x;
   const int P = a.T * a.k;
-  for (int i = threadIdx.x; i < a.d; i += blockDim.x) {
+  for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < a.d; i += gridDim.y * blockDim.x) {
     float acc = 0.f;
     for (int j = 0; j < a.k; ++j) {
       const int p = t * a.k + j;
@@ -271,12 +279,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   const size_t smem_gu = (size_t)kDecMaxRows * (a.d / 64) * (32 * 4 + 4) + 8 * 256 * 4;
   const size_t smem_dn = (size_t)kDecMaxRows * (a.F / 64) * (32 * 4 + 4);
   cudaError_t err;
-  if ((err = cudaFuncSetAttribute(dec_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_gu)) != cudaSuccess)
-    return err;
-  if ((err = cudaFuncSetAttribute(dec_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_dn)) != cudaSuccess)
-    return err;
+  if ((err = ensure_smem_attr((const void*)dec_gateup_kernel, smem_gu)) != cudaSuccess) return err;
+  if ((err = ensure_smem_attr((const void*)dec_down_kernel, smem_dn)) != cudaSuccess) return err;
   prof_begin(K_DEC_GATEUP, s);
   dec_gateup_kernel<<<slots * (a.F / 16), kDecThreads, smem_gu, s>>>(a);
   prof_end(K_DEC_GATEUP, s);
@@ -286,7 +290,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   prof_end(K_DEC_DOWN, s);
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   prof_begin(K_DEC_COMBINE, s);
-  dec_combine_kernel<<<a.T, 256, 0, s>>>(a);
+  dec_combine_kernel<<<dim3(a.T, (a.d + 255) / 256), 256, 0, s>>>(a);
   prof_end(K_DEC_COMBINE, s);
   return cudaGetLastError();
 }

@@ -14,9 +14,10 @@
 //   A = dequantised weight slice, 128 output features x 64 K, fp16, K-major,
 //       128-byte swizzle, written by the dequant warps
 //   B = token rows of one block-map tile (<= BM rows) x 64 K, fp16, K-major,
-//       128-byte swizzle, brought by TMA: gate/up gathers rows of x (its fp16
-//       copy) through the expert-sorted permutation (tile::gather4); down
-//       reads rows of H
+//       128-byte swizzle, brought by TMA in 16-row boxes: gate/up reads xs,
+//       the fp16 rows of x in expert-sorted order written once per layer by
+//       token_rows_kernel (one pass instead of a TMA gather per K-step);
+//       down reads rows of H
 //   D = 128 x N fp32 in TMEM
 // Operand precision: fp16 rather than the pages' bf16.  Rounding the
 // rebuilt weights and H to bf16 alone puts the layer outside max|err| <= 2e-2
@@ -45,8 +46,6 @@ constexpr int kNumDequantWarps = 8;
 constexpr int kNumEpiWarps = 4;
 constexpr int kEpiWarp0 = 2 + kNumDequantWarps;
 constexpr int kGemmThreads = 32 * (2 + kNumDequantWarps + kNumEpiWarps);  // 448
-constexpr int kDequantThreads = 32 * kNumDequantWarps;
-constexpr int kEpiThreads = 32 * kNumEpiWarps;
 constexpr int kMaxStages = 8;
 constexpr int kPackedBytes = 128 * 32;  // 128 rows x 64 4-bit codes
 constexpr int kABytes = 128 * 128;      // 128 rows x 64 fp16
@@ -199,18 +198,13 @@ __device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint16_t
   }
 }
 
-// Token of expert-sorted row r (the row's pair index / k; shared rows are
-// tokens in order).
-__device__ __forceinline__ int row_token(const GemmArgs& a, int r, int P) {
-  return r >= P ? r - P : __ldg(a.perm + r) / a.k;
-}
-
 // Persistent kernel: one CTA per SM loops over the work items.
 template <bool GATEUP, int BM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     w4_gemm_kernel(const __grid_constant__ CUtensorMap tm_q0,
                    const __grid_constant__ CUtensorMap tm_q1,
-                   const __grid_constant__ CUtensorMap tm_b, const GemmArgs a, const int nstages,
+                   const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_b2, const GemmArgs a, const int nstages,
                    const int nsb) {
   using L = GemmLayout<GATEUP, BM>;
   constexpr int MATS = L::kMats;
@@ -269,6 +263,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tensormap(&tm_q0);
     if (GATEUP) prefetch_tensormap(&tm_q1);
     prefetch_tensormap(&tm_b);
+    if (GATEUP) prefetch_tensormap(&tm_b2);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&misc[1]), L::kTmemCols);
@@ -291,13 +286,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       const int N = (itm.rows + 15) & ~15;
       const int wrow = itm.expert * NOUT + itm.slice * 128;
-      // gather rows of this item (gate/up): lane owns gathers q = lane, lane + 32
-      int tok[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int n = 4 * (lane + 32 * (j >> 2)) + (j & 3);
-        tok[j] = GATEUP ? row_token(a, itm.row0 + min(n, itm.rows - 1), P) : 0;
-      }
+      // token rows of the item: gate/up reads the expert-sorted copy xs (or,
+      // for a shared-expert tile, x16 in token order); down reads H
+      const CUtensorMap* tmb = (GATEUP && itm.shared) ? &tm_b2 : &tm_b;
+      const int brow = (GATEUP && itm.shared) ? itm.row0 - P : itm.row0;
       const uint32_t tx_bytes = MATS * kPackedBytes + N * 128;
       for (int kk = 0; kk < G; ++kk, ++it) {
         const int s = it % nstages;
@@ -312,16 +304,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(fb, tx_bytes);
           tma_load_2d(smem_u32(st + BBYTES), &tm_q0, kk * 32, wrow, fb);
           if (GATEUP) tma_load_2d(smem_u32(st + BBYTES + kPackedBytes), &tm_q1, kk * 32, wrow, fb);
-          if (!GATEUP)  // the tile's N rows of H, 16 rows per box
-            for (int r16 = 0; r16 < N; r16 += 16)
-              tma_load_2d(smem_u32(st + r16 * 128), &tm_b, kk * 64, itm.row0 + r16, fb);
-        }
-        if (GATEUP) {
-          if (lane < N / 4)
-            tma_gather4(smem_u32(st + lane * 512), &tm_b, kk * 64, tok[0], tok[1], tok[2], tok[3], fb);
-          if (lane + 32 < N / 4)
-            tma_gather4(smem_u32(st + (lane + 32) * 512), &tm_b, kk * 64, tok[4], tok[5], tok[6],
-                        tok[7], fb);
+          for (int r16 = 0; r16 < N; r16 += 16)  // the tile's N rows, 16 rows per box
+            tma_load_2d(smem_u32(st + r16 * 128), tmb, kk * 64, brow + r16, fb);
         }
         __syncwarp();
       }
@@ -604,7 +588,7 @@ CUresult encode_tiled(CUtensorMap* tm, CUtensorMapDataType dt, uint32_t rank, vo
 
 template <bool GATEUP, int BM>
 static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, const CUtensorMap& q1,
-                                  const CUtensorMap& b, cudaStream_t s) {
+                                  const CUtensorMap& b, const CUtensorMap& b2, cudaStream_t s) {
   const int K = GATEUP ? a.d : a.F;
   const int NOUT = GATEUP ? a.F : a.d;
   int nstages = 0, nsb = 0;
@@ -612,34 +596,31 @@ static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, cons
   if (nstages < 2) return cudaErrorInvalidValue;
   const size_t smem = gemm_smem_bytes(GATEUP, BM, K);
   auto kern = w4_gemm_kernel<GATEUP, BM>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t err = ensure_smem_attr((const void*)kern, smem);
   if (err != cudaSuccess) return err;
   const int P = a.T * a.k;
   const int cap = (P + BM - 1) / BM + (a.E < P ? a.E : P);
   const int nsh = (a.T + BM - 1) / BM;
   const int max_items = (nsh + cap) * (NOUT / 128);
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      num_sms = 148;
-  }
+  int num_sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    num_sms = 148;
   const int grid = max_items < num_sms ? max_items : num_sms;  // persistent: one CTA per SM
   prof_begin(GATEUP ? K_GATEUP : K_DOWN, s);
-  kern<<<grid, kGemmThreads, smem, s>>>(q0, q1, b, a, nstages, nsb);
+  kern<<<grid, kGemmThreads, smem, s>>>(q0, q1, b, b2, a, nstages, nsb);
   prof_end(GATEUP ? K_GATEUP : K_DOWN, s);
   return cudaGetLastError();
 }
 
 template <bool GATEUP>
 static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const CUtensorMap& q1,
-                               const CUtensorMap& b, cudaStream_t s) {
+                               const CUtensorMap& b, const CUtensorMap& b2, cudaStream_t s) {
   switch (a.BM) {
-    case 32: return launch_gemm_bm<GATEUP, 32>(a, q0, q1, b, s);
-    case 64: return launch_gemm_bm<GATEUP, 64>(a, q0, q1, b, s);
-    case 128: return launch_gemm_bm<GATEUP, 128>(a, q0, q1, b, s);
-    case 256: return launch_gemm_bm<GATEUP, 256>(a, q0, q1, b, s);
+    case 32: return launch_gemm_bm<GATEUP, 32>(a, q0, q1, b, b2, s);
+    case 64: return launch_gemm_bm<GATEUP, 64>(a, q0, q1, b, b2, s);
+    case 128: return launch_gemm_bm<GATEUP, 128>(a, q0, q1, b, b2, s);
+    case 256: return launch_gemm_bm<GATEUP, 256>(a, q0, q1, b, b2, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -660,13 +641,46 @@ static bool f16_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, 
                       CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_gateup(const GemmArgs& a, const void* x16, const uint8_t* gq, const uint8_t* uq,
-                          cudaStream_t s) {
-  CUtensorMap q0, q1, b;
+// Token rows of the gate/up GEMM, one warp per output row: rows [0, P) of
+// xs are x[perm[r] / k] (expert-sorted), rows of x16 are x in token order;
+// both fp16, each 8-element chunk in K-chunk order.  Values beyond the fp16
+// range set LILY_STATUS_F16_RANGE.
+__global__ void __launch_bounds__(256) token_rows_kernel(const uint4* __restrict__ x,
+                                                         const int32_t* __restrict__ perm, int k,
+                                                         int P, int T, int d8, uint4* __restrict__ xs,
+                                                         uint4* __restrict__ x16, uint32_t* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool ok = true;
+  for (int row = blockIdx.x * 8 + warp; row < P + T; row += gridDim.x * 8) {
+    const int tok = row < P ? __ldg(perm + row) / k : row - P;
+    const uint4* src = x + (size_t)tok * d8;
+    uint4* dst = row < P ? xs + (size_t)row * d8 : x16 + (size_t)(row - P) * d8;
+    for (int c = lane; c < d8; c += 32) dst[c] = bf8_to_h8_kchunk(__ldg(src + c), ok);
+  }
+  if (!ok) set_status(status, LILY_STATUS_F16_RANGE);
+}
+
+cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* x16,
+                              cudaStream_t s) {
+  const int P = a.T * a.k;
+  int blocks = (P + a.T + 7) / 8;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  prof_begin(K_TOKEN_ROWS, s);
+  token_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), a.perm, a.k, P, a.T,
+                                           a.d / 8, static_cast<uint4*>(xs),
+                                           static_cast<uint4*>(x16), a.status);
+  prof_end(K_TOKEN_ROWS, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, const uint8_t* gq,
+                          const uint8_t* uq, cudaStream_t s) {
+  CUtensorMap q0, q1, b, b2;
+  const int P = a.T * a.k;
   if (!packed_map(&q0, gq, a.d, (a.E + 1) * a.F) || !packed_map(&q1, uq, a.d, (a.E + 1) * a.F) ||
-      !f16_rows_map(&b, x16, a.d, a.T, 1))
+      !f16_rows_map(&b, xs, a.d, P, 16) || !f16_rows_map(&b2, x16, a.d, a.T, 16))
     return cudaErrorInvalidValue;
-  return launch_gemm<true>(a, q0, q1, b, s);
+  return launch_gemm<true>(a, q0, q1, b, b2, s);
 }
 
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
@@ -674,7 +688,7 @@ cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
   const int P = a.T * a.k;
   if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d) || !f16_rows_map(&b, a.H, a.F, P + a.T, 16))
     return cudaErrorInvalidValue;
-  return launch_gemm<false>(a, q0, q0, b, s);
+  return launch_gemm<false>(a, q0, q0, b, b, s);
 }
 
 // y = bf16(yacc), 8 elements per thread.

@@ -26,8 +26,14 @@ enum KernelKind : int {
   K_MEMSET = 11,
   K_ROUTER_PREP = 12,
   K_ROUTER_REDUCE = 13,
-  K_NUM = 14
+  K_TOKEN_ROWS = 14,
+  K_NUM = 15
 };
+
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device; remembered, so the runtime call happens once per kernel,
+// device and size (api.cu).
+cudaError_t ensure_smem_attr(const void* func, size_t bytes);
 
 // Profiling hooks (api.cu): bracket one launch with events when enabled.
 void prof_begin(int kind, cudaStream_t s);
@@ -54,20 +60,17 @@ struct RouteArgs {
   uint32_t* bar;       // workspace: grid barrier {count, generation}
   uint32_t* status;    // workspace status word
 };
-// T <= 8 only.  Also writes x16 (fp16 copy of x, for the grouped GEMM) when
-// x16 != NULL.
+// Router logits for T <= 8 (one warp per expert).
 cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
-                                 int T, int d, int E, void* x16, uint32_t* status,
-                                 cudaStream_t s);
+                                 int T, int d, int E, cudaStream_t s);
 // Router on tensor cores for larger T: W split exactly into three bf16 terms
 // (w_split, [3][E][d]), fp32 partial logits per K-split (partial,
-// [router_splits(T,d)][T][E]) summed in order into logits (+ bias); x16
-// written as above.
+// [router_splits(T,d)][T][E]) summed in order into logits (+ bias).
 int router_splits(int T, int d);
 size_t router_tc_smem(int E);
 cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, int T, int d,
-                             int E, void* w_split, float* partial, float* logits, void* x16,
-                             uint32_t* status, cudaStream_t s);
+                             int E, void* w_split, float* partial, float* logits, uint32_t* status,
+                             cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 int route_max_blocks();  // co-resident blocks of the routing kernel (0 = unknown)
 
@@ -87,10 +90,12 @@ struct GemmArgs {
   float* yacc;         // fp32 [T][d]
   uint32_t* status;
 };
-// Tensor maps are built by the launcher from the raw pointers; x16 is the
-// fp16 copy of x written by the router kernel.
-cudaError_t launch_gateup(const GemmArgs& a, const void* x16, const uint8_t* gq, const uint8_t* uq,
-                          cudaStream_t s);
+// Token rows for the gate/up GEMM: xs[r] = fp16(x[perm[r] / k]) for the P
+// expert-sorted rows and x16[t] = fp16(x[t]), every 8-element chunk in
+// K-chunk order.  Then the gate/up GEMM (tensor maps built from the pointers).
+cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* x16, cudaStream_t s);
+cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, const uint8_t* gq,
+                          const uint8_t* uq, cudaStream_t s);
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s);
 cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s);
 size_t gemm_smem_bytes(bool gateup, int BM, int K);

@@ -17,34 +17,6 @@ namespace lily {
 
 // ============================================================== router logits
 // logits[t][e] = sum_i x[t][i] * W[e][i] (+ b[e]), fp32 accumulation.
-// The router kernels also write x16, the fp16 copy of x that the grouped
-// GEMM's tensor-core operand uses (exact for |x| in [2^-17, 65504]; larger
-// values set LILY_STATUS_F16_RANGE), every 8-element chunk stored in the
-// K-chunk order of the rebuilt weights (kchunk_pos).
-
-// 8 bf16 (one 16-byte chunk of a row of x) -> 8 fp16 in the grouped GEMM's
-// K-chunk order (element e at position kchunk_pos(e)).
-__device__ __forceinline__ uint4 bf8_to_h8_kchunk(uint4 v, bool& ok) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float f[8];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    f[2 * j] = __uint_as_float(w[j] << 16);
-    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-  }
-  uint16_t h[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    ok &= fabsf(f[e]) <= 65504.f;
-    h[kchunk_pos(e)] = __half_as_ushort(__float2half_rn(f[e]));
-  }
-  uint4 o;
-  o.x = h[0] | ((uint32_t)h[1] << 16);
-  o.y = h[2] | ((uint32_t)h[3] << 16);
-  o.z = h[4] | ((uint32_t)h[5] << 16);
-  o.w = h[6] | ((uint32_t)h[7] << 16);
-  return o;
-}
 
 // Small T (decode, T <= 8): one warp per expert row, all tokens at once.
 constexpr int kGemvMaxT = 8;
@@ -52,35 +24,36 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* _
                                                           const float* __restrict__ w,
                                                           const float* __restrict__ b,
                                                           float* __restrict__ logits, int T,
-                                                          int d, int E, uint32_t* __restrict__ x16,
-                                                          uint32_t* status) {
+                                                          int d, int E) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (blockIdx.x == 0 && x16) {  // fp16 copy of the (few) rows
-    bool ok = true;
-    const uint4* xs = reinterpret_cast<const uint4*>(x);
-    for (int i = threadIdx.x; i < T * d / 8; i += blockDim.x)
-      reinterpret_cast<uint4*>(x16)[i] = bf8_to_h8_kchunk(xs[i], ok);
-    if (!ok) set_status(status, LILY_STATUS_F16_RANGE);
-  }
   const int e = blockIdx.x * 8 + warp;
   if (e >= E) return;
   float acc[kGemvMaxT];
 #pragma unroll
   for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.f;
   const float4* wr = reinterpret_cast<const float4*>(w + (size_t)e * d);
-  for (int i4 = lane; i4 < d / 4; i4 += 32) {
-    float4 wv = __ldg(wr + i4);
+  const int n4 = d / 128;  // float4 of this lane (d is a multiple of 128)
+  for (int base = 0; base < n4; base += 8) {
+    float4 wv[8];
 #pragma unroll
-    for (int t = 0; t < kGemvMaxT; ++t) {
-      if (t < T) {
-        const __nv_bfloat162* xp =
-            reinterpret_cast<const __nv_bfloat162*>(x + (size_t)t * d + 4 * i4);
-        float2 x01 = __bfloat1622float2(xp[0]);
-        float2 x23 = __bfloat1622float2(xp[1]);
-        acc[t] = fmaf(wv.x, x01.x, acc[t]);
-        acc[t] = fmaf(wv.y, x01.y, acc[t]);
-        acc[t] = fmaf(wv.z, x23.x, acc[t]);
-        acc[t] = fmaf(wv.w, x23.y, acc[t]);
+    for (int j = 0; j < 8; ++j)  // all loads of the batch issued before use
+      if (base + j < n4) wv[j] = __ldg(wr + lane + 32 * (base + j));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (base + j >= n4) break;
+      const int i4 = lane + 32 * (base + j);
+#pragma unroll
+      for (int t = 0; t < kGemvMaxT; ++t) {
+        if (t < T) {
+          const __nv_bfloat162* xp =
+              reinterpret_cast<const __nv_bfloat162*>(x + (size_t)t * d + 4 * i4);
+          const float2 x01 = __bfloat1622float2(xp[0]);
+          const float2 x23 = __bfloat1622float2(xp[1]);
+          acc[t] = fmaf(wv[j].x, x01.x, acc[t]);
+          acc[t] = fmaf(wv[j].y, x01.y, acc[t]);
+          acc[t] = fmaf(wv[j].z, x23.x, acc[t]);
+          acc[t] = fmaf(wv[j].w, x23.y, acc[t]);
+        }
       }
     }
   }
@@ -93,13 +66,11 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* _
 }
 
 cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
-                                 int T, int d, int E, void* x16, uint32_t* status,
-                                 cudaStream_t s) {
+                                 int T, int d, int E, cudaStream_t s) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  uint32_t* x16w = static_cast<uint32_t*>(x16);
   if (T > kGemvMaxT) return cudaErrorInvalidValue;  // larger T: launch_router_tc
   prof_begin(K_ROUTER_GEMV, s);
-  router_gemv_kernel<<<(E + 7) / 8, 256, 0, s>>>(xb, w, b, logits, T, d, E, x16w, status);
+  router_gemv_kernel<<<(E + 7) / 8, 256, 0, s>>>(xb, w, b, logits, T, d, E);
   prof_end(K_ROUTER_GEMV, s);
   return cudaGetLastError();
 }
@@ -115,11 +86,7 @@ cudaError_t launch_router_logits(const void* x, const float* w, const float* b, 
 
 __global__ void __launch_bounds__(256) router_prep_kernel(const float* __restrict__ w,
                                                           __nv_bfloat16* __restrict__ w3,
-                                                          int64_t n_w,
-                                                          const uint32_t* __restrict__ x,
-                                                          uint32_t* __restrict__ x16,
-                                                          int64_t n_x8, uint32_t* status) {
-  bool ok = true;
+                                                          int64_t n_w) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_w; i += stride) {
     const float v = w[i];
@@ -131,9 +98,6 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float* __restric
     w3[n_w + i] = mid;
     w3[2 * n_w + i] = __float2bfloat16_rn(r2);
   }
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_x8; i += stride)
-    reinterpret_cast<uint4*>(x16)[i] = bf8_to_h8_kchunk(reinterpret_cast<const uint4*>(x)[i], ok);
-  if (!ok) set_status(status, LILY_STATUS_F16_RANGE);
 }
 
 constexpr int kRtThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
@@ -306,8 +270,8 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
 }
 
 cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, int T, int d,
-                             int E, void* w_split, float* partial, float* logits, void* x16,
-                             uint32_t* status, cudaStream_t s) {
+                             int E, void* w_split, float* partial, float* logits, uint32_t* status,
+                             cudaStream_t s) {
   const int NE = router_ne(E);
   CUtensorMap tm_x, tm_w;
   {
@@ -326,18 +290,16 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const int64_t n_w = (int64_t)E * d, n_x8 = (int64_t)T * d / 8;
-  int pblocks = (int)((std::max(n_w, n_x8) + 255) / 256);
+  const int64_t n_w = (int64_t)E * d;
+  int pblocks = (int)((n_w + 255) / 256);
   if (pblocks > 152 * 8) pblocks = 152 * 8;
   prof_begin(K_ROUTER_PREP, s);
-  router_prep_kernel<<<pblocks, 256, 0, s>>>(w, static_cast<__nv_bfloat16*>(w_split), n_w,
-                                             static_cast<const uint32_t*>(x),
-                                             static_cast<uint32_t*>(x16), n_x8, status);
+  router_prep_kernel<<<pblocks, 256, 0, s>>>(w, static_cast<__nv_bfloat16*>(w_split), n_w);
   prof_end(K_ROUTER_PREP, s);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = router_tc_smem(E);
-  err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  err = ensure_smem_attr((const void*)router_tc_kernel, smem);
   if (err != cudaSuccess) return err;
   dim3 grid((T + 127) / 128, router_splits(T, d));
   prof_begin(K_ROUTER_GEMM, s);
@@ -580,12 +542,15 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
 }
 
 int route_max_blocks() {
+  static int cached[64] = {};
   int dev = 0, nsm = 0, per = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, route_kernel, kRouteThreads, 0) !=
       cudaSuccess)
     return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = nsm * per;
   return nsm * per;
 }
 
@@ -594,8 +559,11 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   RouteArgs args = a;
   void* params[] = {&args};
   prof_begin(K_ROUTE, s);
-  cudaError_t err = cudaLaunchCooperativeKernel((const void*)route_kernel, dim3(nblk),
-                                                dim3(kRouteThreads), params, 0, s);
+  // one block needs no co-residency guarantee: a plain launch is cheaper
+  cudaError_t err = nblk == 1 ? cudaLaunchKernel((const void*)route_kernel, dim3(1),
+                                                 dim3(kRouteThreads), params, 0, s)
+                              : cudaLaunchCooperativeKernel((const void*)route_kernel, dim3(nblk),
+                                                            dim3(kRouteThreads), params, 0, s);
   prof_end(K_ROUTE, s);
   return err;
 }
