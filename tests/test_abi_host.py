@@ -51,6 +51,7 @@ def test_check_dims():
         lily.make_dims(512, 2048, 4, 8, 512, 128),
         lily.make_dims(512, 2048, 256, 8, 500, 128),
         lily.make_dims(512, 2048, 256, 8, 512, 48),
+        lily.make_dims(512, 2048, 256, 8, 512, 256),
         lily.make_dims(512, 2048, 256, 8, 512, 128, group=32),
         lily.make_dims(20000, 2048, 256, 8, 512, 128),
         lily.make_dims(512, 2048, 256, 8, 512, 128, out_dtype=7),

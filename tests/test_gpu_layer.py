@@ -32,7 +32,7 @@ def _check_forward(L, rows=None, decode=False):
 
 # ------------------------------------------------------------ full-layer, small
 
-@pytest.mark.parametrize("bm", [32, 64, 128, 256])
+@pytest.mark.parametrize("bm", [32, 64, 128])
 def test_small_layer_all_tile_rows(oracle_lib, bm):
     _check_forward(Layer(synth.SHAPES["small"], seed=1000, tile_rows=bm))
 
@@ -99,8 +99,8 @@ def test_prefill2048_zipf_sampled_rows(oracle_lib):
     assert (counts == 0).any() and counts.max() > 256
 
 
-def test_prefill2048_uniform_sampled_rows_bm256(oracle_lib):
-    L = Layer(synth.SHAPES["prefill2048_zipf"], seed=3100, tile_rows=256)
+def test_prefill2048_uniform_sampled_rows_bm64(oracle_lib):
+    L = Layer(synth.SHAPES["prefill2048_zipf"], seed=3100, tile_rows=64)
     rows = np.random.default_rng(3).choice(2048, 24, replace=False)
     _check_forward(L, rows)
 

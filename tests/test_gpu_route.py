@@ -22,7 +22,7 @@ CASES = [
     ("decode1", synth.LayerShape(1, 2048, 256, 8, 512), 128, None),
     ("decode5", synth.LayerShape(5, 2048, 256, 8, 512), 128, None),
     ("bm32_2048", synth.LayerShape(2048, 2048, 256, 8, 512), 32, None),
-    ("bm256_600", synth.LayerShape(600, 1024, 64, 6, 256), 256, None),
+    ("bm64_600", synth.LayerShape(600, 1024, 64, 6, 256), 64, None),
     ("max_tokens", synth.LayerShape(16384, 128, 256, 8, 128), 64, None),
 ]
 

@@ -287,7 +287,7 @@ int lily_moe_check_dims(const lily_moe_dims* d) {
   if (d->group != 64) return LILY_ERR_UNSUPPORTED_SHAPE;
   if (d->out_dtype != LILY_DTYPE_BF16 && d->out_dtype != LILY_DTYPE_F32)
     return LILY_ERR_UNSUPPORTED_SHAPE;
-  if (d->tile_rows != 32 && d->tile_rows != 64 && d->tile_rows != 128 && d->tile_rows != 256)
+  if (d->tile_rows != 32 && d->tile_rows != 64 && d->tile_rows != 128)
     return LILY_ERR_UNSUPPORTED_SHAPE;
   if (gemm_stages(true, d->tile_rows, d->d_model) < 2 || gemm_stages(false, d->tile_rows, d->d_ff) < 2)
     return LILY_ERR_UNSUPPORTED_SHAPE;
@@ -529,8 +529,10 @@ int lily_moe_profile_read(double* total_ms, int64_t* launches) {
   for (auto& rec : g_prof_open) {
     float ms = 0.f;
     if (cudaEventSynchronize(rec.b) != cudaSuccess ||
-        cudaEventElapsedTime(&ms, rec.a, rec.b) != cudaSuccess)
+        cudaEventElapsedTime(&ms, rec.a, rec.b) != cudaSuccess) {
       rc = LILY_ERR_CUDA;
+      cudaGetLastError();  // do not leave this failure for the next call to find
+    }
     if (rec.kind >= 0 && rec.kind < LILY_KERNEL_KINDS) {
       if (total_ms) total_ms[rec.kind] += ms;
       if (launches) launches[rec.kind] += 1;

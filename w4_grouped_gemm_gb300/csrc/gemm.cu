@@ -38,7 +38,9 @@
 namespace lily {
 
 // Warp roles.  Warp 0: TMA producer.  Warp 1: TMEM owner + MMA issuer (one
-// thread).  Warps 2..9: dequant (one 128-row weight slice per K-step).
+// thread).  Warps 2..9: dequant (one 128-row weight slice per K-step), which
+// write the rebuilt weights straight into tensor memory (tcgen05.st): each
+// warp owns the TMEM lane quadrant warp % 4, i.e. weight rows 32*(warp%4)..+31.
 // Warps 10..13: epilogue (TMEM -> global), overlapped with the next item's
 // main loop through double-buffered accumulators; the epilogue warps also
 // fill the next item's scale/bias table ahead of the dequant warps.
@@ -46,26 +48,30 @@ constexpr int kNumDequantWarps = 8;
 constexpr int kNumEpiWarps = 4;
 constexpr int kEpiWarp0 = 2 + kNumDequantWarps;
 constexpr int kGemmThreads = 32 * (2 + kNumDequantWarps + kNumEpiWarps);  // 448
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
 constexpr int kPackedBytes = 128 * 32;  // 128 rows x 64 4-bit codes
-constexpr int kABytes = 128 * 128;      // 128 rows x 64 fp16
-constexpr int kNumBars = 2 * kMaxStages + 13;
+constexpr int kMaxA = 4;                // dequantised-A ring depth (TMEM)
+constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 9;
 
+// Tensor memory (512 columns x 128 lanes): accumulator sets first, then the
+// ring of dequantised A tiles (128 rows x 64 fp16 = 32 columns per matrix).
 template <bool GATEUP, int BM>
 struct GemmLayout {
   static constexpr int kMats = GATEUP ? 2 : 1;
   static constexpr int kBBytes = BM * 128;
   static constexpr int kStage = kBBytes + kMats * kPackedBytes;
-  static constexpr int kAccCols = GATEUP ? 2 * BM : BM;         // one accumulator set
-  static constexpr int kNumAcc = (2 * kAccCols <= 512) ? 2 : 1;  // TMEM double buffer
-  static constexpr uint32_t kTmemCols =
-      (kAccCols * kNumAcc <= 32) ? 32 : (uint32_t)(kAccCols * kNumAcc);
+  static constexpr int kAccCols = GATEUP ? 2 * BM : BM;  // one accumulator set
+  static constexpr int kNumAcc = (GATEUP ? BM <= 64 : BM <= 128) ? 2 : 1;
+  static constexpr int kAOff = kNumAcc * kAccCols;
+  static constexpr int kNumA =
+      (512 - kAOff) / (kMats * 32) < kMaxA ? (512 - kAOff) / (kMats * 32) : kMaxA;
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kNumA >= 2, "tensor memory too small for the A ring");
 };
 
 __host__ __device__ inline size_t gemm_fixed_bytes(int mats, int BM, int K, int nsb) {
   const int G = K / 64;
   return 1024                                  // alignment slack
-         + (size_t)2 * mats * kABytes          // dequantised A, double-buffered
          + (size_t)nsb * mats * G * 128 * 4    // scale/bias tables (one per item in flight)
          + kNumBars * 8                        // mbarriers
          + 16;                                 // abort flag, TMEM address
@@ -113,10 +119,14 @@ size_t gemm_smem_bytes(bool gateup, int BM, int K) {
 
 // Wait by lane 0 only, result broadcast: keeps every warp-collective op
 // (tcgen05.ld, __syncwarp, shuffles) convergent even when a wait gives up.
+// `spin` = latency-critical pipeline hand-off (poll) rather than a sleep.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+                                          uint32_t* status, bool spin = false) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0)
+    ok = (spin ? mbar_wait_spin(bar, parity, abort, status) : mbar_wait(bar, parity, abort, status))
+             ? 1
+             : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -226,15 +236,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
-  uint8_t* a_base = smem + (size_t)nstages * STAGE;
-  uint32_t* sb = (uint32_t*)(a_base + 2 * MATS * kABytes);  // [nsb][MATS][G][128] scale|bias<<16
+  uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][MATS][G][128] scale|bias<<16
   const int sb_words = MATS * G * 128;                       // one table
   uint64_t* bars = (uint64_t*)(sb + nsb * sb_words);
   uint64_t* full = bars;                      // [kMaxStages] TMA landed
   uint64_t* empty = bars + kMaxStages;        // [kMaxStages] stage consumed by the MMAs
-  uint64_t* afull = bars + 2 * kMaxStages;    // [2] dequantised A ready
-  uint64_t* aempty = afull + 2;               // [2] A consumed by the MMAs
-  uint64_t* accfull = aempty + 2;             // [2] accumulator set final
+  uint64_t* afull = bars + 2 * kMaxStages;    // [kMaxA] dequantised A ready in TMEM
+  uint64_t* aempty = afull + kMaxA;           // [kMaxA] A consumed by the MMAs
+  uint64_t* accfull = aempty + kMaxA;         // [2] accumulator set final
   uint64_t* accempty = accfull + 2;           // [2] accumulator set drained by the epilogue
   uint64_t* sbfull = accempty + 2;            // [2] scale table filled (epilogue -> dequant)
   uint64_t* sbempty = sbfull + 2;             // [2] scale table no longer read (dequant -> epilogue)
@@ -249,9 +258,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMaxA; ++b) {
       mbar_init(smem_u32(&afull[b]), kNumDequantWarps);
       mbar_init(smem_u32(&aempty[b]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&accfull[b]), 1);
       mbar_init(smem_u32(&accempty[b]), kNumEpiWarps);
       mbar_init(smem_u32(&sbfull[b]), kNumEpiWarps);
@@ -294,7 +305,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kk = 0; kk < G; ++kk, ++it) {
         const int s = it % nstages;
         if (it >= (uint32_t)nstages &&
-            !warp_wait(smem_u32(&empty[s]), ((it / nstages) + 1) & 1, abort, a.status)) {
+            !warp_wait(smem_u32(&empty[s]), ((it / nstages) + 1) & 1, abort, a.status, true)) {
           ok = false;
           break;
         }
@@ -332,9 +343,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t dacc = tmem + ab * L::kAccCols;
         for (int kk = 0; kk < G; ++kk, ++it) {
-          const int s = it % nstages, b = it & 1;
-          if (!mbar_wait(smem_u32(&afull[b]), (it >> 1) & 1, abort, a.status) ||
-              !mbar_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status)) {
+          const int s = it % nstages, b = it % L::kNumA;
+          if (!mbar_wait_spin(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status) ||
+              !mbar_wait_spin(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status)) {
             ok = false;
             break;
           }
@@ -342,11 +353,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t bsm = smem_u32(stage_base + (size_t)s * STAGE);
 #pragma unroll
           for (int m = 0; m < MATS; ++m) {
-            const uint32_t asm_ = smem_u32(a_base + (size_t)(b * MATS + m) * kABytes);
+            const uint32_t at = tmem + L::kAOff + (b * MATS + m) * 32;  // A tile in TMEM
 #pragma unroll
             for (int k16 = 0; k16 < 4; ++k16)
-              mma_f16(dacc + m * BM, sdesc_sw128(asm_ + k16 * 32), sdesc_sw128(bsm + k16 * 32),
-                      idesc, (kk | k16) != 0);
+              mma_f16_ts(dacc + m * BM, at + k16 * 8, sdesc_sw128(bsm + k16 * 32), idesc,
+                         (kk | k16) != 0);
           }
           mma_commit(smem_u32(&empty[s]));
           mma_commit(smem_u32(&aempty[b]));
@@ -360,11 +371,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ================================================= dequant
-    const int i = threadIdx.x - 64;
-    int mat, r, c0;
-    if (GATEUP) { mat = i >> 7; r = i & 127; c0 = 0; }
-    else        { mat = 0;      r = i >> 1;  c0 = (i & 1) * 4; }
-    const uint32_t swz = (uint32_t)(r & 7);
+    // gate/up: warps 2..5 rebuild the gate slice, 6..9 the up slice (one
+    // weight row per lane); down: warps 2..5 take K elements 0..31 of each
+    // row, 6..9 elements 32..63.
+    const int q = warp & 3;
+    const int r = q * 32 + lane;          // weight row within the slice = TMEM lane
+    const int hsel = (warp - 2) >> 2;
+    const int mat = GATEUP ? hsel : 0;
+    const uint32_t tlane = (uint32_t)(q * 32) << 16;
     uint32_t it = 0, j = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
@@ -374,19 +388,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!warp_wait(smem_u32(&sbfull[slot]), (j / nsb) & 1, abort, a.status)) break;
       const uint32_t* sbs = sb + slot * sb_words;
       for (int kk = 0; kk < G; ++kk, ++it) {
-        const int s = it % nstages, b = it & 1;
-        bool got = warp_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status);
-        if (got && it >= 2) got = warp_wait(smem_u32(&aempty[b]), ((it >> 1) + 1) & 1, abort, a.status);
+        const int s = it % nstages, b = it % L::kNumA;
+        bool got = warp_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status, true);
+        if (got && it >= (uint32_t)L::kNumA)
+          got = warp_wait(smem_u32(&aempty[b]), ((it / L::kNumA) + 1) & 1, abort, a.status, true);
         if (!got) {
           ok = false;
           break;
         }
-        const uint8_t* pk =
-            stage_base + (size_t)s * STAGE + BBYTES + mat * kPackedBytes + r * 32 + c0 * 4;
+        const uint8_t* pk = stage_base + (size_t)s * STAGE + BBYTES + mat * kPackedBytes + r * 32;
         const uint32_t sbv = sbs[(mat * G + kk) * 128 + r];
         const uint32_t s2 = prmt(sbv, sbv, 0x1010u), b2 = prmt(sbv, sbv, 0x3232u);
-        const uint32_t arow = smem_u32(a_base + (size_t)(b * MATS + mat) * kABytes) + r * 128;
-        uint32_t wd[8];
+        const uint32_t at = tmem + tlane + L::kAOff + (b * MATS + mat) * 32;
         if (GATEUP) {
           // a 32-byte row is read as two 16-byte loads; rows 4..7 of every 8
           // issue the halves in the other order so that each 8 consecutive
@@ -395,22 +408,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint4 v0 = *reinterpret_cast<const uint4*>(pk + (sw ? 16 : 0));
           const uint4 v1 = *reinterpret_cast<const uint4*>(pk + (sw ? 0 : 16));
           const uint4 lo = sw ? v1 : v0, hi = sw ? v0 : v1;
-          wd[0] = lo.x; wd[1] = lo.y; wd[2] = lo.z; wd[3] = lo.w;
-          wd[4] = hi.x; wd[5] = hi.y; wd[6] = hi.z; wd[7] = hi.w;
-        } else {
-          const uint4 v0 = *reinterpret_cast<const uint4*>(pk);
-          wd[0] = v0.x; wd[1] = v0.y; wd[2] = v0.z; wd[3] = v0.w;
-        }
+          const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          uint32_t o[32];
 #pragma unroll
-        for (int jj = 0; jj < (GATEUP ? 8 : 4); ++jj) {  // chunk order uniform across lanes
-          uint32_t o[4];
-          dequant8(wd[jj], s2, b2, o);
-          const uint32_t chunk = (uint32_t)(c0 + jj);
-          st_shared_v4(arow + ((chunk ^ swz) << 4), o[0], o[1], o[2], o[3]);
+          for (int jj = 0; jj < 8; ++jj) {
+            uint32_t t4[4];
+            dequant8(wd[jj], s2, b2, t4);
+            o[4 * jj] = t4[0]; o[4 * jj + 1] = t4[1]; o[4 * jj + 2] = t4[2]; o[4 * jj + 3] = t4[3];
+          }
+          tmem_st32(at, o);
+        } else {
+          const uint4 v0 = *reinterpret_cast<const uint4*>(pk + hsel * 16);
+          const uint32_t wd[4] = {v0.x, v0.y, v0.z, v0.w};
+          uint32_t o[16];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            uint32_t t4[4];
+            dequant8(wd[jj], s2, b2, t4);
+            o[4 * jj] = t4[0]; o[4 * jj + 1] = t4[1]; o[4 * jj + 2] = t4[2]; o[4 * jj + 3] = t4[3];
+          }
+          tmem_st16(at + hsel * 16, o);
         }
-        // every lane makes its stores visible to the tensor core, then one
-        // arrive per warp (256 arrivals on one barrier would serialise)
-        fence_proxy_async_smem();
+        // the stores must be complete before the MMA issuer is told: wait,
+        // order them before the arrive, then one arrive per warp
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
       }
@@ -620,7 +642,6 @@ static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const C
     case 32: return launch_gemm_bm<GATEUP, 32>(a, q0, q1, b, b2, s);
     case 64: return launch_gemm_bm<GATEUP, 64>(a, q0, q1, b, b2, s);
     case 128: return launch_gemm_bm<GATEUP, 128>(a, q0, q1, b, b2, s);
-    case 256: return launch_gemm_bm<GATEUP, 256>(a, q0, q1, b, b2, s);
     default: return cudaErrorInvalidValue;
   }
 }
