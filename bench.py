@@ -235,7 +235,9 @@ def run_lily(args, world, rank, local):
     dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
     # several layers of weights, rotated per step, so no step finds the
     # previous step's weights in L2 (each layer's weights are 455 MB)
-    nl = args.layers
+    # decode touches ~16 MB per layer: rotate >= 16 layers so no step finds
+    # its weights in the 126 MB L2
+    nl = max(args.layers, 16) if decode else args.layers
     layers = []
     for l in range(nl):
         inp = synth.make_layer(shape, 1000 * 2 + 17 * l + 101 * rank, device=dev, zipf_s=zipf)
@@ -246,9 +248,9 @@ def run_lily(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     call = lily.lily_moe_decode if decode else lily.lily_moe_forward
 
-    def step(i):
+    def step(i):  # on the current stream (the capture stream inside a graph)
         x, w = layers[i % nl]
-        call(dims, x, w, r, y, wsb, stream)
+        call(dims, x, w, r, y, wsb, None)
 
     for i in range(args.warmup):
         step(i)
@@ -261,6 +263,25 @@ def run_lily(args, world, rank, local):
         torch.cuda.synchronize()
         counts_by_layer.append(r.counts.cpu().numpy().copy())
 
+    # The timed steps replay a CUDA graph of the C-ABI calls (one command
+    # buffer per group of nl layer steps), so host submission does not gate
+    # the device; fall back to eager launches if capture is not possible.
+    graph = None
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(nl):
+                    step(i)
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:  # noqa: BLE001
+            print(f"graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
+    reps = max(1, args.steps // nl) if graph is not None else args.steps
+    steps_timed = reps * nl if graph is not None else args.steps
+
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -268,26 +289,51 @@ def run_lily(args, world, rank, local):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    lily.lily_moe_profile_enable(True)
-    lily.lily_moe_profile_read()  # reset
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.perf_counter()
     e0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    if graph is not None:
+        for _ in range(reps):
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
     if world > 1:
         torch.distributed.barrier()
-    lily.lily_moe_profile_enable(False)
-    prof = lily.lily_moe_profile_read()
     ms = e0.elapsed_time(e1)
     if sampler:
         time.sleep(0.2)
         sampler.stop()
     ms = max_over_ranks(ms, world, dev)
+    args.steps = steps_timed
+
+    # Per-kernel device time: the library's CUDA events around every kernel,
+    # recorded on the launch stream.  The same steps are captured with the
+    # event records inside the graph and replayed once (eager when no graph).
+    prof_steps = min(steps_timed, 40 * nl)
+    lily.lily_moe_profile_enable(True)
+    lily.lily_moe_profile_read()
+    for i in range(prof_steps):  # eager pass: also fills the library's event pool
+        step(i)
+    torch.cuda.synchronize()
+    prof = lily.lily_moe_profile_read()
+    if graph is not None:
+        try:
+            pgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(pgraph):
+                for i in range(prof_steps):
+                    step(i)
+            pgraph.replay()  # its event records now hold this replay's times
+            torch.cuda.synchronize()
+            prof = lily.lily_moe_profile_read()
+            del pgraph
+        except Exception as exc:  # noqa: BLE001
+            print(f"profiled graph unavailable ({exc}); eager per-kernel times", file=sys.stderr)
+    lily.lily_moe_profile_enable(False)
     status = lily.lily_moe_status(wsb)
     if status:
         raise RuntimeError(f"device status bits set: {status}")
@@ -348,7 +394,8 @@ def run_lily(args, world, rank, local):
                     "frac": achieved / hbm, "traffic": NCU_TRAFFIC.get(key),
                     "kernel": dom, "algorithmic_bytes_per_launch": dbytes,
                     "peak_source": f"hbm_gbs of {peak_src} peaks (copy bandwidth)"}
-    launches = sum(v["launches"] for n, v in prof.items() if n != "memset_acc")
+    per_step = sum(v["launches"] for n, v in prof.items() if n != "memset_acc") / max(prof_steps, 1)
+    launches = int(round(per_step * args.steps))
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
 
     # CPU baseline: the oracle, bounded sample of the same workload
@@ -369,6 +416,7 @@ def run_lily(args, world, rank, local):
             "d_ff": F, "zipf_s": zipf, "tile_rows": args.tile_rows,
             "path": "decode GEMV" if decode else "prefill grouped GEMM",
             "l2": f"inputs larger than L2: {nl} layers of weights rotated per step",
+            "launch": "CUDA graph replay of the C-ABI calls" if graph is not None else "eager",
             "parallelism": f"token data parallel x{world} (replicated weights, no exchange)",
             "experts_touched_per_step": float(np.mean(touched_l)),
             "layer_algorithmic_bytes": step_bytes, "layer_flops": flops,
@@ -398,6 +446,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
+    ap.add_argument("--eager", action="store_true", help="time eager launches, no CUDA graph")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_info()

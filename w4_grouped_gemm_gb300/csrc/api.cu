@@ -23,6 +23,16 @@ std::vector<cudaEvent_t> g_prof_pool;
 int g_prof_kind = -1;
 cudaEvent_t g_prof_start = nullptr;
 
+// Record e on s; inside a stream capture the record must be an external
+// event-record node so that it records each time the graph runs.
+void prof_record(cudaEvent_t e, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, s);
+}
+
 cudaEvent_t prof_event() {
   if (!g_prof_pool.empty()) {
     cudaEvent_t e = g_prof_pool.back();
@@ -40,7 +50,7 @@ void prof_begin(int kind, cudaStream_t s) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   g_prof_kind = kind;
   g_prof_start = prof_event();
-  cudaEventRecord(g_prof_start, s);
+  prof_record(g_prof_start, s);
 }
 
 void prof_end(int kind, cudaStream_t s) {
@@ -48,7 +58,7 @@ void prof_end(int kind, cudaStream_t s) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
   if (g_prof_kind != kind || !g_prof_start) return;
   cudaEvent_t e = prof_event();
-  cudaEventRecord(e, s);
+  prof_record(e, s);
   g_prof_open.push_back({kind, g_prof_start, e});
   g_prof_start = nullptr;
   g_prof_kind = -1;

@@ -117,19 +117,6 @@ size_t gemm_smem_bytes(bool gateup, int BM, int K) {
   return gemm_fixed_bytes(gateup ? 2 : 1, BM, K, n) + (size_t)s * gemm_stage_bytes(gateup, BM);
 }
 
-// Wait by lane 0 only, result broadcast: keeps every warp-collective op
-// (tcgen05.ld, __syncwarp, shuffles) convergent even when a wait gives up.
-// `spin` = latency-critical pipeline hand-off (poll) rather than a sleep.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status, bool spin = false) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0)
-    ok = (spin ? mbar_wait_spin(bar, parity, abort, status) : mbar_wait(bar, parity, abort, status))
-             ? 1
-             : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
 // One work item = one block-map tile (or shared-expert tile) x one 128-row
 // slice of the weight matrix.  Items are numbered tile-major so the slices of
 // one tile, and the tiles of one expert, run at the same time and share the
@@ -309,16 +296,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
+        // whole warp, warp-uniform operands; one elected lane issues
         const uint32_t fb = smem_u32(&full[s]);
-        uint8_t* st = stage_base + (size_t)s * STAGE;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, tx_bytes);
-          tma_load_2d(smem_u32(st + BBYTES), &tm_q0, kk * 32, wrow, fb);
-          if (GATEUP) tma_load_2d(smem_u32(st + BBYTES + kPackedBytes), &tm_q1, kk * 32, wrow, fb);
-          for (int r16 = 0; r16 < N; r16 += 16)  // the tile's N rows, 16 rows per box
-            tma_load_2d(smem_u32(st + r16 * 128), tmb, kk * 64, brow + r16, fb);
-        }
-        __syncwarp();
+        const uint32_t st = smem_u32(stage_base + (size_t)s * STAGE);
+        mbar_arrive_expect_tx_warp(fb, tx_bytes);
+        tma_load_2d_warp(st + BBYTES, &tm_q0, kk * 32, wrow, fb);
+        if (GATEUP) tma_load_2d_warp(st + BBYTES + kPackedBytes, &tm_q1, kk * 32, wrow, fb);
+        for (int r16 = 0; r16 < N; r16 += 16)  // the tile's N rows, 16 rows per box
+          tma_load_2d_warp(st + r16 * 128, tmb, kk * 64, brow + r16, fb);
       }
     }
     if (*abort && lane == 0) {  // let copies still in flight land before exit
@@ -328,46 +313,46 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ================================================= MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, titem = 0;
-      bool ok = true;
-      for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
-        Item itm;
-        if (!get_item<BM>(a, w, nslices, nsh, P, itm)) continue;
-        const int N = (itm.rows + 15) & ~15;
-        const uint32_t idesc = idesc_f16_f32(128, N);
-        const int ab = titem % NACC;
-        if (titem >= (uint32_t)NACC &&
-            !mbar_wait(smem_u32(&accempty[ab]), ((titem / NACC) + 1) & 1, abort, a.status))
+    // The whole warp runs the loop with warp-uniform operands; one elected
+    // lane issues each MMA and commit.
+    uint32_t it = 0, titem = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      Item itm;
+      if (!get_item<BM>(a, w, nslices, nsh, P, itm)) continue;
+      const int N = (itm.rows + 15) & ~15;
+      const uint32_t idesc = idesc_f16_f32(128, N);
+      const int ab = titem % NACC;
+      if (titem >= (uint32_t)NACC &&
+          !warp_wait(smem_u32(&accempty[ab]), ((titem / NACC) + 1) & 1, abort, a.status))
+        break;
+      tc_fence_after();
+      const uint32_t dacc = tmem + ab * L::kAccCols;
+      for (int kk = 0; kk < G; ++kk, ++it) {
+        const int s = it % nstages, b = it % L::kNumA;
+        if (!warp_wait(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status, true) ||
+            !warp_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status, true)) {
+          ok = false;
           break;
-        tc_fence_after();
-        const uint32_t dacc = tmem + ab * L::kAccCols;
-        for (int kk = 0; kk < G; ++kk, ++it) {
-          const int s = it % nstages, b = it % L::kNumA;
-          if (!mbar_wait_spin(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status) ||
-              !mbar_wait_spin(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t bsm = smem_u32(stage_base + (size_t)s * STAGE);
-#pragma unroll
-          for (int m = 0; m < MATS; ++m) {
-            const uint32_t at = tmem + L::kAOff + (b * MATS + m) * 32;  // A tile in TMEM
-#pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16)
-              mma_f16_ts(dacc + m * BM, at + k16 * 8, sdesc_sw128(bsm + k16 * 32), idesc,
-                         (kk | k16) != 0);
-          }
-          mma_commit(smem_u32(&empty[s]));
-          mma_commit(smem_u32(&aempty[b]));
         }
-        if (!ok) break;
-        mma_commit(smem_u32(&accfull[ab]));
-        ++titem;
+        tc_fence_after();
+        const uint64_t bdesc = sdesc_sw128(smem_u32(stage_base + (size_t)s * STAGE));
+#pragma unroll
+        for (int m = 0; m < MATS; ++m) {
+          const uint32_t at = tmem + L::kAOff + (b * MATS + m) * 32;  // A tile in TMEM
+#pragma unroll
+          for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
+            mma_f16_ts_warp(dacc + m * BM, at + k16 * 8, bdesc + 2 * k16, idesc,
+                            (kk | k16) != 0);
+        }
+        mma_commit_warp(smem_u32(&empty[s]));
+        mma_commit_warp(smem_u32(&aempty[b]));
       }
-      mma_commit(smem_u32(drain));  // arrives once every MMA above has finished
+      if (!ok) break;
+      mma_commit_warp(smem_u32(&accfull[ab]));
+      ++titem;
     }
+    mma_commit_warp(smem_u32(drain));  // arrives once every MMA above has finished
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ================================================= dequant
