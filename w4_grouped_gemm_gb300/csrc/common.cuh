@@ -124,6 +124,44 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait run by every lane of a converged warp: all lanes poll
+// test_wait and a vote keeps the outcome warp-uniform, so the warp stays
+// converged without a divergent lane-0 loop and a broadcast.  Used by the
+// warp that issues MMAs, where every synchronising instruction waits for
+// the MMAs already issued to drain, so the fewer the better.  Same limits and
+// abort protocol as mbar_wait.
+__device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              uint32_t* status) {
+  if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (__all_sync(0xffffffffu, mbar_test_wait(bar, parity))) return true;
+    if ((n & 255u) == 0) {
+      if (__any_sync(0xffffffffu, *abort != 0)) return false;
+      if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitLimitNs)) {
+        if ((threadIdx.x & 31) == 0) {
+          *abort = 1;
+          set_status(status, LILY_STATUS_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -314,7 +314,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ================================================= MMA issuer
     // The whole warp runs the loop with warp-uniform operands; one elected
-    // lane issues each MMA and commit.
+    // lane issues each MMA and commit.  It waits on afull alone: the dequant
+    // warps arrive there only after their own wait on the stage's TMA
+    // barrier, so a full A buffer implies that the stage's token rows landed.
     uint32_t it = 0, titem = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
@@ -330,8 +332,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t dacc = tmem + ab * L::kAccCols;
       for (int kk = 0; kk < G; ++kk, ++it) {
         const int s = it % nstages, b = it % L::kNumA;
-        if (!warp_wait(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status, true) ||
-            !warp_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status, true)) {
+        if (!warp_wait_all(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status)) {
           ok = false;
           break;
         }

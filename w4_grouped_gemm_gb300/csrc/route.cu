@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const uint32_t idesc = idesc_bf16_f32(128, NE);
     for (int i = 0; i < nk; ++i) {
       const int st = i % kRtStages;
-      if (!warp_wait(smem_u32(&full[st]), (i / kRtStages) & 1, abort, status)) break;
+      if (!warp_wait_all(smem_u32(&full[st]), (i / kRtStages) & 1, abort, status)) break;
       tc_fence_after();
       const uint32_t a0 = smem_u32(smem + (size_t)st * STAGE);
       const uint64_t ad = sdesc_sw128(a0), bd = sdesc_sw128(a0 + ABYTES);
