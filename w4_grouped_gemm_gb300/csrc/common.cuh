@@ -162,6 +162,31 @@ __device__ __forceinline__ bool warp_wait_all(uint32_t bar, uint32_t parity, vol
   }
 }
 
+// Both phases (bar0, parity0) and (bar1, parity1), or only the first when
+// !need1: one converged poll and one vote per attempt (see warp_wait_all).
+__device__ __forceinline__ bool warp_wait_all2(uint32_t bar0, uint32_t parity0, uint32_t bar1,
+                                               uint32_t parity1, bool need1, volatile int* abort,
+                                               uint32_t* status) {
+  auto ready = [&]() {
+    return mbar_test_wait(bar0, parity0) && (!need1 || mbar_test_wait(bar1, parity1));
+  };
+  if (__all_sync(0xffffffffu, ready())) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (__all_sync(0xffffffffu, ready())) return true;
+    if ((n & 255u) == 0) {
+      if (__any_sync(0xffffffffu, *abort != 0)) return false;
+      if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > kWaitLimitNs)) {
+        if ((threadIdx.x & 31) == 0) {
+          *abort = 1;
+          set_status(status, LILY_STATUS_TIMEOUT);
+        }
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

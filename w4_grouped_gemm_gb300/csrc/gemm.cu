@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int kk = 0; kk < G; ++kk, ++it) {
         const int s = it % nstages;
         if (it >= (uint32_t)nstages &&
-            !warp_wait(smem_u32(&empty[s]), ((it / nstages) + 1) & 1, abort, a.status, true)) {
+            !warp_wait_all(smem_u32(&empty[s]), ((it / nstages) + 1) & 1, abort, a.status)) {
           ok = false;
           break;
         }
@@ -375,9 +375,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t* sbs = sb + slot * sb_words;
       for (int kk = 0; kk < G; ++kk, ++it) {
         const int s = it % nstages, b = it % L::kNumA;
-        bool got = warp_wait(smem_u32(&full[s]), (it / nstages) & 1, abort, a.status, true);
-        if (got && it >= (uint32_t)L::kNumA)
-          got = warp_wait(smem_u32(&aempty[b]), ((it / L::kNumA) + 1) & 1, abort, a.status, true);
+        // the stage's TMA landed and the A buffer was consumed (one vote)
+        const bool got = warp_wait_all2(smem_u32(&full[s]), (it / nstages) & 1,
+                                        smem_u32(&aempty[b]), ((it / L::kNumA) + 1) & 1,
+                                        it >= (uint32_t)L::kNumA, abort, a.status);
         if (!got) {
           ok = false;
           break;
