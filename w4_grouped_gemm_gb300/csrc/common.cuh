@@ -427,15 +427,20 @@ __device__ __forceinline__ uint16_t bf16_to_f16_bits(uint16_t b) {
 // order (q0, q4, q1, q5, q2, q6, q3, q7) -- the order in which one LOP3 per
 // pair extracts them.  The other GEMM operand stores every 8-element K chunk
 // in the same order (kchunk_pos), so the dot products are unchanged.  Each
-// weight is round_fp16(scale * q + bias): 1024 + q is exact in fp16,
-// subtracting 1024 is exact, and the f16x2 FMA rounds once.
+// weight is round_fp16(scale * q + bias).  A code in bits 0..3 of a 16-bit
+// half OR-ed into fp16 1024 (0x6400, unit spacing) reads as 1024 + q; a code
+// in bits 4..7 OR-ed into fp16 64 (0x5400, spacing 1/16) reads as 64 + q, so
+// two of the four pairs need no shift.  Both sums and the subtractions are
+// exact; the f16x2 FMA rounds once.
 __device__ __forceinline__ void dequant8(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
-  const uint32_t kMagic = 0x64006400u;  // fp16 pair (1024, 1024)
-  const uint32_t kMask = 0x000F000Fu;
-  o[0] = h2_fma(s2, h2_sub(lop3_and_or(w, kMask, kMagic), kMagic), b2);        // (q0, q4)
-  o[1] = h2_fma(s2, h2_sub(lop3_and_or(w >> 4, kMask, kMagic), kMagic), b2);   // (q1, q5)
-  o[2] = h2_fma(s2, h2_sub(lop3_and_or(w >> 8, kMask, kMagic), kMagic), b2);   // (q2, q6)
-  o[3] = h2_fma(s2, h2_sub(lop3_and_or(w >> 12, kMask, kMagic), kMagic), b2);  // (q3, q7)
+  const uint32_t kMagicLo = 0x64006400u;  // fp16 pair (1024, 1024)
+  const uint32_t kMagicHi = 0x54005400u;  // fp16 pair (64, 64)
+  const uint32_t kMaskLo = 0x000F000Fu, kMaskHi = 0x00F000F0u;
+  const uint32_t w8 = w >> 8;
+  o[0] = h2_fma(s2, h2_sub(lop3_and_or(w, kMaskLo, kMagicLo), kMagicLo), b2);   // (q0, q4)
+  o[1] = h2_fma(s2, h2_sub(lop3_and_or(w, kMaskHi, kMagicHi), kMagicHi), b2);   // (q1, q5)
+  o[2] = h2_fma(s2, h2_sub(lop3_and_or(w8, kMaskLo, kMagicLo), kMagicLo), b2);  // (q2, q6)
+  o[3] = h2_fma(s2, h2_sub(lop3_and_or(w8, kMaskHi, kMagicHi), kMagicHi), b2);  // (q3, q7)
 }
 // Position of element e (0..7) of an 8-element K chunk in that order.
 __host__ __device__ __forceinline__ int kchunk_pos(int e) { return ((e & 3) << 1) | (e >> 2); }

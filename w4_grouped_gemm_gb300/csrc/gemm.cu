@@ -117,6 +117,18 @@ size_t gemm_smem_bytes(bool gateup, int BM, int K) {
   return gemm_fixed_bytes(gateup ? 2 : 1, BM, K, n) + (size_t)s * gemm_stage_bytes(gateup, BM);
 }
 
+// Position in a ring of n slots: slot index and the parity of its use count
+// (it % n and (it / n) & 1 for the it-th use), advanced without a division.
+struct Ring {
+  uint32_t idx = 0, ph = 0;
+  __device__ __forceinline__ void next(uint32_t n) {
+    if (++idx == n) {
+      idx = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 // One work item = one block-map tile (or shared-expert tile) x one 128-row
 // slice of the weight matrix.  Items are numbered tile-major so the slices of
 // one tile, and the tiles of one expert, run at the same time and share the
@@ -275,6 +287,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     // ================================================= TMA producer
     uint32_t it = 0;  // K-steps issued by this CTA, across items
+    Ring rs;          // stage ring position of step it
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
       Item itm;
@@ -289,10 +302,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const CUtensorMap* tmb = (GATEUP && itm.shared) ? &tm_b2 : &tm_b;
       const int brow = (GATEUP && itm.shared) ? itm.row0 - P : itm.row0;
       const uint32_t tx_bytes = MATS * kPackedBytes + N * 128;
-      for (int kk = 0; kk < G; ++kk, ++it) {
-        const int s = it % nstages;
+      for (int kk = 0; kk < G; ++kk, ++it, rs.next(nstages)) {
+        const int s = rs.idx;
         if (it >= (uint32_t)nstages &&
-            !warp_wait_all(smem_u32(&empty[s]), ((it / nstages) + 1) & 1, abort, a.status)) {
+            !warp_wait_all(smem_u32(&empty[s]), rs.ph ^ 1u, abort, a.status)) {
           ok = false;
           break;
         }
@@ -318,6 +331,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // warps arrive there only after their own wait on the stage's TMA
     // barrier, so a full A buffer implies that the stage's token rows landed.
     uint32_t it = 0, titem = 0;
+    Ring rs;  // stage ring position of step it
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
       Item itm;
@@ -330,8 +344,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * L::kAccCols;
-      for (int kk = 0; kk < G; ++kk, ++it) {
-        const int s = it % nstages, b = it % L::kNumA;
+      for (int kk = 0; kk < G; ++kk, ++it, rs.next(nstages)) {
+        const int s = rs.idx, b = it % L::kNumA;
         if (!warp_wait_all(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status)) {
           ok = false;
           break;
@@ -366,6 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int mat = GATEUP ? hsel : 0;
     const uint32_t tlane = (uint32_t)(q * 32) << 16;
     uint32_t it = 0, j = 0;
+    Ring rs;  // stage ring position of step it
     bool ok = true;
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
       Item itm;
@@ -373,10 +388,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int slot = j % nsb;
       if (!warp_wait(smem_u32(&sbfull[slot]), (j / nsb) & 1, abort, a.status)) break;
       const uint32_t* sbs = sb + slot * sb_words;
-      for (int kk = 0; kk < G; ++kk, ++it) {
-        const int s = it % nstages, b = it % L::kNumA;
+      for (int kk = 0; kk < G; ++kk, ++it, rs.next(nstages)) {
+        const int s = rs.idx, b = it % L::kNumA;
         // the stage's TMA landed and the A buffer was consumed (one vote)
-        const bool got = warp_wait_all2(smem_u32(&full[s]), (it / nstages) & 1,
+        const bool got = warp_wait_all2(smem_u32(&full[s]), rs.ph,
                                         smem_u32(&aempty[b]), ((it / L::kNumA) + 1) & 1,
                                         it >= (uint32_t)L::kNumA, abort, a.status);
         if (!got) {
