@@ -402,14 +402,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t sbv = sbs[(mat * G + kk) * 128 + r];
         const uint32_t s2 = prmt(sbv, sbv, 0x1010u), b2 = prmt(sbv, sbv, 0x3232u);
         const uint32_t at = tmem + tlane + L::kAOff + (b * MATS + mat) * 32;
+        // the stage holds the codes with the 32-byte TMA swizzle: half h of
+        // row r sits at 16 * (h ^ sw), which spreads each 8 consecutive
+        // lanes' loads over all eight 16-byte bank groups
+        const int sw = (r >> 2) & 1;
         if (GATEUP) {
-          // a 32-byte row is read as two 16-byte loads; rows 4..7 of every 8
-          // issue the halves in the other order so that each 8 consecutive
-          // lanes hit all eight 16-byte bank groups, then swap back
-          const int sw = (r >> 2) & 1;
-          const uint4 v0 = *reinterpret_cast<const uint4*>(pk + (sw ? 16 : 0));
-          const uint4 v1 = *reinterpret_cast<const uint4*>(pk + (sw ? 0 : 16));
-          const uint4 lo = sw ? v1 : v0, hi = sw ? v0 : v1;
+          const uint4 lo = *reinterpret_cast<const uint4*>(pk + 16 * sw);
+          const uint4 hi = *reinterpret_cast<const uint4*>(pk + 16 * (sw ^ 1));
           const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
           uint32_t o[32];
 #pragma unroll
@@ -420,7 +419,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tmem_st32(at, o);
         } else {
-          const uint4 v0 = *reinterpret_cast<const uint4*>(pk + hsel * 16);
+          const uint4 v0 = *reinterpret_cast<const uint4*>(pk + 16 * (hsel ^ sw));
           const uint32_t wd[4] = {v0.x, v0.y, v0.z, v0.w};
           uint32_t o[16];
 #pragma unroll
@@ -648,12 +647,15 @@ static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const C
   }
 }
 
+// Packed codes: boxes of 128 rows x 32 bytes with the 32-byte swizzle (the
+// two 16-byte halves of row r swap places when bit 2 of r is set), so that the
+// dequant lanes' 16-byte loads are free of bank conflicts.
 static bool packed_map(CUtensorMap* tm, const uint8_t* q, int K, int rows) {
   uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)rows};
   uint64_t strides[1] = {(uint64_t)K / 2};
   uint32_t box[2] = {32, 128};
   return encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)q, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_NONE) == CUDA_SUCCESS;
+                      CU_TENSOR_MAP_SWIZZLE_32B) == CUDA_SUCCESS;
 }
 
 static bool f16_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, int box_rows) {
