@@ -441,7 +441,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["lily", "reference"], default="lily")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--tile-rows", type=int, default=128)
+    ap.add_argument("--tile-rows", type=int, default=64)
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -53,18 +53,29 @@ constexpr int kPackedBytes = 128 * 32;  // 128 rows x 64 4-bit codes
 constexpr int kMaxA = 4;                // dequantised-A ring depth (TMEM)
 constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 9;
 
+// Quantisation groups (64 K each) per K-step: the down GEMM has half the
+// weight rows per step of gate/up, so it takes two groups per step and the
+// fixed per-step hand-offs are paid half as often.
+__host__ __device__ constexpr int groups_per_step(bool gateup) { return gateup ? 1 : 2; }
+
 // Tensor memory (512 columns x 128 lanes): accumulator sets first, then the
-// ring of dequantised A tiles (128 rows x 64 fp16 = 32 columns per matrix).
+// ring of dequantised A tiles (128 rows x 64 fp16 = 32 columns per matrix and
+// group).  A stage holds, per group, a 128-byte-swizzled tile of the token
+// rows (BM x 64 fp16) and the packed codes of each matrix (128 rows x 32 B).
 template <bool GATEUP, int BM>
 struct GemmLayout {
   static constexpr int kMats = GATEUP ? 2 : 1;
-  static constexpr int kBBytes = BM * 128;
-  static constexpr int kStage = kBBytes + kMats * kPackedBytes;
+  static constexpr int kGroups = groups_per_step(GATEUP);
+  static constexpr int kBTile = BM * 128;  // token rows of one group
+  static constexpr int kBBytes = kGroups * kBTile;
+  static constexpr int kStage = kBBytes + kMats * kGroups * kPackedBytes;
+  static constexpr int kACols = 32 * kGroups;  // one matrix's A tile
   static constexpr int kAccCols = GATEUP ? 2 * BM : BM;  // one accumulator set
   static constexpr int kNumAcc = (GATEUP ? BM <= 64 : BM <= 128) ? 2 : 1;
   static constexpr int kAOff = kNumAcc * kAccCols;
-  static constexpr int kNumA =
-      (512 - kAOff) / (kMats * 32) < kMaxA ? (512 - kAOff) / (kMats * 32) : kMaxA;
+  static constexpr int kNumA = (512 - kAOff) / (kMats * kACols) < kMaxA
+                                   ? (512 - kAOff) / (kMats * kACols)
+                                   : kMaxA;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kNumA >= 2, "tensor memory too small for the A ring");
 };
@@ -78,7 +89,8 @@ __host__ __device__ inline size_t gemm_fixed_bytes(int mats, int BM, int K, int 
 }
 
 size_t gemm_stage_bytes(bool gateup, int BM) {
-  return (size_t)BM * 128 + (gateup ? 2 : 1) * kPackedBytes;
+  const int kg = groups_per_step(gateup);
+  return (size_t)kg * ((size_t)BM * 128 + (gateup ? 2 : 1) * kPackedBytes);
 }
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
@@ -207,6 +219,21 @@ __device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint16_t
   }
 }
 
+// Down epilogue: lane l's row (cb + l of the item, clamped to its last row):
+// the token it belongs to and its gate weight (1 for shared-expert rows).
+__device__ __forceinline__ void row_token_gate(const GemmArgs& a, const Item& it, int cb, int lane,
+                                               int P, int& tok, float& g) {
+  const int rj = it.row0 + min(cb + lane, it.rows - 1);
+  if (it.shared) {
+    tok = rj - P;
+    g = 1.f;
+  } else {
+    const int p = __ldg(a.perm + rj);
+    tok = p / a.k;
+    g = __ldg(a.gates + p);
+  }
+}
+
 // Persistent kernel: one CTA per SM loops over the work items.
 template <bool GATEUP, int BM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -223,7 +250,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int K = GATEUP ? a.d : a.F;     // reduction length
   const int NOUT = GATEUP ? a.F : a.d;  // output features of each matrix
-  const int G = K / 64;                 // K-steps = quantisation groups
+  constexpr int KG = L::kGroups;
+  const int G = K / 64;                 // quantisation groups
+  const int NST = G / KG;               // K-steps per item
   const int nslices = NOUT / 128;
   const int P = a.T * a.k;
   const int nsh = (a.T + BM - 1) / BM;
@@ -301,8 +330,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // for a shared-expert tile, x16 in token order); down reads H
       const CUtensorMap* tmb = (GATEUP && itm.shared) ? &tm_b2 : &tm_b;
       const int brow = (GATEUP && itm.shared) ? itm.row0 - P : itm.row0;
-      const uint32_t tx_bytes = MATS * kPackedBytes + N * 128;
-      for (int kk = 0; kk < G; ++kk, ++it, rs.next(nstages)) {
+      const uint32_t tx_bytes = KG * (MATS * kPackedBytes + N * 128);
+      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx;
         if (it >= (uint32_t)nstages &&
             !warp_wait_all(smem_u32(&empty[s]), rs.ph ^ 1u, abort, a.status)) {
@@ -313,10 +342,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t fb = smem_u32(&full[s]);
         const uint32_t st = smem_u32(stage_base + (size_t)s * STAGE);
         mbar_arrive_expect_tx_warp(fb, tx_bytes);
-        tma_load_2d_warp(st + BBYTES, &tm_q0, kk * 32, wrow, fb);
-        if (GATEUP) tma_load_2d_warp(st + BBYTES + kPackedBytes, &tm_q1, kk * 32, wrow, fb);
-        for (int r16 = 0; r16 < N; r16 += 16)  // the tile's N rows, 16 rows per box
-          tma_load_2d_warp(st + r16 * 128, tmb, kk * 64, brow + r16, fb);
+#pragma unroll
+        for (int g = 0; g < KG; ++g) {
+          const int grp = kk * KG + g;
+          tma_load_2d_warp(st + BBYTES + g * kPackedBytes, &tm_q0, grp * 32, wrow, fb);
+          if (GATEUP)
+            tma_load_2d_warp(st + BBYTES + (KG + g) * kPackedBytes, &tm_q1, grp * 32, wrow, fb);
+          for (int r16 = 0; r16 < N; r16 += 16)  // the tile's N rows, 16 rows per box
+            tma_load_2d_warp(st + g * L::kBTile + r16 * 128, tmb, grp * 64, brow + r16, fb);
+        }
       }
     }
     if (*abort && lane == 0) {  // let copies still in flight land before exit
@@ -344,21 +378,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * L::kAccCols;
-      for (int kk = 0; kk < G; ++kk, ++it, rs.next(nstages)) {
+      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx, b = it % L::kNumA;
         if (!warp_wait_all(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t bdesc = sdesc_sw128(smem_u32(stage_base + (size_t)s * STAGE));
+        const uint32_t sbase = smem_u32(stage_base + (size_t)s * STAGE);
 #pragma unroll
         for (int m = 0; m < MATS; ++m) {
-          const uint32_t at = tmem + L::kAOff + (b * MATS + m) * 32;  // A tile in TMEM
+          const uint32_t at = tmem + L::kAOff + (b * MATS + m) * L::kACols;  // A tile in TMEM
 #pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
-            mma_f16_ts_warp(dacc + m * BM, at + k16 * 8, bdesc + 2 * k16, idesc,
-                            (kk | k16) != 0);
+          for (int g = 0; g < KG; ++g) {
+            const uint64_t bdesc = sdesc_sw128(sbase + g * L::kBTile);
+#pragma unroll
+            for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
+              mma_f16_ts_warp(dacc + m * BM, at + g * 32 + k16 * 8, bdesc + 2 * k16, idesc,
+                              (kk | g | k16) != 0);
+          }
         }
         mma_commit_warp(smem_u32(&empty[s]));
         mma_commit_warp(smem_u32(&aempty[b]));
@@ -371,13 +409,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ================================================= dequant
-    // gate/up: warps 2..5 rebuild the gate slice, 6..9 the up slice (one
-    // weight row per lane); down: warps 2..5 take K elements 0..31 of each
-    // row, 6..9 elements 32..63.
+    // gate/up: warps 2..5 rebuild the gate slice, 6..9 the up slice; down:
+    // warps 2..5 take the first group of each K-step, 6..9 the second.  One
+    // weight row (64 codes of one group) per lane.
     const int q = warp & 3;
     const int r = q * 32 + lane;          // weight row within the slice = TMEM lane
     const int hsel = (warp - 2) >> 2;
     const int mat = GATEUP ? hsel : 0;
+    const int g = GATEUP ? 0 : hsel;      // group within the K-step
     const uint32_t tlane = (uint32_t)(q * 32) << 16;
     uint32_t it = 0, j = 0;
     Ring rs;  // stage ring position of step it
@@ -388,7 +427,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int slot = j % nsb;
       if (!warp_wait(smem_u32(&sbfull[slot]), (j / nsb) & 1, abort, a.status)) break;
       const uint32_t* sbs = sb + slot * sb_words;
-      for (int kk = 0; kk < G; ++kk, ++it, rs.next(nstages)) {
+      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx, b = it % L::kNumA;
         // the stage's TMA landed and the A buffer was consumed (one vote)
         const bool got = warp_wait_all2(smem_u32(&full[s]), rs.ph,
@@ -398,38 +437,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
-        const uint8_t* pk = stage_base + (size_t)s * STAGE + BBYTES + mat * kPackedBytes + r * 32;
-        const uint32_t sbv = sbs[(mat * G + kk) * 128 + r];
+        const uint8_t* pk = stage_base + (size_t)s * STAGE + BBYTES +
+                            (mat * KG + g) * kPackedBytes + r * 32;
+        const uint32_t sbv = sbs[(mat * G + kk * KG + g) * 128 + r];
         const uint32_t s2 = prmt(sbv, sbv, 0x1010u), b2 = prmt(sbv, sbv, 0x3232u);
-        const uint32_t at = tmem + tlane + L::kAOff + (b * MATS + mat) * 32;
+        const uint32_t at = tmem + tlane + L::kAOff + (b * MATS + mat) * L::kACols + g * 32;
         // the stage holds the codes with the 32-byte TMA swizzle: half h of
         // row r sits at 16 * (h ^ sw), which spreads each 8 consecutive
         // lanes' loads over all eight 16-byte bank groups
         const int sw = (r >> 2) & 1;
-        if (GATEUP) {
-          const uint4 lo = *reinterpret_cast<const uint4*>(pk + 16 * sw);
-          const uint4 hi = *reinterpret_cast<const uint4*>(pk + 16 * (sw ^ 1));
-          const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          uint32_t o[32];
+        const uint4 lo = *reinterpret_cast<const uint4*>(pk + 16 * sw);
+        const uint4 hi = *reinterpret_cast<const uint4*>(pk + 16 * (sw ^ 1));
+        const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        uint32_t o[32];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            uint32_t t4[4];
-            dequant8(wd[jj], s2, b2, t4);
-            o[4 * jj] = t4[0]; o[4 * jj + 1] = t4[1]; o[4 * jj + 2] = t4[2]; o[4 * jj + 3] = t4[3];
-          }
-          tmem_st32(at, o);
-        } else {
-          const uint4 v0 = *reinterpret_cast<const uint4*>(pk + 16 * (hsel ^ sw));
-          const uint32_t wd[4] = {v0.x, v0.y, v0.z, v0.w};
-          uint32_t o[16];
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            uint32_t t4[4];
-            dequant8(wd[jj], s2, b2, t4);
-            o[4 * jj] = t4[0]; o[4 * jj + 1] = t4[1]; o[4 * jj + 2] = t4[2]; o[4 * jj + 3] = t4[3];
-          }
-          tmem_st16(at + hsel * 16, o);
+        for (int jj = 0; jj < 8; ++jj) {
+          uint32_t t4[4];
+          dequant8(wd[jj], s2, b2, t4);
+          o[4 * jj] = t4[0]; o[4 * jj + 1] = t4[1]; o[4 * jj + 2] = t4[2]; o[4 * jj + 3] = t4[3];
         }
+        tmem_st32(at, o);
         // the stores must be complete before the MMA issuer is told: wait,
         // order them before the arrive, then one arrive per warp
         tmem_st_wait();
@@ -500,6 +527,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
       const int N = (cur.rows + 15) & ~15;
       const int ab = j % NACC;
+      // down: the first 32 rows' tokens and gate weights, looked up before
+      // the accumulator wait so that the dependent loads overlap it
+      int tok0 = 0;
+      float gate0 = 0.f;
+      if (!GATEUP) row_token_gate(a, cur, 0, lane, P, tok0, gate0);
       if (!warp_wait(smem_u32(&accfull[ab]), (j / NACC) & 1, abort, a.status)) break;
       tc_fence_after();
       const int feat = cur.slice * 128 + q * 32 + lane;
@@ -541,18 +573,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
-          // lane jj looks up row cb + jj: its token and its gate weight
-          const int rj = cur.row0 + min(cb + lane, cur.rows - 1);
-          int tokj;
-          float gj;
-          if (cur.shared) {
-            tokj = rj - P;
-            gj = 1.f;
-          } else {
-            const int p = __ldg(a.perm + rj);
-            tokj = p / a.k;
-            gj = __ldg(a.gates + p);
-          }
+          // lane jj holds row cb + jj's token and gate weight
+          int tokj = tok0;
+          float gj = gate0;
+          if (cb > 0) row_token_gate(a, cur, cb, lane, P, tokj, gj);
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int tj = __shfl_sync(0xffffffffu, tokj, jj);
