@@ -90,7 +90,7 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t ctrl, hist, x16, xs, w3, part, H, acc, total;
+  size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, total;
 };
 
 // ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
@@ -112,6 +112,7 @@ Layout layout(const lily_moe_dims& d) {
   size_t acc = T * D * 4;                         // prefill: fp32 y accumulator
   if (d.T <= 8) acc = std::max(acc, (P + T) * D * 4);  // decode: per-row outputs
   off += up(acc);
+  L.tiles = off; off += up((size_t)tile_count(d.T, d.n_experts, d.top_k, d.tile_rows) * 16);
   L.total = off;
   return L;
 }
@@ -235,6 +236,7 @@ GemmArgs gemm_args(const lily_moe_dims& d, const lily_moe_weights* w, const lily
   a.b1 = w->up_b;
   a.H = base + L.H;
   a.yacc = reinterpret_cast<float*>(base + L.acc);
+  a.tiles = reinterpret_cast<int4*>(base + L.tiles);
   a.status = ws_status(ws);
   return a;
 }

@@ -150,24 +150,23 @@ struct Item {
   bool shared;
 };
 
+// Item w from its tile's table entry {expert, row0, rows, 0} (written by the
+// token-row kernel); false when the tile holds no rows.
+__device__ __forceinline__ int4 load_tile(const GemmArgs& a, int w, int nslices) {
+  return __ldg(a.tiles + w / nslices);
+}
+__device__ __forceinline__ bool item_from(int4 t, int w, int nslices, int nsh, Item& it) {
+  it.slice = w % nslices;
+  it.shared = w / nslices < nsh;
+  it.expert = t.x;
+  it.row0 = t.y;
+  it.rows = t.z;
+  return t.z > 0;
+}
 template <int BM>
 __device__ __forceinline__ bool get_item(const GemmArgs& a, int w, int nslices, int nsh, int P,
                                          Item& it) {
-  const int tile = w / nslices;
-  it.slice = w % nslices;
-  it.shared = tile < nsh;
-  if (it.shared) {
-    it.expert = a.E;
-    it.row0 = P + tile * BM;
-    it.rows = min(BM, P + a.T - it.row0);
-    return true;
-  }
-  const int ti = tile - nsh;
-  it.expert = __ldg(a.block_map + 2 * ti);
-  it.row0 = __ldg(a.block_map + 2 * ti + 1);
-  if (it.expert < 0 || it.expert >= a.E || it.row0 < 0 || it.row0 >= P) return false;
-  it.rows = min(BM, __ldg(a.offsets + it.expert + 1) - it.row0);
-  return it.rows > 0;
+  return item_from(load_tile(a, w, nslices), w, nslices, nsh, it);
 }
 
 // Advance w (stepping by gridDim.x) to the next valid item; false at the end.
@@ -232,6 +231,11 @@ __device__ __forceinline__ void row_token_gate(const GemmArgs& a, const Item& it
     tok = p / a.k;
     g = __ldg(a.gates + p);
   }
+}
+
+// One scale-table word: fp16(scale) | fp16(bias) << 16 from bf16 bit patterns.
+__device__ __forceinline__ uint32_t sb_word(uint16_t sc, uint16_t bi) {
+  return (uint32_t)bf16_to_f16_bits(sc) | ((uint32_t)bf16_to_f16_bits(bi) << 16);
 }
 
 // Persistent kernel: one CTA per SM loops over the work items.
@@ -318,9 +322,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t it = 0;  // K-steps issued by this CTA, across items
     Ring rs;          // stage ring position of step it
     bool ok = true;
+    // the next item's table entry is loaded one item ahead (in every role)
+    int4 tnext = (int)blockIdx.x < n_items ? load_tile(a, blockIdx.x, nslices) : make_int4(0, 0, 0, 0);
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      const int4 tcur = tnext;
+      if (w + (int)gridDim.x < n_items) tnext = load_tile(a, w + gridDim.x, nslices);
       Item itm;
-      if (!get_item<BM>(a, w, nslices, nsh, P, itm)) {
+      if (!item_from(tcur, w, nslices, nsh, itm)) {
         if (lane == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
         continue;
       }
@@ -367,9 +375,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t it = 0, titem = 0;
     Ring rs;  // stage ring position of step it
     bool ok = true;
+    int4 tnext = (int)blockIdx.x < n_items ? load_tile(a, blockIdx.x, nslices) : make_int4(0, 0, 0, 0);
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      const int4 tcur = tnext;
+      if (w + (int)gridDim.x < n_items) tnext = load_tile(a, w + gridDim.x, nslices);
       Item itm;
-      if (!get_item<BM>(a, w, nslices, nsh, P, itm)) continue;
+      if (!item_from(tcur, w, nslices, nsh, itm)) continue;
       const int N = (itm.rows + 15) & ~15;
       const uint32_t idesc = idesc_f16_f32(128, N);
       const int ab = titem % NACC;
@@ -421,11 +432,61 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t it = 0, j = 0;
     Ring rs;  // stage ring position of step it
     bool ok = true;
+    // down: each lane fills its own row's table entries (the groups of its
+    // parity g) in table slot 0, which only it reads; the raw bf16 scales and
+    // biases of the next item are loaded one item ahead, as 16-byte chunks,
+    // when G is 8 or 16 (else read one by one at the item's start)
+    constexpr int kPfChunks = 2;  // 8-group chunks held in registers
+    uint4 pfs[kPfChunks], pfb[kPfChunks];
+    int pf_w = -1;                // work item whose scales pfs/pfb hold
+    auto sb_row = [&](int expert, int slice) {
+      return (size_t)expert * NOUT + (size_t)slice * 128 + r;
+    };
+    auto down_prefetch = [&](int wn, int4 t) {
+      // 16-byte chunks of 8 groups: whole chunks only (G a multiple of 8)
+      if (GATEUP || (G & 7) != 0 || G > 8 * kPfChunks || t.z <= 0) return;
+      const size_t row = sb_row(t.x, wn % nslices);
+#pragma unroll
+      for (int c = 0; c < kPfChunks; ++c)
+        if (c * 8 < G) {
+          pfs[c] = __ldg(reinterpret_cast<const uint4*>(a.s0 + row * G) + c);
+          pfb[c] = __ldg(reinterpret_cast<const uint4*>(a.b0 + row * G) + c);
+        }
+      pf_w = wn;
+    };
+    auto down_fill = [&](int w, const Item& itm) {
+      uint32_t* dst = sb;  // slot 0, entries [group][row]
+      if (pf_w == w) {
+#pragma unroll
+        for (int c = 0; c < kPfChunks; ++c)
+          if (c * 8 < G) {
+            // groups c*8 + 2u + g sit in word u, half g, of each chunk
+            const uint32_t ws[4] = {pfs[c].x, pfs[c].y, pfs[c].z, pfs[c].w};
+            const uint32_t wb[4] = {pfb[c].x, pfb[c].y, pfb[c].z, pfb[c].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[(c * 8 + 2 * u + g) * 128 + r] =
+                  sb_word((uint16_t)(ws[u] >> (16 * g)), (uint16_t)(wb[u] >> (16 * g)));
+          }
+      } else {
+        const size_t row = sb_row(itm.expert, itm.slice);
+        for (int grp = g; grp < G; grp += 2)
+          dst[grp * 128 + r] = sb_word(__ldg(a.s0 + row * G + grp), __ldg(a.b0 + row * G + grp));
+      }
+    };
+    int4 tnext = (int)blockIdx.x < n_items ? load_tile(a, blockIdx.x, nslices) : make_int4(0, 0, 0, 0);
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+      const int4 tcur = tnext;
+      if (w + (int)gridDim.x < n_items) tnext = load_tile(a, w + gridDim.x, nslices);
       Item itm;
-      if (!get_item<BM>(a, w, nslices, nsh, P, itm)) continue;
-      const int slot = j % nsb;
-      if (!warp_wait(smem_u32(&sbfull[slot]), (j / nsb) & 1, abort, a.status)) break;
+      if (!item_from(tcur, w, nslices, nsh, itm)) continue;
+      const int slot = GATEUP ? j % nsb : 0;
+      if (GATEUP) {
+        if (!warp_wait(smem_u32(&sbfull[slot]), (j / nsb) & 1, abort, a.status)) break;
+      } else {
+        down_fill(w, itm);
+        if (w + (int)gridDim.x < n_items) down_prefetch(w + gridDim.x, tnext);
+      }
       const uint32_t* sbs = sb + slot * sb_words;
       for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx, b = it % L::kNumA;
@@ -466,7 +527,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sbempty[slot]));
+      if (GATEUP && lane == 0) mbar_arrive(smem_u32(&sbempty[slot]));
       ++j;
     }
   } else {
@@ -481,49 +542,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto row_of = [&](const Item& it) {
       return (size_t)it.expert * NOUT + (size_t)it.slice * 128 + r;
     };
-    const int nq = (G & 7) == 0 ? MATS * 2 * (G / 8) : 1 << 30;
-    const bool lookahead = !GATEUP && nq <= 4;
-    uint4 la[4];
     int w = blockIdx.x;
     Item cur, nxt, nn;
     bool have = next_item<BM>(a, w, n_items, nslices, nsh, P, cur);
-    if (have) {
+    if (GATEUP && have) {
       scale_fill<MATS>(a, row_of(cur), G, r, slot_ptr(0));
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sbfull[0]));
     }
     int wn = w + gridDim.x;
     bool have_next = have && next_item<BM>(a, wn, n_items, nslices, nsh, P, nxt);
-    if (lookahead && have_next) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (c < nq) la[c] = scale_chunk_load(a, row_of(nxt), G, c);
-    }
     uint32_t j = 0;
     while (have) {
-      if (have_next) {
+      if (GATEUP && have_next) {
         const uint32_t jn = j + 1;
         const int slot = jn % nsb;
         if (jn >= (uint32_t)nsb &&
             !warp_wait(smem_u32(&sbempty[slot]), ((jn / nsb) + 1) & 1, abort, a.status))
           break;
-        if (lookahead) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (c < nq) scale_chunk_store(slot_ptr(slot), G, c, r, la[c]);
-        } else {
-          scale_fill<MATS>(a, row_of(nxt), G, r, slot_ptr(slot));
-        }
+        scale_fill<MATS>(a, row_of(nxt), G, r, slot_ptr(slot));
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sbfull[slot]));
       }
       int wnn = wn + gridDim.x;
       const bool have_nn = have_next && next_item<BM>(a, wnn, n_items, nslices, nsh, P, nn);
-      if (lookahead && have_nn) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (c < nq) la[c] = scale_chunk_load(a, row_of(nn), G, c);
-      }
 
       const int N = (cur.rows + 15) & ~15;
       const int ab = j % NACC;
@@ -697,8 +739,27 @@ static bool f16_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, 
 __global__ void __launch_bounds__(256) token_rows_kernel(const uint4* __restrict__ x,
                                                          const int32_t* __restrict__ perm, int k,
                                                          int P, int T, int d8, uint4* __restrict__ xs,
-                                                         uint4* __restrict__ x16, uint32_t* status) {
+                                                         uint4* __restrict__ x16, uint32_t* status,
+                                                         const GemmArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // tile table: {expert, row0, rows, 0}, shared-expert tiles first
+  const int nsh = (T + a.BM - 1) / a.BM;
+  const int ntab = tile_count(T, a.E, k, a.BM);
+  const int cap = ntab - nsh;
+  const int ntiles = min(max(*a.n_tiles, 0), cap);
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < ntab; t += gridDim.x * blockDim.x) {
+    int4 v = make_int4(0, 0, 0, 0);
+    if (t < nsh) {
+      v = make_int4(a.E, P + t * a.BM, min(a.BM, T - t * a.BM), 0);
+    } else if (t - nsh < ntiles) {
+      const int e = __ldg(a.block_map + 2 * (t - nsh)), row0 = __ldg(a.block_map + 2 * (t - nsh) + 1);
+      if (e >= 0 && e < a.E && row0 >= 0 && row0 < P) {
+        const int rows = min(a.BM, __ldg(a.offsets + e + 1) - row0);
+        if (rows > 0) v = make_int4(e, row0, rows, 0);
+      }
+    }
+    a.tiles[t] = v;
+  }
   bool ok = true;
   for (int row = blockIdx.x * 8 + warp; row < P + T; row += gridDim.x * 8) {
     const int tok = row < P ? __ldg(perm + row) / k : row - P;
@@ -713,11 +774,13 @@ cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* 
                               cudaStream_t s) {
   const int P = a.T * a.k;
   int blocks = (P + a.T + 7) / 8;
+  const int tb = (tile_count(a.T, a.E, a.k, a.BM) + 255) / 256;
+  if (blocks < tb) blocks = tb;
   if (blocks > 152 * 8) blocks = 152 * 8;
   prof_begin(K_TOKEN_ROWS, s);
   token_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), a.perm, a.k, P, a.T,
                                            a.d / 8, static_cast<uint4*>(xs),
-                                           static_cast<uint4*>(x16), a.status);
+                                           static_cast<uint4*>(x16), a.status, a);
   prof_end(K_TOKEN_ROWS, s);
   return cudaGetLastError();
 }

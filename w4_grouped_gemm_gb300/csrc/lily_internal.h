@@ -88,11 +88,20 @@ struct GemmArgs {
   const uint16_t* b1;
   void* H;             // fp16 [P+T][F], 8-element chunks in K-chunk order
   float* yacc;         // fp32 [T][d]
+  int4* tiles;         // [tile_count(T, E, k, BM)] {expert, row0, rows, 0}: shared-expert
+                       // tiles first, then the block map's; rows = 0 marks no tile
   uint32_t* status;
 };
+// Tiles of the grouped GEMMs: ceil(T / BM) shared-expert tiles plus the block
+// map's capacity.
+__host__ __device__ inline int tile_count(int T, int E, int k, int BM) {
+  const int P = T * k;
+  return (T + BM - 1) / BM + (P + BM - 1) / BM + (E < P ? E : P);
+}
 // Token rows for the gate/up GEMM: xs[r] = fp16(x[perm[r] / k]) for the P
 // expert-sorted rows and x16[t] = fp16(x[t]), every 8-element chunk in
-// K-chunk order.  Then the gate/up GEMM (tensor maps built from the pointers).
+// K-chunk order; the same launch writes the tile table a.tiles.  Then the
+// gate/up GEMM (tensor maps built from the pointers).
 cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* x16, cudaStream_t s);
 cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, const uint8_t* gq,
                           const uint8_t* uq, cudaStream_t s);
