@@ -488,42 +488,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (w + (int)gridDim.x < n_items) down_prefetch(w + gridDim.x, tnext);
       }
       const uint32_t* sbs = sb + slot * sb_words;
-      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
-        const int s = rs.idx, b = it % L::kNumA;
-        // the stage's TMA landed and the A buffer was consumed (one vote)
-        const bool got = warp_wait_all2(smem_u32(&full[s]), rs.ph,
-                                        smem_u32(&aempty[b]), ((it / L::kNumA) + 1) & 1,
-                                        it >= (uint32_t)L::kNumA, abort, a.status);
+      // gate/up: two K-steps per iteration (one when a single step is left):
+      // their loads, arithmetic and tensor-memory stores interleave, and one
+      // store wait covers both before the two arrivals.  Down takes one step
+      // per iteration (its items are four steps long).
+      for (int kk = 0; kk < NST;) {
+        const bool two = GATEUP && kk + 1 < NST;
+        Ring rs1 = rs;
+        rs1.next(nstages);
+        const uint32_t it1 = it + 1;
+        const int s0 = rs.idx, b0 = it % L::kNumA, s1 = rs1.idx, b1 = it1 % L::kNumA;
+        // the stages' TMA landed and the A buffers were consumed
+        bool got = warp_wait_all2(smem_u32(&full[s0]), rs.ph, smem_u32(&aempty[b0]),
+                                  ((it / L::kNumA) + 1) & 1, it >= (uint32_t)L::kNumA, abort,
+                                  a.status);
+        if (got && two)
+          got = warp_wait_all2(smem_u32(&full[s1]), rs1.ph, smem_u32(&aempty[b1]),
+                               ((it1 / L::kNumA) + 1) & 1, it1 >= (uint32_t)L::kNumA, abort,
+                               a.status);
         if (!got) {
           ok = false;
           break;
         }
-        const uint8_t* pk = stage_base + (size_t)s * STAGE + BBYTES +
-                            (mat * KG + g) * kPackedBytes + r * 32;
-        const uint32_t sbv = sbs[(mat * G + kk * KG + g) * 128 + r];
-        const uint32_t s2 = prmt(sbv, sbv, 0x1010u), b2 = prmt(sbv, sbv, 0x3232u);
-        const uint32_t at = tmem + tlane + L::kAOff + (b * MATS + mat) * L::kACols + g * 32;
         // the stage holds the codes with the 32-byte TMA swizzle: half h of
         // row r sits at 16 * (h ^ sw), which spreads each 8 consecutive
         // lanes' loads over all eight 16-byte bank groups
         const int sw = (r >> 2) & 1;
-        const uint4 lo = *reinterpret_cast<const uint4*>(pk + 16 * sw);
-        const uint4 hi = *reinterpret_cast<const uint4*>(pk + 16 * (sw ^ 1));
-        const uint32_t wd[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-        uint32_t o[32];
+        const size_t poff = BBYTES + (size_t)(mat * KG + g) * kPackedBytes + r * 32;
+        const uint8_t* pk0 = stage_base + (size_t)s0 * STAGE + poff;
+        const uint8_t* pk1 = stage_base + (size_t)s1 * STAGE + poff;
+        const uint4 lo0 = *reinterpret_cast<const uint4*>(pk0 + 16 * sw);
+        const uint4 hi0 = *reinterpret_cast<const uint4*>(pk0 + 16 * (sw ^ 1));
+        uint4 lo1 = lo0, hi1 = hi0;
+        if (two) {
+          lo1 = *reinterpret_cast<const uint4*>(pk1 + 16 * sw);
+          hi1 = *reinterpret_cast<const uint4*>(pk1 + 16 * (sw ^ 1));
+        }
+        const uint32_t sbv0 = sbs[(mat * G + kk * KG + g) * 128 + r];
+        const uint32_t sbv1 = two ? sbs[(mat * G + (kk + 1) * KG + g) * 128 + r] : sbv0;
+        const uint32_t s20 = prmt(sbv0, sbv0, 0x1010u), b20 = prmt(sbv0, sbv0, 0x3232u);
+        const uint32_t s21 = prmt(sbv1, sbv1, 0x1010u), b21 = prmt(sbv1, sbv1, 0x3232u);
+        const uint32_t wd0[8] = {lo0.x, lo0.y, lo0.z, lo0.w, hi0.x, hi0.y, hi0.z, hi0.w};
+        const uint32_t wd1[8] = {lo1.x, lo1.y, lo1.z, lo1.w, hi1.x, hi1.y, hi1.z, hi1.w};
+        uint32_t o0[32], o1[32];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          uint32_t t4[4];
-          dequant8(wd[jj], s2, b2, t4);
-          o[4 * jj] = t4[0]; o[4 * jj + 1] = t4[1]; o[4 * jj + 2] = t4[2]; o[4 * jj + 3] = t4[3];
+          uint32_t t4[4], u4[4];
+          dequant8(wd0[jj], s20, b20, t4);
+          dequant8(wd1[jj], s21, b21, u4);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o0[4 * jj + e] = t4[e];
+            o1[4 * jj + e] = u4[e];
+          }
         }
-        tmem_st32(at, o);
+        const uint32_t acol = tmem + tlane + L::kAOff + mat * L::kACols + g * 32;
+        tmem_st32(acol + b0 * MATS * L::kACols, o0);
+        if (two) tmem_st32(acol + b1 * MATS * L::kACols, o1);
         // the stores must be complete before the MMA issuer is told: wait,
-        // order them before the arrive, then one arrive per warp
+        // order them before the arrive, then one arrive per warp and step
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&afull[b]));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&afull[b0]));
+          if (two) mbar_arrive(smem_u32(&afull[b1]));
+        }
+        const int adv = two ? 2 : 1;
+        kk += adv;
+        it += adv;
+        rs.next(nstages);
+        if (two) rs.next(nstages);
       }
       if (!ok) break;
       __syncwarp();
