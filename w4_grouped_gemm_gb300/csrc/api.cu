@@ -249,10 +249,7 @@ int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights
   if (rc) return rc;
   GemmArgs a = gemm_args(d, w, r, ws);
   if (yacc) a.yacc = yacc;
-  prof_begin(K_MEMSET, s);
-  cudaError_t e = cudaMemsetAsync(a.yacc, 0, (size_t)d.T * d.d_model * 4, s);
-  prof_end(K_MEMSET, s);
-  if (e != cudaSuccess) return LILY_ERR_CUDA;
+  if (!aligned16(a.yacc)) return LILY_ERR_MISALIGNED;
   const Layout L = layout(d);
   uint8_t* base = static_cast<uint8_t*>(ws);
   if (launch_token_rows(a, x, base + L.xs, base + L.x16, s) != cudaSuccess) return LILY_ERR_CUDA;

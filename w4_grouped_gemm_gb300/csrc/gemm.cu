@@ -777,6 +777,14 @@ __global__ void __launch_bounds__(256) token_rows_kernel(const uint4* __restrict
                                                          uint4* __restrict__ x16, uint32_t* status,
                                                          const GemmArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the fp32 output accumulator starts at zero (the down GEMM adds into it)
+  {
+    float4* acc4 = reinterpret_cast<float4*>(a.yacc);
+    const int64_t n4 = (int64_t)T * a.d / 4;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+         i += (int64_t)gridDim.x * blockDim.x)
+      acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   // tile table: {expert, row0, rows, 0}, shared-expert tiles first
   const int nsh = (T + a.BM - 1) / a.BM;
   const int ntab = tile_count(T, a.E, k, a.BM);

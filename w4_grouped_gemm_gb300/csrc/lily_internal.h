@@ -100,8 +100,9 @@ __host__ __device__ inline int tile_count(int T, int E, int k, int BM) {
 }
 // Token rows for the gate/up GEMM: xs[r] = fp16(x[perm[r] / k]) for the P
 // expert-sorted rows and x16[t] = fp16(x[t]), every 8-element chunk in
-// K-chunk order; the same launch writes the tile table a.tiles.  Then the
-// gate/up GEMM (tensor maps built from the pointers).
+// K-chunk order; the same launch writes the tile table a.tiles and zeroes the
+// fp32 accumulator a.yacc ([T][d], 16-byte aligned).  Then the gate/up GEMM
+// (tensor maps built from the pointers).
 cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* x16, cudaStream_t s);
 cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, const uint8_t* gq,
                           const uint8_t* uq, cudaStream_t s);
