@@ -384,7 +384,7 @@ def run_lily(args, world, rank, local):
             dbytes = touched * (F * d // 2 + F * d // 64 * 4) + T * d * 2
         elif dom in ("dec_gateup",):
             dbytes = gateup_bytes(T, d, F, touched)
-        elif dom in ("dec_down",):
+        elif dom in ("dec_down_combine",):
             dbytes = touched * (F * d // 2 + F * d // 64 * 4)
         else:
             dbytes = step_bytes

@@ -109,9 +109,7 @@ Layout layout(const lily_moe_dims& d) {
   L.part = off; off += tc_router ? up((size_t)router_splits(d.T, d.d_model) * T * E * 4) : 0;
   L.H = off;    off += up((P + T) * F * 2);
   L.acc = off;
-  size_t acc = T * D * 4;                         // prefill: fp32 y accumulator
-  if (d.T <= 8) acc = std::max(acc, (P + T) * D * 4);  // decode: per-row outputs
-  off += up(acc);
+  off += up(T * D * 4);  // prefill: fp32 y accumulator
   L.tiles = off; off += up((size_t)tile_count(d.T, d.n_experts, d.top_k, d.tile_rows) * 16);
   L.total = off;
   return L;
@@ -188,8 +186,10 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
       if (e != cudaSuccess) return LILY_ERR_CUDA;
       a.logits_src = r.logits;
     } else {
-      cudaError_t e = launch_router_logits(x, w->router_w, w->router_bias, r.logits, d.T,
-                                           d.d_model, d.n_experts, s);
+      // x in the decode GEMV's fragment order, in the x16 / xs regions
+      cudaError_t e = launch_router_logits(
+          x, w->router_w, w->router_bias, r.logits, d.T, d.d_model, d.n_experts,
+          reinterpret_cast<uint32_t*>(base + L.x16), reinterpret_cast<float*>(base + L.xs), s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
       a.logits_src = r.logits;
     }
@@ -376,8 +376,9 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_wei
   a.uq = w->up_q;   a.us = w->up_s;   a.ub = w->up_b;
   a.dq = w->down_q; a.ds = w->down_s; a.db = w->down_b;
   a.x = x;
+  a.xpg = reinterpret_cast<const uint32_t*>(base + L.x16);
+  a.xsg = reinterpret_cast<const float*>(base + L.xs);
   a.H = base + L.H;
-  a.O = reinterpret_cast<float*>(base + L.acc);
   a.y = y;
   a.y_f32 = dims->out_dtype == LILY_DTYPE_F32;
   a.status = ws_status(ws);
@@ -555,7 +556,7 @@ int lily_moe_profile_read(double* total_ms, int64_t* launches) {
 
 const char* lily_moe_kernel_name(int kind) {
   static const char* names[] = {"router_gemm", "router_gemv", "route", "gateup_gemm",
-                                "down_gemm",   "finalize",    "dec_gateup", "dec_down",
+                                "down_gemm",   "finalize",    "dec_gateup", "dec_down_combine",
                                 "dec_combine", "rmsnorm",     "stack_boundary", "memset_acc",
                                 "router_prep", "router_reduce", "token_rows"};
   if (kind < 0 || kind >= (int)(sizeof(names) / sizeof(names[0]))) return "unused";

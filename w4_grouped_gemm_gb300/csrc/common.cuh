@@ -187,6 +187,20 @@ __device__ __forceinline__ bool warp_wait_all2(uint32_t bar0, uint32_t parity0, 
   }
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start while its predecessor in the
+// stream still runs.  pdl_wait() returns once the predecessor has completed
+// and its memory is visible (immediately when there is no such predecessor);
+// loads of data the predecessor does not write (weights) may go before it.
+// pdl_trigger() lets this kernel's own dependent start; it is called after
+// pdl_wait(), so a dependent never overlaps anything older than its direct
+// predecessor.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

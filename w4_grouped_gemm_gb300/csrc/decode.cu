@@ -16,8 +16,8 @@
 // scale/bias arithmetic is needed.  Gate/up multiply bf16 x (c = 128, the
 // bf16 magic); down multiplies the fp16 H (c = 1024, the fp16 magic).  The
 // pairs come out as (q_i, q_{i+4}) of each 8-code word; the activations are
-// laid out in shared memory in that same order, so the K order of both
-// operands agrees.
+// laid out in that same order (x staged in shared memory; H written in it by
+// the gate/up kernel), so the K order of both operands agrees.
 #include "common.cuh"
 
 namespace lily {
@@ -56,9 +56,15 @@ __device__ __forceinline__ void code_pairs(uint32_t w, uint32_t (&p)[4]) {
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t h) {
   return __uint_as_float((uint32_t)h << 16);
 }
-template <bool F16>
-__device__ __forceinline__ float act_to_float(uint16_t h) {
-  return F16 ? __half2float(__ushort_as_half(h)) : bf16_bits_to_float(h);
+
+// Position of element j (0..63) of a 64-group in the pair order used for H:
+// 16-bit index 2*word + half, word = c*8 + w*4 + (e & 3), half = e >> 2, for
+// j = c*16 + 8w + e.  Word `word` of a group holds the (i, i+4) pair that one
+// mma B-fragment register takes, so the down GEMV reads its fragments with
+// plain 16-byte loads.
+__host__ __device__ __forceinline__ int hpair_pos(int j) {
+  const int c = j >> 4, w = (j >> 3) & 1, e = j & 7;
+  return 2 * (c * 8 + w * 4 + (e & 3)) + (e >> 2);
 }
 
 // Which tile a decode CTA serves.  Slot 0 = shared expert (rows P..P+T-1);
@@ -84,215 +90,257 @@ __device__ __forceinline__ bool decode_tile(const DecodeArgs& a, int slot, int& 
   return rows > 0;
 }
 
-// Activation rows -> shared memory in the permuted pair order, plus the
-// per-group sums X_g.  src(n, i) gives the 16-bit pattern of element i of
-// row n (n < rows), bf16 or fp16 as F16 says.
-//   xp[(n*G + g)*32 + c*8 + w*4 + m*2 + r] =
-//     (x[n][g*64 + c*16 + 8w + 2m + r], x[n][... + 4])
-template <bool F16, typename Src>
-__device__ void stage_rows(uint32_t* xp, float* xs, int rows, int K, Src src) {
-  const int G = K / 64;
-  const int total = kDecMaxRows * G * 32;
-  for (int e = threadIdx.x; e < total; e += kDecThreads) {
-    const int n = e / (G * 32), rem = e % (G * 32), g = rem / 32, idx = rem % 32;
-    const int c = idx >> 3, w = (idx >> 2) & 1, m = (idx >> 1) & 1, r = idx & 1;
-    uint32_t v = 0;
-    if (n < rows) {
-      const int i = g * 64 + c * 16 + 8 * w + 2 * m + r;
-      v = (uint32_t)src(n, i) | ((uint32_t)src(n, i + 4) << 16);
-    }
-    xp[e] = v;
-  }
-  __syncthreads();
-  // group sums from the staged copy (shared memory), not from global memory
-  for (int e = threadIdx.x; e < kDecMaxRows * G; e += kDecThreads) {
-    const int n = e / G;
-    float s = 0.f;
-    if (n < rows) {
-      const uint32_t* p = xp + (size_t)e * 32;
-#pragma unroll 8
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t v = p[i];
-        s += act_to_float<F16>((uint16_t)(v & 0xFFFFu)) + act_to_float<F16>((uint16_t)(v >> 16));
-      }
-    }
-    xs[e] = s;
-  }
-}
-
-// 16 weight rows [r0, r0+16) of one packed matrix (row length K) times the
-// staged activations, over the groups g = g_begin, g_begin + g_step, ...
-// Accumulates into out[4] = (row g, tok 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1).
-template <bool F16>
-__device__ __forceinline__ void gemv16(const uint8_t* __restrict__ q, const uint16_t* __restrict__ s,
-                                       const uint16_t* __restrict__ b, size_t r0, int K,
-                                       const uint32_t* xp, const float* xs, int g_begin,
-                                       int g_step, float (&out)[4]) {
+// Up to kChunk groups of 16 weight rows [r0, r0+16) of one packed matrix
+// (row length K): the codes of rows gi and gi+8 for this lane's 8 K values,
+// and the rows' scales and biases, loaded into registers ahead of use so the
+// loads of a chunk are in flight together.
+constexpr int kChunk = 4;
+struct WChunk {
+  uint2 wa[kChunk], wb[kChunk];
+  float sa[kChunk], sb[kChunk], ba[kChunk], bb[kChunk];
+};
+__device__ __forceinline__ void load_wchunk(WChunk& w, const uint8_t* __restrict__ q,
+                                            const uint16_t* __restrict__ s,
+                                            const uint16_t* __restrict__ b, size_t r0, int K,
+                                            int g0, int gstep) {
   const int lane = threadIdx.x & 31, gi = lane >> 2, c = lane & 3;
   const int G = K / 64;
   const uint8_t* qa = q + (r0 + gi) * (size_t)(K / 2) + c * 8;
   const uint8_t* qb = qa + 8 * (size_t)(K / 2);
   const uint16_t* sa = s + (r0 + gi) * (size_t)G;
-  const uint16_t* sb_ = sa + 8 * (size_t)G;
   const uint16_t* ba = b + (r0 + gi) * (size_t)G;
-  const uint16_t* bb = ba + 8 * (size_t)G;
-  for (int g = g_begin; g < G; g += g_step) {
-    const uint2 wa = __ldcs(reinterpret_cast<const uint2*>(qa + g * 32));
-    const uint2 wb = __ldcs(reinterpret_cast<const uint2*>(qb + g * 32));
-    const float s_a = bf16_bits_to_float(__ldg(sa + g)), s_b = bf16_bits_to_float(__ldg(sb_ + g));
-    const float b_a = bf16_bits_to_float(__ldg(ba + g)), b_b = bf16_bits_to_float(__ldg(bb + g));
-    const uint32_t* xg = xp + ((size_t)gi * G + g) * 32 + c * 8;  // token n = gi for B
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      uint32_t pa[4], pb[4];
-      code_pairs<F16>(w == 0 ? wa.x : wa.y, pa);
-      code_pairs<F16>(w == 0 ? wb.x : wb.y, pb);
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const uint32_t afrag[4] = {pa[2 * m], pb[2 * m], pa[2 * m + 1], pb[2 * m + 1]};
-        mma_16816<F16>(acc, afrag, xg[w * 4 + m * 2], xg[w * 4 + m * 2 + 1]);
-      }
+  for (int i = 0; i < kChunk; ++i) {
+    const int g = g0 + i * gstep;
+    if (g < G) {
+      w.wa[i] = __ldcs(reinterpret_cast<const uint2*>(qa + g * 32));
+      w.wb[i] = __ldcs(reinterpret_cast<const uint2*>(qb + g * 32));
+      w.sa[i] = bf16_bits_to_float(__ldg(sa + g));
+      w.sb[i] = bf16_bits_to_float(__ldg(sa + 8 * G + g));
+      w.ba[i] = bf16_bits_to_float(__ldg(ba + g));
+      w.bb[i] = bf16_bits_to_float(__ldg(ba + 8 * G + g));
     }
-    constexpr float off = F16 ? 1024.f : 128.f;  // the code offset of the magic
-    const float x0 = xs[(2 * c) * G + g], x1 = xs[(2 * c + 1) * G + g];
-    out[0] += s_a * (acc[0] - off * x0) + b_a * x0;
-    out[1] += s_a * (acc[1] - off * x1) + b_a * x1;
-    out[2] += s_b * (acc[2] - off * x0) + b_b * x0;
-    out[3] += s_b * (acc[3] - off * x1) + b_b * x1;
   }
+}
+// Group i of a loaded chunk against B fragments xw (8 words: this lane's
+// (i, i+4) pairs) and the group sums x0, x1 of accumulator columns 2c, 2c+1.
+template <bool F16>
+__device__ __forceinline__ void chunk_group(const WChunk& w, int i, const uint32_t (&xw)[8],
+                                            float x0, float x1, float (&out)[4]) {
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pa[4], pb[4];
+    code_pairs<F16>(h == 0 ? w.wa[i].x : w.wa[i].y, pa);
+    code_pairs<F16>(h == 0 ? w.wb[i].x : w.wb[i].y, pb);
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const uint32_t afrag[4] = {pa[2 * m], pb[2 * m], pa[2 * m + 1], pb[2 * m + 1]};
+      mma_16816<F16>(acc, afrag, xw[h * 4 + m * 2], xw[h * 4 + m * 2 + 1]);
+    }
+  }
+  constexpr float off = F16 ? 1024.f : 128.f;  // the code offset of the magic
+  out[0] += w.sa[i] * (acc[0] - off * x0) + w.ba[i] * x0;
+  out[1] += w.sa[i] * (acc[1] - off * x1) + w.ba[i] * x1;
+  out[2] += w.sb[i] * (acc[2] - off * x0) + w.bb[i] * x0;
+  out[3] += w.sb[i] * (acc[3] - off * x1) + w.bb[i] * x1;
 }
 
 // Gate/up: CTA = (tile slot, 16 features); 8 warps split K; H = silu(g) * u.
+// B fragments and group sums come from x in fragment order (xpg, xsg, written
+// by the router launch), so no activation staging is needed.
 __global__ void __launch_bounds__(kDecThreads) dec_gateup_kernel(const DecodeArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  const int G = a.d / 64;
-  uint32_t* xp = reinterpret_cast<uint32_t*>(smem_raw);    // [8][G][32]
-  float* xs = reinterpret_cast<float*>(xp + kDecMaxRows * G * 32);  // [8][G]
-  float* part = xs + kDecMaxRows * G;                      // [8 warps][2][16][8]
+  __shared__ float part[8][2][16][kDecMaxRows];  // per-warp partial outputs
   __shared__ int tok[kDecMaxRows];
-
+  const int G = a.d / 64;
   const int nfb = a.F / 16;
   const int slot = blockIdx.x / nfb, fb = blockIdx.x % nfb;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = lane >> 2, c = lane & 3;
+  // this warp's first chunk of weight groups (g = warp, warp + 8, ...); the
+  // shared expert's (slot 0) goes before the wait for the routing
+  WChunk wg, wu;
+  if (slot == 0) {
+    const size_t r0s = (size_t)a.E * a.F + (size_t)fb * 16;
+    load_wchunk(wg, a.gq, a.gs, a.gb, r0s, a.d, warp, 8);
+    load_wchunk(wu, a.uq, a.us, a.ub, r0s, a.d, warp, 8);
+  }
+  pdl_wait();
+  pdl_trigger();
   int expert, row0, rows;
   if (!decode_tile(a, slot, expert, row0, rows)) return;
-  const int P = a.T * a.k;
+  const size_t r0 = (size_t)expert * a.F + (size_t)fb * 16;
+  if (slot != 0) {
+    load_wchunk(wg, a.gq, a.gs, a.gb, r0, a.d, warp, 8);
+    load_wchunk(wu, a.uq, a.us, a.ub, r0, a.d, warp, 8);
+  }
   if (threadIdx.x < kDecMaxRows) {
     const int n = min((int)threadIdx.x, rows - 1);
     tok[threadIdx.x] = (slot == 0) ? n : a.perm[row0 + n] / a.k;
   }
   __syncthreads();
-  const uint16_t* x = static_cast<const uint16_t*>(a.x);
-  stage_rows<false>(xp, xs, rows, a.d, [&](int n, int i) { return x[(size_t)tok[n] * a.d + i]; });
-  __syncthreads();
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t r0 = (size_t)expert * a.F + (size_t)fb * 16;
+  // B-fragment row of this lane: slot row gi (zero beyond the slot's rows);
+  // group sums of accumulator columns 2c, 2c+1
+  const uint32_t* xrow = a.xpg + (size_t)tok[min(gi, rows - 1)] * G * 32 + c * 8;
+  const float* xs0 = a.xsg + (size_t)tok[min(2 * c, rows - 1)] * G;
+  const float* xs1 = a.xsg + (size_t)tok[min(2 * c + 1, rows - 1)] * G;
   float og[4] = {0.f, 0.f, 0.f, 0.f}, ou[4] = {0.f, 0.f, 0.f, 0.f};
-  gemv16<false>(a.gq, a.gs, a.gb, r0, a.d, xp, xs, warp, 8, og);
-  gemv16<false>(a.uq, a.us, a.ub, r0, a.d, xp, xs, warp, 8, ou);
-  {
-    const int gi = lane >> 2, c = lane & 3;
-    float* pw = part + warp * 256;
-    pw[0 * 128 + gi * 8 + 2 * c] = og[0];
-    pw[0 * 128 + gi * 8 + 2 * c + 1] = og[1];
-    pw[0 * 128 + (gi + 8) * 8 + 2 * c] = og[2];
-    pw[0 * 128 + (gi + 8) * 8 + 2 * c + 1] = og[3];
-    pw[1 * 128 + gi * 8 + 2 * c] = ou[0];
-    pw[1 * 128 + gi * 8 + 2 * c + 1] = ou[1];
-    pw[1 * 128 + (gi + 8) * 8 + 2 * c] = ou[2];
-    pw[1 * 128 + (gi + 8) * 8 + 2 * c + 1] = ou[3];
+  for (int g0 = warp; g0 < G; g0 += 8 * kChunk) {
+    if (g0 != warp) {
+      load_wchunk(wg, a.gq, a.gs, a.gb, r0, a.d, g0, 8);
+      load_wchunk(wu, a.uq, a.us, a.ub, r0, a.d, g0, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int g = g0 + 8 * i;
+      if (g < G) {
+        uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+        if (gi < rows) {
+          h0 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32));
+          h1 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32 + 4));
+        }
+        const uint32_t xw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        const float x0 = 2 * c < rows ? __ldg(xs0 + g) : 0.f;
+        const float x1 = 2 * c + 1 < rows ? __ldg(xs1 + g) : 0.f;
+        chunk_group<false>(wg, i, xw, x0, x1, og);
+        chunk_group<false>(wu, i, xw, x0, x1, ou);
+      }
+    }
   }
+  part[warp][0][gi][2 * c] = og[0];
+  part[warp][0][gi][2 * c + 1] = og[1];
+  part[warp][0][gi + 8][2 * c] = og[2];
+  part[warp][0][gi + 8][2 * c + 1] = og[3];
+  part[warp][1][gi][2 * c] = ou[0];
+  part[warp][1][gi][2 * c + 1] = ou[1];
+  part[warp][1][gi + 8][2 * c] = ou[2];
+  part[warp][1][gi + 8][2 * c + 1] = ou[3];
   __syncthreads();
-  if (threadIdx.x < 128) {
-    const int t = threadIdx.x;  // (row, token) = (t / 8, t % 8)
+  if (threadIdx.x < 16 * kDecMaxRows) {
+    const int row = threadIdx.x / kDecMaxRows, n = threadIdx.x % kDecMaxRows;
     float g = 0.f, u = 0.f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) {
-      g += part[w * 256 + t];
-      u += part[w * 256 + 128 + t];
+      g += part[w][0][row][n];
+      u += part[w][1][row][n];
     }
-    const int row = t >> 3, n = t & 7;
     if (n < rows) {
       const float h = g / (1.f + __expf(-g)) * u;
       if (!(fabsf(h) <= 65504.f)) set_status(a.status, LILY_STATUS_F16_RANGE);
-      static_cast<__half*>(a.H)[(size_t)(row0 + n) * a.F + fb * 16 + row] = __float2half_rn(h);
+      const int f = fb * 16 + row;  // H row in pair order, one 64-group after another
+      static_cast<__half*>(a.H)[(size_t)(row0 + n) * a.F + (f & ~63) + hpair_pos(f & 63)] =
+          __float2half_rn(h);
     }
   }
-  (void)P;
 }
 
-// Down: CTA = (tile slot, 128 output features); each warp owns 16 features
-// over all of K = F.  Writes O[row][feature] (fp32, expert-sorted rows).
-__global__ void __launch_bounds__(kDecThreads) dec_down_kernel(const DecodeArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  const int G = a.F / 64;
-  uint32_t* xp = reinterpret_cast<uint32_t*>(smem_raw);
-  float* xs = reinterpret_cast<float*>(xp + kDecMaxRows * G * 32);
-
-  const int nob = a.d / 128;
-  const int slot = blockIdx.x / nob, ob = blockIdx.x % nob;
-  int expert, row0, rows;
-  if (!decode_tile(a, slot, expert, row0, rows)) return;
-  const uint16_t* H = static_cast<const uint16_t*>(a.H);
-  stage_rows<true>(xp, xs, rows, a.F, [&](int n, int i) { return H[(size_t)(row0 + n) * a.F + i]; });
-  __syncthreads();
-
+// Down + combine: CTA = 16 output features over every active tile slot; warp
+// w of 16 takes slots w, w + 16, ...  For each slot it runs the 16-row W4
+// GEMV over K = F against that slot's H rows (B fragments loaded straight
+// from H, kept in pair order by the gate/up kernel; group sums X_g from the
+// same loads), with the next chunk of weight groups in flight, then adds
+// gate * out into its own [token][feature] tile in shared memory.  The tiles
+// are summed in warp order, so the result is deterministic.
+constexpr int kDownWarps = 16;
+__global__ void __launch_bounds__(32 * kDownWarps) dec_down_combine_kernel(const DecodeArgs a) {
+  __shared__ float ytile[kDownWarps][kDecMaxRows][16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int feat0 = ob * 128 + warp * 16;
-  float o[4] = {0.f, 0.f, 0.f, 0.f};
-  gemv16<true>(a.dq, a.ds, a.db, (size_t)expert * a.d + feat0, a.F, xp, xs, 0, 1, o);
   const int gi = lane >> 2, c = lane & 3;
-  const int n0 = 2 * c, n1 = 2 * c + 1;
-  if (n0 < rows) {
-    a.O[(size_t)(row0 + n0) * a.d + feat0 + gi] = o[0];
-    a.O[(size_t)(row0 + n0) * a.d + feat0 + gi + 8] = o[2];
-  }
-  if (n1 < rows) {
-    a.O[(size_t)(row0 + n1) * a.d + feat0 + gi] = o[1];
-    a.O[(size_t)(row0 + n1) * a.d + feat0 + gi + 8] = o[3];
-  }
-}
-
-// y[t] = sum_j gate[t][j] * O[inv[t*k+j]] + O[P + t], in slot order (fp32,
-// or rounded once to bf16).  Grid: (T, d / 256).
-__global__ void __launch_bounds__(256) dec_combine_kernel(const DecodeArgs a) {
-  const int t = blockIdx.x;
-  const int P = a.T * a.k;
-  for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < a.d; i += gridDim.y * blockDim.x) {
-    float acc = 0.f;
-    for (int j = 0; j < a.k; ++j) {
-      const int p = t * a.k + j;
-      acc += a.gates[p] * a.O[(size_t)a.inv[p] * a.d + i];
+  const int G = a.F / 64;
+  const int f0 = blockIdx.x * 16;  // output features [f0, f0 + 16)
+  pdl_wait();
+  pdl_trigger();
+  for (int i = threadIdx.x; i < kDownWarps * kDecMaxRows * 16; i += blockDim.x)
+    (&ytile[0][0][0])[i] = 0.f;
+  __syncthreads();
+  const int nslots = 1 + min(max(*a.n_tiles, 0), a.cap);
+  const uint16_t* H = static_cast<const uint16_t*>(a.H);
+  for (int slot = warp; slot < nslots; slot += kDownWarps) {
+    int expert, row0, rows;
+    if (!decode_tile(a, slot, expert, row0, rows)) continue;
+    const size_t r0 = (size_t)expert * a.d + f0;
+    // this lane's B-fragment row: slot row n = gi (zero beyond the slot's rows)
+    const uint16_t* hrow = H + (size_t)(row0 + min(gi, rows - 1)) * a.F + c * 16;
+    WChunk wd, wn;
+    load_wchunk(wd, a.dq, a.ds, a.db, r0, a.F, 0, 1);
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int g0 = 0; g0 < G; g0 += kChunk) {
+      uint4 hh[kChunk][2];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        hh[i][0] = hh[i][1] = make_uint4(0, 0, 0, 0);
+        if (g0 + i < G && gi < rows) {
+          hh[i][0] = *reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64);
+          hh[i][1] = *reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64 + 8);
+        }
+      }
+      if (g0 + kChunk < G) load_wchunk(wn, a.dq, a.ds, a.db, r0, a.F, g0 + kChunk, 1);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        if (g0 + i < G) {
+          const uint32_t xw[8] = {hh[i][0].x, hh[i][0].y, hh[i][0].z, hh[i][0].w,
+                                  hh[i][1].x, hh[i][1].y, hh[i][1].z, hh[i][1].w};
+          // X_g of slot row gi: this lane's 16 values, then over the 4 lanes c
+          float xsum = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            xsum += __half2float(__ushort_as_half((uint16_t)(xw[e] & 0xFFFFu))) +
+                    __half2float(__ushort_as_half((uint16_t)(xw[e] >> 16)));
+          xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+          xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+          // accumulator columns 2c, 2c+1 are slot rows 2c, 2c+1: their X_g
+          const float x0 = __shfl_sync(0xffffffffu, xsum, (2 * c) * 4);
+          const float x1 = __shfl_sync(0xffffffffu, xsum, (2 * c + 1) * 4);
+          chunk_group<true>(wd, i, xw, x0, x1, o);
+        }
+      }
+      wd = wn;
     }
-    acc += a.O[(size_t)(P + t) * a.d + i];
+    // gate * out into this warp's tile: slot row n -> its token and gate
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int n = 2 * c + h;
+      if (n < rows) {
+        int tok;
+        float gate;
+        if (slot == 0) {
+          tok = n;
+          gate = 1.f;
+        } else {
+          const int p = __ldg(a.perm + row0 + n);
+          tok = p / a.k;
+          gate = __ldg(a.gates + p);
+        }
+        ytile[warp][tok][gi] += gate * o[h];
+        ytile[warp][tok][gi + 8] += gate * o[2 + h];
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.T * 16; i += blockDim.x) {
+    const int t = i >> 4, f = i & 15;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDownWarps; ++w) acc += ytile[w][t][f];
     if (a.y_f32)
-      static_cast<float*>(a.y)[(size_t)t * a.d + i] = acc;
+      static_cast<float*>(a.y)[(size_t)t * a.d + f0 + f] = acc;
     else
-      static_cast<__nv_bfloat16*>(a.y)[(size_t)t * a.d + i] = __float2bfloat16_rn(acc);
+      static_cast<__nv_bfloat16*>(a.y)[(size_t)t * a.d + f0 + f] = __float2bfloat16_rn(acc);
   }
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  if (a.T < 1 || a.T > kDecMaxRows) return cudaErrorInvalidValue;
+  if (a.T < 1 || a.T > kDecMaxRows || a.d % 16) return cudaErrorInvalidValue;
   const int slots = 1 + a.cap;
-  const size_t smem_gu = (size_t)kDecMaxRows * (a.d / 64) * (32 * 4 + 4) + 8 * 256 * 4;
-  const size_t smem_dn = (size_t)kDecMaxRows * (a.F / 64) * (32 * 4 + 4);
-  cudaError_t err;
-  if ((err = ensure_smem_attr((const void*)dec_gateup_kernel, smem_gu)) != cudaSuccess) return err;
-  if ((err = ensure_smem_attr((const void*)dec_down_kernel, smem_dn)) != cudaSuccess) return err;
   prof_begin(K_DEC_GATEUP, s);
-  dec_gateup_kernel<<<slots * (a.F / 16), kDecThreads, smem_gu, s>>>(a);
+  cudaError_t err =
+      launch_pdl(dec_gateup_kernel, dim3(slots * (a.F / 16)), dim3(kDecThreads), 0, s, a);
   prof_end(K_DEC_GATEUP, s);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   prof_begin(K_DEC_DOWN, s);
-  dec_down_kernel<<<slots * (a.d / 128), kDecThreads, smem_dn, s>>>(a);
+  err = launch_pdl(dec_down_combine_kernel, dim3(a.d / 16), dim3(32 * kDownWarps), 0, s, a);
   prof_end(K_DEC_DOWN, s);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  prof_begin(K_DEC_COMBINE, s);
-  dec_combine_kernel<<<dim3(a.T, (a.d + 255) / 256), 256, 0, s>>>(a);
-  prof_end(K_DEC_COMBINE, s);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace lily

@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -20,7 +21,7 @@ enum KernelKind : int {
   K_FINALIZE = 5,
   K_DEC_GATEUP = 6,
   K_DEC_DOWN = 7,
-  K_DEC_COMBINE = 8,
+  K_DEC_COMBINE = 8,  // (fused into K_DEC_DOWN)
   K_RMSNORM = 9,
   K_STACK_BOUNDARY = 10,
   K_MEMSET = 11,
@@ -43,6 +44,24 @@ void prof_end(int kind, cudaStream_t s);
 constexpr int kRouteTok = 32;
 constexpr int kRouteThreads = 256;
 
+// Launch with the programmatic stream-serialization attribute (the kernel
+// calls pdl_wait() before reading what its predecessor wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ---------------------------------------------------------------- routing
 struct RouteArgs {
   const float* logits_src;  // fp32 [T][E]
@@ -60,9 +79,11 @@ struct RouteArgs {
   uint32_t* bar;       // workspace: grid barrier {count, generation}
   uint32_t* status;    // workspace status word
 };
-// Router logits for T <= 8 (one warp per expert).
+// Router logits for T <= 8 (one CTA per expert); also writes x in the decode
+// GEMV's B-fragment order (xpg, [T][d/64][32] words) with its 64-group sums
+// (xsg, [T][d/64]) unless they are NULL.
 cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
-                                 int T, int d, int E, cudaStream_t s);
+                                 int T, int d, int E, uint32_t* xpg, float* xsg, cudaStream_t s);
 // Router on tensor cores for larger T: W split exactly into three bf16 terms
 // (w_split, [3][E][d]), fp32 partial logits per K-split (partial,
 // [router_splits(T,d)][T][E]) summed in order into logits (+ bias).
@@ -124,8 +145,9 @@ struct DecodeArgs {
   const uint8_t* uq; const uint16_t* us; const uint16_t* ub;
   const uint8_t* dq; const uint16_t* ds; const uint16_t* db;
   const void* x;   // bf16 [T][d]
-  void* H;         // fp16 [P+T][F]
-  float* O;        // fp32 [P+T][d]
+  const uint32_t* xpg;  // x in B-fragment pair order [T][d/64][32] (router launch)
+  const float* xsg;     // x 64-group sums [T][d/64]
+  void* H;         // fp16 [P+T][F], each 64-group in the mma pair order
   void* y;         // [T][d], fp32 if y_f32 else bf16
   bool y_f32;
   uint32_t* status;
