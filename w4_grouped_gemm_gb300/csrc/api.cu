@@ -93,7 +93,8 @@ struct Layout {
   size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, total;
 };
 
-// ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
+// ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation,
+// [3] blocks done in the small-T router launch
 Layout layout(const lily_moe_dims& d) {
   const size_t T = d.T, E = d.n_experts, k = d.top_k, F = d.d_ff, D = d.d_model;
   const size_t P = T * k;
@@ -171,29 +172,16 @@ int check_ws(const lily_moe_dims* d, void* ws, size_t bytes) {
 
 uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws)); }
 
-// Routing on `s` (logits computed unless logits_in is given).
+// Routing on `s` (logits computed unless logits_in is given).  For T <= 8
+// with computed logits the router launch runs the routing itself (its last
+// block), so no separate routing launch is made.
 int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
              const lily_moe_weights* w, const lily_moe_routing& r, void* ws, cudaStream_t s) {
   const Layout L = layout(d);
   uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
   RouteArgs a;
-  a.logits_src = logits_in;
-  if (!logits_in) {
-    if (d.T > 8) {
-      float* part = reinterpret_cast<float*>(base + L.part);
-      cudaError_t e = launch_router_tc(x, w->router_w, w->router_bias, d.T, d.d_model,
-                                       d.n_experts, base + L.w3, part, r.logits, ws_status(ws), s);
-      if (e != cudaSuccess) return LILY_ERR_CUDA;
-      a.logits_src = r.logits;
-    } else {
-      // x in the decode GEMV's fragment order, in the x16 / xs regions
-      cudaError_t e = launch_router_logits(
-          x, w->router_w, w->router_bias, r.logits, d.T, d.d_model, d.n_experts,
-          reinterpret_cast<uint32_t*>(base + L.x16), reinterpret_cast<float*>(base + L.xs), s);
-      if (e != cudaSuccess) return LILY_ERR_CUDA;
-      a.logits_src = r.logits;
-    }
-  }
+  a.logits_src = logits_in ? logits_in : r.logits;
   a.logits_dst = r.logits;
   a.T = d.T;
   a.E = d.n_experts;
@@ -209,8 +197,22 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
   a.block_map = r.block_map;
   a.n_tiles = r.n_tiles;
   a.hist = reinterpret_cast<int32_t*>(base + L.hist);
-  a.bar = reinterpret_cast<uint32_t*>(base + L.ctrl) + 1;
+  a.bar = ctrl + 1;
   a.status = ws_status(ws);
+  if (!logits_in) {
+    if (d.T > 8) {
+      float* part = reinterpret_cast<float*>(base + L.part);
+      cudaError_t e = launch_router_tc(x, w->router_w, w->router_bias, d.T, d.d_model,
+                                       d.n_experts, base + L.w3, part, r.logits, ws_status(ws), s);
+      if (e != cudaSuccess) return LILY_ERR_CUDA;
+    } else {
+      // x in the decode GEMV's fragment order, in the x16 / xs regions
+      return cuda_rc(launch_router_logits(
+          x, w->router_w, w->router_bias, r.logits, d.T, d.d_model, d.n_experts,
+          reinterpret_cast<uint32_t*>(base + L.x16), reinterpret_cast<float*>(base + L.xs), &a,
+          ctrl + 3, s));
+    }
+  }
   return cuda_rc(launch_route(a, s));
 }
 

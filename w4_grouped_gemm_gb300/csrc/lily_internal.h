@@ -82,8 +82,12 @@ struct RouteArgs {
 // Router logits for T <= 8 (one CTA per expert); also writes x in the decode
 // GEMV's B-fragment order (xpg, [T][d/64][32] words) with its 64-group sums
 // (xsg, [T][d/64]) unless they are NULL.
+// With `route` set, the block that finishes last also runs the routing
+// (route_kernel's work for one block; T <= 32) on the new logits; `done` is a
+// zero-initialised counter that returns to zero.
 cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
-                                 int T, int d, int E, uint32_t* xpg, float* xsg, cudaStream_t s);
+                                 int T, int d, int E, uint32_t* xpg, float* xsg,
+                                 const RouteArgs* route, uint32_t* done, cudaStream_t s);
 // Router on tensor cores for larger T: W split exactly into three bf16 terms
 // (w_split, [3][E][d]), fp32 partial logits per K-split (partial,
 // [router_splits(T,d)][T][E]) summed in order into logits (+ bias).

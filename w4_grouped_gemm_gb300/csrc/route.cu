@@ -18,95 +18,6 @@ namespace lily {
 // ============================================================== router logits
 // logits[t][e] = sum_i x[t][i] * W[e][i] (+ b[e]), fp32 accumulation.
 
-// Small T (decode, T <= 8): one CTA per expert row, its 8 warps split d
-// (float4 f of the row goes to warp (f / 32) % 8, lane f % 32); per-token
-// sums reduced in the warp, then over the warps in order (deterministic).
-// The same launch writes x once in the decode GEMV's B-fragment order with
-// its 64-group sums (xpg, xsg; skipped when NULL):
-//   xpg[(t*G + g)*32 + c*8 + w*4 + e] = (x[t][g*64 + c*16 + 8w + e], x[...+4])
-//   xsg[t*G + g] = sum of x[t][g*64 .. g*64+63]
-constexpr int kGemvMaxT = 8;
-constexpr int kGemvMaxPer = 4;  // float4 per lane: d <= 4096
-__global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          const float* __restrict__ w,
-                                                          const float* __restrict__ b,
-                                                          float* __restrict__ logits, int T,
-                                                          int d, int E, uint32_t* __restrict__ xpg,
-                                                          float* __restrict__ xsg) {
-  __shared__ float part[8][kGemvMaxT];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x;
-  const float4* wr = reinterpret_cast<const float4*>(w + (size_t)e * d);
-  const int n4 = d / 4;
-  float4 wv[kGemvMaxPer];
-#pragma unroll
-  for (int i = 0; i < kGemvMaxPer; ++i) {  // the weights are static: loaded before the wait
-    const int f = (i * 8 + warp) * 32 + lane;
-    wv[i] = f < n4 ? __ldg(wr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  pdl_wait();  // x comes from the predecessor
-  pdl_trigger();
-  float acc[kGemvMaxT];
-#pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.f;
-#pragma unroll
-  for (int i = 0; i < kGemvMaxPer; ++i) {
-    const int f = (i * 8 + warp) * 32 + lane;
-    if (f < n4) {
-#pragma unroll
-      for (int t = 0; t < kGemvMaxT; ++t) {
-        if (t < T) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * d) + f);
-          const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.x));
-          const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.y));
-          acc[t] = fmaf(wv[i].x, x01.x, acc[t]);
-          acc[t] = fmaf(wv[i].y, x01.y, acc[t]);
-          acc[t] = fmaf(wv[i].z, x23.x, acc[t]);
-          acc[t] = fmaf(wv[i].w, x23.y, acc[t]);
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) {
-    float v = acc[t];
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) part[warp][t] = v;
-  }
-  __syncthreads();
-  if (threadIdx.x < T) {
-    float v = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v += part[i][threadIdx.x];
-    logits[(size_t)threadIdx.x * E + e] = v + (b ? b[e] : 0.f);
-  }
-  if (xpg) {
-    const int G = d / 64;
-    const uint16_t* xh = reinterpret_cast<const uint16_t*>(x);
-    for (int u = blockIdx.x * 8 + warp; u < T * G; u += gridDim.x * 8) {
-      const int t = u / G, g = u % G;
-      const int c = lane >> 3, w2 = (lane >> 2) & 1, e4 = lane & 3;
-      const int i = g * 64 + c * 16 + 8 * w2 + e4;
-      const uint16_t lo = xh[(size_t)t * d + i], hi = xh[(size_t)t * d + i + 4];
-      xpg[(size_t)u * 32 + lane] = (uint32_t)lo | ((uint32_t)hi << 16);
-      float sum = __uint_as_float((uint32_t)lo << 16) + __uint_as_float((uint32_t)hi << 16);
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (lane == 0) xsg[u] = sum;
-    }
-  }
-}
-
-cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
-                                 int T, int d, int E, uint32_t* xpg, float* xsg, cudaStream_t s) {
-  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (T > kGemvMaxT || d > 4 * 32 * 8 * kGemvMaxPer) return cudaErrorInvalidValue;  // larger T: launch_router_tc
-  prof_begin(K_ROUTER_GEMV, s);
-  const cudaError_t err =
-      launch_pdl(router_gemv_kernel, dim3(E), dim3(256), 0, s, xb, w, b, logits, T, d, E, xpg, xsg);
-  prof_end(K_ROUTER_GEMV, s);
-  return err;
-}
-
 // ---------------------------------------------------------------- tensor cores
 // logits = x * W^T with x (bf16, exact) and W = W_hi + W_mid + W_lo, three
 // bf16 terms that together hold every bit of the fp32 W.  Each bf16 x bf16
@@ -417,7 +328,10 @@ __device__ void grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* status) 
 
 constexpr int kMaxE = 256, kMaxK = 8;
 
-__global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
+// Routing of tokens [blk * kRouteTok, ...) as block blk of nblk (the body of
+// route_kernel; also run by the last block of the small-T router launch with
+// blk = 0, nblk = 1).  Needs kRouteThreads threads.
+__device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk) {
   __shared__ int s_ids[kRouteTok * kMaxK];
   __shared__ int s_rank[kRouteTok * kMaxK];
   __shared__ int s_cnt[kMaxE];
@@ -425,10 +339,7 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
   __shared__ int s_off[kMaxE];
   __shared__ int s_scan_tmp[8];
 
-  pdl_wait();  // the logits come from the predecessor
-  pdl_trigger();
   const int T = a.T, E = a.E, k = a.k;
-  const int blk = blockIdx.x, nblk = gridDim.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blk * kRouteTok;
   const int ntok = min(kRouteTok, T - t0);
@@ -445,7 +356,7 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
 #pragma unroll
     for (int c = 0; c < kMaxE / 32; ++c) {
       const int e = lane + 32 * c;
-      lv[i][c] = (tl < ntok && e < E) ? a.logits_src[(size_t)(t0 + tl) * E + e] : 0.f;
+      lv[i][c] = (tl < ntok && e < E) ? __ldcg(a.logits_src + (size_t)(t0 + tl) * E + e) : 0.f;
     }
   }
   if (a.logits_dst != a.logits_src) {
@@ -572,6 +483,120 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
       a.block_map[2 * i + 1] = -1;
     }
   }
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
+  pdl_wait();  // the logits come from the predecessor
+  pdl_trigger();
+  route_body(a, blockIdx.x, gridDim.x);
+}
+
+// Small T (decode, T <= 8): one CTA per expert row, its 8 warps split d
+// (float4 f of the row goes to warp (f / 32) % 8, lane f % 32); per-token
+// sums reduced in the warp, then over the warps in order (deterministic).
+// The same launch writes x once in the decode GEMV's B-fragment order with
+// its 64-group sums (xpg, xsg; skipped when NULL):
+//   xpg[(t*G + g)*32 + c*8 + w*4 + e] = (x[t][g*64 + c*16 + 8w + e], x[...+4])
+//   xsg[t*G + g] = sum of x[t][g*64 .. g*64+63]
+constexpr int kGemvMaxT = 8;
+constexpr int kGemvMaxPer = 4;  // float4 per lane: d <= 4096
+__global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* __restrict__ x,
+                                                          const float* __restrict__ w,
+                                                          const float* __restrict__ b,
+                                                          float* __restrict__ logits, int T,
+                                                          int d, int E, uint32_t* __restrict__ xpg,
+                                                          float* __restrict__ xsg, const RouteArgs ra,
+                                                          uint32_t* done) {
+  __shared__ float part[8][kGemvMaxT];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x;
+  const float4* wr = reinterpret_cast<const float4*>(w + (size_t)e * d);
+  const int n4 = d / 4;
+  float4 wv[kGemvMaxPer];
+#pragma unroll
+  for (int i = 0; i < kGemvMaxPer; ++i) {  // the weights are static: loaded before the wait
+    const int f = (i * 8 + warp) * 32 + lane;
+    wv[i] = f < n4 ? __ldg(wr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait();  // x comes from the predecessor
+  pdl_trigger();
+  float acc[kGemvMaxT];
+#pragma unroll
+  for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kGemvMaxPer; ++i) {
+    const int f = (i * 8 + warp) * 32 + lane;
+    if (f < n4) {
+#pragma unroll
+      for (int t = 0; t < kGemvMaxT; ++t) {
+        if (t < T) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * d) + f);
+          const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.x));
+          const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.y));
+          acc[t] = fmaf(wv[i].x, x01.x, acc[t]);
+          acc[t] = fmaf(wv[i].y, x01.y, acc[t]);
+          acc[t] = fmaf(wv[i].z, x23.x, acc[t]);
+          acc[t] = fmaf(wv[i].w, x23.y, acc[t]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kGemvMaxT; ++t) {
+    float v = acc[t];
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) part[warp][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < T) {
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v += part[i][threadIdx.x];
+    logits[(size_t)threadIdx.x * E + e] = v + (b ? b[e] : 0.f);
+  }
+  if (xpg) {
+    const int G = d / 64;
+    const uint16_t* xh = reinterpret_cast<const uint16_t*>(x);
+    for (int u = blockIdx.x * 8 + warp; u < T * G; u += gridDim.x * 8) {
+      const int t = u / G, g = u % G;
+      const int c = lane >> 3, w2 = (lane >> 2) & 1, e4 = lane & 3;
+      const int i = g * 64 + c * 16 + 8 * w2 + e4;
+      const uint16_t lo = xh[(size_t)t * d + i], hi = xh[(size_t)t * d + i + 4];
+      xpg[(size_t)u * 32 + lane] = (uint32_t)lo | ((uint32_t)hi << 16);
+      float sum = __uint_as_float((uint32_t)lo << 16) + __uint_as_float((uint32_t)hi << 16);
+      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      if (lane == 0) xsg[u] = sum;
+    }
+  }
+  // routing by the block that finishes last (no waiting): every block makes
+  // its logits visible, then counts itself done; the last one sees them all
+  if (done) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      route_body(ra, 0, 1);
+      if (threadIdx.x == 0) *done = 0;  // back to zero for the next call
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
+                                 int T, int d, int E, uint32_t* xpg, float* xsg,
+                                 const RouteArgs* route, uint32_t* done, cudaStream_t s) {
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (T > kGemvMaxT || d > 4 * 32 * 8 * kGemvMaxPer) return cudaErrorInvalidValue;  // larger T: launch_router_tc
+  static_assert(kRouteThreads == 256, "the router launch runs the routing body");
+  RouteArgs ra = {};
+  if (route) ra = *route;
+  prof_begin(K_ROUTER_GEMV, s);
+  const cudaError_t err = launch_pdl(router_gemv_kernel, dim3(E), dim3(256), 0, s, xb, w, b,
+                                     logits, T, d, E, xpg, xsg, ra, route ? done : nullptr);
+  prof_end(K_ROUTER_GEMV, s);
+  return err;
 }
 
 int route_max_blocks() {
