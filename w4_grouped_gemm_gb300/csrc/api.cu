@@ -90,7 +90,7 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, total;
+  size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, plan, total;
 };
 
 // ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation,
@@ -112,6 +112,7 @@ Layout layout(const lily_moe_dims& d) {
   L.acc = off;
   off += up(T * D * 4);  // prefill: fp32 y accumulator
   L.tiles = off; off += up((size_t)tile_count(d.T, d.n_experts, d.top_k, d.tile_rows) * 16);
+  L.plan = off;  off += d.T <= 8 ? up((1 + lily_moe_block_map_cap(&d)) * kPlanWords * 4) : 0;
   L.total = off;
   return L;
 }
@@ -199,6 +200,7 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
   a.hist = reinterpret_cast<int32_t*>(base + L.hist);
   a.bar = ctrl + 1;
   a.status = ws_status(ws);
+  a.plan = nullptr;
   if (!logits_in) {
     if (d.T > 8) {
       float* part = reinterpret_cast<float*>(base + L.part);
@@ -206,6 +208,7 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
                                        d.n_experts, base + L.w3, part, r.logits, ws_status(ws), s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
     } else {
+      a.plan = reinterpret_cast<int32_t*>(base + L.plan);  // the decode GEMVs' slot table
       // x in the decode GEMV's fragment order, in the x16 / xs regions
       return cuda_rc(launch_router_logits(
           x, w->router_w, w->router_bias, r.logits, d.T, d.d_model, d.n_experts,
@@ -378,6 +381,7 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_wei
   a.uq = w->up_q;   a.us = w->up_s;   a.ub = w->up_b;
   a.dq = w->down_q; a.ds = w->down_s; a.db = w->down_b;
   a.x = x;
+  a.plan = reinterpret_cast<const int32_t*>(base + L.plan);
   a.xpg = reinterpret_cast<const uint32_t*>(base + L.x16);
   a.xsg = reinterpret_cast<const float*>(base + L.xs);
   a.H = base + L.H;

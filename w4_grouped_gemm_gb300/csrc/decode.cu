@@ -67,27 +67,28 @@ __host__ __device__ __forceinline__ int hpair_pos(int j) {
   return 2 * (c * 8 + w * 4 + (e & 3)) + (e >> 2);
 }
 
-// Which tile a decode CTA serves.  Slot 0 = shared expert (rows P..P+T-1);
-// slot i >= 1 = block-map tile i-1.  Returns false if the slot is unused.
+// Which tile a decode CTA serves: the routing's plan entry of the slot
+// (slot 0 = shared expert, slot i >= 1 = block-map tile i-1), one 16-byte
+// load.  Returns false if the slot is unused.
 __device__ __forceinline__ bool decode_tile(const DecodeArgs& a, int slot, int& expert, int& row0,
                                             int& rows) {
-  const int P = a.T * a.k;
-  if (slot == 0) {
-    expert = a.E;
-    row0 = P;
-    rows = a.T;
-    return true;
-  }
-  const int ti = slot - 1;
-  if (ti >= *a.n_tiles) return false;
-  expert = a.block_map[2 * ti];
-  row0 = a.block_map[2 * ti + 1];
-  if (expert < 0 || expert >= a.E || row0 < 0 || row0 >= P) {
+  const int4 h = __ldcg(reinterpret_cast<const int4*>(a.plan + (size_t)slot * kPlanWords));
+  expert = h.x;
+  row0 = h.y;
+  rows = h.z;
+  if (rows <= 0) return false;
+  if (expert < 0 || expert > a.E || rows > kDecMaxRows) {
     if (threadIdx.x == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
     return false;
   }
-  rows = min(kDecMaxRows, a.offsets[expert + 1] - row0);
-  return rows > 0;
+  return true;
+}
+// Token and gate of row n of a slot (from the plan).
+__device__ __forceinline__ int plan_token(const DecodeArgs& a, int slot, int n) {
+  return __ldcg(a.plan + (size_t)slot * kPlanWords + 8 + n);
+}
+__device__ __forceinline__ float plan_gate(const DecodeArgs& a, int slot, int n) {
+  return __int_as_float(__ldcg(a.plan + (size_t)slot * kPlanWords + 16 + n));
 }
 
 // Up to kChunk groups of 16 weight rows [r0, r0+16) of one packed matrix
@@ -174,10 +175,7 @@ __global__ void __launch_bounds__(kDecThreads) dec_gateup_kernel(const DecodeArg
     load_wchunk(wg, a.gq, a.gs, a.gb, r0, a.d, warp, 8);
     load_wchunk(wu, a.uq, a.us, a.ub, r0, a.d, warp, 8);
   }
-  if (threadIdx.x < kDecMaxRows) {
-    const int n = min((int)threadIdx.x, rows - 1);
-    tok[threadIdx.x] = (slot == 0) ? n : a.perm[row0 + n] / a.k;
-  }
+  if (threadIdx.x < kDecMaxRows) tok[threadIdx.x] = plan_token(a, slot, min((int)threadIdx.x, rows - 1));
   __syncthreads();
   // B-fragment row of this lane: slot row gi (zero beyond the slot's rows);
   // group sums of accumulator columns 2c, 2c+1
@@ -253,7 +251,7 @@ __global__ void __launch_bounds__(32 * kDownWarps) dec_down_combine_kernel(const
   for (int i = threadIdx.x; i < kDownWarps * kDecMaxRows * 16; i += blockDim.x)
     (&ytile[0][0][0])[i] = 0.f;
   __syncthreads();
-  const int nslots = 1 + min(max(*a.n_tiles, 0), a.cap);
+  const int nslots = 1 + a.cap;  // unused slots have rows = 0 in the plan
   const uint16_t* H = static_cast<const uint16_t*>(a.H);
   for (int slot = warp; slot < nslots; slot += kDownWarps) {
     int expert, row0, rows;
@@ -301,16 +299,8 @@ __global__ void __launch_bounds__(32 * kDownWarps) dec_down_combine_kernel(const
     for (int h = 0; h < 2; ++h) {
       const int n = 2 * c + h;
       if (n < rows) {
-        int tok;
-        float gate;
-        if (slot == 0) {
-          tok = n;
-          gate = 1.f;
-        } else {
-          const int p = __ldg(a.perm + row0 + n);
-          tok = p / a.k;
-          gate = __ldg(a.gates + p);
-        }
+        const int tok = plan_token(a, slot, n);
+        const float gate = plan_gate(a, slot, n);
         ytile[warp][tok][gi] += gate * o[h];
         ytile[warp][tok][gi + 8] += gate * o[2 + h];
       }

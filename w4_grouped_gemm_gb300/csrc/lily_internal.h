@@ -78,7 +78,12 @@ struct RouteArgs {
   int32_t* hist;       // workspace [nblk][E]
   uint32_t* bar;       // workspace: grid barrier {count, generation}
   uint32_t* status;    // workspace status word
+  int32_t* plan;       // decode plan [1 + cap][kPlanWords] or NULL (one-block routing only)
 };
+// Decode plan entry of one tile slot: {expert, row0, rows, 0, 4 unused,
+// token[kPlanRows], gate bits[kPlanRows], 8 unused}.
+constexpr int kPlanWords = 32;
+constexpr int kPlanRows = 8;
 // Router logits for T <= 8 (one CTA per expert); also writes x in the decode
 // GEMV's B-fragment order (xpg, [T][d/64][32] words) with its 64-group sums
 // (xsg, [T][d/64]) unless they are NULL.
@@ -149,6 +154,7 @@ struct DecodeArgs {
   const uint8_t* uq; const uint16_t* us; const uint16_t* ub;
   const uint8_t* dq; const uint16_t* ds; const uint16_t* db;
   const void* x;   // bf16 [T][d]
+  const int32_t* plan;  // per tile slot {expert, row0, rows, tokens, gates} (routing)
   const uint32_t* xpg;  // x in B-fragment pair order [T][d/64][32] (router launch)
   const float* xsg;     // x 64-group sums [T][d/64]
   void* H;         // fp16 [P+T][F], each 64-group in the mma pair order

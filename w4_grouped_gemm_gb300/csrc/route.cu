@@ -428,22 +428,29 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
     atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) a.hist[(size_t)blk * E + e] = s_cnt[e];
+  if (nblk > 1) {
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) a.hist[(size_t)blk * E + e] = s_cnt[e];
 
-  grid_barrier(a.bar, nblk, a.status);
+    grid_barrier(a.bar, nblk, a.status);
 
-  // ---- phase 3: global counts, scan, this block's bases, scatter
-  for (int e = threadIdx.x; e < kMaxE; e += kRouteThreads) {
-    int cnt = 0, before = 0;
-    if (e < E) {
-      for (int b = 0; b < nblk; ++b) {
-        int h = __ldcg(&a.hist[(size_t)b * E + e]);
-        cnt += h;
-        before += (b < blk) ? h : 0;
+    // ---- phase 3: global counts, scan, this block's bases, scatter
+    for (int e = threadIdx.x; e < kMaxE; e += kRouteThreads) {
+      int cnt = 0, before = 0;
+      if (e < E) {
+        for (int b = 0; b < nblk; ++b) {
+          int h = __ldcg(&a.hist[(size_t)b * E + e]);
+          cnt += h;
+          before += (b < blk) ? h : 0;
+        }
       }
+      s_cnt[e] = cnt;
+      s_before[e] = before;
     }
-    s_cnt[e] = cnt;
-    s_before[e] = before;
+  } else {  // one block: its histogram is the global one
+    for (int e = threadIdx.x; e < kMaxE; e += kRouteThreads) {
+      if (e >= E) s_cnt[e] = 0;
+      s_before[e] = 0;
+    }
   }
   __syncthreads();
   // kRouteThreads == kMaxE: one expert per thread
@@ -481,6 +488,47 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
     for (int i = s_total + threadIdx.x; i < a.cap; i += kRouteThreads) {
       a.block_map[2 * i] = -1;
       a.block_map[2 * i + 1] = -1;
+    }
+    // decode plan (small T, one block): per slot {expert, row0, rows, 0,
+    // -, -, -, -, token[8], gate bits[8], -...}, slot 0 = the shared expert,
+    // slot i >= 1 = tile i-1; read back from this block's own global stores
+    if (a.plan) {
+      __syncthreads();
+      const int P = T * k;
+      for (int slot = threadIdx.x; slot < 1 + a.cap; slot += kRouteThreads) {
+        int32_t* pl = a.plan + (size_t)slot * kPlanWords;
+        int e = -1, row0 = 0, rows = 0;
+        if (slot == 0) {
+          e = E;
+          row0 = P;
+          rows = T;
+        } else if (slot - 1 < s_total) {
+          e = __ldcg(a.block_map + 2 * (slot - 1));
+          row0 = __ldcg(a.block_map + 2 * (slot - 1) + 1);
+          rows = min(a.BM, __ldcg(a.offsets + e + 1) - row0);
+        }
+        rows = min(rows, kPlanRows);
+        pl[0] = e;
+        pl[1] = row0;
+        pl[2] = rows;
+        pl[3] = 0;
+        for (int n = 0; n < kPlanRows; ++n) {
+          int tok = 0;
+          float g = 0.f;
+          if (n < rows) {
+            if (slot == 0) {
+              tok = n;
+              g = 1.f;
+            } else {
+              const int p = __ldcg(a.perm + row0 + n);
+              tok = p / k;
+              g = __ldcg(a.gates + p);
+            }
+          }
+          pl[8 + n] = tok;
+          pl[16 + n] = __float_as_int(g);
+        }
+      }
     }
   }
 }
