@@ -42,6 +42,7 @@ WORKLOADS = {
     "prefill2048": (2048, 2048, 256, 8, 512, None),
     "decode1": (1, 2048, 256, 8, 512, None),
     "decode5": (5, 2048, 256, 8, 512, None),
+    "prefill8192": (8192, 2048, 256, 8, 512, None),  # one unchunked call
     "small": (32, 512, 32, 4, 128, None),
 }
 DEFAULT_WORKLOAD = "prefill512"
@@ -431,6 +432,12 @@ def run_lily(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if decode and graph is not None:
+        # the graph replays nl consecutive layers (each its own weights, chained
+        # with programmatic dependent launch): one token through an nl-layer
+        # MoE stack
+        out["config"]["stack_layers"] = nl
+        out["config"]["stack_step_us"] = 1e3 * ms / args.steps * nl
     print(json.dumps(out), flush=True)
 
 

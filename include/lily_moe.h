@@ -66,7 +66,7 @@ extern "C" {
  * d_ff       expert SwiGLU width F; multiple of 128, 128 <= F <= 4096
  * group      quantisation group; must be 64
  * tile_rows  BM, rows of one block-map tile (the grouped GEMM's N tile);
- *            one of 32, 64, 128
+ *            one of 16, 32, 64, 128
  * out_dtype  element type of the layer output y: LILY_DTYPE_F32 (the fp32
  *            accumulator itself) or LILY_DTYPE_BF16 (rounded once)
  */

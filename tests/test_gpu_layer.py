@@ -32,7 +32,7 @@ def _check_forward(L, rows=None, decode=False):
 
 # ------------------------------------------------------------ full-layer, small
 
-@pytest.mark.parametrize("bm", [32, 64, 128])
+@pytest.mark.parametrize("bm", [16, 32, 64, 128])
 def test_small_layer_all_tile_rows(oracle_lib, bm):
     _check_forward(Layer(synth.SHAPES["small"], seed=1000, tile_rows=bm))
 

@@ -301,7 +301,7 @@ int lily_moe_check_dims(const lily_moe_dims* d) {
   if (d->group != 64) return LILY_ERR_UNSUPPORTED_SHAPE;
   if (d->out_dtype != LILY_DTYPE_BF16 && d->out_dtype != LILY_DTYPE_F32)
     return LILY_ERR_UNSUPPORTED_SHAPE;
-  if (d->tile_rows != 32 && d->tile_rows != 64 && d->tile_rows != 128)
+  if (d->tile_rows != 16 && d->tile_rows != 32 && d->tile_rows != 64 && d->tile_rows != 128)
     return LILY_ERR_UNSUPPORTED_SHAPE;
   if (gemm_stages(true, d->tile_rows, d->d_model) < 2 || gemm_stages(false, d->tile_rows, d->d_ff) < 2)
     return LILY_ERR_UNSUPPORTED_SHAPE;

@@ -741,6 +741,7 @@ template <bool GATEUP>
 static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const CUtensorMap& q1,
                                const CUtensorMap& b, const CUtensorMap& b2, cudaStream_t s) {
   switch (a.BM) {
+    case 16: return launch_gemm_bm<GATEUP, 16>(a, q0, q1, b, b2, s);
     case 32: return launch_gemm_bm<GATEUP, 32>(a, q0, q1, b, b2, s);
     case 64: return launch_gemm_bm<GATEUP, 64>(a, q0, q1, b, b2, s);
     case 128: return launch_gemm_bm<GATEUP, 128>(a, q0, q1, b, b2, s);
