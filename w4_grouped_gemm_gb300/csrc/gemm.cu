@@ -180,40 +180,54 @@ __device__ __forceinline__ bool next_item(const GemmArgs& a, int& w, int n_items
 
 // Scale/bias table of one item: sb[mat][g][r] = (fp16 scale | fp16 bias << 16)
 // for the item's 128 weight rows r and every group g.  Filled by the epilogue
-// threads, thread r owning row r.  One 16-byte chunk = 8 groups of one array
-// (scale or bias) of one matrix; chunk q -> (mat, array, 8-group block).
-__device__ __forceinline__ uint4 scale_chunk_load(const GemmArgs& a, size_t row, int G, int q) {
-  const int per = G / 8;
-  const int mat = q / (2 * per), arr = (q / per) & 1, ch = q % per;
-  const uint16_t* src = mat == 0 ? (arr ? a.b0 : a.s0) : (arr ? a.b1 : a.s1);
-  return __ldg(reinterpret_cast<const uint4*>(src + row * G + ch * 8));
-}
-__device__ __forceinline__ void scale_chunk_store(uint16_t* sbh, int G, int q, int r, uint4 v) {
-  const int per = G / 8;
-  const int mat = q / (2 * per), arr = (q / per) & 1, ch = q % per;
-  const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
-#pragma unroll
-  for (int e = 0; e < 8; ++e)
-    sbh[2 * ((mat * G + ch * 8 + e) * 128 + r) + arr] = bf16_to_f16_bits(h[e]);
-}
+// threads, thread r owning row r: 16-byte loads of 8 scales and the 8
+// matching biases, one f16x2 conversion and one 4-byte store per group.
 template <int MATS>
-__device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint16_t* sbh) {
+__device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint32_t* sbw) {
   if ((G & 7) == 0) {
-    const int nq = MATS * 2 * (G / 8);
-    for (int base = 0; base < nq; base += 8) {
-      uint4 v[8];
+    const int per = G / 8;
+    const int npair = MATS * per;  // (matrix, 8-group chunk) pairs
+    for (int base = 0; base < npair; base += 4) {
+      uint4 vs[4], vb[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (base + j < nq) v[j] = scale_chunk_load(a, row, G, base + j);
+      for (int j = 0; j < 4; ++j) {
+        const int q = base + j;
+        if (q < npair) {
+          const int mat = q / per, ch = q % per;
+          const uint16_t* sp = (mat == 0 ? a.s0 : a.s1) + row * G + ch * 8;
+          const uint16_t* bp = (mat == 0 ? a.b0 : a.b1) + row * G + ch * 8;
+          vs[j] = __ldg(reinterpret_cast<const uint4*>(sp));
+          vb[j] = __ldg(reinterpret_cast<const uint4*>(bp));
+        }
+      }
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (base + j < nq) scale_chunk_store(sbh, G, base + j, r, v[j]);
+      for (int j = 0; j < 4; ++j) {
+        const int q = base + j;
+        if (q < npair) {
+          const int mat = q / per, ch = q % per;
+          const uint32_t ws[4] = {vs[j].x, vs[j].y, vs[j].z, vs[j].w};
+          const uint32_t wb[4] = {vb[j].x, vb[j].y, vb[j].z, vb[j].w};
+          uint32_t* dst = sbw + (size_t)(mat * G + ch * 8) * 128 + r;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {  // groups 2u (low halves) and 2u+1 (high halves)
+            const __half2 lo = __floats2half2_rn(__uint_as_float(ws[u] << 16),
+                                                 __uint_as_float(wb[u] << 16));
+            const __half2 hi = __floats2half2_rn(__uint_as_float(ws[u] & 0xFFFF0000u),
+                                                 __uint_as_float(wb[u] & 0xFFFF0000u));
+            dst[(2 * u) * 128] = *reinterpret_cast<const uint32_t*>(&lo);
+            dst[(2 * u + 1) * 128] = *reinterpret_cast<const uint32_t*>(&hi);
+          }
+        }
+      }
     }
   } else {
-    for (int q = 0; q < MATS * 2 * G; ++q) {
-      const int mat = q / (2 * G), arr = (q / G) & 1, g = q % G;
-      const uint16_t* src = mat == 0 ? (arr ? a.b0 : a.s0) : (arr ? a.b1 : a.s1);
-      sbh[2 * ((mat * G + g) * 128 + r) + arr] = bf16_to_f16_bits(__ldg(src + row * G + g));
+    for (int q = 0; q < MATS * G; ++q) {
+      const int mat = q / G, g = q % G;
+      const uint16_t* sp = mat == 0 ? a.s0 : a.s1;
+      const uint16_t* bp = mat == 0 ? a.b0 : a.b1;
+      sbw[(size_t)(mat * G + g) * 128 + r] =
+          (uint32_t)bf16_to_f16_bits(__ldg(sp + row * G + g)) |
+          ((uint32_t)bf16_to_f16_bits(__ldg(bp + row * G + g)) << 16);
     }
   }
 }
@@ -572,8 +586,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // registers, (3) drain item j's accumulators to global memory.
     const int q = warp & 3;  // TMEM lane quadrant of this warp
     const int r = threadIdx.x - 32 * kEpiWarp0;
-    uint16_t* sbh = reinterpret_cast<uint16_t*>(sb);
-    auto slot_ptr = [&](int slot) { return sbh + (size_t)slot * sb_words * 2; };
+    auto slot_ptr = [&](int slot) { return sb + (size_t)slot * sb_words; };
     auto row_of = [&](const Item& it) {
       return (size_t)it.expert * NOUT + (size_t)it.slice * 128 + r;
     };
