@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc = idesc_f16_f32(128, N);
       const int ab = titem % NACC;
       if (titem >= (uint32_t)NACC &&
-          !warp_wait(smem_u32(&accempty[ab]), ((titem / NACC) + 1) & 1, abort, a.status))
+          !warp_wait_all(smem_u32(&accempty[ab]), ((titem / NACC) + 1) & 1, abort, a.status))
         break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * L::kAccCols;
