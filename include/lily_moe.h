@@ -156,6 +156,21 @@ int lily_moe_forward(const lily_moe_dims* dims, const void* x,
                      const lily_moe_weights* weights, lily_moe_routing* routing,
                      void* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The expert part of lily_moe_forward alone: the gate/up and down grouped
+ * GEMMs (shared expert included) from routing already in `routing` --
+ * topk_gates, offsets, perm, block_map and n_tiles as lily_moe_route writes
+ * them, e.g. from that call or built by the caller (page "Revolutionizing
+ * Local AI Inference on Apple Silicon", section "Enhanced Tile and Scan
+ * Operations": the dispatch tables feed the expert GEMMs).  With the same
+ * routing the result equals lily_moe_forward's.  A perm entry outside
+ * [0, T*k) or a block-map tile outside the pairs sets LILY_STATUS_BAD_TILE
+ * and is clamped, never read out of bounds.
+ *   x  bf16 [T][d] device in; y [T][d] device out, fp32 or bf16 per
+ *   dims->out_dtype. */
+int lily_moe_experts(const lily_moe_dims* dims, const void* x,
+                     const lily_moe_weights* weights, const lily_moe_routing* routing,
+                     void* y, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Same result as lily_moe_forward for T = 1..8 rows (batch-1 decode and
  * speculative-verify sizes), through the bandwidth-bound W4 GEMV path that
  * streams each distinct active expert's weights once. */

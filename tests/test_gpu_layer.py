@@ -162,3 +162,47 @@ def test_bf16_output_is_rounded_fp32_output(oracle_lib, decode):
     assert Lb.y.dtype == torch.bfloat16
     bound = yf.abs() * 2.0 ** -8 + 1e-6 * yf.pow(2).mean().sqrt()
     assert bool(((yb - yf).abs() <= bound).all())
+
+
+def test_experts_entry_with_host_routing(oracle_lib):
+    """lily_moe_experts on routing built on the host (the oracle's routing of
+    the GPU's fp32 logits, uploaded) reproduces lily_moe_forward: the same
+    routing and expert kernels; only the order of the fp32 atomic adds that
+    combine the experts into y can differ, so the bound is a few fp32 ulps."""
+    L = Layer(synth.SHAPES["small"], seed=4242, tile_rows=32)
+    y_fwd = L.forward().clone()
+    ro = L.oracle_route()
+    r2 = lily.RoutingBuffers(L.dims)
+    dev = r2.perm.device
+
+    def up(a, like):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev, like.dtype).reshape(like.shape)
+
+    r2.logits.copy_(L.r.logits)
+    r2.topk_gates.copy_(L.r.topk_gates)  # fp32 gates as the GPU computed them
+    r2.topk_ids.copy_(up(ro["ids"], r2.topk_ids))
+    r2.counts.copy_(up(ro["counts"], r2.counts))
+    r2.offsets.copy_(up(ro["offsets"], r2.offsets))
+    r2.perm.copy_(up(ro["perm"], r2.perm))
+    r2.inv_perm.copy_(up(ro["inv"], r2.inv_perm))
+    r2.block_map.copy_(up(ro["block_map"], r2.block_map))
+    r2.n_tiles.fill_(ro["n_tiles"])
+    y2 = torch.empty_like(y_fwd)
+    lily.lily_moe_experts(L.dims, L.x, L.w, r2, y2, L.ws)
+    torch.cuda.synchronize()
+    assert L.status() == 0
+    scale = float(y_fwd.abs().max())
+    assert float((y2 - y_fwd).abs().max()) <= 1e-5 * scale
+
+
+def test_experts_entry_flags_bad_perm(oracle_lib):
+    """Out-of-range perm entries are clamped and flagged, never read out of
+    bounds."""
+    L = Layer(synth.SHAPES["small"], seed=4343, tile_rows=32)
+    L.forward()
+    assert L.status() == 0
+    L.r.perm[3] = 1 << 20
+    y2 = torch.empty_like(L.y)
+    lily.lily_moe_experts(L.dims, L.x, L.w, L.r, y2, L.ws)
+    torch.cuda.synchronize()
+    assert L.status() & lily.LILY_STATUS_BAD_TILE

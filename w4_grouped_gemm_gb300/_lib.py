@@ -32,7 +32,8 @@ LILY_KERNEL_KINDS = 16
 # Every symbol include/lily_moe.h declares.
 EXPORTS = (
     "lily_moe_workspace_bytes", "lily_moe_block_map_cap", "lily_moe_check_dims",
-    "lily_moe_route", "lily_moe_forward", "lily_moe_decode", "lily_moe_decode_static",
+    "lily_moe_route", "lily_moe_forward", "lily_moe_experts", "lily_moe_decode",
+    "lily_moe_decode_static",
     "lily_moe_forward_host",
     "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_workspace_bytes",
     "lily_moe_status", "lily_moe_strerror", "lily_moe_profile_enable", "lily_moe_profile_read",
@@ -88,6 +89,7 @@ def lib():
             "lily_moe_check_dims": (I, [DP]),
             "lily_moe_route": (I, [DP, P, P, WP, RP, P, SZ, P]),
             "lily_moe_forward": (I, [DP, P, WP, RP, P, P, SZ, P]),
+            "lily_moe_experts": (I, [DP, P, WP, RP, P, P, SZ, P]),
             "lily_moe_decode": (I, [DP, P, WP, RP, P, P, SZ, P]),
             "lily_moe_decode_static": (I, [DP, P, WP, RP, P, P]),
             "lily_moe_forward_host": (I, [DP, P, P, WP, RP, P, P, P, SZ, P]),
@@ -218,6 +220,14 @@ def lily_moe_forward(dims, x, weights: LayerWeights, routing: RoutingBuffers, y,
                                 ctypes.byref(routing.c), _ptr(y), _ptr(ws), ws.numel(),
                                 _stream(stream))
     _check(rc, "lily_moe_forward")
+
+
+def lily_moe_experts(dims, x, weights: LayerWeights, routing: RoutingBuffers, y, ws, stream=None):
+    """The expert GEMMs alone, from routing already in `routing`."""
+    rc = lib().lily_moe_experts(ctypes.byref(dims), _ptr(x), ctypes.byref(weights.c),
+                                ctypes.byref(routing.c), _ptr(y), _ptr(ws), ws.numel(),
+                                _stream(stream))
+    _check(rc, "lily_moe_experts")
 
 
 def lily_moe_decode(dims, x, weights: LayerWeights, routing: RoutingBuffers, y, ws, stream=None):

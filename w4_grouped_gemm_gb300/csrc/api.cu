@@ -248,10 +248,11 @@ GemmArgs gemm_args(const lily_moe_dims& d, const lily_moe_weights* w, const lily
 
 // Routing + grouped GEMMs.  The layer output is accumulated in fp32 into
 // yacc (the workspace accumulator when NULL).
-int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
+// The grouped GEMMs (token rows, gate/up + SwiGLU, down + gated combine)
+// from routing already in r.  The layer output is accumulated in fp32 into
+// yacc (the workspace accumulator when NULL).
+int do_experts_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
                    const lily_moe_routing& r, void* ws, cudaStream_t s, float* yacc = nullptr) {
-  int rc = do_route(d, x, nullptr, w, r, ws, s);
-  if (rc) return rc;
   GemmArgs a = gemm_args(d, w, r, ws);
   if (yacc) a.yacc = yacc;
   if (!aligned16(a.yacc)) return LILY_ERR_MISALIGNED;
@@ -266,6 +267,14 @@ int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights
   a.b1 = nullptr;
   if (launch_down(a, w->down_q, s) != cudaSuccess) return LILY_ERR_CUDA;
   return LILY_OK;
+}
+
+// Routing + grouped GEMMs.
+int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
+                   const lily_moe_routing& r, void* ws, cudaStream_t s, float* yacc = nullptr) {
+  const int rc = do_route(d, x, nullptr, w, r, ws, s);
+  if (rc) return rc;
+  return do_experts_acc(d, x, w, r, ws, s, yacc);
 }
 
 int common_checks(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
@@ -338,6 +347,19 @@ int lily_moe_route(const lily_moe_dims* dims, const void* x, const float* logits
   const int maxb = route_max_blocks();
   if (maxb > 0 && (dims->T + kRouteTok - 1) / kRouteTok > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
   return do_route(*dims, x, logits_in, w, *r, ws, (cudaStream_t)stream);
+}
+
+int lily_moe_experts(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
+                     const lily_moe_routing* r, void* y, void* ws, size_t ws_bytes, void* stream) {
+  int rc = common_checks(dims, x, w, r, y, ws, ws_bytes, true);
+  if (rc) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (dims->out_dtype == LILY_DTYPE_F32)
+    return do_experts_acc(*dims, x, w, *r, ws, s, static_cast<float*>(y));
+  if ((rc = do_experts_acc(*dims, x, w, *r, ws, s))) return rc;
+  const Layout L = layout(*dims);
+  return cuda_rc(launch_finalize(reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.acc), y,
+                                 (int64_t)dims->T * dims->d_model, s));
 }
 
 int lily_moe_forward(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,

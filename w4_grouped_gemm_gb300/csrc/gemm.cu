@@ -241,7 +241,7 @@ __device__ __forceinline__ void row_token_gate(const GemmArgs& a, const Item& it
     tok = rj - P;
     g = 1.f;
   } else {
-    const int p = __ldg(a.perm + rj);
+    const int p = min(max(__ldg(a.perm + rj), 0), P - 1);  // out-of-range entries were flagged
     tok = p / a.k;
     g = __ldg(a.gates + p);
   }
@@ -811,15 +811,24 @@ __global__ void __launch_bounds__(256) token_rows_kernel(const uint4* __restrict
     } else if (t - nsh < ntiles) {
       const int e = __ldg(a.block_map + 2 * (t - nsh)), row0 = __ldg(a.block_map + 2 * (t - nsh) + 1);
       if (e >= 0 && e < a.E && row0 >= 0 && row0 < P) {
-        const int rows = min(a.BM, __ldg(a.offsets + e + 1) - row0);
+        const int rows = min(min(a.BM, __ldg(a.offsets + e + 1) - row0), P - row0);
         if (rows > 0) v = make_int4(e, row0, rows, 0);
+      } else {
+        set_status(a.status, LILY_STATUS_BAD_TILE);
       }
     }
     a.tiles[t] = v;
   }
   bool ok = true;
   for (int row = blockIdx.x * 8 + warp; row < P + T; row += gridDim.x * 8) {
-    const int tok = row < P ? __ldg(perm + row) / k : row - P;
+    int tok = row - P;
+    if (row < P) {
+      const int p = __ldg(perm + row);
+      if (p < 0 || p >= P) {  // not a permutation entry: flagged, row 0 used
+        if (lane == 0) set_status(status, LILY_STATUS_BAD_TILE);
+      }
+      tok = min(max(p, 0), P - 1) / k;
+    }
     const uint4* src = x + (size_t)tok * d8;
     uint4* dst = row < P ? xs + (size_t)row * d8 : x16 + (size_t)(row - P) * d8;
     for (int c = lane; c < d8; c += 32) dst[c] = bf8_to_h8_kchunk(__ldg(src + c), ok);
