@@ -441,6 +441,113 @@ def run_lily(args, world, rank, local):
     print(json.dumps(out), flush=True)
 
 
+def run_ablation(args, world, rank, local):
+    """Bench-only ablations of two design points of the path, each timed eagerly
+    against the fused path in the same run (one JSON line):
+      host_routing -- routing on the GPU, then a host sync, a copy of the
+        counts to the host, the block map built on the host and copied back,
+        then the expert GEMMs (lily_moe_experts);
+      dequant_hbm -- every expert's weights dequantised to fp16 in HBM each
+        step (torch element-wise ops: unpack, then one multiply-add pass),
+        then batched fp16 GEMMs (torch.bmm, cuBLAS) over expert-padded rows,
+        with the same GPU routing.
+    Both check their layer output against the fused path's."""
+    import w4_grouped_gemm_gb300 as lily
+    from w4_grouped_gemm_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    T, d, E, k, F, zipf = WORKLOADS[args.workload]
+    if T <= 8:
+        raise SystemExit("ablations are prefill-only")
+    shape = synth.LayerShape(T, d, E, k, F)
+    dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
+    inp = synth.make_layer(shape, 1000 * 2 + 17, device=dev, zipf_s=zipf)
+    x = inp["x"]
+    w = lily.LayerWeights(inp["router_w"], inp["router_b"], inp["experts"])
+    r = lily.RoutingBuffers(dims, dev)
+    ws = lily.alloc_workspace(lily.lily_moe_workspace_bytes(dims), dev)
+    y_ref = torch.empty(T, d, dtype=torch.float32, device=dev)
+    y = torch.empty_like(y_ref)
+    BM, P, cap = args.tile_rows, T * k, lily.lily_moe_block_map_cap(dims)
+
+    def fused():
+        lily.lily_moe_forward(dims, x, w, r, y_ref, ws)
+
+    def host_routing():
+        lily.lily_moe_route(dims, x, None, w, r, ws)
+        counts = r.counts.cpu().numpy()  # waits for the routing, copies to the host
+        off = np.concatenate([[0], np.cumsum(counts)])
+        tiles = [(e, off[e] + i * BM) for e in range(E) for i in range(-(-int(counts[e]) // BM))]
+        bm = np.full((cap, 2), -1, np.int32)
+        bm[:len(tiles)] = np.asarray(tiles, np.int32).reshape(-1, 2)
+        r.block_map.copy_(torch.from_numpy(bm))
+        r.n_tiles.fill_(len(tiles))
+        lily.lily_moe_experts(dims, x, w, r, y, ws)
+
+    ex = inp["experts"]
+
+    def deq(q, sc, bi):  # fp16 [n][rows][cols] = scale * q + bias, in HBM
+        n, rows, half = q.shape
+        qq = torch.stack((q & 15, q >> 4), dim=-1).view(n, rows, half * 2 // 64, 64).half()
+        return torch.addcmul(bi.half()[..., None], qq, sc.half()[..., None]).view(n, rows, -1)
+
+    def dequant_hbm():
+        lily.lily_moe_route(dims, x, None, w, r, ws)
+        wg = deq(ex["gate_q"], ex["gate_s"], ex["gate_b"])
+        wu = deq(ex["up_q"], ex["up_s"], ex["up_b"])
+        wd = deq(ex["down_q"], ex["down_s"], ex["down_b"])
+        pad = int(r.counts.max())
+        pos = torch.arange(P, device=dev)
+        e_of = torch.searchsorted(r.offsets[1:].contiguous(), pos.int(), right=True)
+        slot = pos - r.offsets[e_of].long()
+        p = r.perm.long()
+        tok = p // k
+        gate = r.topk_gates.reshape(-1)[p]
+        xh = x.half()
+        X = torch.zeros(E, pad, d, dtype=torch.half, device=dev)
+        X[e_of, slot] = xh[tok]
+        H = torch.nn.functional.silu(torch.bmm(X, wg[:E].transpose(1, 2))) * torch.bmm(
+            X, wu[:E].transpose(1, 2))
+        O = torch.bmm(H, wd[:E].transpose(1, 2))
+        y.zero_()
+        y.index_add_(0, tok, O[e_of, slot].float() * gate[:, None])
+        hs = torch.nn.functional.silu(xh @ wg[E].t()) * (xh @ wu[E].t())
+        y.add_((hs @ wd[E].t()).float())
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / n
+
+    abl = {"host_routing": host_routing, "dequant_hbm": dequant_hbm}[args.ablation]
+    n = max(3, min(args.steps, 50))
+    t_fused = timed(fused, n)
+    t_abl = timed(abl, n)
+    fused()
+    abl()
+    torch.cuda.synchronize()
+    err = float((y - y_ref).abs().max() / y_ref.pow(2).mean().sqrt())
+    out = {
+        "metric": METRIC, "value": T / t_abl, "unit": UNIT, "n_gpus": 1, "steps": n,
+        "warmup": 3, "ms_per_step": 1e3 * t_abl, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp16 weights in HBM" if args.ablation == "dequant_hbm"
+        else "f16 tensor-core operands (W4 weights, bf16 x), fp32 accumulate, fp32 out",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "impl": "lily", "ablation": args.ablation,
+        "config": {"workload": args.workload, "T": T, "tile_rows": BM, "launch": "eager",
+                   "fused_eager_us": 1e6 * t_fused, "ablation_us": 1e6 * t_abl,
+                   "slowdown_vs_fused": t_abl / t_fused,
+                   "max_err_vs_fused_over_rms": err},
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -454,6 +561,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (profiling)")
     ap.add_argument("--eager", action="store_true", help="time eager launches, no CUDA graph")
+    ap.add_argument("--ablation", choices=["host_routing", "dequant_hbm"], default=None,
+                    help="bench-only ablation of a design point (prefill workloads)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_info()
@@ -465,6 +574,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.ablation:
+            run_ablation(args, world, rank, local)
         else:
             run_lily(args, world, rank, local)
     finally:
