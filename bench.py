@@ -51,7 +51,10 @@ DEFAULT_WORKLOAD = "prefill512"
 # by workload and by a hash of the kernel's source files: a changed kernel
 # reports null until it is profiled again.
 KERNEL_SOURCES = ["w4_grouped_gemm_gb300/csrc/gemm.cu", "w4_grouped_gemm_gb300/csrc/common.cuh"]
-NCU_TRAFFIC = {}  # {(workload, kernel, source_hash): bytes}
+NCU_TRAFFIC = {  # {(workload, kernel, source_hash): bytes}
+    # ncu --set full, w4_gemm_kernel<1, 64>, prefill512 layer: 322.19 MB read + 6.44 MB written
+    ("prefill512", "gateup_gemm", "c961518f6586c5ef"): 328623872,
+}
 
 
 def source_hash(files) -> str:
@@ -533,6 +536,14 @@ def run_ablation(args, world, rank, local):
     abl()
     torch.cuda.synchronize()
     err = float((y - y_ref).abs().max() / y_ref.pow(2).mean().sqrt())
+    floor_us = None
+    if args.ablation == "dequant_hbm":
+        # HBM floor of this path whatever its kernels: read the packed weights,
+        # write them as fp16, read the fp16 weights back in the GEMMs
+        hbm, _, _, _ = measured_peaks()
+        packed = sum(t.numel() * t.element_size() for t in ex.values())
+        fp16 = sum(t.numel() * 2 * 2 for n, t in ex.items() if n.endswith("_q"))
+        floor_us = 1e6 * (packed + 2 * fp16) / (hbm * 1e9)
     out = {
         "metric": METRIC, "value": T / t_abl, "unit": UNIT, "n_gpus": 1, "steps": n,
         "warmup": 3, "ms_per_step": 1e3 * t_abl, "higher_is_better": True, "scaling": "weak",
@@ -543,7 +554,7 @@ def run_ablation(args, world, rank, local):
         "config": {"workload": args.workload, "T": T, "tile_rows": BM, "launch": "eager",
                    "fused_eager_us": 1e6 * t_fused, "ablation_us": 1e6 * t_abl,
                    "slowdown_vs_fused": t_abl / t_fused,
-                   "max_err_vs_fused_over_rms": err},
+                   "max_err_vs_fused_over_rms": err, "hbm_floor_us": floor_us},
     }
     print(json.dumps(out), flush=True)
 
