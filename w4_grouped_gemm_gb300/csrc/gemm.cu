@@ -330,6 +330,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = (uint32_t)misc[1];
+  pdl_wait();  // the set-up above overlaps the predecessor; its outputs are read below
+  pdl_trigger();
 
   if (warp == 0) {
     // ================================================= TMA producer
@@ -745,9 +747,9 @@ static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, cons
     num_sms = 148;
   const int grid = max_items < num_sms ? max_items : num_sms;  // persistent: one CTA per SM
   prof_begin(GATEUP ? K_GATEUP : K_DOWN, s);
-  kern<<<grid, kGemmThreads, smem, s>>>(q0, q1, b, b2, a, nstages, nsb);
+  err = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, s, q0, q1, b, b2, a, nstages, nsb);
   prof_end(GATEUP ? K_GATEUP : K_DOWN, s);
-  return cudaGetLastError();
+  return err;
 }
 
 template <bool GATEUP>
@@ -791,6 +793,8 @@ __global__ void __launch_bounds__(256) token_rows_kernel(const uint4* __restrict
                                                          uint4* __restrict__ x16, uint32_t* status,
                                                          const GemmArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();  // routing (perm, block map) comes from the predecessor
+  pdl_trigger();
   // the fp32 output accumulator starts at zero (the down GEMM adds into it)
   {
     float4* acc4 = reinterpret_cast<float4*>(a.yacc);
@@ -844,11 +848,11 @@ cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* 
   if (blocks < tb) blocks = tb;
   if (blocks > 152 * 8) blocks = 152 * 8;
   prof_begin(K_TOKEN_ROWS, s);
-  token_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), a.perm, a.k, P, a.T,
-                                           a.d / 8, static_cast<uint4*>(xs),
-                                           static_cast<uint4*>(x16), a.status, a);
+  const cudaError_t err = launch_pdl(token_rows_kernel, dim3(blocks), dim3(256), 0, s,
+                                     static_cast<const uint4*>(x), a.perm, a.k, P, a.T, a.d / 8,
+                                     static_cast<uint4*>(xs), static_cast<uint4*>(x16), a.status, a);
   prof_end(K_TOKEN_ROWS, s);
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, const uint8_t* gq,

@@ -30,6 +30,8 @@ namespace lily {
 __global__ void __launch_bounds__(256) router_prep_kernel(const float* __restrict__ w,
                                                           __nv_bfloat16* __restrict__ w3,
                                                           int64_t n_w) {
+  pdl_wait();  // w3 may still be read by the predecessor (the previous layer's router)
+  pdl_trigger();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_w; i += stride) {
     const float v = w[i];
@@ -99,6 +101,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = (uint32_t)misc[1];
+  pdl_wait();  // the split weights and x come from before
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -186,6 +190,8 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
                                                             int S, const float* __restrict__ b,
                                                             float* __restrict__ logits, int T,
                                                             int E) {
+  pdl_wait();  // the partial logits come from the predecessor
+  pdl_trigger();
   const int64_t n = (int64_t)T * E;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if ((E & 3) == 0) {
@@ -236,25 +242,27 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
   int pblocks = (int)((n_w + 255) / 256);
   if (pblocks > 152 * 8) pblocks = 152 * 8;
   prof_begin(K_ROUTER_PREP, s);
-  router_prep_kernel<<<pblocks, 256, 0, s>>>(w, static_cast<__nv_bfloat16*>(w_split), n_w);
+  cudaError_t err = launch_pdl(router_prep_kernel, dim3(pblocks), dim3(256), 0, s, w,
+                               static_cast<__nv_bfloat16*>(w_split), n_w);
   prof_end(K_ROUTER_PREP, s);
-  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   const size_t smem = router_tc_smem(E);
   err = ensure_smem_attr((const void*)router_tc_kernel, smem);
   if (err != cudaSuccess) return err;
   dim3 grid((T + 127) / 128, router_splits(T, d));
   prof_begin(K_ROUTER_GEMM, s);
-  router_tc_kernel<<<grid, kRtThreads, smem, s>>>(tm_x, tm_w, T, d, E, NE, partial, status);
+  err = launch_pdl(router_tc_kernel, grid, dim3(kRtThreads), smem, s, tm_x, tm_w, T, d, E, NE,
+                   partial, status);
   prof_end(K_ROUTER_GEMM, s);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  if (err != cudaSuccess) return err;
   const int64_t nr = (E & 3) == 0 ? (int64_t)T * E / 4 : (int64_t)T * E;
   int rblocks = (int)((nr + 255) / 256);
   if (rblocks > 152 * 8) rblocks = 152 * 8;
   prof_begin(K_ROUTER_REDUCE, s);
-  router_reduce_kernel<<<rblocks, 256, 0, s>>>(partial, grid.y, bias, logits, T, E);
+  err = launch_pdl(router_reduce_kernel, dim3(rblocks), dim3(256), 0, s, partial, (int)grid.y,
+                   bias, logits, T, E);
   prof_end(K_ROUTER_REDUCE, s);
-  return cudaGetLastError();
+  return err;
 }
 
 // ============================================================== routing kernel
