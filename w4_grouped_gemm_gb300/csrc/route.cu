@@ -541,6 +541,135 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
   }
 }
 
+// Routing of T <= kPlanRows tokens by one block of kRouteThreads threads
+// (the small-T router launch's last block): the same outputs as route_body
+// with one block, built from shared memory without read-backs -- top-k and
+// gates by one warp per token, counts by counting, positions by counting the
+// earlier pairs of the same expert (stable by pair index), tiles of each
+// expert in ascending order, and the decode plan (a.plan, required).
+__device__ __forceinline__ void route_small_body(const RouteArgs& a) {
+  constexpr int kMaxP = kPlanRows * kMaxK;
+  __shared__ int s_e[kMaxP];      // expert of pair p = t * k + j
+  __shared__ float s_g[kMaxP];    // its gate
+  __shared__ int s_perm[kMaxP];   // pair at sorted position
+  __shared__ int s_cnt[kMaxE], s_off[kMaxE], s_toff[kMaxE];
+  __shared__ int s_scan_tmp[8];
+  __shared__ int s_total;
+  const int T = a.T, E = a.E, k = a.k, P = T * k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < T) {
+    const int t = warp;
+    uint32_t key[kMaxE / 32];
+    uint32_t avail = 0;
+    bool saw_nan = false;
+#pragma unroll
+    for (int c = 0; c < kMaxE / 32; ++c) {
+      const int e = lane + 32 * c;
+      key[c] = 0;
+      if (e < E) {
+        const float v = __ldcg(a.logits_src + (size_t)t * E + e);
+        if (a.logits_dst != a.logits_src) a.logits_dst[(size_t)t * E + e] = v;
+        saw_nan |= (v != v);
+        key[c] = logit_key(v);
+        avail |= 1u << c;
+      }
+    }
+    if (__any_sync(0xffffffffu, saw_nan) && lane == 0) set_status(a.status, LILY_STATUS_NAN_LOGIT);
+    float my_logit = 0.f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+      uint32_t bk = 0;
+      int bc = -1;
+#pragma unroll
+      for (int c = 0; c < kMaxE / 32; ++c)
+        if ((avail >> c) & 1u)
+          if (bc < 0 || key[c] > bk) { bk = key[c]; bc = c; }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bc >= 0 ? bk : 0u);
+      const uint32_t cand = (bc >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bc) : 0xFFFFFFFFu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      if ((int)(win & 31u) == lane) avail &= ~(1u << (win >> 5));
+      if (lane == j) { my_logit = key_logit(kmax); my_id = (int)win; }
+    }
+    const float lmax = __shfl_sync(0xffffffffu, my_logit, 0);
+    float wgt = 0.f;
+    if (lane < k) wgt = (my_logit == lmax) ? 1.f : expf(my_logit - lmax);
+    float z = wgt;
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane < k) {
+      a.ids[(size_t)t * k + lane] = my_id;
+      a.gates[(size_t)t * k + lane] = wgt / z;
+      s_e[t * k + lane] = my_id;
+      s_g[t * k + lane] = wgt / z;
+    }
+  }
+  __syncthreads();
+  // counts and offsets: thread e counts its pairs
+  const int e_me = threadIdx.x;  // kRouteThreads == kMaxE
+  int cnt = 0;
+  for (int p = 0; p < P; ++p) cnt += (s_e[p] == e_me);
+  if (e_me >= E) cnt = 0;
+  const int off_me = block_exclusive_scan(cnt, s_scan_tmp);
+  s_cnt[e_me] = cnt;
+  s_off[e_me] = off_me;
+  const int ntile = (cnt + a.BM - 1) / a.BM;
+  __syncthreads();
+  const int toff = block_exclusive_scan(ntile, s_scan_tmp);
+  s_toff[e_me] = toff;
+  if (e_me == kMaxE - 1) s_total = toff + ntile;
+  if (e_me < E) {
+    a.counts[e_me] = cnt;
+    a.offsets[e_me] = off_me;
+  }
+  if (e_me == 0) a.offsets[E] = P;
+  __syncthreads();
+  // pair p's position: its expert's offset + the earlier pairs of that expert
+  for (int p = threadIdx.x; p < P; p += kRouteThreads) {
+    const int e = s_e[p];
+    int r = 0;
+    for (int q = 0; q < p; ++q) r += (s_e[q] == e);
+    const int pos = s_off[e] + r;
+    a.perm[pos] = p;
+    a.inv[p] = pos;
+    s_perm[pos] = p;
+  }
+  __syncthreads();
+  // block map and plan: thread e writes its tiles; slot 0 = shared expert
+  const int total = s_total;
+  for (int i = 0; i < ntile; ++i) {
+    const int row0 = off_me + i * a.BM, rows = min(a.BM, cnt - i * a.BM);
+    a.block_map[2 * (toff + i)] = e_me;
+    a.block_map[2 * (toff + i) + 1] = row0;
+    int32_t* pl = a.plan + (size_t)(1 + toff + i) * kPlanWords;
+    const int pr = min(rows, kPlanRows);
+    pl[0] = e_me;
+    pl[1] = row0;
+    pl[2] = pr;
+    pl[3] = 0;
+    for (int n = 0; n < kPlanRows; ++n) {
+      const int p = n < pr ? s_perm[row0 + n] : 0;
+      pl[8 + n] = n < pr ? p / k : 0;
+      pl[16 + n] = __float_as_int(n < pr ? s_g[p] : 0.f);
+    }
+  }
+  if (e_me == 0) {
+    *a.n_tiles = total;
+    int32_t* pl = a.plan;
+    pl[0] = E;
+    pl[1] = P;
+    pl[2] = T;
+    pl[3] = 0;
+    for (int n = 0; n < kPlanRows; ++n) {
+      pl[8 + n] = n < T ? n : 0;
+      pl[16 + n] = __float_as_int(n < T ? 1.f : 0.f);
+    }
+  }
+  for (int i = total + threadIdx.x; i < a.cap; i += kRouteThreads) {
+    a.block_map[2 * i] = -1;
+    a.block_map[2 * i + 1] = -1;
+    a.plan[(size_t)(1 + i) * kPlanWords + 2] = 0;  // unused slot: no rows
+  }
+}
+
 __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
   pdl_wait();  // the logits come from the predecessor
   pdl_trigger();
@@ -634,7 +763,10 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* _
     __syncthreads();
     if (s_last) {
       __threadfence();
-      route_body(ra, 0, 1);
+      if (ra.T <= kPlanRows && ra.plan)
+        route_small_body(ra);
+      else
+        route_body(ra, 0, 1);
       if (threadIdx.x == 0) *done = 0;  // back to zero for the next call
     }
   }
