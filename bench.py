@@ -390,6 +390,8 @@ def run_lily(args, world, rank, local):
             dbytes = gateup_bytes(T, d, F, touched)
         elif dom in ("dec_down_combine",):
             dbytes = touched * (F * d // 2 + F * d // 64 * 4)
+        elif dom in ("router_gemv", "router_gemm"):
+            dbytes = E * d * 4 + T * d * 2  # router weights (fp32) and x
         else:
             dbytes = step_bytes
         achieved = dbytes / dur / 1e9
