@@ -657,24 +657,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
         } else {
-          uint32_t orr[32];
-          tmem_ld32(tl + cb, orr);
-          tmem_ld_wait();
-          if (last) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
-          }
-          // lane jj holds row cb + jj's token and gate weight
+          // lane jj holds row cb + jj's output-row offset (token * d) and gate
           int tokj = tok0;
           float gj = gate0;
           if (cb > 0) row_token_gate(a, cur, cb, lane, P, tokj, gj);
+          const uint32_t offj = (uint32_t)tokj * (uint32_t)a.d;  // this lane adds its feature
+          // 16 accumulator columns (token rows) at a time: a 16-row tile reads
+          // and reduces only its own columns
+          const int nh = N - cb > 16 ? 2 : 1;
+          for (int hh = 0; hh < nh; ++hh) {
+            uint32_t orr[16];
+            tmem_ld16(tl + cb + 16 * hh, orr);
+            tmem_ld_wait();
+            if (last && hh == nh - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
+            }
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int tj = __shfl_sync(0xffffffffu, tokj, jj);
-            const float g = __shfl_sync(0xffffffffu, gj, jj);
-            if (cb + jj < cur.rows)
-              red_add_f32(a.yacc + (size_t)tj * a.d + feat, g * __uint_as_float(orr[jj]));
+            for (int jj = 0; jj < 16; ++jj) {
+              const uint32_t off = __shfl_sync(0xffffffffu, offj, 16 * hh + jj);
+              const float g = __shfl_sync(0xffffffffu, gj, 16 * hh + jj);
+              if (cb + 16 * hh + jj < cur.rows)
+                red_add_f32(a.yacc + off + feat, g * __uint_as_float(orr[jj]));
+            }
           }
         }
       }
