@@ -203,14 +203,30 @@ int lily_moe_decode_static(const lily_moe_dims* dims, const void* x,
                            void* y, void* stream);
 
 /* End-to-end form of lily_moe_forward (T >= 9) / lily_moe_decode (T <= 8) for
- * callers holding activations in HOST memory: copies x_host (bf16 [T][d],
- * pinned for best speed) to x_dev, runs the layer, copies y_dev back into
- * y_host and synchronises `stream` before returning.  x_dev/y_dev are device
- * staging buffers of T*d elements (bf16 for x, out_dtype for y). */
+ * callers holding activations in HOST memory: copies x_host (bf16 [T][d]) to
+ * x_dev, runs the layer, copies y_dev back into y_host and synchronises
+ * `stream` before returning.  x_dev/y_dev are device staging buffers of T*d
+ * elements (bf16 for x, out_dtype for y).
+ *   - Copies are cudaMemcpyAsync on `stream`; page-locked host buffers
+ *     (cudaHostAlloc / cudaHostRegister) copy fastest.
+ *   - With both host buffers page-locked, the first call with a given
+ *     argument set (dims and every pointer, on the current device) runs
+ *     eagerly and then captures the whole copy-layer-copy sequence as a CUDA
+ *     graph on a stream of the library's own; later calls with the same
+ *     arguments replay that graph on `stream`.  The graph reads every buffer
+ *     by address: contents may change between calls, and a buffer freed and
+ *     re-allocated at the same address is simply reused.  At most 128 graphs
+ *     are kept (least recently used evicted); lily_moe_host_graphs(0) drops
+ *     them all and turns the cache off.  Calls made while per-kernel
+ *     profiling is enabled always run eagerly. */
 int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x_dev,
                           const lily_moe_weights* weights, lily_moe_routing* routing,
                           void* y_dev, void* y_host, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/* Turn the end-to-end graph cache on (enable != 0, the default) or off; either
+ * way every cached graph is destroyed.  Returns the previous setting (0/1). */
+int lily_moe_host_graphs(int enable);
 
 /* Unit-weight RMSNorm, out = bf16(x / sqrt(mean(x^2) + eps)), x fp32 [T][d],
  * out bf16 [T][d].  The pre-norm of the stacked-layer prefill. */

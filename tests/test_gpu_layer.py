@@ -150,6 +150,48 @@ def test_forward_host_entry(oracle_lib):
     assert rel < 1e-2
 
 
+@pytest.mark.parametrize("T", [64, 5])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_forward_host_graph_cache(oracle_lib, T, pinned):
+    """Repeated host-buffer calls with one argument set: the first runs
+    eagerly and captures a graph, the next ones replay it.  The host input
+    changes between calls, so a replay that read stale data fails; every call
+    must match the device entry point on the same x."""
+    shape = synth.LayerShape(T, 512, 32, 4, 128)
+    L = Layer(shape, seed=4310 + T, tile_rows=32)
+    run = L.decode if T <= 8 else L.forward
+    lily.lily_moe_host_graphs(True)
+    xh = torch.empty(T, 512, dtype=torch.bfloat16)
+    yh = torch.empty(T, 512, dtype=L.y.dtype)
+    if pinned:
+        xh, yh = xh.pin_memory(), yh.pin_memory()
+    xd = torch.empty_like(L.x)
+    yd = torch.empty_like(L.y)
+    g = torch.Generator().manual_seed(77 + T)
+    try:
+        for call in range(4):
+            x = (torch.randn(T, 512, generator=g) * (1.0 + call)).to(torch.bfloat16)
+            L.x.copy_(x)
+            yref = run().float().cpu().clone()
+            xh.copy_(x)
+            yh.fill_(float("nan"))
+            lily.lily_moe_forward_host(L.dims, xh, xd, L.w, L.r, yd, yh, L.ws)
+            assert L.status() == 0
+            rel = (yh.float() - yref).abs().max().item() / yref.pow(2).mean().sqrt().item()
+            assert rel < 1e-4, f"call {call}: rel {rel}"
+        # profiling forces the eager path: same result
+        lily.lily_moe_profile_enable(True)
+        yh.fill_(float("nan"))
+        lily.lily_moe_forward_host(L.dims, xh, xd, L.w, L.r, yd, yh, L.ws)
+        lily.lily_moe_profile_read()
+        lily.lily_moe_profile_enable(False)
+        rel = (yh.float() - yref).abs().max().item() / yref.pow(2).mean().sqrt().item()
+        assert rel < 1e-4, f"eager call: rel {rel}"
+    finally:
+        lily.lily_moe_profile_enable(False)
+        lily.lily_moe_host_graphs(True)
+
+
 @pytest.mark.parametrize("decode", [False, True])
 def test_bf16_output_is_rounded_fp32_output(oracle_lib, decode):
     """out_dtype = bf16 gives the fp32 output rounded once (to within the fp32

@@ -7,6 +7,7 @@ work without the compiled library -- there is no fallback path.
 from __future__ import annotations
 
 import ctypes
+import operator
 from dataclasses import dataclass
 from pathlib import Path
 
@@ -34,7 +35,7 @@ EXPORTS = (
     "lily_moe_workspace_bytes", "lily_moe_block_map_cap", "lily_moe_check_dims",
     "lily_moe_route", "lily_moe_forward", "lily_moe_experts", "lily_moe_decode",
     "lily_moe_decode_static",
-    "lily_moe_forward_host",
+    "lily_moe_forward_host", "lily_moe_host_graphs",
     "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_workspace_bytes",
     "lily_moe_status", "lily_moe_strerror", "lily_moe_profile_enable", "lily_moe_profile_read",
     "lily_moe_kernel_name", "lily_moe_version",
@@ -93,6 +94,7 @@ def lib():
             "lily_moe_decode": (I, [DP, P, WP, RP, P, P, SZ, P]),
             "lily_moe_decode_static": (I, [DP, P, WP, RP, P, P]),
             "lily_moe_forward_host": (I, [DP, P, P, WP, RP, P, P, P, SZ, P]),
+            "lily_moe_host_graphs": (I, [I]),
             "lily_moe_rmsnorm": (I, [ctypes.c_int32, ctypes.c_int32, P, ctypes.c_float, P, P]),
             "lily_moe_stack_prefill": (I, [DP, ctypes.c_int32, ctypes.c_int32, WP, P,
                                            ctypes.c_float, P, P, P, SZ, P]),
@@ -128,8 +130,13 @@ def _ptr(t):
     return t.data_ptr()
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
     if stream is None:
+        if _raw_stream is not None:  # the current stream's handle, no Stream object
+            return _raw_stream(torch.cuda.current_device())
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
@@ -160,6 +167,17 @@ def lily_moe_block_map_cap(dims: Dims) -> int:
     return int(lib().lily_moe_block_map_cap(ctypes.byref(dims)))
 
 
+def _cached_view(owner, refs: tuple, struct):
+    """ctypes struct of the tensors `refs`, rebuilt only when one of them is
+    replaced by another object (a call then costs no data_ptr() lookups)."""
+    hit = owner.__dict__.get("_cview")
+    if hit is not None and all(map(operator.is_, hit[0], refs)):
+        return hit[1]
+    view = struct(*(_ptr(t) for t in refs))
+    owner.__dict__["_cview"] = (refs, view)
+    return view
+
+
 @dataclass
 class LayerWeights:
     """torch tensors of one layer; .c is the ctypes view (keeps the tensors alive)."""
@@ -170,9 +188,9 @@ class LayerWeights:
     @property
     def c(self) -> Weights:
         e = self.experts
-        return Weights(_ptr(self.router_w), _ptr(self.router_b), _ptr(e["gate_q"]),
-                       _ptr(e["gate_s"]), _ptr(e["gate_b"]), _ptr(e["up_q"]), _ptr(e["up_s"]),
-                       _ptr(e["up_b"]), _ptr(e["down_q"]), _ptr(e["down_s"]), _ptr(e["down_b"]))
+        refs = (self.router_w, self.router_b, e["gate_q"], e["gate_s"], e["gate_b"], e["up_q"],
+                e["up_s"], e["up_b"], e["down_q"], e["down_s"], e["down_b"])
+        return _cached_view(self, refs, Weights)
 
 
 class RoutingBuffers:
@@ -195,7 +213,7 @@ class RoutingBuffers:
 
     @property
     def c(self) -> Routing:
-        return Routing(*(_ptr(getattr(self, n)) for n, _ in Routing._fields_))
+        return _cached_view(self, tuple(getattr(self, n) for n, _ in Routing._fields_), Routing)
 
     def host(self) -> dict:
         return {n: getattr(self, n).cpu().numpy() for n, _ in Routing._fields_}
@@ -244,6 +262,12 @@ def lily_moe_forward_host(dims, x_host, x_dev, weights: LayerWeights, routing: R
                                      _ptr(y_dev), _ptr(y_host), _ptr(ws), ws.numel(),
                                      _stream(stream))
     _check(rc, "lily_moe_forward_host")
+
+
+def lily_moe_host_graphs(enable: bool) -> bool:
+    """Turn the end-to-end call's graph cache on or off (dropping cached
+    graphs); returns the previous setting."""
+    return bool(lib().lily_moe_host_graphs(1 if enable else 0))
 
 
 def lily_moe_rmsnorm(x, out, eps=1e-6, stream=None):

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI (include/lily_moe.h): argument validation, workspace
 // layout and the launch sequence of each call.  No call allocates device
 // memory; every launch goes to the caller's stream.
+#include <array>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -291,6 +292,136 @@ int common_checks(const lily_moe_dims* dims, const void* x, const lily_moe_weigh
   return check_arch();
 }
 
+// ---- end-to-end calls: host buffers in and out
+
+size_t host_x_bytes(const lily_moe_dims& d) { return (size_t)d.T * d.d_model * 2; }
+size_t host_y_bytes(const lily_moe_dims& d) {
+  return (size_t)d.T * d.d_model * (d.out_dtype == LILY_DTYPE_F32 ? 4 : 2);
+}
+
+// Whether a host buffer is page-locked (cudaHostAlloc / cudaHostRegister):
+// only such copies can be captured in a graph.  (Copies by the SMs through the
+// buffer's device mapping were measured slower than the copy engines at every
+// size from 4 KB to 8 MB, so the copy engines move the data either way.)
+bool host_pinned(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+struct HostStep {
+  const lily_moe_dims* dims;
+  const void* x_host;
+  void* x_dev;
+  const lily_moe_weights* w;
+  lily_moe_routing* r;
+  void* y_dev;
+  void* y_host;
+  void* ws;
+  size_t ws_bytes;
+};
+
+// Copy in, run the layer, copy out, all on `s` (no synchronisation).
+int host_step(const HostStep& h, cudaStream_t s) {
+  if (cudaMemcpyAsync(h.x_dev, h.x_host, host_x_bytes(*h.dims), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return LILY_ERR_CUDA;
+  const int rc = h.dims->T <= 8
+                     ? lily_moe_decode(h.dims, h.x_dev, h.w, h.r, h.y_dev, h.ws, h.ws_bytes, s)
+                     : lily_moe_forward(h.dims, h.x_dev, h.w, h.r, h.y_dev, h.ws, h.ws_bytes, s);
+  if (rc) return rc;
+  return cuda_rc(
+      cudaMemcpyAsync(h.y_host, h.y_dev, host_y_bytes(*h.dims), cudaMemcpyDeviceToHost, s));
+}
+
+// Instantiated graphs of host_step, one per argument set (dims, every pointer,
+// the device), least recently used evicted.  A graph reads its buffers by
+// address, so their contents may change freely between calls.  The capacity
+// holds one graph per layer of a deep stack called layer by layer.
+using HostGraphKey = std::array<uint64_t, 40>;
+struct HostGraph {
+  cudaGraphExec_t exec;  // nullptr: capture failed, these arguments run eagerly
+  uint64_t used;
+};
+constexpr size_t kHostGraphs = 128;
+std::mutex g_hg_mu;
+bool g_hg_on = true;
+uint64_t g_hg_tick = 0;
+std::map<HostGraphKey, HostGraph> g_hg;
+std::map<int, cudaStream_t> g_hg_streams;  // capture stream per device
+
+HostGraphKey host_graph_key(const HostStep& h) {
+  HostGraphKey k{};
+  size_t n = 0;
+  auto put = [&](uint64_t v) { k[n++] = v; };
+  auto ptr = [&](const void* p) { put((uint64_t)(uintptr_t)p); };
+  const lily_moe_dims& d = *h.dims;
+  for (int32_t v : {d.T, d.d_model, d.n_experts, d.top_k, d.d_ff, d.group, d.tile_rows,
+                    d.out_dtype})
+    put((uint64_t)(uint32_t)v);
+  for (const void* p : {h.x_host, (const void*)h.x_dev, (const void*)h.y_dev,
+                        (const void*)h.y_host, (const void*)h.ws})
+    ptr(p);
+  put((uint64_t)h.ws_bytes);
+  const lily_moe_weights& w = *h.w;
+  for (const void* p : {(const void*)w.router_w, (const void*)w.router_bias,
+                        (const void*)w.gate_q, (const void*)w.gate_s, (const void*)w.gate_b,
+                        (const void*)w.up_q, (const void*)w.up_s, (const void*)w.up_b,
+                        (const void*)w.down_q, (const void*)w.down_s, (const void*)w.down_b})
+    ptr(p);
+  const lily_moe_routing& r = *h.r;
+  for (const void* p : {(const void*)r.logits, (const void*)r.topk_ids,
+                        (const void*)r.topk_gates, (const void*)r.counts, (const void*)r.offsets,
+                        (const void*)r.perm, (const void*)r.inv_perm, (const void*)r.block_map,
+                        (const void*)r.n_tiles})
+    ptr(p);
+  int dev = -1;
+  cudaGetDevice(&dev);
+  put((uint64_t)(uint32_t)dev);
+  return k;  // 8 + 5 + 1 + 11 + 9 + 1 = 35 words used
+}
+
+// Capture host_step for these arguments on the library's own stream (the
+// caller's may be the legacy default stream, which cannot be captured) and
+// keep the instantiated graph; a failed capture is remembered as such.
+void host_graph_capture(const HostStep& h, const HostGraphKey& key) {
+  std::lock_guard<std::mutex> lk(g_hg_mu);
+  if (!g_hg_on || g_hg.count(key)) return;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  cudaStream_t& cs = g_hg_streams[dev];
+  if (!cs && cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    cs = nullptr;
+    cudaGetLastError();
+    return;
+  }
+  cudaGraphExec_t exec = nullptr;
+  cudaGraph_t g = nullptr;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+    const int rc = host_step(h, cs);
+    const cudaError_t e = cudaStreamEndCapture(cs, &g);
+    if (rc == LILY_OK && e == cudaSuccess && g &&
+        cudaGraphInstantiate(&exec, g, 0) != cudaSuccess)
+      exec = nullptr;
+    if (g) cudaGraphDestroy(g);
+  }
+  cudaGetLastError();  // a refused capture leaves no error for the next call
+  if (g_hg.size() >= kHostGraphs) {
+    auto lru = g_hg.begin();
+    for (auto it = g_hg.begin(); it != g_hg.end(); ++it)
+      if (it->second.used < lru->second.used) lru = it;
+    if (lru->second.exec) cudaGraphExecDestroy(lru->second.exec);
+    g_hg.erase(lru);
+  }
+  g_hg[key] = {exec, ++g_hg_tick};
+}
+
 }  // namespace
 }  // namespace lily
 
@@ -420,16 +551,46 @@ int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x
   int rc = common_checks(dims, x_dev, w, r, y_dev, ws, ws_bytes, true);
   if (rc) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  const size_t n = (size_t)dims->T * dims->d_model;
-  if (cudaMemcpyAsync(x_dev, x_host, n * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
-    return LILY_ERR_CUDA;
-  rc = dims->T <= 8 ? lily_moe_decode(dims, x_dev, w, r, y_dev, ws, ws_bytes, stream)
-                    : lily_moe_forward(dims, x_dev, w, r, y_dev, ws, ws_bytes, stream);
-  if (rc) return rc;
-  const size_t ybytes = n * (dims->out_dtype == LILY_DTYPE_F32 ? 4 : 2);
-  if (cudaMemcpyAsync(y_host, y_dev, ybytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return LILY_ERR_CUDA;
-  return cuda_rc(cudaStreamSynchronize(s));
+  const HostStep h = {dims, x_host, x_dev, w, r, y_dev, y_host, ws, ws_bytes};
+  bool prof;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof = g_prof_on;
+  }
+  // Pinned buffers on both sides: replay this argument set's graph, or run
+  // the step eagerly and then capture one for the next call.
+  const bool graphable = !prof && host_pinned(x_host) && host_pinned(y_host);
+  HostGraphKey key{};
+  if (graphable) {
+    key = host_graph_key(h);
+    int launched = 0;  // 1 launched, -1 launch failed
+    {
+      // launched under the lock: an eviction may destroy the graph only
+      // after its launch is queued (destruction then waits for it)
+      std::lock_guard<std::mutex> lk(g_hg_mu);
+      auto it = g_hg_on ? g_hg.find(key) : g_hg.end();
+      if (it != g_hg.end() && it->second.exec) {  // (none: capture failed, run eagerly)
+        it->second.used = ++g_hg_tick;
+        launched = cudaGraphLaunch(it->second.exec, s) == cudaSuccess ? 1 : -1;
+      }
+    }
+    if (launched < 0) return LILY_ERR_CUDA;
+    if (launched > 0) return cuda_rc(cudaStreamSynchronize(s));
+  }
+  if ((rc = host_step(h, s))) return rc;
+  if ((rc = cuda_rc(cudaStreamSynchronize(s)))) return rc;
+  if (graphable) host_graph_capture(h, key);
+  return LILY_OK;
+}
+
+int lily_moe_host_graphs(int enable) {
+  std::lock_guard<std::mutex> lk(g_hg_mu);
+  const int was = g_hg_on ? 1 : 0;
+  for (auto& e : g_hg)
+    if (e.second.exec) cudaGraphExecDestroy(e.second.exec);
+  g_hg.clear();
+  g_hg_on = enable != 0;
+  return was;
 }
 
 int lily_moe_rmsnorm(int32_t T, int32_t d, const float* x, float eps, void* out, void* stream) {
