@@ -122,15 +122,15 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Compute capability 10.3 of the current device, checked once per device.
 int check_arch() {
-  static int verdict[64] = {};  // 0 unknown, 1 sm_103, -1 other
+  static int arch_seen[64] = {};  // 0 unknown, 1 sm_103, -1 other
   int dev = 0, maj = 0, min = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LILY_ERR_CUDA;
-  if (dev >= 0 && dev < 64 && verdict[dev]) return verdict[dev] > 0 ? LILY_OK : LILY_ERR_ARCH;
+  if (dev >= 0 && dev < 64 && arch_seen[dev]) return arch_seen[dev] > 0 ? LILY_OK : LILY_ERR_ARCH;
   if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return LILY_ERR_CUDA;
   const bool ok = maj == 10 && min == 3;
-  if (dev >= 0 && dev < 64) verdict[dev] = ok ? 1 : -1;
+  if (dev >= 0 && dev < 64) arch_seen[dev] = ok ? 1 : -1;
   return ok ? LILY_OK : LILY_ERR_ARCH;
 }
 
