@@ -650,7 +650,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int n = cb + jj;
             if (n < cur.rows) {
               const float gv = __uint_as_float(gr[jj]), uv = __uint_as_float(ur[jj]);
-              const float h = gv / (1.f + __expf(-gv)) * uv;
+              // silu(g) * u with the fast reciprocal: its few-ulp fp32 error is
+              // far below the fp16 rounding of H; g -> -inf gives 0 as it should
+              const float h = __fdividef(gv * uv, 1.f + __expf(-gv));
               range_ok &= fabsf(h) <= 65504.f;
               H[(size_t)(cur.row0 + n) * a.F + hcol] = __float2half_rn(h);
             }
