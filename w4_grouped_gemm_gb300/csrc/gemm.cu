@@ -67,6 +67,9 @@ struct GemmLayout {
   static constexpr int kMats = GATEUP ? 2 : 1;
   static constexpr int kGroups = groups_per_step(GATEUP);
   static constexpr int kBTile = BM * 128;  // token rows of one group
+  // token rows per TMA box: fewer, taller boxes per step (the rows past an
+  // item's last are other tiles' rows or zero fill, never stored)
+  static constexpr int kBoxRows = BM < 64 ? BM : 64;
   static constexpr int kBBytes = kGroups * kBTile;
   static constexpr int kStage = kBBytes + kMats * kGroups * kPackedBytes;
   static constexpr int kACols = 32 * kGroups;  // one matrix's A tile
@@ -354,7 +357,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // for a shared-expert tile, x16 in token order); down reads H
       const CUtensorMap* tmb = (GATEUP && itm.shared) ? &tm_b2 : &tm_b;
       const int brow = (GATEUP && itm.shared) ? itm.row0 - P : itm.row0;
-      const uint32_t tx_bytes = KG * (MATS * kPackedBytes + N * 128);
+      const int nbox = (N + L::kBoxRows - 1) / L::kBoxRows;
+      const uint32_t tx_bytes = KG * (MATS * kPackedBytes + nbox * L::kBoxRows * 128);
       for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx;
         if (it >= (uint32_t)nstages &&
@@ -372,8 +376,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tma_load_2d_warp(st + BBYTES + g * kPackedBytes, &tm_q0, grp * 32, wrow, fb);
           if (GATEUP)
             tma_load_2d_warp(st + BBYTES + (KG + g) * kPackedBytes, &tm_q1, grp * 32, wrow, fb);
-          for (int r16 = 0; r16 < N; r16 += 16)  // the tile's N rows, 16 rows per box
-            tma_load_2d_warp(st + g * L::kBTile + r16 * 128, tmb, grp * 64, brow + r16, fb);
+          for (int rb = 0; rb < nbox; ++rb)  // the tile's N rows
+            tma_load_2d_warp(st + g * L::kBTile + rb * L::kBoxRows * 128, tmb, grp * 64,
+                             brow + rb * L::kBoxRows, fb);
         }
       }
     }
@@ -783,6 +788,9 @@ static bool packed_map(CUtensorMap* tm, const uint8_t* q, int K, int rows) {
                       CU_TENSOR_MAP_SWIZZLE_32B) == CUDA_SUCCESS;
 }
 
+// Token rows per TMA box (GemmLayout::kBoxRows).
+static int box_rows(int BM) { return BM < 64 ? BM : 64; }
+
 static bool f16_rows_map(CUtensorMap* tm, const void* base, int cols, int rows, int box_rows) {
   uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows};
   uint64_t strides[1] = {(uint64_t)cols * 2};
@@ -868,7 +876,8 @@ cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, co
   CUtensorMap q0, q1, b, b2;
   const int P = a.T * a.k;
   if (!packed_map(&q0, gq, a.d, (a.E + 1) * a.F) || !packed_map(&q1, uq, a.d, (a.E + 1) * a.F) ||
-      !f16_rows_map(&b, xs, a.d, P, 16) || !f16_rows_map(&b2, x16, a.d, a.T, 16))
+      !f16_rows_map(&b, xs, a.d, P, box_rows(a.BM)) ||
+      !f16_rows_map(&b2, x16, a.d, a.T, box_rows(a.BM)))
     return cudaErrorInvalidValue;
   return launch_gemm<true>(a, q0, q1, b, b2, s);
 }
@@ -876,7 +885,8 @@ cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, co
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
   CUtensorMap q0, b;
   const int P = a.T * a.k;
-  if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d) || !f16_rows_map(&b, a.H, a.F, P + a.T, 16))
+  if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d) ||
+      !f16_rows_map(&b, a.H, a.F, P + a.T, box_rows(a.BM)))
     return cudaErrorInvalidValue;
   return launch_gemm<false>(a, q0, q0, b, b, s);
 }
