@@ -187,6 +187,19 @@ __device__ __forceinline__ bool warp_wait_all2(uint32_t bar0, uint32_t parity0, 
   }
 }
 
+// One lane of the converged warp (elect.sync): the producer issues a whole
+// K-step's expect-tx and TMA copies from it in one branch, which measured
+// faster than one election per copy.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // ------------------------------------------------------------------ dependent launch
 // Programmatic dependent launch: a kernel launched with the programmatic
 // stream-serialization attribute may start while its predecessor in the
@@ -212,25 +225,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(tm), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-// Warp-collective forms of the two calls above (one elected lane issues).
-__device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint32_t bar, uint32_t bytes) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar),
-      "r"(bytes)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_2d_warp(uint32_t dst, const CUtensorMap* tm, int32_t c0,
-                                                 int32_t c1, uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(dst),
       "l"(tm), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }

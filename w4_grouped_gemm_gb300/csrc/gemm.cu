@@ -366,20 +366,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
-        // whole warp, warp-uniform operands; one elected lane issues
+        // whole warp, warp-uniform operands; one elected lane issues the step
         const uint32_t fb = smem_u32(&full[s]);
         const uint32_t st = smem_u32(stage_base + (size_t)s * STAGE);
-        mbar_arrive_expect_tx_warp(fb, tx_bytes);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(fb, tx_bytes);
 #pragma unroll
-        for (int g = 0; g < KG; ++g) {
-          const int grp = kk * KG + g;
-          tma_load_2d_warp(st + BBYTES + g * kPackedBytes, &tm_q0, grp * 32, wrow, fb);
-          if (GATEUP)
-            tma_load_2d_warp(st + BBYTES + (KG + g) * kPackedBytes, &tm_q1, grp * 32, wrow, fb);
-          for (int rb = 0; rb < nbox; ++rb)  // the tile's N rows
-            tma_load_2d_warp(st + g * L::kBTile + rb * L::kBoxRows * 128, tmb, grp * 64,
-                             brow + rb * L::kBoxRows, fb);
+          for (int g = 0; g < KG; ++g) {
+            const int grp = kk * KG + g;
+            tma_load_2d(st + BBYTES + g * kPackedBytes, &tm_q0, grp * 32, wrow, fb);
+            if (GATEUP)
+              tma_load_2d(st + BBYTES + (KG + g) * kPackedBytes, &tm_q1, grp * 32, wrow, fb);
+            for (int rb = 0; rb < nbox; ++rb)  // the tile's N rows
+              tma_load_2d(st + g * L::kBTile + rb * L::kBoxRows * 128, tmb, grp * 64,
+                          brow + rb * L::kBoxRows, fb);
+          }
         }
+        __syncwarp();
       }
     }
     if (*abort && lane == 0) {  // let copies still in flight land before exit
