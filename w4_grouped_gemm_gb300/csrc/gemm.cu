@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ================================================= MMA issuer
     // The whole warp runs the loop with warp-uniform operands; one elected
-    // lane issues each MMA and commit.  It waits on afull alone: the dequant
+    // lane issues a K-step's MMAs and commits in one branch (measured faster
+    // than an election per instruction).  It waits on afull alone: the dequant
     // warps arrive there only after their own wait on the stage's TMA
     // barrier, so a full A buffer implies that the stage's token rows landed.
     uint32_t it = 0, titem = 0;
@@ -421,20 +422,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t sbase = smem_u32(stage_base + (size_t)s * STAGE);
+        if (elect_one()) {
 #pragma unroll
-        for (int m = 0; m < MATS; ++m) {
-          const uint32_t at = tmem + L::kAOff + (b * MATS + m) * L::kACols;  // A tile in TMEM
+          for (int m = 0; m < MATS; ++m) {
+            const uint32_t at = tmem + L::kAOff + (b * MATS + m) * L::kACols;  // A tile in TMEM
 #pragma unroll
-          for (int g = 0; g < KG; ++g) {
-            const uint64_t bdesc = sdesc_sw128(sbase + g * L::kBTile);
+            for (int g = 0; g < KG; ++g) {
+              const uint64_t bdesc = sdesc_sw128(sbase + g * L::kBTile);
 #pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
-              mma_f16_ts_warp(dacc + m * BM, at + g * 32 + k16 * 8, bdesc + 2 * k16, idesc,
-                              (kk | g | k16) != 0);
+              for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
+                mma_f16_ts(dacc + m * BM, at + g * 32 + k16 * 8, bdesc + 2 * k16, idesc,
+                           (kk | g | k16) != 0);
+            }
           }
+          mma_commit(smem_u32(&empty[s]));
+          mma_commit(smem_u32(&aempty[b]));
         }
-        mma_commit_warp(smem_u32(&empty[s]));
-        mma_commit_warp(smem_u32(&aempty[b]));
+        __syncwarp();
       }
       if (!ok) break;
       mma_commit_warp(smem_u32(&accfull[ab]));

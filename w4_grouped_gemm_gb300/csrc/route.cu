@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // whole warp, warp-uniform operands; one elected lane issues
+    // whole warp, warp-uniform operands; one elected lane issues the step
     const uint32_t idesc = idesc_bf16_f32(128, NE);
     for (int i = 0; i < nk; ++i) {
       const int st = i % kRtStages;
@@ -135,10 +135,13 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       tc_fence_after();
       const uint32_t a0 = smem_u32(smem + (size_t)st * STAGE);
       const uint64_t ad = sdesc_sw128(a0), bd = sdesc_sw128(a0 + ABYTES);
+      if (elect_one()) {
 #pragma unroll
-      for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in each descriptor
-        mma_f16_warp(tmem, ad + 2 * k16, bd + 2 * k16, idesc, (i | k16) != 0);
-      mma_commit_warp(smem_u32(&empty[st]));
+        for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in each descriptor
+          mma_f16(tmem, ad + 2 * k16, bd + 2 * k16, idesc, (i | k16) != 0);
+        mma_commit(smem_u32(&empty[st]));
+      }
+      __syncwarp();
     }
     mma_commit_warp(smem_u32(accfull));
     __syncwarp();
