@@ -688,12 +688,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               __syncwarp();
               if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
             }
+            // 4x4 blocks (4 lanes = 4 features, 4 token columns) transposed in
+            // two butterfly stages (lanes ^2, then ^1): lane 4i + r ends with
+            // features 4i..4i+3 of column 4m + r, one 16-byte reduction
+            const int rq = lane & 3;
+            const bool qhi = (rq & 2) != 0, qlo = (rq & 1) != 0;
+            float* ybase = a.yacc + (feat & ~3);
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
-              const uint32_t off = __shfl_sync(0xffffffffu, offj, 16 * hh + jj);
-              const float g = __shfl_sync(0xffffffffu, gj, 16 * hh + jj);
-              if (cb + 16 * hh + jj < cur.rows)
-                red_add_f32(a.yacc + off + feat, g * __uint_as_float(orr[jj]));
+            for (int m = 0; m < 4; ++m) {
+              const float a0 = __uint_as_float(orr[4 * m]), a1 = __uint_as_float(orr[4 * m + 1]);
+              const float a2 = __uint_as_float(orr[4 * m + 2]), a3 = __uint_as_float(orr[4 * m + 3]);
+              // stage 1: keep columns (2hi, 2hi + 1), take the partner's
+              const float o0 = qhi ? a2 : a0, o1 = qhi ? a3 : a1;
+              const float t0 = __shfl_xor_sync(0xffffffffu, qhi ? a0 : a2, 2);
+              const float t1 = __shfl_xor_sync(0xffffffffu, qhi ? a1 : a3, 2);
+              // stage 2: keep column r of rows r and r^2, take rows r^1, r^3
+              const float k0 = qlo ? o1 : o0, k1 = qlo ? t1 : t0;
+              const float v0 = __shfl_xor_sync(0xffffffffu, qlo ? o0 : o1, 1);
+              const float v1 = __shfl_xor_sync(0xffffffffu, qlo ? t0 : t1, 1);
+              // rows r, r^1, r^2, r^3 hold k0, v0, k1, v1: in feature order
+              const float p0 = qlo ? v0 : k0, p1 = qlo ? k0 : v0;
+              const float s0 = qlo ? v1 : k1, s1 = qlo ? k1 : v1;
+              const int col = 16 * hh + 4 * m + rq;  // this lane's column in the 32-block
+              const uint32_t off = __shfl_sync(0xffffffffu, offj, col);
+              const float g = __shfl_sync(0xffffffffu, gj, col);
+              if (cb + col < cur.rows)
+                red_add_v4_f32(ybase + off, g * (qhi ? s0 : p0), g * (qhi ? s1 : p1),
+                               g * (qhi ? p0 : s0), g * (qhi ? p1 : s1));
             }
           }
         }
