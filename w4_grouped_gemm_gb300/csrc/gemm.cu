@@ -639,9 +639,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!warp_wait(smem_u32(&accfull[ab]), (j / NACC) & 1, abort, a.status)) break;
       tc_fence_after();
       const int feat = cur.slice * 128 + q * 32 + lane;
-      // H stores each 8-feature chunk in K-chunk order: it is the down GEMM's
-      // K operand against weights rebuilt in that order
-      const int hcol = (feat & ~7) | kchunk_pos(feat & 7);
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + ab * L::kAccCols;
       for (int cb = 0; cb < N; cb += 32) {
         const bool last = cb + 32 >= N;
@@ -655,18 +652,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
-          __half* H = static_cast<__half*>(a.H);
           bool range_ok = true;
+          // H holds each 8-feature chunk in K-chunk order (it is the down
+          // GEMM's K operand against weights rebuilt in that order), so
+          // features e and e + 4 sit side by side: lanes with e < 4 store the
+          // pair of column jj,
+          // lanes with e >= 4 that of column jj + 1, one 4-byte store each
+          const bool up4 = (lane & 4) != 0;
+          __half2* Hp = reinterpret_cast<__half2*>(
+              static_cast<__half*>(a.H) + ((feat & ~7) | ((feat & 3) << 1)));
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int n = cb + jj;
-            if (n < cur.rows) {
-              const float gv = __uint_as_float(gr[jj]), uv = __uint_as_float(ur[jj]);
+          for (int jj = 0; jj < 32; jj += 2) {
+            if (cb + jj >= N) break;  // (warp-uniform; N is a multiple of 16)
+            float hv[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const float gv = __uint_as_float(gr[jj + t]), uv = __uint_as_float(ur[jj + t]);
               // silu(g) * u with the fast reciprocal: its few-ulp fp32 error is
               // far below the fp16 rounding of H; g -> -inf gives 0 as it should
-              const float h = __fdividef(gv * uv, 1.f + __expf(-gv));
-              range_ok &= fabsf(h) <= 65504.f;
-              H[(size_t)(cur.row0 + n) * a.F + hcol] = __float2half_rn(h);
+              hv[t] = __fdividef(gv * uv, 1.f + __expf(-gv));
+            }
+            const float recv = __shfl_xor_sync(0xffffffffu, up4 ? hv[0] : hv[1], 4);
+            const float lo = up4 ? recv : hv[0], hi = up4 ? hv[1] : recv;
+            const int n = cb + jj + (up4 ? 1 : 0);
+            if (n < cur.rows) {
+              range_ok &= fabsf(lo) <= 65504.f && fabsf(hi) <= 65504.f;
+              Hp[(size_t)(cur.row0 + n) * (a.F / 2)] = __floats2half2_rn(lo, hi);
             }
           }
           if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
