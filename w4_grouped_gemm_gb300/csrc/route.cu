@@ -427,16 +427,32 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
       s_ids[tl * k + lane] = my_id;
     }
   }
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) s_cnt[e] = 0;
+  // ---- phase 2: block histogram and stable local rank of each pair (one
+  // pair per thread): the rank among the warp's pairs of the same expert
+  // from a match, plus that expert's pairs in the earlier warps
+  static_assert(kRouteTok * kMaxK <= kRouteThreads, "one pair per thread");
+  constexpr int kRouteWarps = kRouteThreads / 32;
+  __shared__ int s_wcnt[kRouteWarps][kMaxE];
+  for (int i = threadIdx.x; i < kRouteWarps * kMaxE; i += kRouteThreads) (&s_wcnt[0][0])[i] = 0;
   __syncthreads();
-
-  // ---- phase 2: block histogram and stable local rank of each pair
-  for (int q = threadIdx.x; q < npair; q += kRouteThreads) {
-    const int e = s_ids[q];
-    int r = 0;
-    for (int q2 = 0; q2 < q; ++q2) r += (s_ids[q2] == e);
-    s_rank[q] = r;
-    atomicAdd(&s_cnt[e], 1);
+  {
+    const int q = threadIdx.x;
+    const int e = q < npair ? s_ids[q] : -1;
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int lrank = __popc(same & ((1u << lane) - 1u));
+    if (e >= 0 && lrank == 0) s_wcnt[warp][e] = __popc(same);
+    __syncthreads();
+    if (e >= 0) {
+      int rk = lrank;
+      for (int w2 = 0; w2 < warp; ++w2) rk += s_wcnt[w2][e];
+      s_rank[q] = rk;
+    }
+    for (int e2 = threadIdx.x; e2 < E; e2 += kRouteThreads) {
+      int c = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kRouteWarps; ++w2) c += s_wcnt[w2][e2];
+      s_cnt[e2] = c;
+    }
   }
   __syncthreads();
   if (nblk > 1) {
@@ -448,6 +464,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
     for (int e = threadIdx.x; e < kMaxE; e += kRouteThreads) {
       int cnt = 0, before = 0;
       if (e < E) {
+#pragma unroll 8
         for (int b = 0; b < nblk; ++b) {
           int h = __ldcg(&a.hist[(size_t)b * E + e]);
           cnt += h;
