@@ -66,12 +66,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
   return ok != 0;
 }
 
-// Bounded spin-wait for latency-critical hand-offs (pipeline stages): polls
-// try_wait without the suspend hint, checking the abort flag and the 2 s
-// limit every 1024 polls.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort,
-                                               uint32_t* status);
-
 // Bounded wait for the phase with the given parity.  The waiting thread
 // sleeps in try_wait (up to 100 us per attempt); the wait gives up after
 // kWaitLimitNs of wall time, or early when *abort is set by another role of
@@ -94,33 +88,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, volatile int* abort,
-                                               uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 1023u) == 0) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        set_status(status, LILY_STATUS_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
 // Wait by lane 0 only, result broadcast: keeps every warp-collective op
 // (tcgen05.ld, __syncwarp, shuffles) convergent even when a wait gives up.
-// `spin` = latency-critical pipeline hand-off (poll) rather than a sleep.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status, bool spin = false) {
+                                          uint32_t* status) {
   int ok = 1;
-  if ((threadIdx.x & 31) == 0)
-    ok = (spin ? mbar_wait_spin(bar, parity, abort, status) : mbar_wait(bar, parity, abort, status))
-             ? 1
-             : 0;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
@@ -226,25 +199,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(tm), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-// Four rows (r0..r3) of a 2-D tensor, columns [c0, c0 + box0), one-row box.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int32_t c0,
-                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(tm), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-// Plain bulk copy global -> shared (16-byte aligned addresses, size % 16 == 0).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
@@ -470,9 +424,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
                "r"(d)
                : "memory");
-}
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 // Four consecutive floats added in one reduction (p 16-byte aligned).
 __device__ __forceinline__ void red_add_v4_f32(float* p, float x, float y, float z, float w) {

@@ -3,18 +3,20 @@
 // The expert GEMMs take about 90% of prefill time (page "Revolutionizing Local
 // AI Inference on Apple Silicon", section "Enhanced Tile and Scan
 // Operations").  Weights stay 4-bit in HBM; each CTA streams one 128-row slice
-// of one expert's packed codes with TMA, rebuilds it as fp16 one 64-wide
-// K-step at a time in shared memory (w = scale*q + bias), and feeds tcgen05
+// of one expert's packed codes with TMA, rebuilds it as fp16 one K-step at a
+// time in tensor memory (w = scale*q + bias), and feeds tcgen05
 // MMAs that accumulate in FP32 in tensor memory, so the expanded weights never
 // reach HBM (page "Lily Beats MLX-LM 1.35x on Decode: Perplexity's Rust+Metal
 // Engine for Apple Silicon", section "Prefill: fusing dequantisation and
 // keeping routing GPU-resident").
 //
 // Operand roles (weights as the M=128 operand, token rows as N):
-//   A = dequantised weight slice, 128 output features x 64 K, fp16, K-major,
-//       128-byte swizzle, written by the dequant warps
+//   A = dequantised weight slice, 128 output features x 64 K per group, fp16,
+//       in tensor memory (lane = feature, two K elements per 32-bit column),
+//       written by the dequant warps with tcgen05.st
 //   B = token rows of one block-map tile (<= BM rows) x 64 K, fp16, K-major,
-//       128-byte swizzle, brought by TMA in 16-row boxes: gate/up reads xs,
+//       128-byte swizzle, brought by TMA in boxes of up to 64 rows: gate/up
+//       reads xs,
 //       the fp16 rows of x in expert-sorted order written once per layer by
 //       token_rows_kernel (one pass instead of a TMA gather per K-step);
 //       down reads rows of H
@@ -25,7 +27,8 @@
 // kind::f16 tensor rate, and holds x, the group scales and biases exactly in
 // [2^-17, 65504] (values beyond 65504 set LILY_STATUS_F16_RANGE).
 // Epilogues: gate/up writes H = silu(gate) * up (fp16) in expert-sorted row
-// order; down adds gate * out into the fp32 token-order accumulator.
+// order; down adds gate * out into the fp32 token-order accumulator, four
+// consecutive outputs per 16-byte reduction.
 // K order: the rebuilt weights come out of the nibble extraction with each
 // 8-element K chunk in the order (0,4,1,5,2,6,3,7); the K operands x16 and H
 // are stored in that same order, so no shuffle is needed.
