@@ -32,16 +32,23 @@ __global__ void __launch_bounds__(256) router_prep_kernel(const float* __restric
                                                           int64_t n_w) {
   pdl_wait();  // w3 may still be read by the predecessor (the previous layer's router)
   pdl_trigger();
+  // four weights per thread: one 16-byte load, three 8-byte stores (n_w is a
+  // multiple of 4: d is a multiple of 128; w is 16-byte aligned)
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_w; i += stride) {
-    const float v = w[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    w3[i] = hi;
-    w3[n_w + i] = mid;
-    w3[2 * n_w + i] = __float2bfloat16_rn(r2);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_w / 4; i += stride) {
+    const float4 v4 = reinterpret_cast<const float4*>(w)[i];
+    const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+    __nv_bfloat16 hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      hi[u] = __float2bfloat16_rn(v[u]);
+      const float r1 = v[u] - __bfloat162float(hi[u]);
+      mid[u] = __float2bfloat16_rn(r1);
+      lo[u] = __float2bfloat16_rn(r1 - __bfloat162float(mid[u]));
+    }
+    reinterpret_cast<uint2*>(w3)[i] = *reinterpret_cast<const uint2*>(hi);
+    reinterpret_cast<uint2*>(w3 + n_w)[i] = *reinterpret_cast<const uint2*>(mid);
+    reinterpret_cast<uint2*>(w3 + 2 * n_w)[i] = *reinterpret_cast<const uint2*>(lo);
   }
 }
 
@@ -199,11 +206,17 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if ((E & 3) == 0) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n / 4; i += stride) {
-      float4 acc = __ldcg(reinterpret_cast<const float4*>(partial) + i);
-      for (int sp = 1; sp < S; ++sp) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(partial + (int64_t)sp * n) + i);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
+      // every split's load issued before the (in-order) sum
+      float4 v[kRtMaxSplits];
+#pragma unroll
+      for (int sp = 0; sp < kRtMaxSplits; ++sp)
+        if (sp < S) v[sp] = __ldcg(reinterpret_cast<const float4*>(partial + (int64_t)sp * n) + i);
+      float4 acc = v[0];
+#pragma unroll
+      for (int sp = 1; sp < kRtMaxSplits; ++sp)
+        if (sp < S) {
+          acc.x += v[sp].x; acc.y += v[sp].y; acc.z += v[sp].z; acc.w += v[sp].w;
+        }
       if (b) {
         const int e = (int)((4 * i) % E);
         acc.x += b[e]; acc.y += b[e + 1]; acc.z += b[e + 2]; acc.w += b[e + 3];
@@ -242,7 +255,7 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
       return cudaErrorInvalidValue;
   }
   const int64_t n_w = (int64_t)E * d;
-  int pblocks = (int)((n_w + 255) / 256);
+  int pblocks = (int)((n_w / 4 + 255) / 256);
   if (pblocks > 152 * 8) pblocks = 152 * 8;
   prof_begin(K_ROUTER_PREP, s);
   cudaError_t err = launch_pdl(router_prep_kernel, dim3(pblocks), dim3(256), 0, s, w,
