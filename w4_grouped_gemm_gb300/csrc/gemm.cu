@@ -56,10 +56,11 @@ constexpr int kPackedBytes = 128 * 32;  // 128 rows x 64 4-bit codes
 constexpr int kMaxA = 4;                // dequantised-A ring depth (TMEM)
 constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 9;
 
-// Quantisation groups (64 K each) per K-step: the down GEMM has half the
-// weight rows per step of gate/up, so it takes two groups per step and the
-// fixed per-step hand-offs are paid half as often.
-__host__ __device__ constexpr int groups_per_step(bool gateup) { return gateup ? 1 : 2; }
+// Quantisation groups (64 K each) per K-step, two in both GEMMs: the fixed
+// per-step hand-offs of every warp role (the producer's expect-tx and copies,
+// the MMA warp's wait and commits, the dequant warps' waits, tensor-memory
+// store wait and arrival) are paid once per 128 K.
+__host__ __device__ constexpr int groups_per_step(bool /*gateup*/) { return 2; }
 
 // Tensor memory (512 columns x 128 lanes): accumulator sets first, then the
 // ring of dequantised A tiles (128 rows x 64 fp16 = 32 columns per matrix and
@@ -451,9 +452,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ================================================= dequant
-    // gate/up: warps 2..5 rebuild the gate slice, 6..9 the up slice; down:
-    // warps 2..5 take the first group of each K-step, 6..9 the second.  One
-    // weight row (64 codes of one group) per lane.
+    // gate/up: warps 2..5 rebuild the gate slice, 6..9 the up slice, both
+    // groups of each K-step; down: warps 2..5 take the first group of each
+    // K-step, 6..9 the second.  One weight row per lane.
     const int q = warp & 3;
     const int r = q * 32 + lane;          // weight row within the slice = TMEM lane
     const int hsel = (warp - 2) >> 2;
@@ -519,25 +520,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (w + (int)gridDim.x < n_items) down_prefetch(w + gridDim.x, tnext);
       }
       const uint32_t* sbs = sb + slot * sb_words;
-      // gate/up: two K-steps per iteration (one when a single step is left):
-      // their loads, arithmetic and tensor-memory stores interleave, and one
-      // store wait covers both before the two arrivals.  Down takes one step
-      // per iteration (its items are four steps long).
-      for (int kk = 0; kk < NST;) {
-        const bool two = GATEUP && kk + 1 < NST;
-        Ring rs1 = rs;
-        rs1.next(nstages);
-        const uint32_t it1 = it + 1;
-        const int s0 = rs.idx, b0 = it % L::kNumA, s1 = rs1.idx, b1 = it1 % L::kNumA;
-        // the stages' TMA landed and the A buffers were consumed
-        bool got = warp_wait_all2(smem_u32(&full[s0]), rs.ph, smem_u32(&aempty[b0]),
-                                  ((it / L::kNumA) + 1) & 1, it >= (uint32_t)L::kNumA, abort,
-                                  a.status);
-        if (got && two)
-          got = warp_wait_all2(smem_u32(&full[s1]), rs1.ph, smem_u32(&aempty[b1]),
-                               ((it1 / L::kNumA) + 1) & 1, it1 >= (uint32_t)L::kNumA, abort,
-                               a.status);
-        if (!got) {
+      // Per K-step a gate/up warp rebuilds both groups of its matrix (their
+      // loads, arithmetic and tensor-memory stores interleave, and one store
+      // wait and one arrival cover both); a down warp rebuilds its group.
+      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
+        const int s0 = rs.idx, b0 = it % L::kNumA;
+        // the stage's TMA landed and the A buffer was consumed
+        if (!warp_wait_all2(smem_u32(&full[s0]), rs.ph, smem_u32(&aempty[b0]),
+                            ((it / L::kNumA) + 1) & 1, it >= (uint32_t)L::kNumA, abort,
+                            a.status)) {
           ok = false;
           break;
         }
@@ -545,18 +536,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // row r sits at 16 * (h ^ sw), which spreads each 8 consecutive
         // lanes' loads over all eight 16-byte bank groups
         const int sw = (r >> 2) & 1;
-        const size_t poff = BBYTES + (size_t)(mat * KG + g) * kPackedBytes + r * 32;
-        const uint8_t* pk0 = stage_base + (size_t)s0 * STAGE + poff;
-        const uint8_t* pk1 = stage_base + (size_t)s1 * STAGE + poff;
+        const uint8_t* pk0 = stage_base + (size_t)s0 * STAGE + BBYTES +
+                             (size_t)(mat * KG + g) * kPackedBytes + r * 32;
+        const uint8_t* pk1 = pk0 + kPackedBytes;  // gate/up: the step's second group
         const uint4 lo0 = *reinterpret_cast<const uint4*>(pk0 + 16 * sw);
         const uint4 hi0 = *reinterpret_cast<const uint4*>(pk0 + 16 * (sw ^ 1));
         uint4 lo1 = lo0, hi1 = hi0;
-        if (two) {
+        if (GATEUP) {
           lo1 = *reinterpret_cast<const uint4*>(pk1 + 16 * sw);
           hi1 = *reinterpret_cast<const uint4*>(pk1 + 16 * (sw ^ 1));
         }
         const uint32_t sbv0 = sbs[(mat * G + kk * KG + g) * 128 + r];
-        const uint32_t sbv1 = two ? sbs[(mat * G + (kk + 1) * KG + g) * 128 + r] : sbv0;
+        const uint32_t sbv1 = GATEUP ? sbs[(mat * G + kk * KG + 1) * 128 + r] : sbv0;
         const uint32_t s20 = prmt(sbv0, sbv0, 0x1010u), b20 = prmt(sbv0, sbv0, 0x3232u);
         const uint32_t s21 = prmt(sbv1, sbv1, 0x1010u), b21 = prmt(sbv1, sbv1, 0x3232u);
         const uint32_t wd0[8] = {lo0.x, lo0.y, lo0.z, lo0.w, hi0.x, hi0.y, hi0.z, hi0.w};
@@ -566,30 +557,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int jj = 0; jj < 8; ++jj) {
           uint32_t t4[4], u4[4];
           dequant8(wd0[jj], s20, b20, t4);
-          dequant8(wd1[jj], s21, b21, u4);
+          if (GATEUP) dequant8(wd1[jj], s21, b21, u4);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             o0[4 * jj + e] = t4[e];
-            o1[4 * jj + e] = u4[e];
+            o1[4 * jj + e] = GATEUP ? u4[e] : 0u;
           }
         }
-        const uint32_t acol = tmem + tlane + L::kAOff + mat * L::kACols + g * 32;
-        tmem_st32(acol + b0 * MATS * L::kACols, o0);
-        if (two) tmem_st32(acol + b1 * MATS * L::kACols, o1);
+        const uint32_t acol =
+            tmem + tlane + L::kAOff + (b0 * MATS + mat) * L::kACols + g * 32;
+        tmem_st32(acol, o0);
+        if (GATEUP) tmem_st32(acol + 32, o1);
         // the stores must be complete before the MMA issuer is told: wait,
         // order them before the arrive, then one arrive per warp and step
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&afull[b0]));
-          if (two) mbar_arrive(smem_u32(&afull[b1]));
-        }
-        const int adv = two ? 2 : 1;
-        kk += adv;
-        it += adv;
-        rs.next(nstages);
-        if (two) rs.next(nstages);
+        if (lane == 0) mbar_arrive(smem_u32(&afull[b0]));
       }
       if (!ok) break;
       __syncwarp();
