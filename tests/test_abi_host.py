@@ -113,3 +113,26 @@ def test_no_gpu_reports_cuda_or_arch_error(L):
         pytest.skip("a GPU is present")
     d = lily.make_dims(64, 512, 32, 4, 128, 32)
     assert _call_forward(L, d) in (lily.LILY_ERR_CUDA, lily.LILY_ERR_ARCH)
+
+
+def test_host_graph_switch_and_host_entry_arguments(L):
+    """The end-to-end call's graph-cache switch returns the previous setting
+    (with the cache empty it makes no CUDA call), and the host-buffer entry
+    rejects missing host buffers before any copy or launch."""
+    first = L.lily_moe_host_graphs(0)
+    try:
+        assert first in (0, 1)
+        assert L.lily_moe_host_graphs(0) == 0
+        assert L.lily_moe_host_graphs(1) == 0
+        assert L.lily_moe_host_graphs(1) == 1
+    finally:
+        L.lily_moe_host_graphs(1)
+    d = lily.make_dims(64, 512, 32, 4, 128, 32)
+    wt = _lib.Weights(*([256] * 11))
+    rt = _lib.Routing(*([256] * 9))
+    args = dict(x_host=16, x_dev=16, y_dev=16, y_host=16)
+    for missing in ("x_host", "y_host"):
+        a = dict(args, **{missing: None})
+        rc = L.lily_moe_forward_host(ctypes.byref(d), a["x_host"], a["x_dev"], ctypes.byref(wt),
+                                     ctypes.byref(rt), a["y_dev"], a["y_host"], 16, 1 << 40, None)
+        assert rc == lily.LILY_ERR_INVALID_ARG, missing
