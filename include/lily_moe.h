@@ -186,8 +186,9 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x,
  * tokens.  Same arguments and result as lily_moe_decode minus the workspace.
  *   - Scratch comes from one array of 1 MiB declared at file scope in the
  *     library; every device that loads the library holds it until the
- *     process exits.  Dims whose workspace (lily_moe_workspace_bytes) exceeds
- *     1 MiB are refused with LILY_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *     process exits.  T > 8 is refused with LILY_ERR_UNSUPPORTED_SHAPE, and
+ *     dims whose workspace (lily_moe_workspace_bytes) exceeds 1 MiB with
+ *     LILY_ERR_WORKSPACE_TOO_SMALL, both before any launch.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
@@ -251,9 +252,19 @@ int lily_moe_stack_prefill(const lily_moe_dims* dims, int32_t T_total, int32_t n
 size_t lily_moe_stack_workspace_bytes(const lily_moe_dims* dims);
 
 /* Synchronises `stream`, returns the device status bits accumulated in the
- * workspace since the last call (0 = none) and clears them.  Negative on a
- * CUDA error. */
+ * workspace since the last call (0 = none) and clears them; after a
+ * LILY_STATUS_TIMEOUT it also zeroes the workspace's grid-barrier counters.
+ * Negative on a CUDA error. */
 int lily_moe_status(void* workspace, void* stream);
+
+/* Give-up limit, in nanoseconds, of the one wait in the routing kernel that
+ * spans blocks (its grid barrier, used when T > 32): 2 s by default.  Returns
+ * the previous limit.  A block whose wait runs out sets LILY_STATUS_TIMEOUT and
+ * writes none of its tokens' scatter outputs (perm, inv_perm; counts, offsets
+ * and block_map too if it is block 0), so that call's routing is invalid.
+ * For tests of the error path; 0 makes every waiting block give up at once.
+ * Applies to calls issued after it; the waits of the GEMM kernels keep 2 s. */
+uint64_t lily_moe_set_route_wait_ns(uint64_t ns);
 
 /* Static text for an error code. */
 const char* lily_moe_strerror(int code);

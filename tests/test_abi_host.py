@@ -136,3 +136,28 @@ def test_host_graph_switch_and_host_entry_arguments(L):
         rc = L.lily_moe_forward_host(ctypes.byref(d), a["x_host"], a["x_dev"], ctypes.byref(wt),
                                      ctypes.byref(rt), a["y_dev"], a["y_host"], 16, 1 << 40, None)
         assert rc == lily.LILY_ERR_INVALID_ARG, missing
+
+
+def test_route_wait_limit_setter_returns_previous(L):
+    """The routing wait limit defaults to 2 s and the setter returns the
+    previous value (host state only: no CUDA call)."""
+    prev = lily.lily_moe_set_route_wait_ns(12345)
+    try:
+        assert prev == 2_000_000_000
+        assert lily.lily_moe_set_route_wait_ns(0) == 12345
+    finally:
+        assert lily.lily_moe_set_route_wait_ns(prev) == 0
+
+
+def test_static_decode_refuses_rows_before_size(L):
+    """The static-scratch decode refuses T > 8 as a shape error even when the
+    dims would also exceed its fixed scratch, and oversized dims as a
+    workspace error, before any CUDA call."""
+    w = _lib.Weights(*([256] * 11))
+    r = _lib.Routing(*([256] * 9))
+    many = lily.make_dims(9, 4096, 256, 8, 4096, 128)
+    assert L.lily_moe_decode_static(ctypes.byref(many), 256, ctypes.byref(w), ctypes.byref(r),
+                                    256, None) == lily.LILY_ERR_UNSUPPORTED_SHAPE
+    big = lily.make_dims(8, 4096, 256, 8, 4096, 128)
+    assert L.lily_moe_decode_static(ctypes.byref(big), 256, ctypes.byref(w), ctypes.byref(r),
+                                    256, None) == lily.LILY_ERR_WORKSPACE_TOO_SMALL

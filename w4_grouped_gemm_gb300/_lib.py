@@ -37,7 +37,7 @@ EXPORTS = (
     "lily_moe_decode_static",
     "lily_moe_forward_host", "lily_moe_host_graphs",
     "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_workspace_bytes",
-    "lily_moe_status", "lily_moe_strerror", "lily_moe_profile_enable", "lily_moe_profile_read",
+    "lily_moe_status", "lily_moe_set_route_wait_ns", "lily_moe_strerror", "lily_moe_profile_enable", "lily_moe_profile_read",
     "lily_moe_kernel_name", "lily_moe_version",
 )
 
@@ -99,6 +99,7 @@ def lib():
             "lily_moe_stack_prefill": (I, [DP, ctypes.c_int32, ctypes.c_int32, WP, P,
                                            ctypes.c_float, P, P, P, SZ, P]),
             "lily_moe_status": (I, [P, P]),
+            "lily_moe_set_route_wait_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
             "lily_moe_strerror": (ctypes.c_char_p, [I]),
             "lily_moe_profile_enable": (I, [I]),
             "lily_moe_profile_read": (I, [P, P]),
@@ -291,6 +292,12 @@ def lily_moe_status(ws, stream=None) -> int:
     if rc < 0:
         raise LilyError(rc, "lily_moe_status")
     return rc
+
+
+def lily_moe_set_route_wait_ns(ns: int) -> int:
+    """Give-up limit of the routing kernel's grid-barrier wait; returns the
+    previous limit (nanoseconds)."""
+    return int(lib().lily_moe_set_route_wait_ns(int(ns)))
 
 
 def lily_moe_profile_enable(on: bool = True):

@@ -2,6 +2,7 @@
 // layout and the launch sequence of each call.  No call allocates device
 // memory; every launch goes to the caller's stream.
 #include <array>
+#include <atomic>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -64,6 +65,12 @@ void prof_end(int kind, cudaStream_t s) {
   g_prof_start = nullptr;
   g_prof_kind = -1;
 }
+
+// ---------------------------------------------------------------- wait limit
+namespace {
+std::atomic<uint64_t> g_route_wait_ns{2000000000ull};
+}
+uint64_t route_wait_limit_ns() { return g_route_wait_ns.load(std::memory_order_relaxed); }
 
 // ---------------------------------------------------------------- host caches
 namespace {
@@ -202,6 +209,7 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
   a.bar = ctrl + 1;
   a.status = ws_status(ws);
   a.plan = nullptr;
+  a.wait_ns = route_wait_limit_ns();
   if (!logits_in) {
     if (d.T > 8) {
       float* part = reinterpret_cast<float*>(base + L.part);
@@ -693,9 +701,16 @@ int lily_moe_status(void* ws, void* stream) {
   if (cudaMemcpyAsync(&v, ws_status(ws), 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return LILY_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
-  if (v && cudaMemsetAsync(ws_status(ws), 0, 4, s) != cudaSuccess) return LILY_ERR_CUDA;
+  // clear the bits; after a give-up also the grid-barrier and block-done
+  // counters (words 1..3), so that no later call starts from a stale count
+  const size_t clear = (v & LILY_STATUS_TIMEOUT) ? 16 : 4;
+  if (v && cudaMemsetAsync(ws_status(ws), 0, clear, s) != cudaSuccess) return LILY_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
   return (int)v;
+}
+
+uint64_t lily_moe_set_route_wait_ns(uint64_t ns) {
+  return g_route_wait_ns.exchange(ns);
 }
 
 const char* lily_moe_strerror(int code) {

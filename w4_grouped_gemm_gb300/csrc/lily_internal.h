@@ -79,7 +79,11 @@ struct RouteArgs {
   uint32_t* bar;       // workspace: grid barrier {count, generation}
   uint32_t* status;    // workspace status word
   int32_t* plan;       // decode plan [1 + cap][kPlanWords] or NULL (one-block routing only)
+  uint64_t wait_ns;    // give-up limit of the grid barrier's wait (route_wait_limit_ns())
 };
+// Current give-up limit of the routing kernel's grid-barrier wait (api.cu):
+// 2 s unless lily_moe_set_route_wait_ns() changed it.
+uint64_t route_wait_limit_ns();
 // Decode plan entry of one tile slot: {expert, row0, rows, 0, 4 unused,
 // token[kPlanRows], gate bits[kPlanRows], 8 unused}.
 constexpr int kPlanWords = 32;

@@ -323,10 +323,17 @@ __device__ int block_exclusive_scan(int v, int* tmp /* [8] */) {
 }
 
 // Grid-wide barrier for a cooperative launch (all blocks co-resident), with a
-// bounded wait: gives up after ~2 s and flags LILY_STATUS_TIMEOUT.
-__device__ void grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* status) {
+// bounded wait: a block that has waited limit_ns (2 s unless a test lowers
+// it) gives up, flags LILY_STATUS_TIMEOUT and gets false, the same value in
+// every thread of the block.  Its arrival is already counted, so the last
+// block to arrive still resets the count and releases the generation; the
+// barrier words end consistent for the next call either way.
+__device__ bool grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* status,
+                             uint64_t limit_ns) {
+  __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
+    int ok = 1;
     volatile uint32_t* gen = bar + 1;
     uint32_t g = *gen;
     __threadfence();
@@ -336,18 +343,21 @@ __device__ void grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* status) 
       __threadfence();
       atomicAdd(bar + 1, 1u);
     } else {
-      uint64_t t0 = globaltimer_ns();
+      const uint64_t t0 = globaltimer_ns();
       while (*gen == g) {
-        __nanosleep(64);
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 >= limit_ns) {
           set_status(status, LILY_STATUS_TIMEOUT);
+          ok = 0;
           break;
         }
+        __nanosleep(64);
       }
     }
     __threadfence();
+    s_ok = ok;
   }
   __syncthreads();
+  return s_ok != 0;
 }
 
 constexpr int kMaxE = 256, kMaxK = 8;
@@ -471,7 +481,9 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
   if (nblk > 1) {
     for (int e = threadIdx.x; e < E; e += kRouteThreads) a.hist[(size_t)blk * E + e] = s_cnt[e];
 
-    grid_barrier(a.bar, nblk, a.status);
+    // a block whose wait ran out leaves every output of its pairs unwritten:
+    // the other blocks' histogram rows may not have been written yet
+    if (!grid_barrier(a.bar, nblk, a.status, a.wait_ns)) return;
 
     // ---- phase 3: global counts, scan, this block's bases, scatter
     for (int e = threadIdx.x; e < kMaxE; e += kRouteThreads) {

@@ -54,6 +54,8 @@ extern "C" int lily_moe_decode_static(const lily_moe_dims* dims, const void* x,
   if (!dims) return LILY_ERR_INVALID_ARG;
   const size_t need = lily_moe_workspace_bytes(dims);
   if (need == 0) return lily_moe_check_dims(dims);
+  // more rows than the decode path takes is a shape error, whatever the size
+  if (dims->T > 8) return LILY_ERR_UNSUPPORTED_SHAPE;
   if (need > kStaticScratchBytes) return LILY_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   int rc = scratch_address(&ws);
