@@ -1,17 +1,20 @@
 #!/usr/bin/env python3
 """Benchmark of the W4 MoE expert layer on GB300.
 
-One step = one whole MoE layer (router logits, top-k + gates, histogram,
-scan, scatter, block map, gate/up grouped GEMM with fused dequant + SwiGLU,
-down grouped GEMM with fused dequant + gated combine, bf16 output) over one
-batch of T tokens, through the library's C ABI.
+One step of a layer workload = one whole MoE layer (router logits, top-k +
+gates, histogram, scan, scatter, block map, gate/up grouped GEMM with fused
+dequant + SwiGLU, down grouped GEMM with fused dequant + gated combine; fp32
+output) over one batch of T tokens, through the library's C ABI.  One step of
+the stacked workload `stack8192` = one 8192-token prompt through 40 pre-norm
+MoE layers in chunks of 2048 tokens.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the FP64 CPU oracle, timed
 
-Prints ONE JSON line (rank 0).  Multi-GPU runs (torchrun) are token data
+Prints ONE JSON line (rank 0).  With --gpus N > 1 outside a launcher it runs
+itself as N ranks under torch.distributed.run.  Multi-GPU runs are token data
 parallel with replicated weights and no exchange: every rank runs its own
-batch (weak scaling).
+batch (weak scaling); the time is the slowest rank's.
 """
 from __future__ import annotations
 
@@ -35,15 +38,21 @@ import torch  # noqa: E402
 METRIC = "MoE-layer tokens/s"
 UNIT = "tokens/s"
 
+def _wl(kind, T, d, E, k, F, zipf=None, bm=128, **kw):
+    return dict(kind=kind, T=T, d=d, E=E, k=k, F=F, zipf=zipf, bm=bm, **kw)
+
+
 WORKLOADS = {
-    # name: (T, d, E, k, F, zipf)
-    "prefill512": (512, 2048, 256, 8, 512, None),
-    "prefill2048_zipf": (2048, 2048, 256, 8, 512, 1.1),
-    "prefill2048": (2048, 2048, 256, 8, 512, None),
-    "decode1": (1, 2048, 256, 8, 512, None),
-    "decode5": (5, 2048, 256, 8, 512, None),
-    "prefill8192": (8192, 2048, 256, 8, 512, None),  # one unchunked call
-    "small": (32, 512, 32, 4, 128, None),
+    # one MoE layer per step
+    "prefill512": _wl("layer", 512, 2048, 256, 8, 512, bm=64),
+    "prefill2048": _wl("layer", 2048, 2048, 256, 8, 512),
+    "prefill2048_zipf": _wl("layer", 2048, 2048, 256, 8, 512, zipf=1.1),
+    "prefill8192": _wl("layer", 8192, 2048, 256, 8, 512),  # one unchunked call
+    "decode1": _wl("layer", 1, 2048, 256, 8, 512),
+    "decode5": _wl("layer", 5, 2048, 256, 8, 512),
+    "small": _wl("layer", 32, 512, 32, 4, 128, bm=32),
+    # 40 pre-norm MoE layers, an 8192-token prompt in chunks of 2048 per step
+    "stack8192": _wl("stack_prefill", 8192, 2048, 256, 8, 512, layers=40, chunk=2048),
 }
 DEFAULT_WORKLOAD = "prefill512"
 
@@ -146,6 +155,49 @@ def dist_info():
     return ws, rank, local
 
 
+def layer_seed(layer: int, rank: int) -> int:
+    """Seed of one layer's synthetic inputs on one rank: every rank draws its
+    own token batch and weights (token data parallel, weak scaling)."""
+    return 2000 + 3 * layer + 10000 * rank  # layer inputs draw from seed, seed+1, seed+2
+
+
+def host_cpu():
+    """(logical CPUs, CPU model) of this host, for the CPU-baseline record."""
+    model = None
+    try:
+        for line in Path("/proc/cpuinfo").read_text().splitlines():
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "cpu model", "hardware") and ":" in line:
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    return os.cpu_count(), model or "unknown"
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Run this script as n ranks on one node (one process per GPU) under
+    torch.distributed.run, as `bench.py --gpus n` asks when no launcher set
+    the rank environment; returns the launcher's exit code."""
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1", f"--master-port={port}",
+           str(Path(__file__).resolve())] + list(argv)
+    return subprocess.call(cmd)
+
+
 def max_over_ranks(value: float, world: int, device=None) -> float:
     """Largest value over all ranks (the job's time is its slowest rank's)."""
     if world <= 1:
@@ -158,18 +210,6 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 def job_throughput(world: int, tokens_per_rank: int, steps: int, seconds: float) -> float:
     """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
     return world * tokens_per_rank * steps / seconds
-
-
-def algorithmic_bytes(T, d, E, k, F, counts, y_bytes=4):
-    """Touched experts' W4 bytes (packed + bf16 scale/bias) + router W + x + y."""
-    per_expert = 3 * (F * d // 2 + F * d // 64 * 4)
-    touched = int((np.asarray(counts) > 0).sum()) + 1  # + shared expert
-    return touched * per_expert + E * d * 4 + T * d * (2 + y_bytes), touched
-
-
-def gateup_bytes(T, d, F, touched):
-    """Gate/up kernel: touched experts' gate+up W4 bytes + x read."""
-    return touched * 2 * (F * d // 2 + F * d // 64 * 4) + T * d * 2
 
 
 def layer_flops(T, d, E, k, F):
@@ -199,34 +239,256 @@ def oracle_sample(shape_args, seed, n_rows, rows_offset=0):
 
 
 def run_reference(args, ws, rank):
-    """--impl reference: the oracle as it stands, on the host cores."""
+    """--impl reference: the oracle as it stands, on the host cores (rank 0
+    only; under a multi-rank launch the other ranks exit without work)."""
     if rank != 0:
         return
     wl = WORKLOADS[args.workload]
-    T, d, E, k, F, zipf = wl
-    # one step = one token row of the workload through the oracle layer
+    stack = wl["kind"] == "stack_prefill"
+    T = wl.get("chunk", wl["T"]) if stack else wl["T"]
+    shape = (T, wl["d"], wl["E"], wl["k"], wl["F"], wl["zipf"])
+    nlay = wl["layers"] if stack else 1
+    # one step = one token row of the workload through the oracle layer (for
+    # the stacked prefill: one row of one layer, its time counted once per layer)
     n_rows = 1
     for i in range(args.warmup):
-        oracle_sample(wl, 1000, n_rows, i)
+        oracle_sample(shape, 1000, n_rows, i)
     t = 0.0
     for i in range(args.steps):
-        t += oracle_sample(wl, 1000, n_rows, args.warmup + i)
+        t += oracle_sample(shape, 1000, n_rows, args.warmup + i)
+    t *= nlay
     value = args.steps * n_rows / t
+    ncpu, model = host_cpu()
+    sample = f"{n_rows} token row per step, {args.steps} steps"
+    if stack:
+        sample += f"; one layer's time x {nlay} layers (extrapolated)"
     out = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "T": T, "d_model": d, "n_experts": E, "top_k": k,
-                   "d_ff": F, "zipf_s": zipf, "step_sample": f"{n_rows} token row(s) per step"},
+        "config": {"workload": args.workload, "T": wl["T"], "d_model": wl["d"],
+                   "n_experts": wl["E"], "top_k": wl["k"], "d_ff": wl["F"], "zipf_s": wl["zipf"],
+                   "step_sample": f"{n_rows} token row(s) per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{n_rows} token row per step, {args.steps} steps"},
+                         "nproc": ncpu, "cpu_model": model, "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
 
 
 # ----------------------------------------------------------------- GPU arm
+def expert_matrix_bytes(d, F):
+    """One W4 matrix of one expert: packed codes + bf16 scale and bias."""
+    return F * d // 2 + F * d // 64 * 4
+
+
+def kernel_work(name, T, d, E, k, F, touched):
+    """Algorithmic (bytes, flops) of one launch of a kernel of the layer, or
+    None: weights of the touched experts (routed experts with rows + shared)
+    once, activations in and out once; H, tiles and accumulators are the
+    implementation's traffic and are not counted."""
+    mb = expert_matrix_bytes(d, F)
+    P = T * k
+    if name in ("gateup_gemm", "dec_gateup"):
+        return touched * 2 * mb + T * d * 2, 4 * (P + T) * d * F
+    if name in ("down_gemm", "dec_down_combine"):
+        return touched * mb + T * d * 4, 2 * (P + T) * d * F
+    if name in ("router_gemm", "router_gemv", "dec_router"):
+        return E * d * 4 + T * d * 2 + T * E * 4, 2 * T * d * E
+    if name == "route":
+        return T * E * 4 + T * k * 8, 0
+    return None
+
+
+def roofline_of(name, dur_s, work, hbm, tflops, peak_src):
+    """Roofline object of one kernel: the bound whose time is longer (bytes at
+    the measured copy bandwidth, or flops at the measured bf16 tensor rate --
+    the fp16 kind::f16 MMAs run at the bf16 rate)."""
+    nbytes, flops = work
+    t_hbm = nbytes / (hbm * 1e9)
+    t_tc = flops / (tflops * 1e12) if flops else 0.0
+    if t_tc > t_hbm:
+        achieved = flops / dur_s / 1e12
+        return {"bound": "tensor", "achieved": achieved, "peak": tflops, "unit": "TFLOP/s",
+                "frac": achieved / tflops, "kernel": name,
+                "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": nbytes,
+                "peak_source": f"bf16_tflops (burst) of {peak_src} peaks"}
+    achieved = nbytes / dur_s / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "kernel": name, "algorithmic_bytes_per_launch": nbytes,
+            "algorithmic_flops_per_launch": flops,
+            "peak_source": f"hbm_gbs of {peak_src} peaks (copy bandwidth)"}
+
+
+def group_sizes(counts_list):
+    """Rows per routed expert (the grouped GEMM's group sizes), over the
+    layers a step rotates through."""
+    c = np.concatenate([np.asarray(x) for x in counts_list])
+    return {"min": int(c.min()), "median": float(np.median(c)), "p90": float(np.percentile(c, 90)),
+            "max": int(c.max()), "empty_experts_per_layer": float((c == 0).sum() / len(counts_list)),
+            "experts": int(len(counts_list[0]))}
+
+
+class LayerRun:
+    """One MoE layer per step (lily_moe_forward, or lily_moe_decode for T <= 8),
+    rotating through several layers of weights so no step finds its weights
+    in L2."""
+
+    def __init__(self, lily, synth, wl, args, rank, dev):
+        T, d, E, k, F = wl["T"], wl["d"], wl["E"], wl["k"], wl["F"]
+        self.lily, self.wl, self.dev = lily, wl, dev
+        self.decode = T <= 8
+        shape = synth.LayerShape(T, d, E, k, F)
+        self.dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
+        # prefill weights are 455 MB a layer; decode touches ~16 MB a layer, so
+        # it rotates >= 16 layers to stay well above the 126 MB L2
+        self.nl = max(args.layers, 16) if self.decode else args.layers
+        self.layers = []
+        for l in range(self.nl):
+            inp = synth.make_layer(shape, layer_seed(l, rank), device=dev, zipf_s=wl["zipf"])
+            self.layers.append((inp["x"], lily.LayerWeights(inp["router_w"], inp["router_b"],
+                                                            inp["experts"])))
+        self.r = lily.RoutingBuffers(self.dims, dev)
+        self.ws = lily.alloc_workspace(lily.lily_moe_workspace_bytes(self.dims), dev)
+        self.y = torch.empty(T, d, dtype=lily.out_torch_dtype(self.dims), device=dev)
+        self.call = lily.lily_moe_decode if self.decode else lily.lily_moe_forward
+        self.tokens_per_step = T
+        self.rotation = self.nl
+        self.counts = []
+
+    def step(self, i):
+        x, w = self.layers[i % self.nl]
+        self.call(self.dims, x, w, self.r, self.y, self.ws, None)
+
+    def after_warmup(self):
+        for l in range(self.nl):
+            self.step(l)
+            torch.cuda.synchronize()
+            self.counts.append(self.r.counts.cpu().numpy().copy())
+
+    def status(self):
+        return self.lily.lily_moe_status(self.ws)
+
+    def launches_per_layer(self, name):
+        return 1
+
+    def touched(self):
+        return float(np.mean([(c > 0).sum() + 1 for c in self.counts]))
+
+    def layer_work(self):
+        wl, T = self.wl, self.wl["T"]
+        d, F, E = wl["d"], wl["F"], wl["E"]
+        nbytes = self.touched() * 3 * expert_matrix_bytes(d, F) + E * d * 4 + T * d * (2 + 4)
+        return nbytes, layer_flops(T, d, E, wl["k"], F), self.nl
+
+    # end to end: host x in, the layer through the host-buffer entry point, host y out
+    def e2e_prepare(self):
+        T, d = self.wl["T"], self.wl["d"]
+        self.xh = [self.layers[l][0].cpu().pin_memory() for l in range(self.nl)]
+        self.yh = torch.empty(T, d, dtype=self.y.dtype).pin_memory()
+        self.xd = torch.empty(T, d, dtype=torch.bfloat16, device=self.dev)
+        self.h2d = T * d * 2
+        self.d2h = T * d * self.y.element_size()
+
+    def e2e_step(self, i):
+        self.lily.lily_moe_forward_host(self.dims, self.xh[i % self.nl], self.xd,
+                                        self.layers[i % self.nl][1], self.r, self.y, self.yh,
+                                        self.ws, None)
+
+    def config(self):
+        c = {"l2": f"inputs larger than L2: {self.nl} layers of weights rotated per step",
+             "path": "decode GEMV" if self.decode else "prefill grouped GEMM",
+             "experts_touched_per_step": self.touched(),
+             "expert_group_rows": group_sizes(self.counts)}
+        return c
+
+
+class StackPrefillRun:
+    """The stacked-layer prefill: one step is one T_total-token prompt through
+    n_layers pre-norm MoE layers with an fp32 residual, in chunks of `chunk`
+    tokens (lily_moe_stack_prefill).  The 40 layers' weights (18.2 GB) dwarf
+    L2.  Each step first restores the prompt's input x (one device copy of
+    T_total * d fp32, 64 MB, about 0.1% of a step), because the call updates x
+    in place."""
+
+    def __init__(self, lily, synth, wl, args, rank, dev):
+        d, E, k, F = wl["d"], wl["E"], wl["k"], wl["F"]
+        self.lily, self.wl, self.dev = lily, wl, dev
+        self.chunk, self.T_total, self.nlay = wl["chunk"], wl["T"], wl["layers"]
+        self.dims = lily.make_dims(self.chunk, d, E, k, F, args.tile_rows)
+        self.weights = []
+        for l in range(self.nlay):
+            wr, br = synth.make_router(E, d, layer_seed(l, rank) + 1, dev)
+            ex = synth.make_experts(E, d, F, layer_seed(l, rank) + 2, dev)
+            self.weights.append(lily.LayerWeights(wr, br, ex))
+        g = torch.Generator(device=dev)
+        g.manual_seed(layer_seed(0, rank))
+        self.x0 = torch.randn(self.T_total, d, generator=g, device=dev, dtype=torch.float32)
+        self.x = self.x0.clone()
+        self.ws = lily.alloc_workspace(lily.lily_moe_stack_workspace_bytes(self.dims), dev)
+        self.tokens_per_step = self.T_total
+        self.rotation = 1
+        self.nchunks = self.T_total // self.chunk
+        self.touched_l = []
+
+    def step(self, i):
+        self.x.copy_(self.x0)
+        self.lily.lily_moe_stack_prefill(self.dims, self.x, self.weights, 1e-6, None, None,
+                                         self.ws, None)
+
+    def after_warmup(self):
+        # experts touched per (layer, chunk), from one traced pass
+        E, d = self.wl["E"], self.wl["d"]
+        logits = torch.empty(self.nlay, self.T_total, E, dtype=torch.float32, device=self.dev)
+        self.x.copy_(self.x0)
+        self.lily.lily_moe_stack_prefill(self.dims, self.x, self.weights, 1e-6, None, logits,
+                                         self.ws, None)
+        torch.cuda.synchronize()
+        k = self.wl["k"]
+        top = torch.topk(logits.view(self.nlay, self.nchunks, self.chunk, E), k, dim=-1).indices
+        for l in range(self.nlay):
+            for c in range(self.nchunks):
+                self.touched_l.append(int(torch.unique(top[l, c]).numel()) + 1)
+        del logits
+
+    def status(self):
+        return self.lily.lily_moe_status(self.ws)
+
+    def launches_per_layer(self, name):
+        return self.nlay * self.nchunks
+
+    def touched(self):
+        return float(np.mean(self.touched_l))
+
+    def layer_work(self):
+        wl = self.wl
+        d, F, E, k = wl["d"], wl["F"], wl["E"], wl["k"]
+        per = self.touched() * 3 * expert_matrix_bytes(d, F) + E * d * 4 + self.chunk * d * 12
+        n = self.nlay * self.nchunks
+        return per * n, layer_flops(self.chunk, d, E, k, F) * n, 1
+
+    def e2e_prepare(self):
+        self.xh = self.x0.cpu().pin_memory()
+        self.xo = torch.empty_like(self.xh).pin_memory()
+        self.h2d = self.xh.numel() * 4
+        self.d2h = self.xo.numel() * 4
+
+    def e2e_step(self, i):
+        self.x.copy_(self.xh, non_blocking=True)
+        self.lily.lily_moe_stack_prefill(self.dims, self.x, self.weights, 1e-6, None, None,
+                                         self.ws, None)
+        self.xo.copy_(self.x, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def config(self):
+        return {"l2": f"inputs larger than L2: {self.nlay} layers of weights (18.2 GB) per step",
+                "path": "stacked prefill (pre-norm MoE layers, fp32 residual)",
+                "layers": self.nlay, "chunk_tokens": self.chunk, "prompt_tokens": self.T_total,
+                "experts_touched_per_layer_chunk": self.touched(),
+                "step_restores_input": "one 64 MB device copy of x per step"}
+
+
 def run_lily(args, world, rank, local):
     import w4_grouped_gemm_gb300 as lily
     from w4_grouped_gemm_gb300 import synth
@@ -234,58 +496,44 @@ def run_lily(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     lily.lib()
-    T, d, E, k, F, zipf = WORKLOADS[args.workload]
-    decode = T <= 8
-    shape = synth.LayerShape(T, d, E, k, F)
-    dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
-    # several layers of weights, rotated per step, so no step finds the
-    # previous step's weights in L2 (each layer's weights are 455 MB)
-    # decode touches ~16 MB per layer: rotate >= 16 layers so no step finds
-    # its weights in the 126 MB L2
-    nl = max(args.layers, 16) if decode else args.layers
-    layers = []
-    for l in range(nl):
-        inp = synth.make_layer(shape, 1000 * 2 + 17 * l + 101 * rank, device=dev, zipf_s=zipf)
-        layers.append((inp["x"], lily.LayerWeights(inp["router_w"], inp["router_b"], inp["experts"])))
-    r = lily.RoutingBuffers(dims, dev)
-    wsb = lily.alloc_workspace(lily.lily_moe_workspace_bytes(dims), dev)
-    y = torch.empty(T, d, dtype=lily.out_torch_dtype(dims), device=dev)
+    wl = WORKLOADS[args.workload]
+    T, d, E, k, F = wl["T"], wl["d"], wl["E"], wl["k"], wl["F"]
+    run = {"layer": LayerRun, "stack_prefill": StackPrefillRun}[wl["kind"]](
+        lily, synth, wl, args, rank, dev)
     stream = torch.cuda.current_stream(dev)
-    call = lily.lily_moe_decode if decode else lily.lily_moe_forward
-
-    def step(i):  # on the current stream (the capture stream inside a graph)
-        x, w = layers[i % nl]
-        call(dims, x, w, r, y, wsb, None)
 
     for i in range(args.warmup):
-        step(i)
+        run.step(i)
     torch.cuda.synchronize()
-    if lily.lily_moe_status(wsb) != 0:
+    if run.status() != 0:
         raise RuntimeError("device status bits set during warm-up")
-    counts_by_layer = []
-    for l in range(nl):
-        step(l)
-        torch.cuda.synchronize()
-        counts_by_layer.append(r.counts.cpu().numpy().copy())
+    run.after_warmup()
 
-    # The timed steps replay a CUDA graph of the C-ABI calls (one command
-    # buffer per group of nl layer steps), so host submission does not gate
-    # the device; fall back to eager launches if capture is not possible.
-    graph = None
+    # The timed steps replay CUDA graphs of the C-ABI calls: one graph of
+    # `rotation` consecutive steps replayed steps // rotation times, then one
+    # of the remaining steps, so exactly `steps` steps run; eager launches if
+    # capture is not possible.
+    rot = run.rotation
+    reps, rem = divmod(args.steps, rot)
+    graphs = None
     if not args.eager:
         try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                for i in range(nl):
-                    step(i)
-            graph.replay()
+            graphs = []
+            for n in (rot if reps else 0, rem):
+                if n == 0:
+                    graphs.append(None)
+                    continue
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(n):
+                        run.step(i)
+                g.replay()
+                graphs.append(g)
             torch.cuda.synchronize()
         except Exception as exc:  # noqa: BLE001
             print(f"graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
-            graph = None
+            graphs = None
             torch.cuda.synchronize()
-    reps = max(1, args.steps // nl) if graph is not None else args.steps
-    steps_timed = reps * nl if graph is not None else args.steps
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -298,12 +546,14 @@ def run_lily(args, world, rank, local):
     e1 = torch.cuda.Event(enable_timing=True)
     t_wall0 = time.perf_counter()
     e0.record(stream)
-    if graph is not None:
+    if graphs is not None:
         for _ in range(reps):
-            graph.replay()
+            graphs[0].replay()
+        if graphs[1] is not None:
+            graphs[1].replay()
     else:
         for i in range(args.steps):
-            step(i)
+            run.step(i)
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
@@ -314,24 +564,24 @@ def run_lily(args, world, rank, local):
         time.sleep(0.2)
         sampler.stop()
     ms = max_over_ranks(ms, world, dev)
-    args.steps = steps_timed
+    del graphs
 
     # Per-kernel device time: the library's CUDA events around every kernel,
-    # recorded on the launch stream.  The same steps are captured with the
-    # event records inside the graph and replayed once (eager when no graph).
-    prof_steps = min(steps_timed, 40 * nl)
+    # recorded on the launch stream, in a captured graph of the same steps
+    # replayed once (eager when no graph).
+    prof_steps = max(1, min(args.steps, 10 * rot))
     lily.lily_moe_profile_enable(True)
     lily.lily_moe_profile_read()
     for i in range(prof_steps):  # eager pass: also fills the library's event pool
-        step(i)
+        run.step(i)
     torch.cuda.synchronize()
     prof = lily.lily_moe_profile_read()
-    if graph is not None:
+    if not args.eager:
         try:
             pgraph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(pgraph):
                 for i in range(prof_steps):
-                    step(i)
+                    run.step(i)
             pgraph.replay()  # its event records now hold this replay's times
             torch.cuda.synchronize()
             prof = lily.lily_moe_profile_read()
@@ -339,111 +589,100 @@ def run_lily(args, world, rank, local):
         except Exception as exc:  # noqa: BLE001
             print(f"profiled graph unavailable ({exc}); eager per-kernel times", file=sys.stderr)
     lily.lily_moe_profile_enable(False)
-    status = lily.lily_moe_status(wsb)
+    status = run.status()
     if status:
         raise RuntimeError(f"device status bits set: {status}")
 
-    # end to end through the host-buffer entry point (pinned host x and y)
-    e2e_steps = 3 if args.no_e2e else max(3, min(args.steps, 200))
-    xh = [layers[l][0].cpu().pin_memory() for l in range(nl)]
-    yh = torch.empty(T, d, dtype=y.dtype).pin_memory()
-    xd = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    # end to end through the public API with host buffers
+    run.e2e_prepare()
+    e2e_steps = 3 if args.no_e2e else max(3, min(args.steps, 200 if wl["kind"] == "layer" else 5))
     for i in range(3):
-        lily.lily_moe_forward_host(dims, xh[i % nl], xd, layers[i % nl][1], r, y, yh, wsb, stream)
+        run.e2e_step(i)
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        lily.lily_moe_forward_host(dims, xh[i % nl], xd, layers[i % nl][1], r, y, yh, wsb, stream)
+        run.e2e_step(i)
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world, dev)
 
     if rank != 0:
         return
     hbm, tf_burst, tf_sus, peak_src = measured_peaks()
-    value = job_throughput(world, T, args.steps, ms / 1000.0)
-    e2e_value = job_throughput(world, T, e2e_steps, e2e_s)
-    alg_bytes = []
-    touched_l = []
-    for c in counts_by_layer:
-        b, tch = algorithmic_bytes(T, d, E, k, F, c)
-        alg_bytes.append(b)
-        touched_l.append(tch)
-    step_bytes = float(np.mean(alg_bytes))
-    flops = layer_flops(T, d, E, k, F)
+    tps = run.tokens_per_step
+    value = job_throughput(world, tps, args.steps, ms / 1000.0)
+    e2e_value = job_throughput(world, tps, e2e_steps, e2e_s)
     step_s = ms / 1000.0 / args.steps
-    layer_t_hbm = step_bytes / (hbm * 1e9)
-    layer_t_tc = flops / (tf_sus * 1e12)
-    # dominant kernel of the step by device time
-    kernels = {n: {"ms_per_launch": v["ms"] / v["launches"], "launches": v["launches"],
-                   "share": v["ms"] / sum(u["ms"] for u in prof.values())}
-               for n, v in prof.items()}
+    step_bytes, step_flops, _ = run.layer_work()
+    step_t_hbm = step_bytes / (hbm * 1e9)
+    step_t_tc = step_flops / (tf_sus * 1e12)
+    total_ms = sum(u["ms"] for u in prof.values())
+    kernels = {n: {"us_per_launch": 1e3 * v["ms"] / v["launches"], "launches": v["launches"],
+                   "share": v["ms"] / total_ms} for n, v in prof.items()}
     dom = max(prof, key=lambda n: prof[n]["ms"]) if prof else None
     roofline = None
+    touched = run.touched()
+    chunk_T = run.dims.T
+    for n in kernels:
+        work = kernel_work(n, chunk_T, d, E, k, F, touched)
+        if work:
+            rf = roofline_of(n, kernels[n]["us_per_launch"] * 1e-6, work, hbm, tf_burst, peak_src)
+            kernels[n]["bound"], kernels[n]["frac"] = rf["bound"], rf["frac"]
     if dom:
-        dur = prof[dom]["ms"] / prof[dom]["launches"] / 1000.0
-        touched = float(np.mean(touched_l))
-        if dom == "gateup_gemm":
-            dbytes = gateup_bytes(T, d, F, touched)
-        elif dom == "down_gemm":
-            dbytes = touched * (F * d // 2 + F * d // 64 * 4) + T * d * 2
-        elif dom in ("dec_gateup",):
-            dbytes = gateup_bytes(T, d, F, touched)
-        elif dom in ("dec_down_combine",):
-            dbytes = touched * (F * d // 2 + F * d // 64 * 4)
-        elif dom in ("router_gemv", "router_gemm"):
-            dbytes = E * d * 4 + T * d * 2  # router weights (fp32) and x
-        else:
-            dbytes = step_bytes
-        achieved = dbytes / dur / 1e9
-        key = (args.workload, dom, source_hash(KERNEL_SOURCES))
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": NCU_TRAFFIC.get(key),
-                    "kernel": dom, "algorithmic_bytes_per_launch": dbytes,
-                    "peak_source": f"hbm_gbs of {peak_src} peaks (copy bandwidth)"}
-    per_step = sum(v["launches"] for n, v in prof.items() if n != "memset_acc") / max(prof_steps, 1)
-    launches = int(round(per_step * args.steps))
+        work = kernel_work(dom, chunk_T, d, E, k, F, touched)
+        if work:
+            roofline = roofline_of(dom, kernels[dom]["us_per_launch"] * 1e-6, work, hbm, tf_burst,
+                                   peak_src)
+            roofline["traffic"] = NCU_TRAFFIC.get((args.workload, dom,
+                                                   source_hash(KERNEL_SOURCES)))
+    launches = int(round(sum(v["launches"] for v in prof.values()) / prof_steps * args.steps))
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
 
     # CPU baseline: the oracle, bounded sample of the same workload
     cpu = None
     if not args.no_cpu_baseline:
-        n_rows = 1 if decode else args.cpu_rows
-        t_cpu = oracle_sample(WORKLOADS[args.workload], 1000, n_rows)
-        cpu = {"value": n_rows / t_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{n_rows} token rows of the {args.workload} layer (router logits, "
-                         f"routing, explicit dequant of every touched expert, FP64 layer)"}
+        ncpu, model = host_cpu()
+        layer_shape = (chunk_T, d, E, k, F, wl["zipf"])
+        if wl["kind"] == "stack_prefill":
+            n_rows = args.cpu_rows
+            t_cpu = oracle_sample(layer_shape, 1000, n_rows)
+            nl = wl["layers"]
+            cpu = {"value": n_rows / (t_cpu * nl), "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "nproc": ncpu, "cpu_model": model, "extrapolated": True,
+                   "sample": f"{n_rows} token rows of one {chunk_T}-token layer, time x {nl} "
+                             f"layers (extrapolated: the prompt is {nl} layers x "
+                             f"{run.nchunks} chunks of {chunk_T} tokens)"}
+        else:
+            n_rows = 1 if run.decode else args.cpu_rows
+            t_cpu = oracle_sample(layer_shape, 1000, n_rows)
+            cpu = {"value": n_rows / t_cpu, "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "nproc": ncpu, "cpu_model": model,
+                   "sample": f"{n_rows} token rows of the {args.workload} layer (router logits, "
+                             f"routing, explicit dequant of every touched expert, FP64 layer)"}
+    cfg = {"workload": args.workload, "T": T, "d_model": d, "n_experts": E, "top_k": k,
+           "d_ff": F, "zipf_s": wl["zipf"], "tile_rows": args.tile_rows,
+           "launch": "CUDA graph replay of the C-ABI calls" if not args.eager else "eager",
+           "parallelism": f"token data parallel x{world} (replicated weights, no exchange)",
+           "step_algorithmic_bytes": step_bytes, "step_flops": step_flops,
+           "step_roofline_us": 1e6 * max(step_t_hbm, step_t_tc),
+           "step_frac_of_roofline": max(step_t_hbm, step_t_tc) / step_s,
+           "step_bound": "tensor" if step_t_tc > step_t_hbm else "hbm",
+           "kernels": kernels}
+    cfg.update(run.config())
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16 tensor-core operands (W4 weights, bf16 x), fp32 accumulate, fp32 out",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 tensor-core operands (W4 weights, bf16 x), fp32 accumulate, fp32 out",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {
-            "workload": args.workload, "T": T, "d_model": d, "n_experts": E, "top_k": k,
-            "d_ff": F, "zipf_s": zipf, "tile_rows": args.tile_rows,
-            "path": "decode GEMV" if decode else "prefill grouped GEMM",
-            "l2": f"inputs larger than L2: {nl} layers of weights rotated per step",
-            "launch": "CUDA graph replay of the C-ABI calls" if graph is not None else "eager",
-            "parallelism": f"token data parallel x{world} (replicated weights, no exchange)",
-            "experts_touched_per_step": float(np.mean(touched_l)),
-            "layer_algorithmic_bytes": step_bytes, "layer_flops": flops,
-            "layer_roofline_us": 1e6 * max(layer_t_hbm, layer_t_tc),
-            "layer_frac_of_roofline": max(layer_t_hbm, layer_t_tc) / step_s,
-            "kernels": kernels,
-        },
+        "config": cfg,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": T * d * 2,
-                "d2h_bytes_per_step": T * d * y.element_size()},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": run.h2d,
+                "d2h_bytes_per_step": run.d2h},
         "gpu_launches": launches,
         "clocks": clocks,
     }
-    if decode and graph is not None:
-        # the graph replays nl consecutive layers (each its own weights, chained
-        # with programmatic dependent launch): one token through an nl-layer
-        # MoE stack
-        out["config"]["stack_layers"] = nl
-        out["config"]["stack_step_us"] = 1e3 * ms / args.steps * nl
     print(json.dumps(out), flush=True)
 
 
@@ -463,9 +702,10 @@ def run_ablation(args, world, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    T, d, E, k, F, zipf = WORKLOADS[args.workload]
-    if T <= 8:
-        raise SystemExit("ablations are prefill-only")
+    wl = WORKLOADS[args.workload]
+    T, d, E, k, F, zipf = wl["T"], wl["d"], wl["E"], wl["k"], wl["F"], wl["zipf"]
+    if T <= 8 or wl["kind"] != "layer":
+        raise SystemExit("ablations are single-layer prefill only")
     shape = synth.LayerShape(T, d, E, k, F)
     dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
     inp = synth.make_layer(shape, 1000 * 2 + 17, device=dev, zipf_s=zipf)
@@ -569,7 +809,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["lily", "reference"], default="lily")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--tile-rows", type=int, default=64)
+    ap.add_argument("--tile-rows", type=int, default=None,
+                    help="block-map tile rows BM (default: the workload's, 64 at T=512, else 128)")
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -579,7 +820,13 @@ def main():
                     help="bench-only ablation of a design point (prefill workloads)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.tile_rows is None:
+        args.tile_rows = WORKLOADS[args.workload]["bm"]
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
     world, rank, local = dist_info()
+    if args.gpus != world:
+        raise SystemExit(f"--gpus {args.gpus} but {world} rank(s) were launched")
     if world > 1:
         backend = "nccl" if torch.cuda.is_available() and args.impl == "lily" else "gloo"
         if backend == "nccl":

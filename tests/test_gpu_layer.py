@@ -105,14 +105,39 @@ def test_prefill2048_uniform_sampled_rows_bm64(oracle_lib):
     _check_forward(L, rows)
 
 
+def test_prefill2048_uniform_sampled_rows_bm128(oracle_lib):
+    L = Layer(synth.SHAPES["prefill2048_zipf"], seed=3200, tile_rows=128)
+    rows = np.random.default_rng(4).choice(2048, 24, replace=False)
+    _check_forward(L, rows)
+
+
+def test_prefill512_bm16_sampled_rows(oracle_lib):
+    L = Layer(synth.SHAPES["prefill512"], seed=2100, tile_rows=16)
+    rows = np.random.default_rng(5).choice(512, 24, replace=False)
+    _check_forward(L, rows)
+
+
+def test_prefill8192_one_call_sampled_rows(oracle_lib):
+    """The unchunked long-prompt layer: one call of T = 8192 tokens (weights
+    read once), bit-exact routing and 64 sampled rows spread over the whole
+    range (one from each block of 128 tokens) against the oracle."""
+    L = Layer(synth.LayerShape(8192, 2048, 256, 8, 512), seed=3300, tile_rows=128)
+    rng = np.random.default_rng(6)
+    rows = np.arange(0, 8192, 128) + rng.integers(0, 128, 64)
+    _check_forward(L, rows)
+
+
 def test_forward_repeat_is_stable(oracle_lib):
-    """Two calls on the same workspace give the same routing and outputs that
-    agree to fp32 atomic-order noise."""
+    """Two calls on the same workspace give the same routing, and outputs that
+    differ only by the order of the fp32 additions that combine the experts
+    into y (a few fp32 ulps of the largest terms)."""
     L = Layer(synth.LayerShape(256, 1024, 64, 8, 256), seed=91, tile_rows=64)
     y1 = L.forward().float().clone()
+    ids1 = L.r.topk_ids.clone()
     y2 = L.forward().float()
+    assert torch.equal(ids1, L.r.topk_ids)
     rel = (y1 - y2).abs().max().item() / y1.pow(2).mean().sqrt().item()
-    assert rel < 1e-2
+    assert rel < 1e-5
 
 
 # ------------------------------------------------------------ decode path
@@ -147,7 +172,7 @@ def test_forward_host_entry(oracle_lib):
     yd = torch.empty_like(L.y)
     lily.lily_moe_forward_host(L.dims, xh, xd, L.w, L.r, yd, yh, L.ws)
     rel = (yh.float() - ydev.cpu().float()).abs().max().item() / ydev.float().pow(2).mean().sqrt().item()
-    assert rel < 1e-2
+    assert rel < 1e-5
 
 
 @pytest.mark.parametrize("T", [64, 5])

@@ -52,3 +52,37 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(1.5, 1) == 1.5
     assert bench.job_throughput(1, 512, 10, 2.0) == 2560.0
+
+
+def test_rank_seeds_are_disjoint():
+    """Every rank draws its own batch and weights: the three seeds of each
+    (layer, rank) never coincide with another's."""
+    import bench
+    seen = {}
+    for rank in range(8):
+        for layer in range(64):
+            s = bench.layer_seed(layer, rank)
+            for off in range(3):
+                assert (s + off) not in seen, (layer, rank, seen.get(s + off))
+                seen[s + off] = (layer, rank)
+
+
+def test_bench_gpus_flag_launches_ranks():
+    """`bench.py --gpus 2` outside a launcher runs itself as two ranks under
+    torch.distributed.run (gloo here, no GPU: the reference arm, which rank 0
+    alone runs and prints); the line reports n_gpus = 2 and both ranks exit 0."""
+    import json
+    import subprocess
+    import sys
+    from pathlib import Path
+    root = Path(__file__).resolve().parent.parent
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, str(root / "bench.py"), "--impl", "reference", "--gpus",
+                        "2", "--workload", "small", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, env=env, cwd=str(root))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["n_gpus"] == 2 and out["impl"] == "reference" and out["steps"] == 1
