@@ -53,6 +53,9 @@ WORKLOADS = {
     "small": _wl("layer", 32, 512, 32, 4, 128, bm=32),
     # 40 pre-norm MoE layers, an 8192-token prompt in chunks of 2048 per step
     "stack8192": _wl("stack_prefill", 8192, 2048, 256, 8, 512, layers=40, chunk=2048),
+    # one decode step (T rows) through 40 pre-norm MoE layers per step
+    "decode1_stack40": _wl("stack_decode", 1, 2048, 256, 8, 512, layers=40),
+    "decode5_stack40": _wl("stack_decode", 5, 2048, 256, 8, 512, layers=40),
 }
 DEFAULT_WORKLOAD = "prefill512"
 
@@ -370,8 +373,6 @@ class LayerRun:
     def status(self):
         return self.lily.lily_moe_status(self.ws)
 
-    def launches_per_layer(self, name):
-        return 1
 
     def touched(self):
         return float(np.mean([(c > 0).sum() + 1 for c in self.counts]))
@@ -455,8 +456,6 @@ class StackPrefillRun:
     def status(self):
         return self.lily.lily_moe_status(self.ws)
 
-    def launches_per_layer(self, name):
-        return self.nlay * self.nchunks
 
     def touched(self):
         return float(np.mean(self.touched_l))
@@ -489,6 +488,82 @@ class StackPrefillRun:
                 "step_restores_input": "one 64 MB device copy of x per step"}
 
 
+class StackDecodeRun:
+    """The stacked decode step: one step is T rows (one token of T sequences,
+    or a speculative-verify batch) through n_layers pre-norm MoE layers with
+    an fp32 residual, every launch chained on the device
+    (lily_moe_stack_decode).  The step reads each layer's router and touched
+    experts (~18 MB a layer at T=1; 40 layers: far above L2).  Each step first
+    restores the input x (a T * d fp32 device copy), because the call updates
+    x in place."""
+
+    def __init__(self, lily, synth, wl, args, rank, dev):
+        T, d, E, k, F = wl["T"], wl["d"], wl["E"], wl["k"], wl["F"]
+        self.lily, self.wl, self.dev = lily, wl, dev
+        self.nlay = wl["layers"]
+        self.dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
+        self.weights = []
+        for l in range(self.nlay):
+            wr, br = synth.make_router(E, d, layer_seed(l, rank) + 1, dev)
+            ex = synth.make_experts(E, d, F, layer_seed(l, rank) + 2, dev)
+            self.weights.append(lily.LayerWeights(wr, br, ex))
+        g = torch.Generator(device=dev)
+        g.manual_seed(layer_seed(0, rank))
+        self.x0 = torch.randn(T, d, generator=g, device=dev, dtype=torch.float32)
+        self.x = self.x0.clone()
+        self.ws = lily.alloc_workspace(lily.lily_moe_stack_workspace_bytes(self.dims), dev)
+        self.tokens_per_step = T
+        self.rotation = 1
+        self.touched_l = []
+
+    def step(self, i):
+        self.x.copy_(self.x0)
+        self.lily.lily_moe_stack_decode(self.dims, self.x, self.weights, 1e-6, None, None,
+                                        self.ws, None)
+
+    def after_warmup(self):
+        T, E, k = self.wl["T"], self.wl["E"], self.wl["k"]
+        logits = torch.empty(self.nlay, T, E, dtype=torch.float32, device=self.dev)
+        self.x.copy_(self.x0)
+        self.lily.lily_moe_stack_decode(self.dims, self.x, self.weights, 1e-6, None, logits,
+                                        self.ws, None)
+        torch.cuda.synchronize()
+        top = torch.topk(logits, k, dim=-1).indices
+        for l in range(self.nlay):
+            self.touched_l.append(int(torch.unique(top[l]).numel()) + 1)
+
+    def status(self):
+        return self.lily.lily_moe_status(self.ws)
+
+    def touched(self):
+        return float(np.mean(self.touched_l))
+
+    def layer_work(self):
+        wl = self.wl
+        T, d, F, E, k = wl["T"], wl["d"], wl["F"], wl["E"], wl["k"]
+        per = self.touched() * 3 * expert_matrix_bytes(d, F) + E * d * 4 + T * d * 8
+        return per * self.nlay, layer_flops(T, d, E, k, F) * self.nlay, 1
+
+    def e2e_prepare(self):
+        self.xh = self.x0.cpu().pin_memory()
+        self.xo = torch.empty_like(self.xh).pin_memory()
+        self.h2d = self.xh.numel() * 4
+        self.d2h = self.xo.numel() * 4
+
+    def e2e_step(self, i):
+        self.x.copy_(self.xh, non_blocking=True)
+        self.lily.lily_moe_stack_decode(self.dims, self.x, self.weights, 1e-6, None, None,
+                                        self.ws, None)
+        self.xo.copy_(self.x, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    def config(self):
+        return {"l2": f"inputs larger than L2: {self.nlay} layers' routers and touched experts "
+                      f"per step", "path": "stacked decode (pre-norm MoE layers, fp32 residual)",
+                "layers": self.nlay, "experts_touched_per_layer": self.touched(),
+                "step_us": None, "step_restores_input": "one T x d fp32 device copy per step"}
+
+
 def run_lily(args, world, rank, local):
     import w4_grouped_gemm_gb300 as lily
     from w4_grouped_gemm_gb300 import synth
@@ -498,7 +573,8 @@ def run_lily(args, world, rank, local):
     lily.lib()
     wl = WORKLOADS[args.workload]
     T, d, E, k, F = wl["T"], wl["d"], wl["E"], wl["k"], wl["F"]
-    run = {"layer": LayerRun, "stack_prefill": StackPrefillRun}[wl["kind"]](
+    run = {"layer": LayerRun, "stack_prefill": StackPrefillRun,
+           "stack_decode": StackDecodeRun}[wl["kind"]](
         lily, synth, wl, args, rank, dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -595,7 +671,8 @@ def run_lily(args, world, rank, local):
 
     # end to end through the public API with host buffers
     run.e2e_prepare()
-    e2e_steps = 3 if args.no_e2e else max(3, min(args.steps, 200 if wl["kind"] == "layer" else 5))
+    e2e_steps = 3 if args.no_e2e else max(3, min(args.steps, 5 if wl["kind"] == "stack_prefill"
+                                                  else 200))
     for i in range(3):
         run.e2e_step(i)
     if world > 1:
@@ -669,6 +746,9 @@ def run_lily(args, world, rank, local):
            "step_bound": "tensor" if step_t_tc > step_t_hbm else "hbm",
            "kernels": kernels}
     cfg.update(run.config())
+    if "step_us" in cfg:
+        cfg["step_us"] = 1e3 * ms / args.steps
+        cfg["layer_us"] = cfg["step_us"] / wl["layers"]
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,

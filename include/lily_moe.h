@@ -55,8 +55,9 @@ extern "C" {
 #define LILY_STATUS_NAN_LOGIT 0x1u       /* a router logit was NaN             */
 #define LILY_STATUS_TIMEOUT 0x2u         /* a bounded on-chip wait gave up     */
 #define LILY_STATUS_BAD_TILE 0x4u        /* a block-map entry was out of range */
-#define LILY_STATUS_F16_RANGE 0x8u       /* |x| or |silu(g)*u| above 65504, the fp16
-                                            range of the tensor-core operands    */
+#define LILY_STATUS_F16_RANGE 0x8u       /* |x| or |gate*silu(g)*u| (decode:
+                                            |silu(g)*u|) above 65504, the fp16 range
+                                            of the tensor-core operands          */
 
 /* ------------------------------------------------------------------ shapes
  * T          tokens (rows) of this call; 1 <= T <= 16384 (decode: 1..8)
@@ -149,7 +150,10 @@ int lily_moe_route(const lily_moe_dims* dims, const void* x, const float* logits
 
 /* The whole layer for prefill-sized T: routing as in lily_moe_route, then the
  * gate/up grouped GEMM (fused 4-bit dequant + SwiGLU) and the down grouped GEMM
- * (fused dequant + gated scatter-add back to token order).
+ * (fused dequant + gated scatter-add back to token order: each output row,
+ * already weighted by its gate, is added into y by bulk reductions, so the
+ * order of the fp32 additions, and the last bits of y, can differ between
+ * runs).
  *   x  bf16 [T][d] device in; y [T][d] device out, fp32 or bf16 per
  *   dims->out_dtype. */
 int lily_moe_forward(const lily_moe_dims* dims, const void* x,
@@ -248,8 +252,30 @@ int lily_moe_stack_prefill(const lily_moe_dims* dims, int32_t T_total, int32_t n
                            float* layer_inputs, float* layer_logits,
                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes for lily_moe_stack_prefill with chunk size dims->T. */
+/* Workspace bytes for lily_moe_stack_prefill with chunk size dims->T, and
+ * for lily_moe_stack_decode with dims->T rows. */
 size_t lily_moe_stack_workspace_bytes(const lily_moe_dims* dims);
+
+/* Stacked decode step: n_layers MoE layers with residual for dims->T = 1..8
+ * rows (one token per sequence, or a speculative-verify batch):
+ *   for l in 0..n_layers-1:  x <- x + MoE_l(bf16(rmsnorm(x)))
+ * x fp32 [T][d] device, updated in place; layers[l] are the weights of layer
+ * l; dims->out_dtype is ignored (the layer output is added in fp32).  Each
+ * layer is three launches -- the router (RMSNorm, logits and the routing, in
+ * one cluster of CTAs), the gate/up GEMV and the down GEMV, which adds its
+ * output into x -- every one chained to the previous with programmatic
+ * dependent launch, so the whole step runs with no host work between layers
+ * and can be captured in one CUDA graph (page "Lily Beats MLX-LM 1.35x on
+ * Decode: Perplexity's Rust+Metal Engine for Apple Silicon", section
+ * "Decode: eliminating per-token CPU round trips": a decode step recorded
+ * once and replayed, its kernels ordered only by their real data
+ * dependencies).  layer_inputs (fp32 [n_layers][T][d]) and layer_logits
+ * (fp32 [n_layers][T][E]) are optional device traces (NULL to skip; the
+ * input trace adds a copy per layer).  Workspace: lily_moe_stack_workspace_bytes. */
+int lily_moe_stack_decode(const lily_moe_dims* dims, int32_t n_layers,
+                          const lily_moe_weights* layers, float* x, float eps,
+                          float* layer_inputs, float* layer_logits, void* workspace,
+                          size_t workspace_bytes, void* stream);
 
 /* Synchronises `stream`, returns the device status bits accumulated in the
  * workspace since the last call (0 = none) and clears them; after a

@@ -36,7 +36,8 @@ EXPORTS = (
     "lily_moe_route", "lily_moe_forward", "lily_moe_experts", "lily_moe_decode",
     "lily_moe_decode_static",
     "lily_moe_forward_host", "lily_moe_host_graphs",
-    "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_workspace_bytes",
+    "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_decode",
+    "lily_moe_stack_workspace_bytes",
     "lily_moe_status", "lily_moe_set_route_wait_ns", "lily_moe_strerror", "lily_moe_profile_enable", "lily_moe_profile_read",
     "lily_moe_kernel_name", "lily_moe_version",
 )
@@ -98,6 +99,8 @@ def lib():
             "lily_moe_rmsnorm": (I, [ctypes.c_int32, ctypes.c_int32, P, ctypes.c_float, P, P]),
             "lily_moe_stack_prefill": (I, [DP, ctypes.c_int32, ctypes.c_int32, WP, P,
                                            ctypes.c_float, P, P, P, SZ, P]),
+            "lily_moe_stack_decode": (I, [DP, ctypes.c_int32, WP, P, ctypes.c_float, P, P, P,
+                                          SZ, P]),
             "lily_moe_status": (I, [P, P]),
             "lily_moe_set_route_wait_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
             "lily_moe_strerror": (ctypes.c_char_p, [I]),
@@ -285,6 +288,17 @@ def lily_moe_stack_prefill(dims, x, layers: list, eps=1e-6, layer_inputs=None,
                                       _ptr(layer_inputs), _ptr(layer_logits), _ptr(ws),
                                       ws.numel(), _stream(stream))
     _check(rc, "lily_moe_stack_prefill")
+
+
+def lily_moe_stack_decode(dims, x, layers: list, eps=1e-6, layer_inputs=None,
+                          layer_logits=None, ws=None, stream=None):
+    """n_layers pre-norm MoE layers on the fp32 residual x [T][d] (T <= 8),
+    in place."""
+    arr = (Weights * len(layers))(*[l.c for l in layers])
+    rc = lib().lily_moe_stack_decode(ctypes.byref(dims), len(layers), arr, _ptr(x), eps,
+                                     _ptr(layer_inputs), _ptr(layer_logits), _ptr(ws), ws.numel(),
+                                     _stream(stream))
+    _check(rc, "lily_moe_stack_decode")
 
 
 def lily_moe_status(ws, stream=None) -> int:

@@ -101,8 +101,7 @@ struct Layout {
   size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, plan, total;
 };
 
-// ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation,
-// [3] blocks done in the small-T router launch
+// ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
 Layout layout(const lily_moe_dims& d) {
   const size_t T = d.T, E = d.n_experts, k = d.top_k, F = d.d_ff, D = d.d_model;
   const size_t P = T * k;
@@ -182,10 +181,13 @@ int check_ws(const lily_moe_dims* d, void* ws, size_t bytes) {
 uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws)); }
 
 // Routing on `s` (logits computed unless logits_in is given).  For T <= 8
-// with computed logits the router launch runs the routing itself (its last
-// block), so no separate routing launch is made.
+// with computed logits the router launch runs the routing itself (its CTA 0),
+// so no separate routing launch is made.
+// With norm (the stacked decode, T <= 8 only) x is the fp32 residual and the
+// router scores bf16(rmsnorm(x, eps)).
 int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
-             const lily_moe_weights* w, const lily_moe_routing& r, void* ws, cudaStream_t s) {
+             const lily_moe_weights* w, const lily_moe_routing& r, void* ws, cudaStream_t s,
+             bool norm = false, float eps = 0.f) {
   const Layout L = layout(d);
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
@@ -219,10 +221,19 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
     } else {
       a.plan = reinterpret_cast<int32_t*>(base + L.plan);  // the decode GEMVs' slot table
       // x in the decode GEMV's fragment order, in the x16 / xs regions
-      return cuda_rc(launch_router_logits(
-          x, w->router_w, w->router_bias, r.logits, d.T, d.d_model, d.n_experts,
-          reinterpret_cast<uint32_t*>(base + L.x16), reinterpret_cast<float*>(base + L.xs), &a,
-          ctrl + 3, s));
+      DecRouterArgs da = {};
+      da.x = x;
+      da.w = w->router_w;
+      da.b = w->router_bias;
+      da.logits = r.logits;
+      da.xpg = reinterpret_cast<uint32_t*>(base + L.x16);
+      da.xsg = reinterpret_cast<float*>(base + L.xs);
+      da.eps = eps;
+      da.T = d.T;
+      da.d = d.d_model;
+      da.E = d.n_experts;
+      da.ra = a;
+      return cuda_rc(launch_dec_router(da, norm, s));
     }
   }
   return cuda_rc(launch_route(a, s));
@@ -276,6 +287,40 @@ int do_experts_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights
   a.b1 = nullptr;
   if (launch_down(a, w->down_q, s) != cudaSuccess) return LILY_ERR_CUDA;
   return LILY_OK;
+}
+
+// Arguments of the decode GEMV launches (after do_route for T <= 8): the
+// layer output goes to y, or is added to the fp32 residual `resid`.
+DecodeArgs decode_args(const lily_moe_dims& d, const lily_moe_weights* w,
+                       const lily_moe_routing& r, void* ws, void* y, float* resid) {
+  const Layout L = layout(d);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  DecodeArgs a;
+  a.T = d.T;
+  a.E = d.n_experts;
+  a.k = d.top_k;
+  a.d = d.d_model;
+  a.F = d.d_ff;
+  a.cap = (int)lily_moe_block_map_cap(&d);
+  a.block_map = r.block_map;
+  a.n_tiles = r.n_tiles;
+  a.offsets = r.offsets;
+  a.perm = r.perm;
+  a.inv = r.inv_perm;
+  a.gates = r.topk_gates;
+  a.gq = w->gate_q; a.gs = w->gate_s; a.gb = w->gate_b;
+  a.uq = w->up_q;   a.us = w->up_s;   a.ub = w->up_b;
+  a.dq = w->down_q; a.ds = w->down_s; a.db = w->down_b;
+  a.x = nullptr;
+  a.plan = reinterpret_cast<const int32_t*>(base + L.plan);
+  a.xpg = reinterpret_cast<const uint32_t*>(base + L.x16);
+  a.xsg = reinterpret_cast<const float*>(base + L.xs);
+  a.H = base + L.H;
+  a.y = y;
+  a.y_f32 = d.out_dtype == LILY_DTYPE_F32;
+  a.resid = resid;
+  a.status = ws_status(ws);
+  return a;
 }
 
 // Routing + grouped GEMMs.
@@ -523,33 +568,7 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_wei
   if (dims->T > 8) return LILY_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
   if ((rc = do_route(*dims, x, nullptr, w, *r, ws, s))) return rc;
-  const Layout L = layout(*dims);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  DecodeArgs a;
-  a.T = dims->T;
-  a.E = dims->n_experts;
-  a.k = dims->top_k;
-  a.d = dims->d_model;
-  a.F = dims->d_ff;
-  a.cap = (int)lily_moe_block_map_cap(dims);
-  a.block_map = r->block_map;
-  a.n_tiles = r->n_tiles;
-  a.offsets = r->offsets;
-  a.perm = r->perm;
-  a.inv = r->inv_perm;
-  a.gates = r->topk_gates;
-  a.gq = w->gate_q; a.gs = w->gate_s; a.gb = w->gate_b;
-  a.uq = w->up_q;   a.us = w->up_s;   a.ub = w->up_b;
-  a.dq = w->down_q; a.ds = w->down_s; a.db = w->down_b;
-  a.x = x;
-  a.plan = reinterpret_cast<const int32_t*>(base + L.plan);
-  a.xpg = reinterpret_cast<const uint32_t*>(base + L.x16);
-  a.xsg = reinterpret_cast<const float*>(base + L.xs);
-  a.H = base + L.H;
-  a.y = y;
-  a.y_f32 = dims->out_dtype == LILY_DTYPE_F32;
-  a.status = ws_status(ws);
-  return cuda_rc(launch_decode(a, s));
+  return cuda_rc(launch_decode(decode_args(*dims, w, *r, ws, y, nullptr), s));
 }
 
 int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x_dev,
@@ -633,6 +652,20 @@ StackLayout stack_layout(const lily_moe_dims& d) {
   S.total = off;
   return S;
 }
+// The routing buffers of a stack workspace.
+lily_moe_routing stack_routing(uint8_t* base, const StackLayout& S) {
+  lily_moe_routing r;
+  r.logits = reinterpret_cast<float*>(base + S.logits);
+  r.topk_ids = reinterpret_cast<int32_t*>(base + S.ids);
+  r.topk_gates = reinterpret_cast<float*>(base + S.gates);
+  r.counts = reinterpret_cast<int32_t*>(base + S.counts);
+  r.offsets = reinterpret_cast<int32_t*>(base + S.offsets);
+  r.perm = reinterpret_cast<int32_t*>(base + S.perm);
+  r.inv_perm = reinterpret_cast<int32_t*>(base + S.inv);
+  r.block_map = reinterpret_cast<int32_t*>(base + S.bmap);
+  r.n_tiles = reinterpret_cast<int32_t*>(base + S.ntiles);
+  return r;
+}
 }  // namespace
 
 size_t lily_moe_stack_workspace_bytes(const lily_moe_dims* d) {
@@ -661,16 +694,7 @@ int lily_moe_stack_prefill(const lily_moe_dims* dims, int32_t T_total, int32_t n
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* base = static_cast<uint8_t*>(ws);
   void* lws = base + S.ws;
-  lily_moe_routing r;
-  r.logits = reinterpret_cast<float*>(base + S.logits);
-  r.topk_ids = reinterpret_cast<int32_t*>(base + S.ids);
-  r.topk_gates = reinterpret_cast<float*>(base + S.gates);
-  r.counts = reinterpret_cast<int32_t*>(base + S.counts);
-  r.offsets = reinterpret_cast<int32_t*>(base + S.offsets);
-  r.perm = reinterpret_cast<int32_t*>(base + S.perm);
-  r.inv_perm = reinterpret_cast<int32_t*>(base + S.inv);
-  r.block_map = reinterpret_cast<int32_t*>(base + S.bmap);
-  r.n_tiles = reinterpret_cast<int32_t*>(base + S.ntiles);
+  lily_moe_routing r = stack_routing(base, S);
   void* xn = base + S.xn;
   const Layout L = layout(*dims);
   float* yacc = reinterpret_cast<float*>(static_cast<uint8_t*>(lws) + L.acc);
@@ -694,6 +718,45 @@ int lily_moe_stack_prefill(const lily_moe_dims* dims, int32_t T_total, int32_t n
   return LILY_OK;
 }
 
+int lily_moe_stack_decode(const lily_moe_dims* dims, int32_t n_layers,
+                          const lily_moe_weights* layers, float* x, float eps,
+                          float* layer_inputs, float* layer_logits, void* ws, size_t ws_bytes,
+                          void* stream) {
+  if (!dims || !layers || !x || !ws || n_layers < 1) return LILY_ERR_INVALID_ARG;
+  int rc = lily_moe_check_dims(dims);
+  if (rc) return rc;
+  if (dims->T > 8) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(ws) || (layer_inputs && !aligned16(layer_inputs)) ||
+      (layer_logits && !aligned16(layer_logits)))
+    return LILY_ERR_MISALIGNED;
+  const int T = dims->T, D = dims->d_model, E = dims->n_experts;
+  if (layer_logits && ((size_t)T * E) % 4) return LILY_ERR_MISALIGNED;  // per-layer slices
+  for (int l = 0; l < n_layers; ++l)
+    if ((rc = check_weights(&layers[l], true, true))) return rc;
+  const StackLayout S = stack_layout(*dims);
+  if (ws_bytes < S.total) return LILY_ERR_WORKSPACE_TOO_SMALL;
+  if ((rc = check_arch())) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* lws = base + S.ws;
+  lily_moe_routing r = stack_routing(base, S);
+  for (int l = 0; l < n_layers; ++l) {
+    if (layer_inputs &&
+        cudaMemcpyAsync(layer_inputs + (size_t)l * T * D, x, (size_t)T * D * 4,
+                        cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return LILY_ERR_CUDA;
+    lily_moe_routing rl = r;
+    if (layer_logits) rl.logits = layer_logits + (size_t)l * T * E;
+    // router (on bf16(rmsnorm(x))) with the routing, then the expert GEMVs,
+    // whose output is added to x: three launches per layer, each chained to
+    // the previous one with programmatic dependent launch
+    if ((rc = do_route(*dims, x, nullptr, &layers[l], rl, lws, s, true, eps))) return rc;
+    if ((rc = cuda_rc(launch_decode(decode_args(*dims, &layers[l], rl, lws, nullptr, x), s))))
+      return rc;
+  }
+  return LILY_OK;
+}
+
 int lily_moe_status(void* ws, void* stream) {
   if (!ws) return LILY_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
@@ -701,9 +764,9 @@ int lily_moe_status(void* ws, void* stream) {
   if (cudaMemcpyAsync(&v, ws_status(ws), 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return LILY_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
-  // clear the bits; after a give-up also the grid-barrier and block-done
-  // counters (words 1..3), so that no later call starts from a stale count
-  const size_t clear = (v & LILY_STATUS_TIMEOUT) ? 16 : 4;
+  // clear the bits; after a give-up also the grid-barrier counters (words
+  // 1..2), so that no later call starts from a stale count
+  const size_t clear = (v & LILY_STATUS_TIMEOUT) ? 12 : 4;
   if (v && cudaMemsetAsync(ws_status(ws), 0, clear, s) != cudaSuccess) return LILY_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
   return (int)v;

@@ -1,11 +1,20 @@
 // decode.cu -- W4 GEMV path for batch-1 / small-batch decode (1..8 rows).
 //
-// Batch-1 decode is bandwidth-bound, so the aim is the fewest bytes and the
-// fewest instructions per weight byte (page "Lily Beats MLX-LM 1.35x on
-// Decode: Perplexity's Rust+Metal Engine for Apple Silicon", section "Decode:
-// eliminating per-token CPU round trips"; verify batches of two to five rows
-// are the speculative-decoding shapes of the same section).  Each distinct
-// active expert (block-map tile) is streamed once for all its rows.
+// Batch-1 decode is bandwidth-bound, so the aim is every weight byte in
+// flight as early as possible and the fewest instructions per weight byte
+// (page "Lily Beats MLX-LM 1.35x on Decode: Perplexity's Rust+Metal Engine
+// for Apple Silicon", section "Decode: eliminating per-token CPU round trips";
+// verify batches of two to five rows are the speculative-decoding shapes of
+// the same section).  Each distinct active expert (block-map tile) is
+// streamed once for all its rows.
+//
+// Data movement: a work unit is 16 weight rows of one expert (the mma M).
+// Its packed codes arrive by TMA in boxes of 16 rows x 128 bytes (64 bytes
+// for 64-byte rows) with the matching 128- (64-) byte swizzle, so the mma
+// fragment loads of eight rows at one K offset hit eight different bank
+// groups; its scales and biases arrive by plain bulk copies.  One producer
+// lane per CTA issues the copies of a ring of stages far ahead; eight
+// consumer warps compute.
 //
 // Arithmetic per 64-weight group g of a row (w = s*q + b):
 //   sum_k w_k x_k = s * (sum_k (q_k + c) x_k - c * X_g) + b * X_g,
@@ -16,14 +25,23 @@
 // scale/bias arithmetic is needed.  Gate/up multiply bf16 x (c = 128, the
 // bf16 magic); down multiplies the fp16 H (c = 1024, the fp16 magic).  The
 // pairs come out as (q_i, q_{i+4}) of each 8-code word; the activations are
-// laid out in that same order (x staged in shared memory; H written in it by
-// the gate/up kernel), so the K order of both operands agrees.
+// laid out in that same order (x by the decode router; H by the gate/up
+// kernel), so the K order of both operands agrees.
 #include "common.cuh"
 
 namespace lily {
 
-constexpr int kDecThreads = 256;
-constexpr int kDecMaxRows = 8;  // mma N
+constexpr int kDecMaxRows = 8;        // mma N: token rows of one slot
+constexpr int kDecUnitRows = 16;      // weight rows of one work unit (mma M)
+constexpr int kDecConsumers = 8;      // consumer warps
+constexpr int kDecThreads = 32 * (1 + kDecConsumers);  // warp 0: producer
+// Two CTAs per SM by registers: a down CTA fits beside a gate/up CTA, so it
+// can start streaming its weights while the gate/up kernel finishes.
+constexpr int kDecMinBlocks = 2;
+constexpr size_t kGuSmemBudget = 160 * 1024;  // gate/up stages + partial sums
+constexpr size_t kDnSmemBudget = 60 * 1024;   // down stages
+constexpr int kGuMaxStages = 6;
+constexpr int kDnMaxStages = 16;
 
 template <bool F16>
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -67,23 +85,55 @@ __host__ __device__ __forceinline__ int hpair_pos(int j) {
   return 2 * (c * 8 + w * 4 + (e & 3)) + (e >> 2);
 }
 
-// Which tile a decode CTA serves: the routing's plan entry of the slot
-// (slot 0 = shared expert, slot i >= 1 = block-map tile i-1), one 16-byte
-// load.  Returns false if the slot is unused.
-__device__ __forceinline__ bool decode_tile(const DecodeArgs& a, int slot, int& expert, int& row0,
-                                            int& rows) {
+// ---------------------------------------------------------------- layout
+// Codes of a 16-row unit: row_bytes / rb boxes of [16 rows][rb bytes], rb =
+// min(row_bytes, 128), with the TMA swizzle of that width: the 16-byte chunk
+// index of row r is XOR-ed with (r & 7) for 128-byte rows and ((r >> 1) & 3)
+// for 64-byte rows.
+__host__ __device__ __forceinline__ int box_bytes(int row_bytes) {
+  return row_bytes < 128 ? row_bytes : 128;
+}
+// Shared-memory offset of byte `off` of row r (0..15) of a unit.
+__device__ __forceinline__ uint32_t unit_off(int r, int off, int rb) {
+  const int box = off / rb, b = off % rb;
+  const int phase = rb == 128 ? (r & 7) : ((r >> 1) & 3);
+  return (uint32_t)(box * kDecUnitRows * rb + r * rb + ((((b >> 4) ^ phase)) << 4) + (b & 15));
+}
+__host__ __device__ __forceinline__ uint32_t round1k(uint32_t v) { return (v + 1023u) & ~1023u; }
+// Gate/up stage: gate codes, up codes (16 rows x d/2 bytes each), then the
+// gate scales, gate biases, up scales, up biases (16 rows x d/64 bf16 each).
+__host__ __device__ __forceinline__ uint32_t gu_stage_bytes(int d) {
+  return round1k((uint32_t)(2 * kDecUnitRows * (d / 2) + 4 * kDecUnitRows * (d / 64) * 2));
+}
+// Down stage: codes (16 rows x F/2 bytes), scales, biases (16 rows x F/64 bf16).
+__host__ __device__ __forceinline__ uint32_t dn_stage_bytes(int F) {
+  return round1k((uint32_t)(kDecUnitRows * (F / 2) + 2 * kDecUnitRows * (F / 64) * 2));
+}
+constexpr uint32_t kGuPartBytes = 2 * kDecConsumers * 2 * kDecUnitRows * kDecMaxRows * 4;
+constexpr uint32_t kDnTileBytes = kDecConsumers * kDecMaxRows * kDecUnitRows * 4;
+constexpr uint32_t kBarBytes = 512;  // mbarriers and flags
+
+// ---------------------------------------------------------------- plan
+// Slot s of the routing's decode plan: {expert, first H row, rows, 0, -, -,
+// -, -, token[8], gate bits[8], ...}; slot 0 = shared expert, slot i >= 1 =
+// block-map tile i-1; rows = 0 marks an unused slot.  Returns false for an
+// unused or malformed slot (the latter flagged).
+struct Slot {
+  int expert, row0, rows;
+};
+__device__ __forceinline__ bool plan_slot(const DecodeArgs& a, int slot, Slot& sl) {
   const int4 h = __ldcg(reinterpret_cast<const int4*>(a.plan + (size_t)slot * kPlanWords));
-  expert = h.x;
-  row0 = h.y;
-  rows = h.z;
-  if (rows <= 0) return false;
-  if (expert < 0 || expert > a.E || rows > kDecMaxRows) {
-    if (threadIdx.x == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
+  sl.expert = h.x;
+  sl.row0 = h.y;
+  sl.rows = h.z;
+  if (sl.rows <= 0) return false;
+  if (sl.expert < 0 || sl.expert > a.E || sl.rows > kDecMaxRows || sl.row0 < 0 ||
+      sl.row0 + sl.rows > a.T * a.k + a.T) {
+    if ((threadIdx.x & 31) == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
     return false;
   }
   return true;
 }
-// Token and gate of row n of a slot (from the plan).
 __device__ __forceinline__ int plan_token(const DecodeArgs& a, int slot, int n) {
   return __ldcg(a.plan + (size_t)slot * kPlanWords + 8 + n);
 }
@@ -91,49 +141,20 @@ __device__ __forceinline__ float plan_gate(const DecodeArgs& a, int slot, int n)
   return __int_as_float(__ldcg(a.plan + (size_t)slot * kPlanWords + 16 + n));
 }
 
-// Up to kChunk groups of 16 weight rows [r0, r0+16) of one packed matrix
-// (row length K): the codes of rows gi and gi+8 for this lane's 8 K values,
-// and the rows' scales and biases, loaded into registers ahead of use so the
-// loads of a chunk are in flight together.
-constexpr int kChunk = 4;
-struct WChunk {
-  uint2 wa[kChunk], wb[kChunk];
-  float sa[kChunk], sb[kChunk], ba[kChunk], bb[kChunk];
-};
-__device__ __forceinline__ void load_wchunk(WChunk& w, const uint8_t* __restrict__ q,
-                                            const uint16_t* __restrict__ s,
-                                            const uint16_t* __restrict__ b, size_t r0, int K,
-                                            int g0, int gstep) {
-  const int lane = threadIdx.x & 31, gi = lane >> 2, c = lane & 3;
-  const int G = K / 64;
-  const uint8_t* qa = q + (r0 + gi) * (size_t)(K / 2) + c * 8;
-  const uint8_t* qb = qa + 8 * (size_t)(K / 2);
-  const uint16_t* sa = s + (r0 + gi) * (size_t)G;
-  const uint16_t* ba = b + (r0 + gi) * (size_t)G;
-#pragma unroll
-  for (int i = 0; i < kChunk; ++i) {
-    const int g = g0 + i * gstep;
-    if (g < G) {
-      w.wa[i] = __ldcs(reinterpret_cast<const uint2*>(qa + g * 32));
-      w.wb[i] = __ldcs(reinterpret_cast<const uint2*>(qb + g * 32));
-      w.sa[i] = bf16_bits_to_float(__ldg(sa + g));
-      w.sb[i] = bf16_bits_to_float(__ldg(sa + 8 * G + g));
-      w.ba[i] = bf16_bits_to_float(__ldg(ba + g));
-      w.bb[i] = bf16_bits_to_float(__ldg(ba + 8 * G + g));
-    }
-  }
-}
-// Group i of a loaded chunk against B fragments xw (8 words: this lane's
-// (i, i+4) pairs) and the group sums x0, x1 of accumulator columns 2c, 2c+1.
+// One 64-group of 16 weight rows against B fragments xw (this lane's 8
+// words: the (i, i+4) pairs of its K values for B column gi) and the group
+// sums x0, x1 of accumulator columns 2c, 2c+1.  wa / wb: the lane's 16 codes
+// of rows gi and gi+8; sa, ba, sb, bb: those rows' scale and bias.
 template <bool F16>
-__device__ __forceinline__ void chunk_group(const WChunk& w, int i, const uint32_t (&xw)[8],
-                                            float x0, float x1, float (&out)[4]) {
+__device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, float sa, float ba, float sb,
+                                          float bb, const uint32_t (&xw)[8], float x0, float x1,
+                                          float (&out)[4]) {
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t pa[4], pb[4];
-    code_pairs<F16>(h == 0 ? w.wa[i].x : w.wa[i].y, pa);
-    code_pairs<F16>(h == 0 ? w.wb[i].x : w.wb[i].y, pb);
+    code_pairs<F16>(h == 0 ? wa.x : wa.y, pa);
+    code_pairs<F16>(h == 0 ? wb.x : wb.y, pb);
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const uint32_t afrag[4] = {pa[2 * m], pb[2 * m], pa[2 * m + 1], pb[2 * m + 1]};
@@ -141,194 +162,440 @@ __device__ __forceinline__ void chunk_group(const WChunk& w, int i, const uint32
     }
   }
   constexpr float off = F16 ? 1024.f : 128.f;  // the code offset of the magic
-  out[0] += w.sa[i] * (acc[0] - off * x0) + w.ba[i] * x0;
-  out[1] += w.sa[i] * (acc[1] - off * x1) + w.ba[i] * x1;
-  out[2] += w.sb[i] * (acc[2] - off * x0) + w.bb[i] * x0;
-  out[3] += w.sb[i] * (acc[3] - off * x1) + w.bb[i] * x1;
+  out[0] += sa * (acc[0] - off * x0) + ba * x0;
+  out[1] += sa * (acc[1] - off * x1) + ba * x1;
+  out[2] += sb * (acc[2] - off * x0) + bb * x0;
+  out[3] += sb * (acc[3] - off * x1) + bb * x1;
 }
 
-// Gate/up: CTA = (tile slot, 16 features); 8 warps split K; H = silu(g) * u.
-// B fragments and group sums come from x in fragment order (xpg, xsg, written
-// by the router launch), so no activation staging is needed.
-__global__ void __launch_bounds__(kDecThreads) dec_gateup_kernel(const DecodeArgs a) {
-  __shared__ float part[8][2][16][kDecMaxRows];  // per-warp partial outputs
-  __shared__ int tok[kDecMaxRows];
-  const int G = a.d / 64;
-  const int nfb = a.F / 16;
-  const int slot = blockIdx.x / nfb, fb = blockIdx.x % nfb;
+// Codes of rows gi and gi+8 for this lane's 16 K values of group g.
+__device__ __forceinline__ void unit_codes(const uint8_t* unit, int g, int gi, int c, int rb,
+                                           uint2& wa, uint2& wb) {
+  const int off = g * 32 + c * 8;
+  wa = *reinterpret_cast<const uint2*>(unit + unit_off(gi, off, rb));
+  wb = *reinterpret_cast<const uint2*>(unit + unit_off(gi + 8, off, rb));
+}
+
+// Give-up flag shared by the roles of a CTA (see mbar_wait).
+struct DecFlags {
+  int abort;
+};
+
+// ======================================================= gate/up + SwiGLU
+// Work item = (tile slot, 16 rows of F) for both matrices; item i runs on
+// CTA i % grid.  Shared-expert items (slot 0) need no routing and are
+// fetched before the wait for the router.  Per item each consumer warp takes
+// the groups g = warp, warp + 8, ... of both matrices; the eight partial
+// 16 x 8 results are summed in a fixed order and H = silu(g) * u is written
+// as fp16 in the pair order the down GEMV reads.
+__global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
+    dec_gateup_kernel(const __grid_constant__ CUtensorMap tm_g,
+                      const __grid_constant__ CUtensorMap tm_u, const DecodeArgs a,
+                      const int nstages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int d = a.d, F = a.F, G = d / 64;
+  const int rb = box_bytes(d / 2), nbox = (d / 2) / rb;
+  const uint32_t SB = gu_stage_bytes(d);
+  const uint32_t code_bytes = kDecUnitRows * (d / 2), sc_bytes = kDecUnitRows * G * 2;
+  float* part = (float*)(smem + (size_t)nstages * SB);  // [2][warps][2][16][8]
+  uint64_t* full = (uint64_t*)((uint8_t*)part + kGuPartBytes);
+  uint64_t* empty = full + kGuMaxStages;
+  uint64_t* cons = empty + kGuMaxStages;                 // [2] consumer warps' hand-off
+  DecFlags* fl = (DecFlags*)(cons + 2);
+  volatile int* abort = &fl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gi = lane >> 2, c = lane & 3;
-  // this warp's first chunk of weight groups (g = warp, warp + 8, ...); the
-  // shared expert's (slot 0) goes before the wait for the routing
-  WChunk wg, wu;
-  if (slot == 0) {
-    const size_t r0s = (size_t)a.E * a.F + (size_t)fb * 16;
-    load_wchunk(wg, a.gq, a.gs, a.gb, r0s, a.d, warp, 8);
-    load_wchunk(wu, a.uq, a.us, a.ub, r0s, a.d, warp, 8);
+  const int nfb = F / kDecUnitRows;
+  const int n_items = (1 + a.cap) * nfb;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nstages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    mbar_init(smem_u32(&cons[0]), kDecConsumers);
+    mbar_init(smem_u32(&cons[1]), kDecConsumers);
+    fl->abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tm_g);
+    prefetch_tensormap(&tm_u);
   }
+  __syncthreads();
+
+  // the item sequence both roles walk: unused slots are skipped by both
+  auto item_slot = [&](int it, bool waited, Slot& sl) {
+    const int slot = it / nfb;
+    if (slot == 0) {  // shared expert: every token, no routing needed
+      sl.expert = a.E;
+      sl.row0 = a.T * a.k;
+      sl.rows = a.T;
+      return true;
+    }
+    return waited && plan_slot(a, slot, sl);
+  };
+
+  if (warp == 0) {
+    // ================================================= producer (one lane)
+    if (lane == 0) {
+      bool waited = false, ok = true;
+      uint32_t u = 0;
+      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+        if (!waited && it >= nfb) {
+          pdl_wait();  // the plan comes from the router
+          pdl_trigger();
+          waited = true;
+        }
+        Slot sl;
+        if (!item_slot(it, waited, sl)) continue;
+        const uint32_t st = u % nstages;
+        if (u >= (uint32_t)nstages &&
+            !mbar_wait(smem_u32(&empty[st]), ((u / nstages) - 1) & 1, abort, a.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t* sp = smem + (size_t)st * SB;
+        const uint32_t fb = smem_u32(&full[st]);
+        mbar_arrive_expect_tx(fb, 2 * code_bytes + 4 * sc_bytes);
+        const int row0 = sl.expert * F + (it % nfb) * kDecUnitRows;
+        for (int b = 0; b < nbox; ++b) {
+          tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_g, b * rb, row0, fb);
+          tma_load_2d(smem_u32(sp + code_bytes + b * kDecUnitRows * rb), &tm_u, b * rb, row0, fb);
+        }
+        const size_t so = (size_t)row0 * G;
+        bulk_load(smem_u32(sp + 2 * code_bytes), a.gs + so, sc_bytes, fb);
+        bulk_load(smem_u32(sp + 2 * code_bytes + sc_bytes), a.gb + so, sc_bytes, fb);
+        bulk_load(smem_u32(sp + 2 * code_bytes + 2 * sc_bytes), a.us + so, sc_bytes, fb);
+        bulk_load(smem_u32(sp + 2 * code_bytes + 3 * sc_bytes), a.ub + so, sc_bytes, fb);
+        ++u;
+      }
+      if (!waited) {
+        pdl_wait();
+        pdl_trigger();
+      }
+      if (*abort) {  // let the copies in flight land before the CTA exits
+        int never = 0;
+        for (uint32_t k2 = (u > (uint32_t)nstages ? u - nstages : 0); k2 < u; ++k2)
+          mbar_wait(smem_u32(&full[k2 % nstages]), (k2 / nstages) & 1, &never, a.status);
+      }
+    } else {
+      pdl_wait();
+      pdl_trigger();
+    }
+    return;
+  }
+
+  // =================================================== consumers (8 warps)
   pdl_wait();
   pdl_trigger();
-  int expert, row0, rows;
-  if (!decode_tile(a, slot, expert, row0, rows)) return;
-  const size_t r0 = (size_t)expert * a.F + (size_t)fb * 16;
-  if (slot != 0) {
-    load_wchunk(wg, a.gq, a.gs, a.gb, r0, a.d, warp, 8);
-    load_wchunk(wu, a.uq, a.us, a.ub, r0, a.d, warp, 8);
-  }
-  if (threadIdx.x < kDecMaxRows) tok[threadIdx.x] = plan_token(a, slot, min((int)threadIdx.x, rows - 1));
-  __syncthreads();
-  // B-fragment row of this lane: slot row gi (zero beyond the slot's rows);
-  // group sums of accumulator columns 2c, 2c+1
-  const uint32_t* xrow = a.xpg + (size_t)tok[min(gi, rows - 1)] * G * 32 + c * 8;
-  const float* xs0 = a.xsg + (size_t)tok[min(2 * c, rows - 1)] * G;
-  const float* xs1 = a.xsg + (size_t)tok[min(2 * c + 1, rows - 1)] * G;
-  float og[4] = {0.f, 0.f, 0.f, 0.f}, ou[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int g0 = warp; g0 < G; g0 += 8 * kChunk) {
-    if (g0 != warp) {
-      load_wchunk(wg, a.gq, a.gs, a.gb, r0, a.d, g0, 8);
-      load_wchunk(wu, a.uq, a.us, a.ub, r0, a.d, g0, 8);
+  const int cw = warp - 1, ct = threadIdx.x - 32;
+  const int gi = lane >> 2, c = lane & 3;
+  uint32_t u = 0;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    Slot sl;
+    if (!item_slot(it, true, sl)) continue;
+    const int slot = it / nfb, fb = it % nfb;
+    const uint32_t st = u % nstages;
+    if (!warp_wait(smem_u32(&full[st]), (u / nstages) & 1, abort, a.status)) break;
+    // B column gi: slot row gi (zero beyond the slot's rows); accumulator
+    // columns 2c, 2c+1 take their rows' group sums
+    const int rows = sl.rows;
+    const int tg = slot == 0 ? min(gi, rows - 1) : plan_token(a, slot, min(gi, rows - 1));
+    const int t0 = slot == 0 ? min(2 * c, rows - 1) : plan_token(a, slot, min(2 * c, rows - 1));
+    const int t1 =
+        slot == 0 ? min(2 * c + 1, rows - 1) : plan_token(a, slot, min(2 * c + 1, rows - 1));
+    const uint32_t* xrow = a.xpg + (size_t)tg * G * 32 + c * 8;
+    const uint8_t* sp = smem + (size_t)st * SB;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(sp + 2 * code_bytes);
+    float og[4] = {0.f, 0.f, 0.f, 0.f}, ou[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int g = cw; g < G; g += kDecConsumers) {
+      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+      if (gi < rows) {
+        h0 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32));
+        h1 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32 + 4));
+      }
+      const uint32_t xw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      const float x0 = 2 * c < rows ? __ldg(a.xsg + (size_t)t0 * G + g) : 0.f;
+      const float x1 = 2 * c + 1 < rows ? __ldg(a.xsg + (size_t)t1 * G + g) : 0.f;
+      uint2 wa, wb;
+      unit_codes(sp, g, gi, c, rb, wa, wb);
+      group_mma<false>(wa, wb, bf16_bits_to_float(sc[gi * G + g]),
+                       bf16_bits_to_float(sc[kDecUnitRows * G + gi * G + g]),
+                       bf16_bits_to_float(sc[(gi + 8) * G + g]),
+                       bf16_bits_to_float(sc[kDecUnitRows * G + (gi + 8) * G + g]), xw, x0, x1, og);
+      unit_codes(sp + code_bytes, g, gi, c, rb, wa, wb);
+      group_mma<false>(wa, wb, bf16_bits_to_float(sc[2 * kDecUnitRows * G + gi * G + g]),
+                       bf16_bits_to_float(sc[3 * kDecUnitRows * G + gi * G + g]),
+                       bf16_bits_to_float(sc[2 * kDecUnitRows * G + (gi + 8) * G + g]),
+                       bf16_bits_to_float(sc[3 * kDecUnitRows * G + (gi + 8) * G + g]), xw, x0,
+                       x1, ou);
     }
+    float* pb = part + (size_t)(u & 1) * (kDecConsumers * 2 * kDecUnitRows * kDecMaxRows);
+    float* pg = pb + (size_t)cw * 2 * kDecUnitRows * kDecMaxRows;
+    float* pu = pg + kDecUnitRows * kDecMaxRows;
+    pg[gi * 8 + 2 * c] = og[0];
+    pg[gi * 8 + 2 * c + 1] = og[1];
+    pg[(gi + 8) * 8 + 2 * c] = og[2];
+    pg[(gi + 8) * 8 + 2 * c + 1] = og[3];
+    pu[gi * 8 + 2 * c] = ou[0];
+    pu[gi * 8 + 2 * c + 1] = ou[1];
+    pu[(gi + 8) * 8 + 2 * c] = ou[2];
+    pu[(gi + 8) * 8 + 2 * c + 1] = ou[3];
+    // every consumer warp has read the stage and written its partials
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&cons[u & 1]));
+    if (!warp_wait(smem_u32(&cons[u & 1]), (u >> 1) & 1, abort, a.status)) break;
+    if (ct == 0) mbar_arrive(smem_u32(&empty[st]));
+    if (ct < kDecUnitRows * kDecMaxRows) {
+      const int row = ct >> 3, n = ct & 7;
+      float gs = 0.f, us = 0.f;
 #pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      const int g = g0 + 8 * i;
-      if (g < G) {
-        uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
-        if (gi < rows) {
-          h0 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32));
-          h1 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32 + 4));
-        }
-        const uint32_t xw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-        const float x0 = 2 * c < rows ? __ldg(xs0 + g) : 0.f;
-        const float x1 = 2 * c + 1 < rows ? __ldg(xs1 + g) : 0.f;
-        chunk_group<false>(wg, i, xw, x0, x1, og);
-        chunk_group<false>(wu, i, xw, x0, x1, ou);
+      for (int w = 0; w < kDecConsumers; ++w) {
+        gs += pb[(size_t)w * 2 * kDecUnitRows * kDecMaxRows + row * 8 + n];
+        us += pb[(size_t)w * 2 * kDecUnitRows * kDecMaxRows + kDecUnitRows * kDecMaxRows +
+                 row * 8 + n];
+      }
+      if (n < rows) {
+        const float h = gs / (1.f + __expf(-gs)) * us;
+        if (!(fabsf(h) <= 65504.f)) set_status(a.status, LILY_STATUS_F16_RANGE);
+        const int f = fb * kDecUnitRows + row;  // H row in pair order, one 64-group after another
+        static_cast<__half*>(a.H)[(size_t)(sl.row0 + n) * F + (f & ~63) + hpair_pos(f & 63)] =
+            __float2half_rn(h);
       }
     }
-  }
-  part[warp][0][gi][2 * c] = og[0];
-  part[warp][0][gi][2 * c + 1] = og[1];
-  part[warp][0][gi + 8][2 * c] = og[2];
-  part[warp][0][gi + 8][2 * c + 1] = og[3];
-  part[warp][1][gi][2 * c] = ou[0];
-  part[warp][1][gi][2 * c + 1] = ou[1];
-  part[warp][1][gi + 8][2 * c] = ou[2];
-  part[warp][1][gi + 8][2 * c + 1] = ou[3];
-  __syncthreads();
-  if (threadIdx.x < 16 * kDecMaxRows) {
-    const int row = threadIdx.x / kDecMaxRows, n = threadIdx.x % kDecMaxRows;
-    float g = 0.f, u = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      g += part[w][0][row][n];
-      u += part[w][1][row][n];
-    }
-    if (n < rows) {
-      const float h = g / (1.f + __expf(-g)) * u;
-      if (!(fabsf(h) <= 65504.f)) set_status(a.status, LILY_STATUS_F16_RANGE);
-      const int f = fb * 16 + row;  // H row in pair order, one 64-group after another
-      static_cast<__half*>(a.H)[(size_t)(row0 + n) * a.F + (f & ~63) + hpair_pos(f & 63)] =
-          __float2half_rn(h);
-    }
+    ++u;
   }
 }
 
-// Down + combine: CTA = 16 output features over every active tile slot; warp
-// w of 16 takes slots w, w + 16, ...  For each slot it runs the 16-row W4
-// GEMV over K = F against that slot's H rows (B fragments loaded straight
-// from H, kept in pair order by the gate/up kernel; group sums X_g from the
-// same loads), with the next chunk of weight groups in flight, then adds
-// gate * out into its own [token][feature] tile in shared memory.  The tiles
-// are summed in warp order, so the result is deterministic.
-constexpr int kDownWarps = 16;
-__global__ void __launch_bounds__(32 * kDownWarps) dec_down_combine_kernel(const DecodeArgs a) {
-  __shared__ float ytile[kDownWarps][kDecMaxRows][16];
+// ======================================================= down + combine
+// CTA = 16 output features over every active tile slot.  The producer lane
+// reads the plan (complete once the gate/up kernel has started, since that
+// kernel waits for the router before it lets this one launch) and streams
+// each slot's 16 weight rows before this kernel waits for H.  Slot v (in
+// order) goes to consumer warp v % 8, which runs the 16-row W4 GEMV over
+// K = F against the slot's H rows (B fragments loaded straight from H; group
+// sums from the same loads) and adds gate * out into its own [token][feature]
+// tile.  The tiles are summed in warp order, so the result is deterministic.
+// The sum is written to y, or added to the fp32 residual (stacked decode).
+__global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
+    dec_down_kernel(const __grid_constant__ CUtensorMap tm_d, const DecodeArgs a,
+                    const int nstages) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int F = a.F, G = F / 64;
+  const int rb = box_bytes(F / 2), nbox = (F / 2) / rb;
+  const uint32_t SB = dn_stage_bytes(F);
+  const uint32_t code_bytes = kDecUnitRows * (F / 2), sc_bytes = kDecUnitRows * G * 2;
+  float* ytile = (float*)(smem + (size_t)nstages * SB);  // [warps][8 tokens][16 features]
+  uint64_t* full = (uint64_t*)((uint8_t*)ytile + kDnTileBytes);
+  uint64_t* empty = full + kDnMaxStages;
+  uint64_t* done = empty + kDnMaxStages;
+  DecFlags* fl = (DecFlags*)(done + 1);
+  volatile int* abort = &fl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gi = lane >> 2, c = lane & 3;
-  const int G = a.F / 64;
-  const int f0 = blockIdx.x * 16;  // output features [f0, f0 + 16)
-  pdl_wait();
-  pdl_trigger();
-  for (int i = threadIdx.x; i < kDownWarps * kDecMaxRows * 16; i += blockDim.x)
-    (&ytile[0][0][0])[i] = 0.f;
+  const int f0 = blockIdx.x * kDecUnitRows;  // output features [f0, f0 + 16)
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nstages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    mbar_init(smem_u32(done), kDecConsumers);
+    fl->abort = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tm_d);
+  }
   __syncthreads();
-  const int nslots = 1 + a.cap;  // unused slots have rows = 0 in the plan
+  // slots 0 .. n_tiles of the plan (read before the wait: see above)
+  const int nslots = 1 + min(max(__ldcg(a.n_tiles), 0), a.cap);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool waited = false, ok = true;
+      uint32_t v = 0;  // valid slots issued
+      for (int s = 0; ok && s < nslots; ++s) {
+        Slot sl;
+        if (!plan_slot(a, s, sl)) continue;
+        const uint32_t st = v % nstages;
+        if (v >= (uint32_t)nstages) {
+          if (!waited) {
+            pdl_wait();
+            pdl_trigger();
+            waited = true;
+          }
+          if (!mbar_wait(smem_u32(&empty[st]), ((v / nstages) - 1) & 1, abort, a.status)) {
+            ok = false;
+            break;
+          }
+        }
+        uint8_t* sp = smem + (size_t)st * SB;
+        const uint32_t fb = smem_u32(&full[st]);
+        mbar_arrive_expect_tx(fb, code_bytes + 2 * sc_bytes);
+        const int row0 = sl.expert * a.d + f0;
+        for (int b = 0; b < nbox; ++b)
+          tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_d, b * rb, row0, fb);
+        const size_t so = (size_t)row0 * G;
+        bulk_load(smem_u32(sp + code_bytes), a.ds + so, sc_bytes, fb);
+        bulk_load(smem_u32(sp + code_bytes + sc_bytes), a.db + so, sc_bytes, fb);
+        ++v;
+      }
+      if (!waited) {
+        pdl_wait();
+        pdl_trigger();
+      }
+      if (*abort) {
+        int never = 0;
+        for (uint32_t k2 = (v > (uint32_t)nstages ? v - nstages : 0); k2 < v; ++k2)
+          mbar_wait(smem_u32(&full[k2 % nstages]), (k2 / nstages) & 1, &never, a.status);
+      }
+    } else {
+      pdl_wait();
+      pdl_trigger();
+    }
+    return;
+  }
+
+  // =================================================== consumers (8 warps)
+  pdl_wait();  // H comes from the gate/up kernel
+  pdl_trigger();
+  const int cw = warp - 1, ct = threadIdx.x - 32;
+  const int gi = lane >> 2, c = lane & 3;
+  float* yt = ytile + (size_t)cw * kDecMaxRows * kDecUnitRows;
+  for (int i = lane; i < kDecMaxRows * kDecUnitRows; i += 32) yt[i] = 0.f;
+  __syncwarp();
   const uint16_t* H = static_cast<const uint16_t*>(a.H);
-  for (int slot = warp; slot < nslots; slot += kDownWarps) {
-    int expert, row0, rows;
-    if (!decode_tile(a, slot, expert, row0, rows)) continue;
-    const size_t r0 = (size_t)expert * a.d + f0;
-    // this lane's B-fragment row: slot row n = gi (zero beyond the slot's rows)
-    const uint16_t* hrow = H + (size_t)(row0 + min(gi, rows - 1)) * a.F + c * 16;
-    WChunk wd, wn;
-    load_wchunk(wd, a.dq, a.ds, a.db, r0, a.F, 0, 1);
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int g0 = 0; g0 < G; g0 += kChunk) {
-      uint4 hh[kChunk][2];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        hh[i][0] = hh[i][1] = make_uint4(0, 0, 0, 0);
-        if (g0 + i < G && gi < rows) {
-          hh[i][0] = *reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64);
-          hh[i][1] = *reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64 + 8);
-        }
-      }
-      if (g0 + kChunk < G) load_wchunk(wn, a.dq, a.ds, a.db, r0, a.F, g0 + kChunk, 1);
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        if (g0 + i < G) {
-          const uint32_t xw[8] = {hh[i][0].x, hh[i][0].y, hh[i][0].z, hh[i][0].w,
-                                  hh[i][1].x, hh[i][1].y, hh[i][1].z, hh[i][1].w};
-          // X_g of slot row gi: this lane's 16 values, then over the 4 lanes c
-          float xsum = 0.f;
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            xsum += __half2float(__ushort_as_half((uint16_t)(xw[e] & 0xFFFFu))) +
-                    __half2float(__ushort_as_half((uint16_t)(xw[e] >> 16)));
-          xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
-          xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
-          // accumulator columns 2c, 2c+1 are slot rows 2c, 2c+1: their X_g
-          const float x0 = __shfl_sync(0xffffffffu, xsum, (2 * c) * 4);
-          const float x1 = __shfl_sync(0xffffffffu, xsum, (2 * c + 1) * 4);
-          chunk_group<true>(wd, i, xw, x0, x1, o);
-        }
-      }
-      wd = wn;
+  bool ok = true;
+  uint32_t v = 0;
+  for (int s = 0; s < nslots; ++s) {
+    Slot sl;
+    if (!plan_slot(a, s, sl)) continue;
+    const uint32_t vi = v++;
+    if ((int)(vi % kDecConsumers) != cw) continue;
+    const uint32_t st = vi % nstages;
+    if (!warp_wait(smem_u32(&full[st]), (vi / nstages) & 1, abort, a.status)) {
+      ok = false;
+      break;
     }
+    const int rows = sl.rows;
+    // this lane's B column: slot row gi (zero beyond the slot's rows)
+    const uint16_t* hrow = H + (size_t)(sl.row0 + min(gi, rows - 1)) * F + c * 16;
+    const uint8_t* sp = smem + (size_t)st * SB;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(sp + code_bytes);
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int g = 0; g < G; ++g) {
+      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+      if (gi < rows) {
+        h0 = *reinterpret_cast<const uint4*>(hrow + g * 64);
+        h1 = *reinterpret_cast<const uint4*>(hrow + g * 64 + 8);
+      }
+      const uint32_t xw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      // X_g of slot row gi: this lane's 16 values, then over the 4 lanes c
+      float xsum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        xsum += __half2float(__ushort_as_half((uint16_t)(xw[e] & 0xFFFFu))) +
+                __half2float(__ushort_as_half((uint16_t)(xw[e] >> 16)));
+      xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+      xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+      // accumulator columns 2c, 2c+1 are slot rows 2c, 2c+1: their X_g
+      const float x0 = __shfl_sync(0xffffffffu, xsum, (2 * c) * 4);
+      const float x1 = __shfl_sync(0xffffffffu, xsum, (2 * c + 1) * 4);
+      uint2 wa, wb;
+      unit_codes(sp, g, gi, c, rb, wa, wb);
+      group_mma<true>(wa, wb, bf16_bits_to_float(sc[gi * G + g]),
+                      bf16_bits_to_float(sc[kDecUnitRows * G + gi * G + g]),
+                      bf16_bits_to_float(sc[(gi + 8) * G + g]),
+                      bf16_bits_to_float(sc[kDecUnitRows * G + (gi + 8) * G + g]), xw, x0, x1, o);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[st]));  // stage read
     // gate * out into this warp's tile: slot row n -> its token and gate
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int n = 2 * c + h;
       if (n < rows) {
-        const int tok = plan_token(a, slot, n);
-        const float gate = plan_gate(a, slot, n);
-        ytile[warp][tok][gi] += gate * o[h];
-        ytile[warp][tok][gi + 8] += gate * o[2 + h];
+        const int tok = s == 0 ? n : plan_token(a, s, n);
+        const float gate = s == 0 ? 1.f : plan_gate(a, s, n);
+        if (tok >= 0 && tok < a.T) {
+          yt[tok * kDecUnitRows + gi] += gate * o[h];
+          yt[tok * kDecUnitRows + gi + 8] += gate * o[2 + h];
+        }
       }
     }
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < a.T * 16; i += blockDim.x) {
-    const int t = i >> 4, f = i & 15;
+  if (!ok) return;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(done));
+  if (!warp_wait(smem_u32(done), 0, abort, a.status)) return;
+  for (int i = ct; i < a.T * kDecUnitRows; i += 32 * kDecConsumers) {
+    const int t = i / kDecUnitRows, f = i % kDecUnitRows;
     float acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDownWarps; ++w) acc += ytile[w][t][f];
-    if (a.y_f32)
-      static_cast<float*>(a.y)[(size_t)t * a.d + f0 + f] = acc;
+    for (int w = 0; w < kDecConsumers; ++w) acc += ytile[(size_t)w * kDecMaxRows * kDecUnitRows + i];
+    const size_t o = (size_t)t * a.d + f0 + f;
+    if (a.resid)
+      a.resid[o] += acc;
+    else if (a.y_f32)
+      static_cast<float*>(a.y)[o] = acc;
     else
-      static_cast<__nv_bfloat16*>(a.y)[(size_t)t * a.d + f0 + f] = __float2bfloat16_rn(acc);
+      static_cast<__nv_bfloat16*>(a.y)[o] = __float2bfloat16_rn(acc);
   }
 }
 
+// ---------------------------------------------------------------- host side
+static bool codes_map(CUtensorMap* tm, const uint8_t* q, int row_bytes, int rows) {
+  const int rb = box_bytes(row_bytes);
+  uint64_t dims[2] = {(uint64_t)row_bytes, (uint64_t)rows};
+  uint64_t strides[1] = {(uint64_t)row_bytes};
+  uint32_t box[2] = {(uint32_t)rb, (uint32_t)kDecUnitRows};
+  return encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)q, dims, strides, box,
+                      rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ==
+         CUDA_SUCCESS;
+}
+
+static int num_sms() {
+  static int cached[64] = {};
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 148;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  if (a.T < 1 || a.T > kDecMaxRows || a.d % 16) return cudaErrorInvalidValue;
-  const int slots = 1 + a.cap;
+  if (a.T < 1 || a.T > kDecMaxRows || a.d % 128 || a.F % 128) return cudaErrorInvalidValue;
+  CUtensorMap tg, tu, td;
+  if (!codes_map(&tg, a.gq, a.d / 2, (a.E + 1) * a.F) ||
+      !codes_map(&tu, a.uq, a.d / 2, (a.E + 1) * a.F) ||
+      !codes_map(&td, a.dq, a.F / 2, (a.E + 1) * a.d))
+    return cudaErrorInvalidValue;
+  // gate/up: a ring of stages within its budget, persistent CTAs
+  const uint32_t gsb = gu_stage_bytes(a.d);
+  int gst = (int)((kGuSmemBudget - kGuPartBytes) / gsb);
+  gst = gst > kGuMaxStages ? kGuMaxStages : gst;
+  if (gst < 2) gst = 2;
+  const size_t gsmem = 1024 + (size_t)gst * gsb + kGuPartBytes + kBarBytes;
+  const int items = (1 + a.cap) * (a.F / kDecUnitRows);
+  const int ggrid = items < num_sms() ? items : num_sms();
+  cudaError_t err = ensure_smem_attr((const void*)dec_gateup_kernel, gsmem);
+  if (err != cudaSuccess) return err;
   prof_begin(K_DEC_GATEUP, s);
-  cudaError_t err =
-      launch_pdl(dec_gateup_kernel, dim3(slots * (a.F / 16)), dim3(kDecThreads), 0, s, a);
+  err = launch_pdl(dec_gateup_kernel, dim3(ggrid), dim3(kDecThreads), gsmem, s, tg, tu, a, gst);
   prof_end(K_DEC_GATEUP, s);
   if (err != cudaSuccess) return err;
+  // down: as many stages as slots, within its budget
+  const uint32_t dsb = dn_stage_bytes(a.F);
+  int dst = (int)(kDnSmemBudget / dsb);
+  if (dst > 1 + a.cap) dst = 1 + a.cap;
+  if (dst > kDnMaxStages) dst = kDnMaxStages;
+  if (dst < 2) dst = 2;
+  const size_t dsmem = 1024 + (size_t)dst * dsb + kDnTileBytes + kBarBytes;
+  err = ensure_smem_attr((const void*)dec_down_kernel, dsmem);
+  if (err != cudaSuccess) return err;
   prof_begin(K_DEC_DOWN, s);
-  err = launch_pdl(dec_down_combine_kernel, dim3(a.d / 16), dim3(32 * kDownWarps), 0, s, a);
+  err = launch_pdl(dec_down_kernel, dim3(a.d / kDecUnitRows), dim3(kDecThreads), dsmem, s, td, a,
+                   dst);
   prof_end(K_DEC_DOWN, s);
   return err;
 }

@@ -26,9 +26,12 @@
 // of rms on these weight distributions; fp16 is 8x finer, runs at the same
 // kind::f16 tensor rate, and holds x, the group scales and biases exactly in
 // [2^-17, 65504] (values beyond 65504 set LILY_STATUS_F16_RANGE).
-// Epilogues: gate/up writes H = silu(gate) * up (fp16) in expert-sorted row
-// order; down adds gate * out into the fp32 token-order accumulator, four
-// consecutive outputs per 16-byte reduction.
+// Epilogues: gate/up writes H = w * silu(g) * u (fp16) in expert-sorted row
+// order, w the row's routing gate (1 for shared-expert rows), so the down
+// GEMM's output rows come out already weighted; down stages each row's 128
+// outputs of a slice in shared memory and adds them into the fp32
+// token-order accumulator with bulk reductions (cp.reduce.async.bulk), one
+// 128-byte line per operation.
 // K order: the rebuilt weights come out of the nibble extraction with each
 // 8-element K chunk in the order (0,4,1,5,2,6,3,7); the K operands x16 and H
 // are stored in that same order, so no shuffle is needed.
@@ -87,10 +90,15 @@ struct GemmLayout {
   static_assert(kNumA >= 2, "tensor memory too small for the A ring");
 };
 
+// Down epilogue staging: per epilogue warp two buffers of 32 token rows x 32
+// output features (fp32), the source of the bulk reductions into y.
+constexpr int kEpiStageFloats = kNumEpiWarps * 2 * 32 * 32;
+
 __host__ __device__ inline size_t gemm_fixed_bytes(int mats, int BM, int K, int nsb) {
   const int G = K / 64;
   return 1024                                  // alignment slack
          + (size_t)nsb * mats * G * 128 * 4    // scale/bias tables (one per item in flight)
+         + (mats == 1 ? kEpiStageFloats * 4 : 0)  // down: epilogue staging
          + kNumBars * 8                        // mbarriers
          + 16;                                 // abort flag, TMEM address
 }
@@ -239,8 +247,8 @@ __device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint32_t
   }
 }
 
-// Down epilogue: lane l's row (cb + l of the item, clamped to its last row):
-// the token it belongs to and its gate weight (1 for shared-expert rows).
+// Lane l's row (cb + l of the item, clamped to its last row): the token it
+// belongs to and its gate weight (1 for shared-expert rows).
 __device__ __forceinline__ void row_token_gate(const GemmArgs& a, const Item& it, int cb, int lane,
                                                int P, int& tok, float& g) {
   const int rj = it.row0 + min(cb + lane, it.rows - 1);
@@ -291,7 +299,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* stage_base = smem;
   uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][MATS][G][128] scale|bias<<16
   const int sb_words = MATS * G * 128;                       // one table
-  uint64_t* bars = (uint64_t*)(sb + nsb * sb_words);
+  float* estage = (float*)(sb + nsb * sb_words);             // down: epilogue staging
+  uint64_t* bars = (uint64_t*)(estage + (GATEUP ? 0 : kEpiStageFloats));
   uint64_t* full = bars;                      // [kMaxStages] TMA landed
   uint64_t* empty = bars + kMaxStages;        // [kMaxStages] stage consumed by the MMAs
   uint64_t* afull = bars + 2 * kMaxStages;    // [kMaxA] dequantised A ready in TMEM
@@ -602,6 +611,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int wn = w + gridDim.x;
     bool have_next = have && next_item<BM>(a, wn, n_items, nslices, nsh, P, nxt);
     uint32_t j = 0;
+    uint32_t echunk = 0;  // down: staged row chunks (alternating buffers)
     while (have) {
       if (GATEUP && have_next) {
         const uint32_t jn = j + 1;
@@ -618,17 +628,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
       const int N = (cur.rows + 15) & ~15;
       const int ab = j % NACC;
-      // down: the first 32 rows' tokens and gate weights, looked up before
-      // the accumulator wait so that the dependent loads overlap it
+      // the first 32 rows' tokens and gate weights, looked up before the
+      // accumulator wait so that the dependent loads overlap it
       int tok0 = 0;
       float gate0 = 0.f;
-      if (!GATEUP) row_token_gate(a, cur, 0, lane, P, tok0, gate0);
+      row_token_gate(a, cur, 0, lane, P, tok0, gate0);
       if (!warp_wait(smem_u32(&accfull[ab]), (j / NACC) & 1, abort, a.status)) break;
       tc_fence_after();
       const int feat = cur.slice * 128 + q * 32 + lane;
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + ab * L::kAccCols;
       for (int cb = 0; cb < N; cb += 32) {
         const bool last = cb + 32 >= N;
+        int tokj = tok0;
+        float gj = gate0;
+        if (cb > 0) row_token_gate(a, cur, cb, lane, P, tokj, gj);
         if (GATEUP) {
           uint32_t gr[32], ur[32];
           tmem_ld32(tl + cb, gr);
@@ -655,9 +668,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
               const float gv = __uint_as_float(gr[jj + t]), uv = __uint_as_float(ur[jj + t]);
-              // silu(g) * u with the fast reciprocal: its few-ulp fp32 error is
-              // far below the fp16 rounding of H; g -> -inf gives 0 as it should
-              hv[t] = __fdividef(gv * uv, 1.f + __expf(-gv));
+              // gate * silu(g) * u with the fast reciprocal: its few-ulp fp32
+              // error is far below the fp16 rounding of H; g -> -inf gives 0
+              // as it should.  The row's gate weight is applied here, so the
+              // down GEMM's rows come out already weighted.
+              const float gate = __shfl_sync(0xffffffffu, gj, jj + t);
+              hv[t] = __fdividef(gate * gv * uv, 1.f + __expf(-gv));
             }
             const float recv = __shfl_xor_sync(0xffffffffu, up4 ? hv[0] : hv[1], 4);
             const float lo = up4 ? recv : hv[0], hi = up4 ? hv[1] : recv;
@@ -669,52 +685,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
         } else {
-          // lane jj holds row cb + jj's output-row offset (token * d) and gate
-          int tokj = tok0;
-          float gj = gate0;
-          if (cb > 0) row_token_gate(a, cur, cb, lane, P, tokj, gj);
-          const uint32_t offj = (uint32_t)tokj * (uint32_t)a.d;  // this lane adds its feature
-          // 16 accumulator columns (token rows) at a time: a 16-row tile reads
-          // and reduces only its own columns
-          const int nh = N - cb > 16 ? 2 : 1;
-          for (int hh = 0; hh < nh; ++hh) {
-            uint32_t orr[16];
-            tmem_ld16(tl + cb + 16 * hh, orr);
-            tmem_ld_wait();
-            if (last && hh == nh - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
-            }
-            // 4x4 blocks (4 lanes = 4 features, 4 token columns) transposed in
-            // two butterfly stages (lanes ^2, then ^1): lane 4i + r ends with
-            // features 4i..4i+3 of column 4m + r, one 16-byte reduction
-            const int rq = lane & 3;
-            const bool qhi = (rq & 2) != 0, qlo = (rq & 1) != 0;
-            float* ybase = a.yacc + (feat & ~3);
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-              const float a0 = __uint_as_float(orr[4 * m]), a1 = __uint_as_float(orr[4 * m + 1]);
-              const float a2 = __uint_as_float(orr[4 * m + 2]), a3 = __uint_as_float(orr[4 * m + 3]);
-              // stage 1: keep columns (2hi, 2hi + 1), take the partner's
-              const float o0 = qhi ? a2 : a0, o1 = qhi ? a3 : a1;
-              const float t0 = __shfl_xor_sync(0xffffffffu, qhi ? a0 : a2, 2);
-              const float t1 = __shfl_xor_sync(0xffffffffu, qhi ? a1 : a3, 2);
-              // stage 2: keep column r of rows r and r^2, take rows r^1, r^3
-              const float k0 = qlo ? o1 : o0, k1 = qlo ? t1 : t0;
-              const float v0 = __shfl_xor_sync(0xffffffffu, qlo ? o0 : o1, 1);
-              const float v1 = __shfl_xor_sync(0xffffffffu, qlo ? t0 : t1, 1);
-              // rows r, r^1, r^2, r^3 hold k0, v0, k1, v1: in feature order
-              const float p0 = qlo ? v0 : k0, p1 = qlo ? k0 : v0;
-              const float s0 = qlo ? v1 : k1, s1 = qlo ? k1 : v1;
-              const int col = 16 * hh + 4 * m + rq;  // this lane's column in the 32-block
-              const uint32_t off = __shfl_sync(0xffffffffu, offj, col);
-              const float g = __shfl_sync(0xffffffffu, gj, col);
-              if (cb + col < cur.rows)
-                red_add_v4_f32(ybase + off, g * (qhi ? s0 : p0), g * (qhi ? s1 : p1),
-                               g * (qhi ? p0 : s0), g * (qhi ? p1 : s1));
-            }
+          // Rows of the item (gate already applied in H) into y: each warp
+          // stages its 32 features of up to 32 rows in shared memory, row by
+          // row, and each lane adds one row's 128 bytes into y with one bulk
+          // reduction (the L2 adds a whole line per operation).
+          const int ncol = N - cb < 32 ? N - cb : 32;  // 16 or 32
+          uint32_t va[16], vb[16];
+          tmem_ld16(tl + cb, va);
+          if (ncol == 32) tmem_ld16(tl + cb + 16, vb);
+          tmem_ld_wait();
+          if (last) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
+          float* buf = estage + ((size_t)(q * 2 + (echunk & 1)) * 32 * 32);
+          // this buffer's previous reductions have read their rows
+          bulk_wait_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int rr = 0; rr < 16; ++rr) buf[rr * 32 + lane] = __uint_as_float(va[rr]);
+          if (ncol == 32) {
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) buf[(16 + rr) * 32 + lane] = __uint_as_float(vb[rr]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane < ncol && cb + lane < cur.rows)
+            bulk_reduce_add_f32(a.yacc + (size_t)(uint32_t)tokj * a.d + (feat - lane),
+                                smem_u32(buf + lane * 32), 32 * 4);
+          bulk_commit();
+          ++echunk;
         }
       }
       cur = nxt;
@@ -724,6 +725,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       have_next = have_nn;
       ++j;
     }
+    // down: this thread's bulk reductions have read shared memory and landed
+    if (!GATEUP) bulk_wait_all();
   }
 
   // ---- teardown: every MMA has finished before TMEM is released

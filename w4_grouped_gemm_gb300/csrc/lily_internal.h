@@ -88,15 +88,25 @@ uint64_t route_wait_limit_ns();
 // token[kPlanRows], gate bits[kPlanRows], 8 unused}.
 constexpr int kPlanWords = 32;
 constexpr int kPlanRows = 8;
-// Router logits for T <= 8 (one CTA per expert); also writes x in the decode
-// GEMV's B-fragment order (xpg, [T][d/64][32] words) with its 64-group sums
-// (xsg, [T][d/64]) unless they are NULL.
-// With `route` set, the block that finishes last also runs the routing
-// (route_kernel's work for one block; T <= 32) on the new logits; `done` is a
-// zero-initialised counter that returns to zero.
-cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
-                                 int T, int d, int E, uint32_t* xpg, float* xsg,
-                                 const RouteArgs* route, uint32_t* done, cudaStream_t s);
+// Decode router (T <= 8): logits, x in the decode GEMV's B-fragment order
+// (xpg, [T][d/64][32] words) with its 64-group sums (xsg, [T][d/64]), and the
+// routing with the per-slot decode plan (ra.plan), in one cluster launch.
+// With `norm` x is the fp32 residual [T][d] of a layer stack and the scored
+// rows are bf16(rmsnorm(x, eps)); else x is bf16 [T][d].
+struct DecRouterArgs {
+  const void* x;
+  const float* w;   // [E][d]
+  const float* b;   // [E] or NULL
+  float* logits;    // [T][E]
+  uint32_t* xpg;
+  float* xsg;
+  float eps;
+  int T, d, E;
+  int cs, epc;      // cluster size and experts per CTA (set by the launcher)
+  RouteArgs ra;
+};
+constexpr size_t kDecRouterMaxSmem = 200 * 1024;
+cudaError_t launch_dec_router(const DecRouterArgs& a, bool norm, cudaStream_t s);
 // Router on tensor cores for larger T: W split exactly into three bf16 terms
 // (w_split, [3][E][d]), fp32 partial logits per K-split (partial,
 // [router_splits(T,d)][T][E]) summed in order into logits (+ bias).
@@ -164,8 +174,11 @@ struct DecodeArgs {
   void* H;         // fp16 [P+T][F], each 64-group in the mma pair order
   void* y;         // [T][d], fp32 if y_f32 else bf16
   bool y_f32;
+  float* resid;    // non-NULL: x_resid[t][:] += layer output (fp32), y unused (stacked decode)
   uint32_t* status;
 };
+// The two decode GEMV launches (gate/up + SwiGLU, down + combine), chained
+// with programmatic dependent launch after the decode router.
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- misc

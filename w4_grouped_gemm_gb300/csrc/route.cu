@@ -295,8 +295,16 @@ __device__ __forceinline__ float key_logit(uint32_t k) {
   return __uint_as_float(u);
 }
 
-// Exclusive scan of one int per thread over a 256-thread block.
+// Exclusive scan of one int per thread over 256 threads: the whole block, or
+// with NAMED the first 256 threads of a larger block (named barrier 1).
+template <bool NAMED = false>
 __device__ int block_exclusive_scan(int v, int* tmp /* [8] */) {
+  auto sync = [] {
+    if (NAMED)
+      named_sync(1, kRouteThreads);
+    else
+      __syncthreads();
+  };
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
 #pragma unroll
@@ -305,7 +313,7 @@ __device__ int block_exclusive_scan(int v, int* tmp /* [8] */) {
     if (lane >= o) incl += n;
   }
   if (lane == 31) tmp[warp] = incl;
-  __syncthreads();
+  sync();
   if (warp == 0) {
     int w = (lane < kRouteThreads / 32) ? tmp[lane] : 0;
 #pragma unroll
@@ -315,10 +323,10 @@ __device__ int block_exclusive_scan(int v, int* tmp /* [8] */) {
     }
     if (lane < kRouteThreads / 32) tmp[lane] = w;  // inclusive warp totals
   }
-  __syncthreads();
+  sync();
   int base = (warp > 0) ? tmp[warp - 1] : 0;
   int out = base + incl - v;
-  __syncthreads();
+  sync();
   return out;
 }
 
@@ -586,13 +594,15 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
   }
 }
 
-// Routing of T <= kPlanRows tokens by one block of kRouteThreads threads
-// (the small-T router launch's last block): the same outputs as route_body
-// with one block, built from shared memory without read-backs -- top-k and
-// gates by one warp per token, counts by counting, positions by counting the
-// earlier pairs of the same expert (stable by pair index), tiles of each
-// expert in ascending order, and the decode plan (a.plan, required).
-__device__ __forceinline__ void route_small_body(const RouteArgs& a) {
+// Routing of T <= kPlanRows tokens by the first kRouteThreads threads of a
+// block (CTA 0 of the decode router launch), from the logits `lg` ([T][E],
+// here in shared memory): the same outputs as route_body with one block,
+// built without read-backs -- top-k and gates by one warp per token, counts
+// by counting, positions by counting the earlier pairs of the same expert
+// (stable by pair index), tiles of each expert in ascending order, and the
+// decode plan (a.plan, required).  Synchronises on named barrier 1 only, so
+// the block's other threads may have left.
+__device__ __forceinline__ void route_small_body(const RouteArgs& a, const float* lg) {
   constexpr int kMaxP = kPlanRows * kMaxK;
   __shared__ int s_e[kMaxP];      // expert of pair p = t * k + j
   __shared__ float s_g[kMaxP];    // its gate
@@ -612,8 +622,7 @@ __device__ __forceinline__ void route_small_body(const RouteArgs& a) {
       const int e = lane + 32 * c;
       key[c] = 0;
       if (e < E) {
-        const float v = __ldcg(a.logits_src + (size_t)t * E + e);
-        if (a.logits_dst != a.logits_src) a.logits_dst[(size_t)t * E + e] = v;
+        const float v = lg[(size_t)t * E + e];
         saw_nan |= (v != v);
         key[c] = logit_key(v);
         avail |= 1u << c;
@@ -647,18 +656,18 @@ __device__ __forceinline__ void route_small_body(const RouteArgs& a) {
       s_g[t * k + lane] = wgt / z;
     }
   }
-  __syncthreads();
+  named_sync(1, kRouteThreads);
   // counts and offsets: thread e counts its pairs
   const int e_me = threadIdx.x;  // kRouteThreads == kMaxE
   int cnt = 0;
   for (int p = 0; p < P; ++p) cnt += (s_e[p] == e_me);
   if (e_me >= E) cnt = 0;
-  const int off_me = block_exclusive_scan(cnt, s_scan_tmp);
+  const int off_me = block_exclusive_scan<true>(cnt, s_scan_tmp);
   s_cnt[e_me] = cnt;
   s_off[e_me] = off_me;
   const int ntile = (cnt + a.BM - 1) / a.BM;
-  __syncthreads();
-  const int toff = block_exclusive_scan(ntile, s_scan_tmp);
+  named_sync(1, kRouteThreads);
+  const int toff = block_exclusive_scan<true>(ntile, s_scan_tmp);
   s_toff[e_me] = toff;
   if (e_me == kMaxE - 1) s_total = toff + ntile;
   if (e_me < E) {
@@ -666,7 +675,7 @@ __device__ __forceinline__ void route_small_body(const RouteArgs& a) {
     a.offsets[e_me] = off_me;
   }
   if (e_me == 0) a.offsets[E] = P;
-  __syncthreads();
+  named_sync(1, kRouteThreads);
   // pair p's position: its expert's offset + the earlier pairs of that expert
   for (int p = threadIdx.x; p < P; p += kRouteThreads) {
     const int e = s_e[p];
@@ -677,7 +686,7 @@ __device__ __forceinline__ void route_small_body(const RouteArgs& a) {
     a.inv[p] = pos;
     s_perm[pos] = p;
   }
-  __syncthreads();
+  named_sync(1, kRouteThreads);
   // block map and plan: thread e writes its tiles; slot 0 = shared expert
   const int total = s_total;
   for (int i = 0; i < ntile; ++i) {
@@ -721,113 +730,210 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
   route_body(a, blockIdx.x, gridDim.x);
 }
 
-// Small T (decode, T <= 8): one CTA per expert row, its 8 warps split d
-// (float4 f of the row goes to warp (f / 32) % 8, lane f % 32); per-token
-// sums reduced in the warp, then over the warps in order (deterministic).
-// The same launch writes x once in the decode GEMV's B-fragment order with
-// its 64-group sums (xpg, xsg; skipped when NULL):
+// ============================================================== decode router
+// Small T (decode, T <= 8): one cluster of `cs` CTAs (16, else 8).  CTA r
+// scores experts r * epc .. r * epc + epc - 1, one warp per expert (warps
+// take a second expert when epc exceeds the warp count), with the expert's
+// weight row loaded into registers before the wait for the predecessor (the
+// weights are static).  The token rows are staged once in shared memory as
+// fp32 (exact bf16 values).  Each logit goes to the routing output and, by a
+// distributed-shared-memory store, to CTA 0; after a cluster barrier CTA 0
+// routes (top-k, gates, counts, positions, block map, decode plan) from its
+// shared memory, with no global counter or fence.  The same launch writes x
+// in the decode GEMV's B-fragment order with its 64-group sums:
 //   xpg[(t*G + g)*32 + c*8 + w*4 + e] = (x[t][g*64 + c*16 + 8w + e], x[...+4])
 //   xsg[t*G + g] = sum of x[t][g*64 .. g*64+63]
-constexpr int kGemvMaxT = 8;
-constexpr int kGemvMaxPer = 4;  // float4 per lane: d <= 4096
-__global__ void __launch_bounds__(256) router_gemv_kernel(const __nv_bfloat16* __restrict__ x,
-                                                          const float* __restrict__ w,
-                                                          const float* __restrict__ b,
-                                                          float* __restrict__ logits, int T,
-                                                          int d, int E, uint32_t* __restrict__ xpg,
-                                                          float* __restrict__ xsg, const RouteArgs ra,
-                                                          uint32_t* done) {
-  __shared__ float part[8][kGemvMaxT];
-  __shared__ int s_last;
+// With NORM the input is the fp32 residual of a layer stack and the scored
+// rows are bf16(x / sqrt(mean(x^2) + eps)) (unit-weight RMSNorm).
+constexpr int kDecRouterThreads = 512;
+constexpr int kDecRouterWarps = kDecRouterThreads / 32;
+constexpr int kDecRouterWv = 16;  // float4 of a weight row held per lane: 2048 weights
+
+template <bool NORM>
+__global__ void __launch_bounds__(kDecRouterThreads, 1) dec_router_kernel(const DecRouterArgs a) {
+  extern __shared__ __align__(16) float dsm[];
+  float* xs = dsm;                             // [T][d] the scored rows, fp32
+  float* lall = dsm + (size_t)a.T * a.d;       // [T][E] every logit (used in CTA 0)
+  __shared__ float s_red[kDecRouterWarps][kPlanRows];
+  __shared__ float s_inv[kPlanRows];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x;
-  const float4* wr = reinterpret_cast<const float4*>(w + (size_t)e * d);
-  const int n4 = d / 4;
-  float4 wv[kGemvMaxPer];
+  const int T = a.T, d = a.d, E = a.E, n4 = d / 4;
+  const uint32_t rank = cluster_ctarank();
+  const int rounds = (a.epc + kDecRouterWarps - 1) / kDecRouterWarps;
+  float4 wv[kDecRouterWv];
+  auto expert_of = [&](int j) { return (int)rank * a.epc + warp + kDecRouterWarps * j; };
+  auto has_expert = [&](int j) {
+    return warp + kDecRouterWarps * j < a.epc && expert_of(j) < E;
+  };
+  auto load_w = [&](int j, int pass) {
+    const bool has = has_expert(j);
+    const float4* wrow = reinterpret_cast<const float4*>(a.w + (size_t)(has ? expert_of(j) : 0) * d);
 #pragma unroll
-  for (int i = 0; i < kGemvMaxPer; ++i) {  // the weights are static: loaded before the wait
-    const int f = (i * 8 + warp) * 32 + lane;
-    wv[i] = f < n4 ? __ldg(wr + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  pdl_wait();  // x comes from the predecessor
+    for (int i = 0; i < kDecRouterWv; ++i) {
+      const int f = pass * 32 * kDecRouterWv + i * 32 + lane;
+      wv[i] = (has && f < n4) ? __ldg(wrow + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_w(0, 0);  // static: before the wait
+  pdl_wait();    // x comes from the predecessor
   pdl_trigger();
-  float acc[kGemvMaxT];
+
+  // ---- stage the rows that are scored (and fed to the expert GEMVs)
+  if (NORM) {
+    const float* xr = static_cast<const float*>(a.x);
+    for (int t = 0; t < T; ++t) {
+      float ss = 0.f;
+      for (int i = threadIdx.x; i < d; i += kDecRouterThreads) {
+        const float v = xr[(size_t)t * d + i];
+        ss = fmaf(v, v, ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_red[warp][t] = ss;
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+      float tot = 0.f;
 #pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) acc[t] = 0.f;
+      for (int w2 = 0; w2 < kDecRouterWarps; ++w2) tot += s_red[w2][threadIdx.x];
+      s_inv[threadIdx.x] = 1.f / sqrtf(tot / (float)d + a.eps);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < T * d; i += kDecRouterThreads)
+      xs[i] = __bfloat162float(__float2bfloat16_rn(xr[i] * s_inv[i / d]));
+  } else {
+    const uint4* xb = static_cast<const uint4*>(a.x);  // 8 bf16 per 16 bytes
+    for (int i = threadIdx.x; i < T * d / 8; i += kDecRouterThreads) {
+      const uint4 v = __ldg(xb + i);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      float4* dst = reinterpret_cast<float4*>(xs + (size_t)i * 8);
+      dst[0] = make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xFFFF0000u),
+                           __uint_as_float(w4[1] << 16), __uint_as_float(w4[1] & 0xFFFF0000u));
+      dst[1] = make_float4(__uint_as_float(w4[2] << 16), __uint_as_float(w4[2] & 0xFFFF0000u),
+                           __uint_as_float(w4[3] << 16), __uint_as_float(w4[3] & 0xFFFF0000u));
+    }
+  }
+  __syncthreads();
+
+  // ---- logits: per warp and expert, T dot products over d in a fixed order
+  const int npass = (n4 + 32 * kDecRouterWv - 1) / (32 * kDecRouterWv);
+  const uint32_t lall0 = mapa_shared(smem_u32(lall), 0);
+  for (int j = 0; j < rounds; ++j) {
+    float acc[kPlanRows];
 #pragma unroll
-  for (int i = 0; i < kGemvMaxPer; ++i) {
-    const int f = (i * 8 + warp) * 32 + lane;
-    if (f < n4) {
+    for (int t = 0; t < kPlanRows; ++t) acc[t] = 0.f;
+    for (int pass = 0; pass < npass; ++pass) {
+      if (j > 0 || pass > 0) load_w(j, pass);
 #pragma unroll
-      for (int t = 0; t < kGemvMaxT; ++t) {
+      for (int i = 0; i < kDecRouterWv; ++i) {
+        const int f = pass * 32 * kDecRouterWv + i * 32 + lane;
+        if (f < n4) {
+#pragma unroll
+          for (int t = 0; t < kPlanRows; ++t) {
+            if (t < T) {
+              const float4 x4 = reinterpret_cast<const float4*>(xs + (size_t)t * d)[f];
+              acc[t] = fmaf(wv[i].x, x4.x, acc[t]);
+              acc[t] = fmaf(wv[i].y, x4.y, acc[t]);
+              acc[t] = fmaf(wv[i].z, x4.z, acc[t]);
+              acc[t] = fmaf(wv[i].w, x4.w, acc[t]);
+            }
+          }
+        }
+      }
+    }
+    if (has_expert(j)) {
+      const int e = expert_of(j);
+      const float bias = a.b ? __ldg(a.b + e) : 0.f;
+#pragma unroll
+      for (int t = 0; t < kPlanRows; ++t) {
         if (t < T) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * d) + f);
-          const float2 x01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.x));
-          const float2 x23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xv.y));
-          acc[t] = fmaf(wv[i].x, x01.x, acc[t]);
-          acc[t] = fmaf(wv[i].y, x01.y, acc[t]);
-          acc[t] = fmaf(wv[i].z, x23.x, acc[t]);
-          acc[t] = fmaf(wv[i].w, x23.y, acc[t]);
+          const float v = warp_sum(acc[t]) + bias;
+          if (lane == 0) {
+            a.logits[(size_t)t * E + e] = v;
+            st_cluster_f32(lall0 + (uint32_t)((t * E + e) * 4), v);
+          }
         }
       }
     }
   }
-#pragma unroll
-  for (int t = 0; t < kGemvMaxT; ++t) {
-    float v = acc[t];
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) part[warp][t] = v;
+
+  // ---- x in the expert GEMV's fragment order, with its group sums
+  const int G = d / 64;
+  for (int u = (int)rank * kDecRouterWarps + warp; u < T * G; u += a.cs * kDecRouterWarps) {
+    const int t = u / G, g = u % G;
+    const int c = lane >> 3, w2 = (lane >> 2) & 1, e4 = lane & 3;
+    const int i = g * 64 + c * 16 + 8 * w2 + e4;
+    const float lo = xs[(size_t)t * d + i], hi = xs[(size_t)t * d + i + 4];
+    a.xpg[(size_t)u * 32 + lane] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+    const float sum = warp_sum(lo + hi);
+    if (lane == 0) a.xsg[u] = sum;
   }
-  __syncthreads();
-  if (threadIdx.x < T) {
-    float v = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v += part[i][threadIdx.x];
-    logits[(size_t)threadIdx.x * E + e] = v + (b ? b[e] : 0.f);
-  }
-  if (xpg) {
-    const int G = d / 64;
-    const uint16_t* xh = reinterpret_cast<const uint16_t*>(x);
-    for (int u = blockIdx.x * 8 + warp; u < T * G; u += gridDim.x * 8) {
-      const int t = u / G, g = u % G;
-      const int c = lane >> 3, w2 = (lane >> 2) & 1, e4 = lane & 3;
-      const int i = g * 64 + c * 16 + 8 * w2 + e4;
-      const uint16_t lo = xh[(size_t)t * d + i], hi = xh[(size_t)t * d + i + 4];
-      xpg[(size_t)u * 32 + lane] = (uint32_t)lo | ((uint32_t)hi << 16);
-      float sum = __uint_as_float((uint32_t)lo << 16) + __uint_as_float((uint32_t)hi << 16);
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (lane == 0) xsg[u] = sum;
-    }
-  }
-  // routing by the block that finishes last (no waiting): every block makes
-  // its logits visible, then counts itself done; the last one sees them all
-  if (done) {
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
-      if (ra.T <= kPlanRows && ra.plan)
-        route_small_body(ra);
-      else
-        route_body(ra, 0, 1);
-      if (threadIdx.x == 0) *done = 0;  // back to zero for the next call
-    }
-  }
+
+  cluster_sync_all();  // every logit is in CTA 0's shared memory
+  if (rank == 0 && threadIdx.x < kRouteThreads) route_small_body(a.ra, lall);
 }
 
-cudaError_t launch_router_logits(const void* x, const float* w, const float* b, float* logits,
-                                 int T, int d, int E, uint32_t* xpg, float* xsg,
-                                 const RouteArgs* route, uint32_t* done, cudaStream_t s) {
-  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  if (T > kGemvMaxT || d > 4 * 32 * 8 * kGemvMaxPer) return cudaErrorInvalidValue;  // larger T: launch_router_tc
-  static_assert(kRouteThreads == 256, "the router launch runs the routing body");
-  RouteArgs ra = {};
-  if (route) ra = *route;
+int dec_router_cluster_size() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int cs = 0;
+  for (int want : {16, 8}) {
+    for (auto kern : {dec_router_kernel<false>, dec_router_kernel<true>}) {
+      cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kDecRouterMaxSmem);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(want);
+    cfg.blockDim = dim3(kDecRouterThreads);
+    cfg.dynamicSmemBytes = kDecRouterMaxSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = want;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)dec_router_kernel<true>, &cfg) ==
+            cudaSuccess &&
+        n >= 1) {
+      cs = want;
+      break;
+    }
+    cudaGetLastError();
+  }
+  if (dev >= 0 && dev < 64 && cs) cached[dev] = cs;
+  return cs;
+}
+
+cudaError_t launch_dec_router(const DecRouterArgs& in, bool norm, cudaStream_t s) {
+  if (in.T < 1 || in.T > kPlanRows || in.d % 128 || in.E > 256) return cudaErrorInvalidValue;
+  const size_t smem = ((size_t)in.T * in.d + (size_t)in.T * in.E) * 4;
+  if (smem > kDecRouterMaxSmem) return cudaErrorInvalidValue;
+  const int cs = dec_router_cluster_size();
+  if (!cs) return cudaErrorNotSupported;
+  DecRouterArgs a = in;
+  a.cs = cs;
+  a.epc = (a.E + cs - 1) / cs;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cs);
+  cfg.blockDim = dim3(kDecRouterThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   prof_begin(K_ROUTER_GEMV, s);
-  const cudaError_t err = launch_pdl(router_gemv_kernel, dim3(E), dim3(256), 0, s, xb, w, b,
-                                     logits, T, d, E, xpg, xsg, ra, route ? done : nullptr);
+  const cudaError_t err = norm ? cudaLaunchKernelEx(&cfg, dec_router_kernel<true>, a)
+                               : cudaLaunchKernelEx(&cfg, dec_router_kernel<false>, a);
   prof_end(K_ROUTER_GEMV, s);
   return err;
 }
