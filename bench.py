@@ -766,9 +766,9 @@ def run_lily(args, world, rank, local):
     print(json.dumps(out), flush=True)
 
 
-def run_ablation(args, world, rank, local):
-    """Bench-only ablations of two design points of the path, each timed eagerly
-    against the fused path in the same run (one JSON line):
+class Ablation:
+    """The two bench-only ablations of design points of the path, on one
+    seeded prefill layer (shape `shape`, tile rows BM):
       host_routing -- routing on the GPU, then a host sync, a copy of the
         counts to the host, the block map built on the host and copied back,
         then the expert GEMMs (lily_moe_experts);
@@ -776,53 +776,54 @@ def run_ablation(args, world, rank, local):
         step (torch element-wise ops: unpack, then one multiply-add pass),
         then batched fp16 GEMMs (torch.bmm, cuBLAS) over expert-padded rows,
         with the same GPU routing.
-    Both check their layer output against the fused path's."""
-    import w4_grouped_gemm_gb300 as lily
-    from w4_grouped_gemm_gb300 import synth
+    fused() runs the library's layer into y_ref, run(name) an ablation into
+    y; both fp32 [T][d]."""
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    wl = WORKLOADS[args.workload]
-    T, d, E, k, F, zipf = wl["T"], wl["d"], wl["E"], wl["k"], wl["F"], wl["zipf"]
-    if T <= 8 or wl["kind"] != "layer":
-        raise SystemExit("ablations are single-layer prefill only")
-    shape = synth.LayerShape(T, d, E, k, F)
-    dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
-    inp = synth.make_layer(shape, 1000 * 2 + 17, device=dev, zipf_s=zipf)
-    x = inp["x"]
-    w = lily.LayerWeights(inp["router_w"], inp["router_b"], inp["experts"])
-    r = lily.RoutingBuffers(dims, dev)
-    ws = lily.alloc_workspace(lily.lily_moe_workspace_bytes(dims), dev)
-    y_ref = torch.empty(T, d, dtype=torch.float32, device=dev)
-    y = torch.empty_like(y_ref)
-    BM, P, cap = args.tile_rows, T * k, lily.lily_moe_block_map_cap(dims)
+    def __init__(self, lily, synth, shape, BM, seed, dev, zipf=None):
+        T, d, E, k, F = shape.T, shape.d, shape.E, shape.k, shape.F
+        self.lily, self.shape, self.BM, self.dev = lily, shape, BM, dev
+        self.dims = lily.make_dims(T, d, E, k, F, BM)
+        self.inp = synth.make_layer(shape, seed, device=dev, zipf_s=zipf)
+        self.x = self.inp["x"]
+        self.w = lily.LayerWeights(self.inp["router_w"], self.inp["router_b"], self.inp["experts"])
+        self.r = lily.RoutingBuffers(self.dims, dev)
+        self.ws = lily.alloc_workspace(lily.lily_moe_workspace_bytes(self.dims), dev)
+        self.y_ref = torch.empty(T, d, dtype=torch.float32, device=dev)
+        self.y = torch.empty_like(self.y_ref)
+        self.cap = lily.lily_moe_block_map_cap(self.dims)
 
-    def fused():
-        lily.lily_moe_forward(dims, x, w, r, y_ref, ws)
+    def fused(self):
+        self.lily.lily_moe_forward(self.dims, self.x, self.w, self.r, self.y_ref, self.ws)
 
-    def host_routing():
-        lily.lily_moe_route(dims, x, None, w, r, ws)
+    def run(self, name):
+        getattr(self, name)()
+
+    def host_routing(self):
+        lily, r, E, BM = self.lily, self.r, self.shape.E, self.BM
+        lily.lily_moe_route(self.dims, self.x, None, self.w, r, self.ws)
         counts = r.counts.cpu().numpy()  # waits for the routing, copies to the host
         off = np.concatenate([[0], np.cumsum(counts)])
         tiles = [(e, off[e] + i * BM) for e in range(E) for i in range(-(-int(counts[e]) // BM))]
-        bm = np.full((cap, 2), -1, np.int32)
+        bm = np.full((self.cap, 2), -1, np.int32)
         bm[:len(tiles)] = np.asarray(tiles, np.int32).reshape(-1, 2)
         r.block_map.copy_(torch.from_numpy(bm))
         r.n_tiles.fill_(len(tiles))
-        lily.lily_moe_experts(dims, x, w, r, y, ws)
+        lily.lily_moe_experts(self.dims, self.x, self.w, r, self.y, self.ws)
 
-    ex = inp["experts"]
-
-    def deq(q, sc, bi):  # fp16 [n][rows][cols] = scale * q + bias, in HBM
+    @staticmethod
+    def _deq(q, sc, bi):  # fp16 [n][rows][cols] = scale * q + bias, in HBM
         n, rows, half = q.shape
         qq = torch.stack((q & 15, q >> 4), dim=-1).view(n, rows, half * 2 // 64, 64).half()
         return torch.addcmul(bi.half()[..., None], qq, sc.half()[..., None]).view(n, rows, -1)
 
-    def dequant_hbm():
-        lily.lily_moe_route(dims, x, None, w, r, ws)
-        wg = deq(ex["gate_q"], ex["gate_s"], ex["gate_b"])
-        wu = deq(ex["up_q"], ex["up_s"], ex["up_b"])
-        wd = deq(ex["down_q"], ex["down_s"], ex["down_b"])
+    def dequant_hbm(self):
+        lily, r, dev = self.lily, self.r, self.dev
+        T, d, E, k = self.shape.T, self.shape.d, self.shape.E, self.shape.k
+        P, ex, y, x = T * k, self.inp["experts"], self.y, self.x
+        lily.lily_moe_route(self.dims, x, None, self.w, r, self.ws)
+        wg = self._deq(ex["gate_q"], ex["gate_s"], ex["gate_b"])
+        wu = self._deq(ex["up_q"], ex["up_s"], ex["up_b"])
+        wd = self._deq(ex["down_q"], ex["down_s"], ex["down_b"])
         pad = int(r.counts.max())
         pos = torch.arange(P, device=dev)
         e_of = torch.searchsorted(r.offsets[1:].contiguous(), pos.int(), right=True)
@@ -841,6 +842,25 @@ def run_ablation(args, world, rank, local):
         hs = torch.nn.functional.silu(xh @ wg[E].t()) * (xh @ wu[E].t())
         y.add_((hs @ wd[E].t()).float())
 
+
+def run_ablation(args, world, rank, local):
+    """Bench-only ablations (Ablation), each timed eagerly against the fused
+    path in the same run (one JSON line), with its output checked against the
+    fused path's."""
+    import w4_grouped_gemm_gb300 as lily
+    from w4_grouped_gemm_gb300 import synth
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload]
+    T, d, E, k, F, zipf = wl["T"], wl["d"], wl["E"], wl["k"], wl["F"], wl["zipf"]
+    if T <= 8 or wl["kind"] != "layer":
+        raise SystemExit("ablations are single-layer prefill only")
+    ab = Ablation(lily, synth, synth.LayerShape(T, d, E, k, F), args.tile_rows, layer_seed(0, 0),
+                  dev, zipf)
+    y, y_ref, ex, BM = ab.y, ab.y_ref, ab.inp["experts"], args.tile_rows
+    fused = ab.fused
+
     def timed(fn, n):
         for _ in range(3):
             fn()
@@ -851,7 +871,7 @@ def run_ablation(args, world, rank, local):
         torch.cuda.synchronize()
         return (time.perf_counter() - t0) / n
 
-    abl = {"host_routing": host_routing, "dequant_hbm": dequant_hbm}[args.ablation]
+    abl = getattr(ab, args.ablation)
     n = max(3, min(args.steps, 50))
     t_fused = timed(fused, n)
     t_abl = timed(abl, n)

@@ -98,7 +98,7 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, plan, total;
+  size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, total;
 };
 
 // ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
@@ -119,7 +119,6 @@ Layout layout(const lily_moe_dims& d) {
   L.acc = off;
   off += up(T * D * 4);  // prefill: fp32 y accumulator
   L.tiles = off; off += up((size_t)tile_count(d.T, d.n_experts, d.top_k, d.tile_rows) * 16);
-  L.plan = off;  off += d.T <= 8 ? up((1 + lily_moe_block_map_cap(&d)) * kPlanWords * 4) : 0;
   L.total = off;
   return L;
 }
@@ -180,14 +179,8 @@ int check_ws(const lily_moe_dims* d, void* ws, size_t bytes) {
 
 uint32_t* ws_status(void* ws) { return reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws)); }
 
-// Routing on `s` (logits computed unless logits_in is given).  For T <= 8
-// with computed logits the router launch runs the routing itself (its CTA 0),
-// so no separate routing launch is made.
-// With norm (the stacked decode, T <= 8 only) x is the fp32 residual and the
-// router scores bf16(rmsnorm(x, eps)).
-int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
-             const lily_moe_weights* w, const lily_moe_routing& r, void* ws, cudaStream_t s,
-             bool norm = false, float eps = 0.f) {
+RouteArgs route_args(const lily_moe_dims& d, const float* logits_in, const lily_moe_routing& r,
+                     void* ws) {
   const Layout L = layout(d);
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint32_t* ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
@@ -210,8 +203,38 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
   a.hist = reinterpret_cast<int32_t*>(base + L.hist);
   a.bar = ctrl + 1;
   a.status = ws_status(ws);
-  a.plan = nullptr;
   a.wait_ns = route_wait_limit_ns();
+  return a;
+}
+
+// The decode router (T <= 8): logits, and x in the decode GEMV's fragment
+// order in the x16 / xs regions.  With norm (the stacked decode) x is the
+// fp32 residual and the router scores bf16(rmsnorm(x, eps)).
+int do_dec_router(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
+                  const lily_moe_routing& r, void* ws, cudaStream_t s, bool norm = false,
+                  float eps = 0.f) {
+  const Layout L = layout(d);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  DecRouterArgs da = {};
+  da.x = x;
+  da.w = w->router_w;
+  da.b = w->router_bias;
+  da.logits = r.logits;
+  da.xpg = reinterpret_cast<uint32_t*>(base + L.x16);
+  da.xsg = reinterpret_cast<float*>(base + L.xs);
+  da.eps = eps;
+  da.T = d.T;
+  da.d = d.d_model;
+  da.E = d.n_experts;
+  return cuda_rc(launch_dec_router(da, norm, s));
+}
+
+// Routing on `s`: router logits (unless logits_in is given), then the
+// routing kernel.  No host synchronisation.
+int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
+             const lily_moe_weights* w, const lily_moe_routing& r, void* ws, cudaStream_t s) {
+  const Layout L = layout(d);
+  uint8_t* base = static_cast<uint8_t*>(ws);
   if (!logits_in) {
     if (d.T > 8) {
       float* part = reinterpret_cast<float*>(base + L.part);
@@ -219,24 +242,11 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
                                        d.n_experts, base + L.w3, part, r.logits, ws_status(ws), s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
     } else {
-      a.plan = reinterpret_cast<int32_t*>(base + L.plan);  // the decode GEMVs' slot table
-      // x in the decode GEMV's fragment order, in the x16 / xs regions
-      DecRouterArgs da = {};
-      da.x = x;
-      da.w = w->router_w;
-      da.b = w->router_bias;
-      da.logits = r.logits;
-      da.xpg = reinterpret_cast<uint32_t*>(base + L.x16);
-      da.xsg = reinterpret_cast<float*>(base + L.xs);
-      da.eps = eps;
-      da.T = d.T;
-      da.d = d.d_model;
-      da.E = d.n_experts;
-      da.ra = a;
-      return cuda_rc(launch_dec_router(da, norm, s));
+      const int rc = do_dec_router(d, x, w, r, ws, s);
+      if (rc) return rc;
     }
   }
-  return cuda_rc(launch_route(a, s));
+  return cuda_rc(launch_route(route_args(d, logits_in, r, ws), s));
 }
 
 GemmArgs gemm_args(const lily_moe_dims& d, const lily_moe_weights* w, const lily_moe_routing& r,
@@ -301,18 +311,13 @@ DecodeArgs decode_args(const lily_moe_dims& d, const lily_moe_weights* w,
   a.k = d.top_k;
   a.d = d.d_model;
   a.F = d.d_ff;
+  a.BM = d.tile_rows;
   a.cap = (int)lily_moe_block_map_cap(&d);
-  a.block_map = r.block_map;
-  a.n_tiles = r.n_tiles;
-  a.offsets = r.offsets;
-  a.perm = r.perm;
-  a.inv = r.inv_perm;
-  a.gates = r.topk_gates;
+  a.logits = r.logits;
+  a.route = route_args(d, nullptr, r, ws);
   a.gq = w->gate_q; a.gs = w->gate_s; a.gb = w->gate_b;
   a.uq = w->up_q;   a.us = w->up_s;   a.ub = w->up_b;
   a.dq = w->down_q; a.ds = w->down_s; a.db = w->down_b;
-  a.x = nullptr;
-  a.plan = reinterpret_cast<const int32_t*>(base + L.plan);
   a.xpg = reinterpret_cast<const uint32_t*>(base + L.x16);
   a.xsg = reinterpret_cast<const float*>(base + L.xs);
   a.H = base + L.H;
@@ -567,7 +572,8 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_wei
   if (rc) return rc;
   if (dims->T > 8) return LILY_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
-  if ((rc = do_route(*dims, x, nullptr, w, *r, ws, s))) return rc;
+  // router logits, then the GEMVs, which route from them (three launches)
+  if ((rc = do_dec_router(*dims, x, w, *r, ws, s))) return rc;
   return cuda_rc(launch_decode(decode_args(*dims, w, *r, ws, y, nullptr), s));
 }
 
@@ -750,7 +756,7 @@ int lily_moe_stack_decode(const lily_moe_dims* dims, int32_t n_layers,
     // router (on bf16(rmsnorm(x))) with the routing, then the expert GEMVs,
     // whose output is added to x: three launches per layer, each chained to
     // the previous one with programmatic dependent launch
-    if ((rc = do_route(*dims, x, nullptr, &layers[l], rl, lws, s, true, eps))) return rc;
+    if ((rc = do_dec_router(*dims, x, &layers[l], rl, lws, s, true, eps))) return rc;
     if ((rc = cuda_rc(launch_decode(decode_args(*dims, &layers[l], rl, lws, nullptr, x), s))))
       return rc;
   }

@@ -27,7 +27,7 @@
 // pairs come out as (q_i, q_{i+4}) of each 8-code word; the activations are
 // laid out in that same order (x by the decode router; H by the gate/up
 // kernel), so the K order of both operands agrees.
-#include "common.cuh"
+#include "routing.cuh"
 
 namespace lily {
 
@@ -38,9 +38,9 @@ constexpr int kDecThreads = 32 * (1 + kDecConsumers);  // warp 0: producer
 // Two CTAs per SM by registers: a down CTA fits beside a gate/up CTA, so it
 // can start streaming its weights while the gate/up kernel finishes.
 constexpr int kDecMinBlocks = 2;
-constexpr size_t kGuSmemBudget = 160 * 1024;  // gate/up stages + partial sums
-constexpr size_t kDnSmemBudget = 60 * 1024;   // down stages
-constexpr int kGuMaxStages = 6;
+constexpr size_t kGuSmemBudget = 170 * 1024;  // gate/up: stages, partials, x, routing
+constexpr size_t kDnStageBudget = 50 * 1024;  // down: weight stages
+constexpr int kGuMaxStages = 4;
 constexpr int kDnMaxStages = 16;
 
 template <bool F16>
@@ -113,34 +113,6 @@ constexpr uint32_t kGuPartBytes = 2 * kDecConsumers * 2 * kDecUnitRows * kDecMax
 constexpr uint32_t kDnTileBytes = kDecConsumers * kDecMaxRows * kDecUnitRows * 4;
 constexpr uint32_t kBarBytes = 512;  // mbarriers and flags
 
-// ---------------------------------------------------------------- plan
-// Slot s of the routing's decode plan: {expert, first H row, rows, 0, -, -,
-// -, -, token[8], gate bits[8], ...}; slot 0 = shared expert, slot i >= 1 =
-// block-map tile i-1; rows = 0 marks an unused slot.  Returns false for an
-// unused or malformed slot (the latter flagged).
-struct Slot {
-  int expert, row0, rows;
-};
-__device__ __forceinline__ bool plan_slot(const DecodeArgs& a, int slot, Slot& sl) {
-  const int4 h = __ldcg(reinterpret_cast<const int4*>(a.plan + (size_t)slot * kPlanWords));
-  sl.expert = h.x;
-  sl.row0 = h.y;
-  sl.rows = h.z;
-  if (sl.rows <= 0) return false;
-  if (sl.expert < 0 || sl.expert > a.E || sl.rows > kDecMaxRows || sl.row0 < 0 ||
-      sl.row0 + sl.rows > a.T * a.k + a.T) {
-    if ((threadIdx.x & 31) == 0) set_status(a.status, LILY_STATUS_BAD_TILE);
-    return false;
-  }
-  return true;
-}
-__device__ __forceinline__ int plan_token(const DecodeArgs& a, int slot, int n) {
-  return __ldcg(a.plan + (size_t)slot * kPlanWords + 8 + n);
-}
-__device__ __forceinline__ float plan_gate(const DecodeArgs& a, int slot, int n) {
-  return __int_as_float(__ldcg(a.plan + (size_t)slot * kPlanWords + 16 + n));
-}
-
 // One 64-group of 16 weight rows against B fragments xw (this lane's 8
 // words: the (i, i+4) pairs of its K values for B column gi) and the group
 // sums x0, x1 of accumulator columns 2c, 2c+1.  wa / wb: the lane's 16 codes
@@ -176,33 +148,226 @@ __device__ __forceinline__ void unit_codes(const uint8_t* unit, int g, int gi, i
   wb = *reinterpret_cast<const uint2*>(unit + unit_off(gi + 8, off, rb));
 }
 
+
 // Give-up flag shared by the roles of a CTA (see mbar_wait).
 struct DecFlags {
   int abort;
 };
 
+// Logits [T][E] (from the router, complete once this grid may read them)
+// into shared memory, every thread of the CTA loading in parallel.
+__device__ __forceinline__ void load_logits(const float* __restrict__ lg, float* dst, int n) {
+  for (int i = threadIdx.x; i < n / 4; i += blockDim.x)
+    reinterpret_cast<float4*>(dst)[i] = __ldcg(reinterpret_cast<const float4*>(lg) + i);
+  for (int i = (n & ~3) + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(lg + i);
+}
+
+// ======================================================= decode router
+// Logits of T <= 8 rows: CTA b scores experts 2b and 2b+1, four warps per
+// expert, each over a quarter of d, with its quarter of the weight row
+// loaded into registers before the wait for the predecessor (the weights are
+// static); the four quarter sums are added in a fixed order.  The same launch
+// writes x in the expert GEMV's B-fragment order with its 64-group sums:
+//   xpg[(t*G + g)*32 + c*8 + w*4 + e] = (x[t][g*64 + c*16 + 8w + e], x[...+4])
+//   xsg[t*G + g] = sum of x[t][g*64 .. g*64+63]
+// With NORM the input is the fp32 residual of a layer stack and the scored
+// rows are bf16(x / sqrt(mean(x^2) + eps)) (unit-weight RMSNorm).
+constexpr int kDecRouterThreads = 256;
+constexpr int kDecRouterEpb = 2;     // experts per CTA
+constexpr int kDecRouterWv = 8;      // float4 of a quarter row per lane: d <= 4096
+
+template <bool NORM>
+__global__ void __launch_bounds__(kDecRouterThreads) dec_router_kernel(const DecRouterArgs a) {
+  __shared__ float s_part[kDecRouterEpb][4][kDecMaxRows];
+  __shared__ float s_red[kDecRouterThreads / 32][kDecMaxRows];
+  __shared__ float s_inv[kDecMaxRows];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = a.T, d = a.d, E = a.E;
+  const int el = warp >> 2, qd = warp & 3;
+  const int e = blockIdx.x * kDecRouterEpb + el;
+  const bool has = e < E;
+  const int nq4 = d / 16;  // float4 in a quarter row
+  const float4* wq = reinterpret_cast<const float4*>(a.w + (size_t)(has ? e : 0) * d) + qd * nq4;
+  float4 wv[kDecRouterWv];
+#pragma unroll
+  for (int i = 0; i < kDecRouterWv; ++i) {  // static: before the wait
+    const int f = i * 32 + lane;
+    wv[i] = (has && f < nq4) ? __ldg(wq + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait();  // x comes from the predecessor
+  pdl_trigger();
+  if (NORM) {
+    const float* xr = static_cast<const float*>(a.x);
+    for (int t = 0; t < T; ++t) {
+      float ss = 0.f;
+      for (int i = threadIdx.x * 4; i < d; i += kDecRouterThreads * 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(xr + (size_t)t * d + i));
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_red[warp][t] = ss;
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kDecRouterThreads / 32; ++w2) tot += s_red[w2][threadIdx.x];
+      s_inv[threadIdx.x] = 1.f / sqrtf(tot / (float)d + a.eps);
+    }
+    __syncthreads();
+  }
+  // element i of row t as scored: exact bf16 values
+  auto xval4 = [&](int t, int i) {  // i a multiple of 4
+    if (NORM) {
+      const float4 v = __ldcg(
+          reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t * d + i));
+      const float s = s_inv[t];
+      return make_float4(__bfloat162float(__float2bfloat16_rn(v.x * s)),
+                         __bfloat162float(__float2bfloat16_rn(v.y * s)),
+                         __bfloat162float(__float2bfloat16_rn(v.z * s)),
+                         __bfloat162float(__float2bfloat16_rn(v.w * s)));
+    }
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(
+        static_cast<const uint16_t*>(a.x) + (size_t)t * d + i));
+    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  };
+  float acc[kDecMaxRows];
+#pragma unroll
+  for (int t = 0; t < kDecMaxRows; ++t) acc[t] = 0.f;
+#pragma unroll
+  for (int i = 0; i < kDecRouterWv; ++i) {
+    const int f = i * 32 + lane;
+    if (f < nq4) {
+#pragma unroll
+      for (int t = 0; t < kDecMaxRows; ++t) {
+        if (t < T) {
+          const float4 x4 = xval4(t, (qd * nq4 + f) * 4);
+          acc[t] = fmaf(wv[i].x, x4.x, acc[t]);
+          acc[t] = fmaf(wv[i].y, x4.y, acc[t]);
+          acc[t] = fmaf(wv[i].z, x4.z, acc[t]);
+          acc[t] = fmaf(wv[i].w, x4.w, acc[t]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kDecMaxRows; ++t) {
+    const float v = warp_sum(acc[t]);
+    if (lane == 0 && t < T) s_part[el][qd][t] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < kDecRouterEpb * T) {
+    const int el2 = threadIdx.x / T, t = threadIdx.x % T, e2 = blockIdx.x * kDecRouterEpb + el2;
+    if (e2 < E) {
+      float v = s_part[el2][0][t];
+      v += s_part[el2][1][t];
+      v += s_part[el2][2][t];
+      v += s_part[el2][3][t];
+      a.logits[(size_t)t * E + e2] = v + (a.b ? __ldg(a.b + e2) : 0.f);
+    }
+  }
+  // x in the expert GEMV's fragment order, with its group sums
+  const int G = d / 64;
+  for (int u = blockIdx.x * (kDecRouterThreads / 32) + warp; u < T * G;
+       u += gridDim.x * (kDecRouterThreads / 32)) {
+    const int t = u / G, g = u % G;
+    const int c = lane >> 3, w2 = (lane >> 2) & 1, e4 = lane & 3;
+    const int i = g * 64 + c * 16 + 8 * w2 + e4;
+    float lo, hi;
+    if (NORM) {
+      const float* xr = static_cast<const float*>(a.x) + (size_t)t * d;
+      lo = __bfloat162float(__float2bfloat16_rn(__ldcg(xr + i) * s_inv[t]));
+      hi = __bfloat162float(__float2bfloat16_rn(__ldcg(xr + i + 4) * s_inv[t]));
+    } else {
+      const uint16_t* xh = static_cast<const uint16_t*>(a.x) + (size_t)t * d;
+      lo = __uint_as_float((uint32_t)xh[i] << 16);
+      hi = __uint_as_float((uint32_t)xh[i + 4] << 16);
+    }
+    a.xpg[(size_t)u * 32 + lane] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
+    const float sum = warp_sum(lo + hi);
+    if (lane == 0) a.xsg[u] = sum;
+  }
+}
+
+cudaError_t launch_dec_router(const DecRouterArgs& a, bool norm, cudaStream_t s) {
+  if (a.T < 1 || a.T > kDecMaxRows || a.d % 128 || a.d / 16 > 32 * kDecRouterWv || a.E > 256)
+    return cudaErrorInvalidValue;
+  const int grid = (a.E + kDecRouterEpb - 1) / kDecRouterEpb;
+  prof_begin(K_ROUTER_GEMV, s);
+  const cudaError_t err =
+      norm ? launch_pdl(dec_router_kernel<true>, dim3(grid), dim3(kDecRouterThreads), 0, s, a)
+           : launch_pdl(dec_router_kernel<false>, dim3(grid), dim3(kDecRouterThreads), 0, s, a);
+  prof_end(K_ROUTER_GEMV, s);
+  return err;
+}
+
+// Shared-memory regions of the GEMV kernels after their weight stages.
+struct DecSmem {
+  uint32_t lg, slots, xpg, xsg, part, bars, total;
+};
+// gate/up: logits, slots, x fragments and sums, partial sums, barriers
+__host__ __device__ inline DecSmem gu_smem(int T, int E, int d, int nstages) {
+  DecSmem m;
+  const int G = d / 64;
+  uint32_t off = 1024 + (uint32_t)nstages * gu_stage_bytes(d);  // alignment slack + stages
+  m.lg = off;    off += (uint32_t)(T * E * 4 + 15) & ~15u;
+  m.slots = off; off += (uint32_t)kMaxSlots * sizeof(DecSlot);
+  m.xpg = off;   off += (uint32_t)T * G * 128;
+  m.xsg = off;   off += (uint32_t)(T * G * 4 + 15) & ~15u;
+  m.part = off;  off += kGuPartBytes;
+  m.bars = off;  off += kBarBytes;
+  m.total = off;
+  return m;
+}
+// down: logits, slots, per-warp output tiles, barriers
+__host__ __device__ inline DecSmem dn_smem(int T, int E, int F, int nstages) {
+  DecSmem m;
+  uint32_t off = 1024 + (uint32_t)nstages * dn_stage_bytes(F);
+  m.lg = off;    off += (uint32_t)(T * E * 4 + 15) & ~15u;
+  m.slots = off; off += (uint32_t)kMaxSlots * sizeof(DecSlot);
+  m.xpg = m.xsg = 0;
+  m.part = off;  off += kDnTileBytes;
+  m.bars = off;  off += kBarBytes;
+  m.total = off;
+  return m;
+}
+
 // ======================================================= gate/up + SwiGLU
 // Work item = (tile slot, 16 rows of F) for both matrices; item i runs on
-// CTA i % grid.  Shared-expert items (slot 0) need no routing and are
-// fetched before the wait for the router.  Per item each consumer warp takes
-// the groups g = warp, warp + 8, ... of both matrices; the eight partial
-// 16 x 8 results are summed in a fixed order and H = silu(g) * u is written
-// as fp16 in the pair order the down GEMV reads.
+// CTA i % grid.  The first item of CTAs 0 .. F/16-1 belongs to the shared
+// expert (slot 0), which needs no routing: its weights are requested before
+// the wait for the router.  Then every CTA loads the logits and x fragments,
+// routes the T <= 8 tokens in its own shared memory (CTA 0 also writes the
+// routing outputs) and streams its items' weights through a ring of stages.
+// Per item each consumer warp takes the groups g = warp, warp + 8, ... of
+// both matrices; the eight partial 16 x 8 results are summed in a fixed order
+// and H = silu(g) * u is written as fp16 in the pair order the down GEMV reads.
 __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     dec_gateup_kernel(const __grid_constant__ CUtensorMap tm_g,
                       const __grid_constant__ CUtensorMap tm_u, const DecodeArgs a,
                       const int nstages) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const int d = a.d, F = a.F, G = d / 64;
+  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int T = a.T, d = a.d, F = a.F, G = d / 64;
   const int rb = box_bytes(d / 2), nbox = (d / 2) / rb;
   const uint32_t SB = gu_stage_bytes(d);
   const uint32_t code_bytes = kDecUnitRows * (d / 2), sc_bytes = kDecUnitRows * G * 2;
-  float* part = (float*)(smem + (size_t)nstages * SB);  // [2][warps][2][16][8]
-  uint64_t* full = (uint64_t*)((uint8_t*)part + kGuPartBytes);
+  const DecSmem M = gu_smem(T, a.E, d, nstages);
+  uint8_t* smem = base;  // stages at the start
+  float* lg_s = (float*)(base + (M.lg - 1024));
+  DecSlot* slots = (DecSlot*)(base + (M.slots - 1024));
+  uint32_t* xpg_s = (uint32_t*)(base + (M.xpg - 1024));
+  float* xsg_s = (float*)(base + (M.xsg - 1024));
+  float* part = (float*)(base + (M.part - 1024));
+  uint64_t* full = (uint64_t*)(base + (M.bars - 1024));
   uint64_t* empty = full + kGuMaxStages;
-  uint64_t* cons = empty + kGuMaxStages;                 // [2] consumer warps' hand-off
+  uint64_t* cons = empty + kGuMaxStages;  // [2] consumer warps' hand-off
   DecFlags* fl = (DecFlags*)(cons + 2);
+  int* nslots_s = (int*)(fl + 1);
   volatile int* abort = &fl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nfb = F / kDecUnitRows;
@@ -222,100 +387,92 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   }
   __syncthreads();
 
-  // the item sequence both roles walk: unused slots are skipped by both
-  auto item_slot = [&](int it, bool waited, Slot& sl) {
-    const int slot = it / nfb;
-    if (slot == 0) {  // shared expert: every token, no routing needed
-      sl.expert = a.E;
-      sl.row0 = a.T * a.k;
-      sl.rows = a.T;
-      return true;
+  // the weights of item `it` (expert, 16-row block) into stage st
+  auto issue = [&](int it, int expert, uint32_t st) {
+    uint8_t* sp = smem + (size_t)st * SB;
+    const uint32_t fb = smem_u32(&full[st]);
+    mbar_arrive_expect_tx(fb, 2 * code_bytes + 4 * sc_bytes);
+    const int row0 = expert * F + (it % nfb) * kDecUnitRows;
+    for (int b = 0; b < nbox; ++b) {
+      tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_g, b * rb, row0, fb);
+      tma_load_2d(smem_u32(sp + code_bytes + b * kDecUnitRows * rb), &tm_u, b * rb, row0, fb);
     }
-    return waited && plan_slot(a, slot, sl);
+    const size_t so = (size_t)row0 * G;
+    bulk_load(smem_u32(sp + 2 * code_bytes), a.gs + so, sc_bytes, fb);
+    bulk_load(smem_u32(sp + 2 * code_bytes + sc_bytes), a.gb + so, sc_bytes, fb);
+    bulk_load(smem_u32(sp + 2 * code_bytes + 2 * sc_bytes), a.us + so, sc_bytes, fb);
+    bulk_load(smem_u32(sp + 2 * code_bytes + 3 * sc_bytes), a.ub + so, sc_bytes, fb);
   };
+  // the shared expert's first item needs no routing: before the wait
+  const bool early = (int)blockIdx.x < nfb;
+  if (early && threadIdx.x == 0) issue(blockIdx.x, a.E, 0);
+
+  pdl_wait();  // logits and x fragments come from the router
+  pdl_trigger();
+  load_logits(a.logits, lg_s, T * a.E);
+  for (int i = threadIdx.x; i < T * G * 8; i += kDecThreads)
+    reinterpret_cast<uint4*>(xpg_s)[i] = __ldcg(reinterpret_cast<const uint4*>(a.xpg) + i);
+  for (int i = threadIdx.x; i < T * G; i += kDecThreads) xsg_s[i] = __ldcg(a.xsg + i);
+  __syncthreads();
+  if (threadIdx.x < kRouteThreads)
+    small_routing(lg_s, T, a.E, a.k, a.BM, slots, nslots_s, blockIdx.x == 0 ? &a.route : nullptr,
+                  a.status);
+  __syncthreads();
+  const int nslots = *nslots_s;
 
   if (warp == 0) {
     // ================================================= producer (one lane)
     if (lane == 0) {
-      bool waited = false, ok = true;
       uint32_t u = 0;
-      for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-        if (!waited && it >= nfb) {
-          pdl_wait();  // the plan comes from the router
-          pdl_trigger();
-          waited = true;
-        }
-        Slot sl;
-        if (!item_slot(it, waited, sl)) continue;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const int slot = it / nfb;
+        if (slot >= nslots) break;  // items ascend by slot
         const uint32_t st = u % nstages;
-        if (u >= (uint32_t)nstages &&
-            !mbar_wait(smem_u32(&empty[st]), ((u / nstages) - 1) & 1, abort, a.status)) {
-          ok = false;
-          break;
+        if (!(early && it == (int)blockIdx.x)) {
+          if (u >= (uint32_t)nstages &&
+              !mbar_wait(smem_u32(&empty[st]), ((u / nstages) - 1) & 1, abort, a.status))
+            break;
+          issue(it, slots[slot].expert, st);
         }
-        uint8_t* sp = smem + (size_t)st * SB;
-        const uint32_t fb = smem_u32(&full[st]);
-        mbar_arrive_expect_tx(fb, 2 * code_bytes + 4 * sc_bytes);
-        const int row0 = sl.expert * F + (it % nfb) * kDecUnitRows;
-        for (int b = 0; b < nbox; ++b) {
-          tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_g, b * rb, row0, fb);
-          tma_load_2d(smem_u32(sp + code_bytes + b * kDecUnitRows * rb), &tm_u, b * rb, row0, fb);
-        }
-        const size_t so = (size_t)row0 * G;
-        bulk_load(smem_u32(sp + 2 * code_bytes), a.gs + so, sc_bytes, fb);
-        bulk_load(smem_u32(sp + 2 * code_bytes + sc_bytes), a.gb + so, sc_bytes, fb);
-        bulk_load(smem_u32(sp + 2 * code_bytes + 2 * sc_bytes), a.us + so, sc_bytes, fb);
-        bulk_load(smem_u32(sp + 2 * code_bytes + 3 * sc_bytes), a.ub + so, sc_bytes, fb);
         ++u;
-      }
-      if (!waited) {
-        pdl_wait();
-        pdl_trigger();
       }
       if (*abort) {  // let the copies in flight land before the CTA exits
         int never = 0;
         for (uint32_t k2 = (u > (uint32_t)nstages ? u - nstages : 0); k2 < u; ++k2)
           mbar_wait(smem_u32(&full[k2 % nstages]), (k2 / nstages) & 1, &never, a.status);
       }
-    } else {
-      pdl_wait();
-      pdl_trigger();
     }
     return;
   }
 
   // =================================================== consumers (8 warps)
-  pdl_wait();
-  pdl_trigger();
   const int cw = warp - 1, ct = threadIdx.x - 32;
   const int gi = lane >> 2, c = lane & 3;
   uint32_t u = 0;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    Slot sl;
-    if (!item_slot(it, true, sl)) continue;
     const int slot = it / nfb, fb = it % nfb;
+    if (slot >= nslots) break;
+    const DecSlot& sl = slots[slot];
     const uint32_t st = u % nstages;
     if (!warp_wait(smem_u32(&full[st]), (u / nstages) & 1, abort, a.status)) break;
     // B column gi: slot row gi (zero beyond the slot's rows); accumulator
     // columns 2c, 2c+1 take their rows' group sums
     const int rows = sl.rows;
-    const int tg = slot == 0 ? min(gi, rows - 1) : plan_token(a, slot, min(gi, rows - 1));
-    const int t0 = slot == 0 ? min(2 * c, rows - 1) : plan_token(a, slot, min(2 * c, rows - 1));
-    const int t1 =
-        slot == 0 ? min(2 * c + 1, rows - 1) : plan_token(a, slot, min(2 * c + 1, rows - 1));
-    const uint32_t* xrow = a.xpg + (size_t)tg * G * 32 + c * 8;
+    const int tg = sl.tok[min(gi, rows - 1)];
+    const int t0 = sl.tok[min(2 * c, rows - 1)], t1 = sl.tok[min(2 * c + 1, rows - 1)];
+    const uint32_t* xrow = xpg_s + (size_t)tg * G * 32 + c * 8;
     const uint8_t* sp = smem + (size_t)st * SB;
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(sp + 2 * code_bytes);
     float og[4] = {0.f, 0.f, 0.f, 0.f}, ou[4] = {0.f, 0.f, 0.f, 0.f};
     for (int g = cw; g < G; g += kDecConsumers) {
       uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
       if (gi < rows) {
-        h0 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32));
-        h1 = __ldg(reinterpret_cast<const uint4*>(xrow + (size_t)g * 32 + 4));
+        h0 = *reinterpret_cast<const uint4*>(xrow + (size_t)g * 32);
+        h1 = *reinterpret_cast<const uint4*>(xrow + (size_t)g * 32 + 4);
       }
       const uint32_t xw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      const float x0 = 2 * c < rows ? __ldg(a.xsg + (size_t)t0 * G + g) : 0.f;
-      const float x1 = 2 * c + 1 < rows ? __ldg(a.xsg + (size_t)t1 * G + g) : 0.f;
+      const float x0 = 2 * c < rows ? xsg_s[t0 * G + g] : 0.f;
+      const float x1 = 2 * c + 1 < rows ? xsg_s[t1 * G + g] : 0.f;
       uint2 wa, wb;
       unit_codes(sp, g, gi, c, rb, wa, wb);
       group_mma<false>(wa, wb, bf16_bits_to_float(sc[gi * G + g]),
@@ -367,29 +524,36 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
 }
 
 // ======================================================= down + combine
-// CTA = 16 output features over every active tile slot.  The producer lane
-// reads the plan (complete once the gate/up kernel has started, since that
-// kernel waits for the router before it lets this one launch) and streams
-// each slot's 16 weight rows before this kernel waits for H.  Slot v (in
-// order) goes to consumer warp v % 8, which runs the 16-row W4 GEMV over
-// K = F against the slot's H rows (B fragments loaded straight from H; group
-// sums from the same loads) and adds gate * out into its own [token][feature]
-// tile.  The tiles are summed in warp order, so the result is deterministic.
-// The sum is written to y, or added to the fp32 residual (stacked decode).
+// CTA = 16 output features over every slot of the step.  Before waiting for
+// the gate/up kernel the CTA routes the tokens itself from the logits (which
+// the router wrote before the gate/up kernel could start, and this kernel
+// starts only after every gate/up CTA has waited for the router) and its
+// producer lane requests every slot's 16 weight rows, so the weights stream
+// while the gate/up kernel runs.  Slot v goes to consumer warp v % 8, which
+// runs the 16-row W4 GEMV over K = F against the slot's H rows (B fragments
+// loaded from H; group sums from the same loads) and adds gate * out into its
+// own [token][feature] tile.  The tiles are summed in warp order, so the
+// result is deterministic.  The sum is written to y, or added to the fp32
+// residual (stacked decode).
 __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     dec_down_kernel(const __grid_constant__ CUtensorMap tm_d, const DecodeArgs a,
                     const int nstages) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  const int F = a.F, G = F / 64;
+  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int T = a.T, F = a.F, G = F / 64;
   const int rb = box_bytes(F / 2), nbox = (F / 2) / rb;
   const uint32_t SB = dn_stage_bytes(F);
   const uint32_t code_bytes = kDecUnitRows * (F / 2), sc_bytes = kDecUnitRows * G * 2;
-  float* ytile = (float*)(smem + (size_t)nstages * SB);  // [warps][8 tokens][16 features]
-  uint64_t* full = (uint64_t*)((uint8_t*)ytile + kDnTileBytes);
+  const DecSmem M = dn_smem(T, a.E, F, nstages);
+  uint8_t* smem = base;
+  float* lg_s = (float*)(base + (M.lg - 1024));
+  DecSlot* slots = (DecSlot*)(base + (M.slots - 1024));
+  float* ytile = (float*)(base + (M.part - 1024));
+  uint64_t* full = (uint64_t*)(base + (M.bars - 1024));
   uint64_t* empty = full + kDnMaxStages;
   uint64_t* done = empty + kDnMaxStages;
   DecFlags* fl = (DecFlags*)(done + 1);
+  int* nslots_s = (int*)(fl + 1);
   volatile int* abort = &fl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int f0 = blockIdx.x * kDecUnitRows;  // output features [f0, f0 + 16)
@@ -404,17 +568,18 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     fence_mbar_init();
     prefetch_tensormap(&tm_d);
   }
+  load_logits(a.logits, lg_s, T * a.E);  // before the wait: see above
   __syncthreads();
-  // slots 0 .. n_tiles of the plan (read before the wait: see above)
-  const int nslots = 1 + min(max(__ldcg(a.n_tiles), 0), a.cap);
+  if (threadIdx.x < kRouteThreads)
+    small_routing(lg_s, T, a.E, a.k, a.BM, slots, nslots_s, nullptr, a.status);
+  __syncthreads();
+  const int nslots = *nslots_s;
 
   if (warp == 0) {
     if (lane == 0) {
-      bool waited = false, ok = true;
-      uint32_t v = 0;  // valid slots issued
-      for (int s = 0; ok && s < nslots; ++s) {
-        Slot sl;
-        if (!plan_slot(a, s, sl)) continue;
+      bool waited = false;
+      uint32_t v = 0;
+      for (; (int)v < nslots; ++v) {
         const uint32_t st = v % nstages;
         if (v >= (uint32_t)nstages) {
           if (!waited) {
@@ -422,21 +587,17 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
             pdl_trigger();
             waited = true;
           }
-          if (!mbar_wait(smem_u32(&empty[st]), ((v / nstages) - 1) & 1, abort, a.status)) {
-            ok = false;
-            break;
-          }
+          if (!mbar_wait(smem_u32(&empty[st]), ((v / nstages) - 1) & 1, abort, a.status)) break;
         }
         uint8_t* sp = smem + (size_t)st * SB;
         const uint32_t fb = smem_u32(&full[st]);
         mbar_arrive_expect_tx(fb, code_bytes + 2 * sc_bytes);
-        const int row0 = sl.expert * a.d + f0;
+        const int row0 = slots[v].expert * a.d + f0;
         for (int b = 0; b < nbox; ++b)
           tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_d, b * rb, row0, fb);
         const size_t so = (size_t)row0 * G;
         bulk_load(smem_u32(sp + code_bytes), a.ds + so, sc_bytes, fb);
         bulk_load(smem_u32(sp + code_bytes + sc_bytes), a.db + so, sc_bytes, fb);
-        ++v;
       }
       if (!waited) {
         pdl_wait();
@@ -464,47 +625,55 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   __syncwarp();
   const uint16_t* H = static_cast<const uint16_t*>(a.H);
   bool ok = true;
-  uint32_t v = 0;
-  for (int s = 0; s < nslots; ++s) {
-    Slot sl;
-    if (!plan_slot(a, s, sl)) continue;
-    const uint32_t vi = v++;
-    if ((int)(vi % kDecConsumers) != cw) continue;
-    const uint32_t st = vi % nstages;
-    if (!warp_wait(smem_u32(&full[st]), (vi / nstages) & 1, abort, a.status)) {
+  for (int v = cw; v < nslots; v += kDecConsumers) {
+    const DecSlot& sl = slots[v];
+    const uint32_t st = v % nstages;
+    if (!warp_wait(smem_u32(&full[st]), (v / nstages) & 1, abort, a.status)) {
       ok = false;
       break;
     }
     const int rows = sl.rows;
-    // this lane's B column: slot row gi (zero beyond the slot's rows)
+    // this lane's B column: slot row gi (zero beyond the slot's rows); the
+    // slot's H fragments of every group loaded together
     const uint16_t* hrow = H + (size_t)(sl.row0 + min(gi, rows - 1)) * F + c * 16;
     const uint8_t* sp = smem + (size_t)st * SB;
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(sp + code_bytes);
     float o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int g = 0; g < G; ++g) {
-      uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
-      if (gi < rows) {
-        h0 = *reinterpret_cast<const uint4*>(hrow + g * 64);
-        h1 = *reinterpret_cast<const uint4*>(hrow + g * 64 + 8);
-      }
-      const uint32_t xw[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-      // X_g of slot row gi: this lane's 16 values, then over the 4 lanes c
-      float xsum = 0.f;
+    for (int g0 = 0; g0 < G; g0 += 4) {
+      uint4 hh[4][2];
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        xsum += __half2float(__ushort_as_half((uint16_t)(xw[e] & 0xFFFFu))) +
-                __half2float(__ushort_as_half((uint16_t)(xw[e] >> 16)));
-      xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
-      xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
-      // accumulator columns 2c, 2c+1 are slot rows 2c, 2c+1: their X_g
-      const float x0 = __shfl_sync(0xffffffffu, xsum, (2 * c) * 4);
-      const float x1 = __shfl_sync(0xffffffffu, xsum, (2 * c + 1) * 4);
-      uint2 wa, wb;
-      unit_codes(sp, g, gi, c, rb, wa, wb);
-      group_mma<true>(wa, wb, bf16_bits_to_float(sc[gi * G + g]),
-                      bf16_bits_to_float(sc[kDecUnitRows * G + gi * G + g]),
-                      bf16_bits_to_float(sc[(gi + 8) * G + g]),
-                      bf16_bits_to_float(sc[kDecUnitRows * G + (gi + 8) * G + g]), xw, x0, x1, o);
+      for (int i = 0; i < 4; ++i) {
+        hh[i][0] = hh[i][1] = make_uint4(0, 0, 0, 0);
+        if (g0 + i < G && gi < rows) {
+          hh[i][0] = __ldcg(reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64));
+          hh[i][1] = __ldcg(reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64 + 8));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int g = g0 + i;
+        if (g >= G) break;
+        const uint32_t xw[8] = {hh[i][0].x, hh[i][0].y, hh[i][0].z, hh[i][0].w,
+                                hh[i][1].x, hh[i][1].y, hh[i][1].z, hh[i][1].w};
+        // X_g of slot row gi: this lane's 16 values, then over the 4 lanes c
+        float xsum = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          xsum += __half2float(__ushort_as_half((uint16_t)(xw[e] & 0xFFFFu))) +
+                  __half2float(__ushort_as_half((uint16_t)(xw[e] >> 16)));
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+        xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+        // accumulator columns 2c, 2c+1 are slot rows 2c, 2c+1: their X_g
+        const float x0 = __shfl_sync(0xffffffffu, xsum, (2 * c) * 4);
+        const float x1 = __shfl_sync(0xffffffffu, xsum, (2 * c + 1) * 4);
+        uint2 wa, wb;
+        unit_codes(sp, g, gi, c, rb, wa, wb);
+        group_mma<true>(wa, wb, bf16_bits_to_float(sc[gi * G + g]),
+                        bf16_bits_to_float(sc[kDecUnitRows * G + gi * G + g]),
+                        bf16_bits_to_float(sc[(gi + 8) * G + g]),
+                        bf16_bits_to_float(sc[kDecUnitRows * G + (gi + 8) * G + g]), xw, x0, x1,
+                        o);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[st]));  // stage read
@@ -513,12 +682,10 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     for (int h = 0; h < 2; ++h) {
       const int n = 2 * c + h;
       if (n < rows) {
-        const int tok = s == 0 ? n : plan_token(a, s, n);
-        const float gate = s == 0 ? 1.f : plan_gate(a, s, n);
-        if (tok >= 0 && tok < a.T) {
-          yt[tok * kDecUnitRows + gi] += gate * o[h];
-          yt[tok * kDecUnitRows + gi + 8] += gate * o[2 + h];
-        }
+        const int tok = sl.tok[n];
+        const float gate = sl.gate[n];
+        yt[tok * kDecUnitRows + gi] += gate * o[h];
+        yt[tok * kDecUnitRows + gi + 8] += gate * o[2 + h];
       }
     }
   }
@@ -526,7 +693,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(done));
   if (!warp_wait(smem_u32(done), 0, abort, a.status)) return;
-  for (int i = ct; i < a.T * kDecUnitRows; i += 32 * kDecConsumers) {
+  for (int i = ct; i < T * kDecUnitRows; i += 32 * kDecConsumers) {
     const int t = i / kDecUnitRows, f = i % kDecUnitRows;
     float acc = 0.f;
 #pragma unroll
@@ -564,18 +731,18 @@ static int num_sms() {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  if (a.T < 1 || a.T > kDecMaxRows || a.d % 128 || a.F % 128) return cudaErrorInvalidValue;
+  if (a.T < 1 || a.T > kDecMaxRows || a.d % 128 || a.F % 128 || a.E > kMaxE || a.k > kMaxK ||
+      a.BM < kDecMaxRows || 1 + a.cap > kMaxSlots)
+    return cudaErrorInvalidValue;
   CUtensorMap tg, tu, td;
   if (!codes_map(&tg, a.gq, a.d / 2, (a.E + 1) * a.F) ||
       !codes_map(&tu, a.uq, a.d / 2, (a.E + 1) * a.F) ||
       !codes_map(&td, a.dq, a.F / 2, (a.E + 1) * a.d))
     return cudaErrorInvalidValue;
-  // gate/up: a ring of stages within its budget, persistent CTAs
-  const uint32_t gsb = gu_stage_bytes(a.d);
-  int gst = (int)((kGuSmemBudget - kGuPartBytes) / gsb);
-  gst = gst > kGuMaxStages ? kGuMaxStages : gst;
-  if (gst < 2) gst = 2;
-  const size_t gsmem = 1024 + (size_t)gst * gsb + kGuPartBytes + kBarBytes;
+  // gate/up: as many stages as fit beside the other regions
+  int gst = kGuMaxStages;
+  while (gst > 1 && gu_smem(a.T, a.E, a.d, gst).total > kGuSmemBudget) --gst;
+  const size_t gsmem = gu_smem(a.T, a.E, a.d, gst).total;
   const int items = (1 + a.cap) * (a.F / kDecUnitRows);
   const int ggrid = items < num_sms() ? items : num_sms();
   cudaError_t err = ensure_smem_attr((const void*)dec_gateup_kernel, gsmem);
@@ -584,13 +751,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   err = launch_pdl(dec_gateup_kernel, dim3(ggrid), dim3(kDecThreads), gsmem, s, tg, tu, a, gst);
   prof_end(K_DEC_GATEUP, s);
   if (err != cudaSuccess) return err;
-  // down: as many stages as slots, within its budget
-  const uint32_t dsb = dn_stage_bytes(a.F);
-  int dst = (int)(kDnSmemBudget / dsb);
+  // down: one stage per slot up to its budget
+  int dst = (int)(kDnStageBudget / dn_stage_bytes(a.F));
   if (dst > 1 + a.cap) dst = 1 + a.cap;
   if (dst > kDnMaxStages) dst = kDnMaxStages;
-  if (dst < 2) dst = 2;
-  const size_t dsmem = 1024 + (size_t)dst * dsb + kDnTileBytes + kBarBytes;
+  if (dst < 1) dst = 1;
+  const size_t dsmem = dn_smem(a.T, a.E, a.F, dst).total;
   err = ensure_smem_attr((const void*)dec_down_kernel, dsmem);
   if (err != cudaSuccess) return err;
   prof_begin(K_DEC_DOWN, s);

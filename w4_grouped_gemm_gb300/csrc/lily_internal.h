@@ -78,19 +78,13 @@ struct RouteArgs {
   int32_t* hist;       // workspace [nblk][E]
   uint32_t* bar;       // workspace: grid barrier {count, generation}
   uint32_t* status;    // workspace status word
-  int32_t* plan;       // decode plan [1 + cap][kPlanWords] or NULL (one-block routing only)
   uint64_t wait_ns;    // give-up limit of the grid barrier's wait (route_wait_limit_ns())
 };
 // Current give-up limit of the routing kernel's grid-barrier wait (api.cu):
 // 2 s unless lily_moe_set_route_wait_ns() changed it.
 uint64_t route_wait_limit_ns();
-// Decode plan entry of one tile slot: {expert, row0, rows, 0, 4 unused,
-// token[kPlanRows], gate bits[kPlanRows], 8 unused}.
-constexpr int kPlanWords = 32;
-constexpr int kPlanRows = 8;
-// Decode router (T <= 8): logits, x in the decode GEMV's B-fragment order
-// (xpg, [T][d/64][32] words) with its 64-group sums (xsg, [T][d/64]), and the
-// routing with the per-slot decode plan (ra.plan), in one cluster launch.
+// Decode router (T <= 8): logits only, plus x in the decode GEMV's B-fragment
+// order (xpg, [T][d/64][32] words) with its 64-group sums (xsg, [T][d/64]).
 // With `norm` x is the fp32 residual [T][d] of a layer stack and the scored
 // rows are bf16(rmsnorm(x, eps)); else x is bf16 [T][d].
 struct DecRouterArgs {
@@ -102,10 +96,7 @@ struct DecRouterArgs {
   float* xsg;
   float eps;
   int T, d, E;
-  int cs, epc;      // cluster size and experts per CTA (set by the launcher)
-  RouteArgs ra;
 };
-constexpr size_t kDecRouterMaxSmem = 200 * 1024;
 cudaError_t launch_dec_router(const DecRouterArgs& a, bool norm, cudaStream_t s);
 // Router on tensor cores for larger T: W split exactly into three bf16 terms
 // (w_split, [3][E][d]), fp32 partial logits per K-split (partial,
@@ -156,19 +147,16 @@ size_t gemm_smem_bytes(bool gateup, int BM, int K);
 int gemm_stages(bool gateup, int BM, int K);
 
 // ---------------------------------------------------------------- decode
+// The decode GEMVs (T <= 8) route from the router's logits themselves, in
+// each CTA's shared memory; CTA 0 of the gate/up launch also writes the
+// routing outputs (route: ids ... n_tiles; its logits fields are unused).
 struct DecodeArgs {
-  int T, E, k, d, F, cap;
-  const int32_t* block_map;
-  const int32_t* n_tiles;
-  const int32_t* offsets;
-  const int32_t* perm;
-  const int32_t* inv;
-  const float* gates;
+  int T, E, k, d, F, BM, cap;
+  const float* logits;  // [T][E]
+  RouteArgs route;
   const uint8_t* gq; const uint16_t* gs; const uint16_t* gb;
   const uint8_t* uq; const uint16_t* us; const uint16_t* ub;
   const uint8_t* dq; const uint16_t* ds; const uint16_t* db;
-  const void* x;   // bf16 [T][d]
-  const int32_t* plan;  // per tile slot {expert, row0, rows, tokens, gates} (routing)
   const uint32_t* xpg;  // x in B-fragment pair order [T][d/64][32] (router launch)
   const float* xsg;     // x 64-group sums [T][d/64]
   void* H;         // fp16 [P+T][F], each 64-group in the mma pair order

@@ -11,7 +11,7 @@
 // experts and picks eight).
 #include <algorithm>
 
-#include "common.cuh"
+#include "routing.cuh"
 
 namespace lily {
 
@@ -283,53 +283,6 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
 
 // ============================================================== routing kernel
 
-// Order-preserving key of a logit: larger key = ranks first.  -0 and +0 map
-// to the same key; a NaN maps to 0, below every number.
-__device__ __forceinline__ uint32_t logit_key(float v) {
-  if (v != v) return 0u;
-  uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_logit(uint32_t k) {
-  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
-  return __uint_as_float(u);
-}
-
-// Exclusive scan of one int per thread over 256 threads: the whole block, or
-// with NAMED the first 256 threads of a larger block (named barrier 1).
-template <bool NAMED = false>
-__device__ int block_exclusive_scan(int v, int* tmp /* [8] */) {
-  auto sync = [] {
-    if (NAMED)
-      named_sync(1, kRouteThreads);
-    else
-      __syncthreads();
-  };
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) tmp[warp] = incl;
-  sync();
-  if (warp == 0) {
-    int w = (lane < kRouteThreads / 32) ? tmp[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += n;
-    }
-    if (lane < kRouteThreads / 32) tmp[lane] = w;  // inclusive warp totals
-  }
-  sync();
-  int base = (warp > 0) ? tmp[warp - 1] : 0;
-  int out = base + incl - v;
-  sync();
-  return out;
-}
-
 // Grid-wide barrier for a cooperative launch (all blocks co-resident), with a
 // bounded wait: a block that has waited limit_ns (2 s unless a test lowers
 // it) gives up, flags LILY_STATUS_TIMEOUT and gets false, the same value in
@@ -367,8 +320,6 @@ __device__ bool grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* status,
   __syncthreads();
   return s_ok != 0;
 }
-
-constexpr int kMaxE = 256, kMaxK = 8;
 
 // Routing of tokens [blk * kRouteTok, ...) as block blk of nblk (the body of
 // route_kernel; also run by the last block of the small-T router launch with
@@ -415,46 +366,13 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
     const int tl = warp * kWarpTok + i;
     if (tl >= ntok) break;
     const int t = t0 + tl;
-    uint32_t key[kMaxE / 32];
-    uint32_t avail = 0;
-    bool saw_nan = false;
-#pragma unroll
-    for (int c = 0; c < kMaxE / 32; ++c) {
-      const int e = lane + 32 * c;
-      key[c] = 0;
-      if (e < E) {
-        const float v = lv[i][c];
-        saw_nan |= (v != v);
-        key[c] = logit_key(v);
-        avail |= 1u << c;
-      }
-    }
-    if (__any_sync(0xffffffffu, saw_nan) && lane == 0) set_status(a.status, LILY_STATUS_NAN_LOGIT);
-    float my_logit = 0.f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      // lane-local best: largest key, lowest id on ties (c ascending = id ascending)
-      uint32_t bk = 0;
-      int bc = -1;
-#pragma unroll
-      for (int c = 0; c < kMaxE / 32; ++c)
-        if ((avail >> c) & 1u)
-          if (bc < 0 || key[c] > bk) { bk = key[c]; bc = c; }
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bc >= 0 ? bk : 0u);
-      const uint32_t cand = (bc >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bc) : 0xFFFFFFFFu;
-      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-      if ((int)(win & 31u) == lane) avail &= ~(1u << (win >> 5));
-      if (lane == j) { my_logit = key_logit(kmax); my_id = (int)win; }
-    }
-    // gates: softmax over the kept logits; entries equal to the largest weigh 1
-    const float lmax = __shfl_sync(0xffffffffu, my_logit, 0);
-    float wgt = 0.f;
-    if (lane < k) wgt = (my_logit == lmax) ? 1.f : expf(my_logit - lmax);
-    float z = wgt;
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    int my_id;
+    float my_gate;
+    if (warp_topk(lv[i], E, k, my_id, my_gate) && lane == 0)
+      set_status(a.status, LILY_STATUS_NAN_LOGIT);
     if (lane < k) {
       a.ids[(size_t)t * k + lane] = my_id;
-      a.gates[(size_t)t * k + lane] = wgt / z;
+      a.gates[(size_t)t * k + lane] = my_gate;
       s_ids[tl * k + lane] = my_id;
     }
   }
@@ -550,177 +468,6 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
       a.block_map[2 * i] = -1;
       a.block_map[2 * i + 1] = -1;
     }
-    // decode plan (small T, one block): per slot {expert, row0, rows, 0,
-    // -, -, -, -, token[8], gate bits[8], -...}, slot 0 = the shared expert,
-    // slot i >= 1 = tile i-1; read back from this block's own global stores
-    if (a.plan) {
-      __syncthreads();
-      const int P = T * k;
-      for (int slot = threadIdx.x; slot < 1 + a.cap; slot += kRouteThreads) {
-        int32_t* pl = a.plan + (size_t)slot * kPlanWords;
-        int e = -1, row0 = 0, rows = 0;
-        if (slot == 0) {
-          e = E;
-          row0 = P;
-          rows = T;
-        } else if (slot - 1 < s_total) {
-          e = __ldcg(a.block_map + 2 * (slot - 1));
-          row0 = __ldcg(a.block_map + 2 * (slot - 1) + 1);
-          rows = min(a.BM, __ldcg(a.offsets + e + 1) - row0);
-        }
-        rows = min(rows, kPlanRows);
-        pl[0] = e;
-        pl[1] = row0;
-        pl[2] = rows;
-        pl[3] = 0;
-        for (int n = 0; n < kPlanRows; ++n) {
-          int tok = 0;
-          float g = 0.f;
-          if (n < rows) {
-            if (slot == 0) {
-              tok = n;
-              g = 1.f;
-            } else {
-              const int p = __ldcg(a.perm + row0 + n);
-              tok = p / k;
-              g = __ldcg(a.gates + p);
-            }
-          }
-          pl[8 + n] = tok;
-          pl[16 + n] = __float_as_int(g);
-        }
-      }
-    }
-  }
-}
-
-// Routing of T <= kPlanRows tokens by the first kRouteThreads threads of a
-// block (CTA 0 of the decode router launch), from the logits `lg` ([T][E],
-// here in shared memory): the same outputs as route_body with one block,
-// built without read-backs -- top-k and gates by one warp per token, counts
-// by counting, positions by counting the earlier pairs of the same expert
-// (stable by pair index), tiles of each expert in ascending order, and the
-// decode plan (a.plan, required).  Synchronises on named barrier 1 only, so
-// the block's other threads may have left.
-__device__ __forceinline__ void route_small_body(const RouteArgs& a, const float* lg) {
-  constexpr int kMaxP = kPlanRows * kMaxK;
-  __shared__ int s_e[kMaxP];      // expert of pair p = t * k + j
-  __shared__ float s_g[kMaxP];    // its gate
-  __shared__ int s_perm[kMaxP];   // pair at sorted position
-  __shared__ int s_cnt[kMaxE], s_off[kMaxE], s_toff[kMaxE];
-  __shared__ int s_scan_tmp[8];
-  __shared__ int s_total;
-  const int T = a.T, E = a.E, k = a.k, P = T * k;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < T) {
-    const int t = warp;
-    uint32_t key[kMaxE / 32];
-    uint32_t avail = 0;
-    bool saw_nan = false;
-#pragma unroll
-    for (int c = 0; c < kMaxE / 32; ++c) {
-      const int e = lane + 32 * c;
-      key[c] = 0;
-      if (e < E) {
-        const float v = lg[(size_t)t * E + e];
-        saw_nan |= (v != v);
-        key[c] = logit_key(v);
-        avail |= 1u << c;
-      }
-    }
-    if (__any_sync(0xffffffffu, saw_nan) && lane == 0) set_status(a.status, LILY_STATUS_NAN_LOGIT);
-    float my_logit = 0.f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-      uint32_t bk = 0;
-      int bc = -1;
-#pragma unroll
-      for (int c = 0; c < kMaxE / 32; ++c)
-        if ((avail >> c) & 1u)
-          if (bc < 0 || key[c] > bk) { bk = key[c]; bc = c; }
-      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bc >= 0 ? bk : 0u);
-      const uint32_t cand = (bc >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bc) : 0xFFFFFFFFu;
-      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-      if ((int)(win & 31u) == lane) avail &= ~(1u << (win >> 5));
-      if (lane == j) { my_logit = key_logit(kmax); my_id = (int)win; }
-    }
-    const float lmax = __shfl_sync(0xffffffffu, my_logit, 0);
-    float wgt = 0.f;
-    if (lane < k) wgt = (my_logit == lmax) ? 1.f : expf(my_logit - lmax);
-    float z = wgt;
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if (lane < k) {
-      a.ids[(size_t)t * k + lane] = my_id;
-      a.gates[(size_t)t * k + lane] = wgt / z;
-      s_e[t * k + lane] = my_id;
-      s_g[t * k + lane] = wgt / z;
-    }
-  }
-  named_sync(1, kRouteThreads);
-  // counts and offsets: thread e counts its pairs
-  const int e_me = threadIdx.x;  // kRouteThreads == kMaxE
-  int cnt = 0;
-  for (int p = 0; p < P; ++p) cnt += (s_e[p] == e_me);
-  if (e_me >= E) cnt = 0;
-  const int off_me = block_exclusive_scan<true>(cnt, s_scan_tmp);
-  s_cnt[e_me] = cnt;
-  s_off[e_me] = off_me;
-  const int ntile = (cnt + a.BM - 1) / a.BM;
-  named_sync(1, kRouteThreads);
-  const int toff = block_exclusive_scan<true>(ntile, s_scan_tmp);
-  s_toff[e_me] = toff;
-  if (e_me == kMaxE - 1) s_total = toff + ntile;
-  if (e_me < E) {
-    a.counts[e_me] = cnt;
-    a.offsets[e_me] = off_me;
-  }
-  if (e_me == 0) a.offsets[E] = P;
-  named_sync(1, kRouteThreads);
-  // pair p's position: its expert's offset + the earlier pairs of that expert
-  for (int p = threadIdx.x; p < P; p += kRouteThreads) {
-    const int e = s_e[p];
-    int r = 0;
-    for (int q = 0; q < p; ++q) r += (s_e[q] == e);
-    const int pos = s_off[e] + r;
-    a.perm[pos] = p;
-    a.inv[p] = pos;
-    s_perm[pos] = p;
-  }
-  named_sync(1, kRouteThreads);
-  // block map and plan: thread e writes its tiles; slot 0 = shared expert
-  const int total = s_total;
-  for (int i = 0; i < ntile; ++i) {
-    const int row0 = off_me + i * a.BM, rows = min(a.BM, cnt - i * a.BM);
-    a.block_map[2 * (toff + i)] = e_me;
-    a.block_map[2 * (toff + i) + 1] = row0;
-    int32_t* pl = a.plan + (size_t)(1 + toff + i) * kPlanWords;
-    const int pr = min(rows, kPlanRows);
-    pl[0] = e_me;
-    pl[1] = row0;
-    pl[2] = pr;
-    pl[3] = 0;
-    for (int n = 0; n < kPlanRows; ++n) {
-      const int p = n < pr ? s_perm[row0 + n] : 0;
-      pl[8 + n] = n < pr ? p / k : 0;
-      pl[16 + n] = __float_as_int(n < pr ? s_g[p] : 0.f);
-    }
-  }
-  if (e_me == 0) {
-    *a.n_tiles = total;
-    int32_t* pl = a.plan;
-    pl[0] = E;
-    pl[1] = P;
-    pl[2] = T;
-    pl[3] = 0;
-    for (int n = 0; n < kPlanRows; ++n) {
-      pl[8 + n] = n < T ? n : 0;
-      pl[16 + n] = __float_as_int(n < T ? 1.f : 0.f);
-    }
-  }
-  for (int i = total + threadIdx.x; i < a.cap; i += kRouteThreads) {
-    a.block_map[2 * i] = -1;
-    a.block_map[2 * i + 1] = -1;
-    a.plan[(size_t)(1 + i) * kPlanWords + 2] = 0;  // unused slot: no rows
   }
 }
 
@@ -728,214 +475,6 @@ __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
   pdl_wait();  // the logits come from the predecessor
   pdl_trigger();
   route_body(a, blockIdx.x, gridDim.x);
-}
-
-// ============================================================== decode router
-// Small T (decode, T <= 8): one cluster of `cs` CTAs (16, else 8).  CTA r
-// scores experts r * epc .. r * epc + epc - 1, one warp per expert (warps
-// take a second expert when epc exceeds the warp count), with the expert's
-// weight row loaded into registers before the wait for the predecessor (the
-// weights are static).  The token rows are staged once in shared memory as
-// fp32 (exact bf16 values).  Each logit goes to the routing output and, by a
-// distributed-shared-memory store, to CTA 0; after a cluster barrier CTA 0
-// routes (top-k, gates, counts, positions, block map, decode plan) from its
-// shared memory, with no global counter or fence.  The same launch writes x
-// in the decode GEMV's B-fragment order with its 64-group sums:
-//   xpg[(t*G + g)*32 + c*8 + w*4 + e] = (x[t][g*64 + c*16 + 8w + e], x[...+4])
-//   xsg[t*G + g] = sum of x[t][g*64 .. g*64+63]
-// With NORM the input is the fp32 residual of a layer stack and the scored
-// rows are bf16(x / sqrt(mean(x^2) + eps)) (unit-weight RMSNorm).
-constexpr int kDecRouterThreads = 512;
-constexpr int kDecRouterWarps = kDecRouterThreads / 32;
-constexpr int kDecRouterWv = 16;  // float4 of a weight row held per lane: 2048 weights
-
-template <bool NORM>
-__global__ void __launch_bounds__(kDecRouterThreads, 1) dec_router_kernel(const DecRouterArgs a) {
-  extern __shared__ __align__(16) float dsm[];
-  float* xs = dsm;                             // [T][d] the scored rows, fp32
-  float* lall = dsm + (size_t)a.T * a.d;       // [T][E] every logit (used in CTA 0)
-  __shared__ float s_red[kDecRouterWarps][kPlanRows];
-  __shared__ float s_inv[kPlanRows];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = a.T, d = a.d, E = a.E, n4 = d / 4;
-  const uint32_t rank = cluster_ctarank();
-  const int rounds = (a.epc + kDecRouterWarps - 1) / kDecRouterWarps;
-  float4 wv[kDecRouterWv];
-  auto expert_of = [&](int j) { return (int)rank * a.epc + warp + kDecRouterWarps * j; };
-  auto has_expert = [&](int j) {
-    return warp + kDecRouterWarps * j < a.epc && expert_of(j) < E;
-  };
-  auto load_w = [&](int j, int pass) {
-    const bool has = has_expert(j);
-    const float4* wrow = reinterpret_cast<const float4*>(a.w + (size_t)(has ? expert_of(j) : 0) * d);
-#pragma unroll
-    for (int i = 0; i < kDecRouterWv; ++i) {
-      const int f = pass * 32 * kDecRouterWv + i * 32 + lane;
-      wv[i] = (has && f < n4) ? __ldg(wrow + f) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  };
-  load_w(0, 0);  // static: before the wait
-  pdl_wait();    // x comes from the predecessor
-  pdl_trigger();
-
-  // ---- stage the rows that are scored (and fed to the expert GEMVs)
-  if (NORM) {
-    const float* xr = static_cast<const float*>(a.x);
-    for (int t = 0; t < T; ++t) {
-      float ss = 0.f;
-      for (int i = threadIdx.x; i < d; i += kDecRouterThreads) {
-        const float v = xr[(size_t)t * d + i];
-        ss = fmaf(v, v, ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) s_red[warp][t] = ss;
-    }
-    __syncthreads();
-    if (threadIdx.x < T) {
-      float tot = 0.f;
-#pragma unroll
-      for (int w2 = 0; w2 < kDecRouterWarps; ++w2) tot += s_red[w2][threadIdx.x];
-      s_inv[threadIdx.x] = 1.f / sqrtf(tot / (float)d + a.eps);
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < T * d; i += kDecRouterThreads)
-      xs[i] = __bfloat162float(__float2bfloat16_rn(xr[i] * s_inv[i / d]));
-  } else {
-    const uint4* xb = static_cast<const uint4*>(a.x);  // 8 bf16 per 16 bytes
-    for (int i = threadIdx.x; i < T * d / 8; i += kDecRouterThreads) {
-      const uint4 v = __ldg(xb + i);
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-      float4* dst = reinterpret_cast<float4*>(xs + (size_t)i * 8);
-      dst[0] = make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xFFFF0000u),
-                           __uint_as_float(w4[1] << 16), __uint_as_float(w4[1] & 0xFFFF0000u));
-      dst[1] = make_float4(__uint_as_float(w4[2] << 16), __uint_as_float(w4[2] & 0xFFFF0000u),
-                           __uint_as_float(w4[3] << 16), __uint_as_float(w4[3] & 0xFFFF0000u));
-    }
-  }
-  __syncthreads();
-
-  // ---- logits: per warp and expert, T dot products over d in a fixed order
-  const int npass = (n4 + 32 * kDecRouterWv - 1) / (32 * kDecRouterWv);
-  const uint32_t lall0 = mapa_shared(smem_u32(lall), 0);
-  for (int j = 0; j < rounds; ++j) {
-    float acc[kPlanRows];
-#pragma unroll
-    for (int t = 0; t < kPlanRows; ++t) acc[t] = 0.f;
-    for (int pass = 0; pass < npass; ++pass) {
-      if (j > 0 || pass > 0) load_w(j, pass);
-#pragma unroll
-      for (int i = 0; i < kDecRouterWv; ++i) {
-        const int f = pass * 32 * kDecRouterWv + i * 32 + lane;
-        if (f < n4) {
-#pragma unroll
-          for (int t = 0; t < kPlanRows; ++t) {
-            if (t < T) {
-              const float4 x4 = reinterpret_cast<const float4*>(xs + (size_t)t * d)[f];
-              acc[t] = fmaf(wv[i].x, x4.x, acc[t]);
-              acc[t] = fmaf(wv[i].y, x4.y, acc[t]);
-              acc[t] = fmaf(wv[i].z, x4.z, acc[t]);
-              acc[t] = fmaf(wv[i].w, x4.w, acc[t]);
-            }
-          }
-        }
-      }
-    }
-    if (has_expert(j)) {
-      const int e = expert_of(j);
-      const float bias = a.b ? __ldg(a.b + e) : 0.f;
-#pragma unroll
-      for (int t = 0; t < kPlanRows; ++t) {
-        if (t < T) {
-          const float v = warp_sum(acc[t]) + bias;
-          if (lane == 0) {
-            a.logits[(size_t)t * E + e] = v;
-            st_cluster_f32(lall0 + (uint32_t)((t * E + e) * 4), v);
-          }
-        }
-      }
-    }
-  }
-
-  // ---- x in the expert GEMV's fragment order, with its group sums
-  const int G = d / 64;
-  for (int u = (int)rank * kDecRouterWarps + warp; u < T * G; u += a.cs * kDecRouterWarps) {
-    const int t = u / G, g = u % G;
-    const int c = lane >> 3, w2 = (lane >> 2) & 1, e4 = lane & 3;
-    const int i = g * 64 + c * 16 + 8 * w2 + e4;
-    const float lo = xs[(size_t)t * d + i], hi = xs[(size_t)t * d + i + 4];
-    a.xpg[(size_t)u * 32 + lane] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);
-    const float sum = warp_sum(lo + hi);
-    if (lane == 0) a.xsg[u] = sum;
-  }
-
-  cluster_sync_all();  // every logit is in CTA 0's shared memory
-  if (rank == 0 && threadIdx.x < kRouteThreads) route_small_body(a.ra, lall);
-}
-
-int dec_router_cluster_size() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
-  int cs = 0;
-  for (int want : {16, 8}) {
-    for (auto kern : {dec_router_kernel<false>, dec_router_kernel<true>}) {
-      cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      cudaFuncSetAttribute((const void*)kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kDecRouterMaxSmem);
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(want);
-    cfg.blockDim = dim3(kDecRouterThreads);
-    cfg.dynamicSmemBytes = kDecRouterMaxSmem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = want;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)dec_router_kernel<true>, &cfg) ==
-            cudaSuccess &&
-        n >= 1) {
-      cs = want;
-      break;
-    }
-    cudaGetLastError();
-  }
-  if (dev >= 0 && dev < 64 && cs) cached[dev] = cs;
-  return cs;
-}
-
-cudaError_t launch_dec_router(const DecRouterArgs& in, bool norm, cudaStream_t s) {
-  if (in.T < 1 || in.T > kPlanRows || in.d % 128 || in.E > 256) return cudaErrorInvalidValue;
-  const size_t smem = ((size_t)in.T * in.d + (size_t)in.T * in.E) * 4;
-  if (smem > kDecRouterMaxSmem) return cudaErrorInvalidValue;
-  const int cs = dec_router_cluster_size();
-  if (!cs) return cudaErrorNotSupported;
-  DecRouterArgs a = in;
-  a.cs = cs;
-  a.epc = (a.E + cs - 1) / cs;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs);
-  cfg.blockDim = dim3(kDecRouterThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  prof_begin(K_ROUTER_GEMV, s);
-  const cudaError_t err = norm ? cudaLaunchKernelEx(&cfg, dec_router_kernel<true>, a)
-                               : cudaLaunchKernelEx(&cfg, dec_router_kernel<false>, a);
-  prof_end(K_ROUTER_GEMV, s);
-  return err;
 }
 
 int route_max_blocks() {

@@ -1,0 +1,239 @@
+// routing.cuh -- routing building blocks shared by the prefill routing
+// kernel (route.cu) and the decode GEMVs (decode.cu): the order-preserving
+// logit key, the block scan, one token's top-k with renormalised gates, and
+// the whole routing of up to 8 tokens inside one CTA's shared memory.
+//
+// Routing (page "Lily Beats MLX-LM 1.35x on Decode: Perplexity's Rust+Metal
+// Engine for Apple Silicon", sections "Model structure and three workload
+// shapes" and "Prefill: fusing dequantisation and keeping routing
+// GPU-resident"): per token the k experts with the largest logits (ties to
+// the lower id), gates = softmax over the kept logits; per expert the count
+// of (token, slot) pairs, the exclusive prefix scan of the counts, the pairs
+// scattered into expert-contiguous rows (stable by pair index t*k + j) and
+// the block map of tiles of at most BM rows per expert.
+#pragma once
+#include "common.cuh"
+
+namespace lily {
+
+constexpr int kMaxE = 256, kMaxK = 8;
+
+// Order-preserving key of a logit: larger key = ranks first.  -0 and +0 map
+// to the same key; a NaN maps to 0, below every number.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  if (v != v) return 0u;
+  uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// Exclusive scan of one int per thread over 256 threads: the whole block, or
+// with NAMED the first 256 threads of a larger block (named barrier 1).
+template <bool NAMED = false>
+__device__ int block_exclusive_scan(int v, int* tmp /* [8] */) {
+  auto sync = [] {
+    if (NAMED)
+      named_sync(1, kRouteThreads);
+    else
+      __syncthreads();
+  };
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) tmp[warp] = incl;
+  sync();
+  if (warp == 0) {
+    int w = (lane < kRouteThreads / 32) ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    if (lane < kRouteThreads / 32) tmp[lane] = w;  // inclusive warp totals
+  }
+  sync();
+  int base = (warp > 0) ? tmp[warp - 1] : 0;
+  int out = base + incl - v;
+  sync();
+  return out;
+}
+
+// Top-k of one token by one warp: lane l holds the logits of experts
+// l + 32c in lv[c] (c < E/32 rounded up).  On return lane j < k holds the
+// j-th expert (by logit desc, id asc) and its gate.  Returns whether a logit
+// of the token was NaN.
+__device__ __forceinline__ bool warp_topk(const float (&lv)[kMaxE / 32], int E, int k, int& my_id,
+                                          float& my_gate) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[kMaxE / 32];
+  uint32_t avail = 0;
+  bool saw_nan = false;
+#pragma unroll
+  for (int c = 0; c < kMaxE / 32; ++c) {
+    const int e = lane + 32 * c;
+    key[c] = 0;
+    if (e < E) {
+      saw_nan |= (lv[c] != lv[c]);
+      key[c] = logit_key(lv[c]);
+      avail |= 1u << c;
+    }
+  }
+  float my_logit = 0.f;
+  my_id = 0;
+  for (int j = 0; j < k; ++j) {
+    // lane-local best: largest key, lowest id on ties (c ascending = id ascending)
+    uint32_t bk = 0;
+    int bc = -1;
+#pragma unroll
+    for (int c = 0; c < kMaxE / 32; ++c)
+      if ((avail >> c) & 1u)
+        if (bc < 0 || key[c] > bk) { bk = key[c]; bc = c; }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bc >= 0 ? bk : 0u);
+    const uint32_t cand = (bc >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bc) : 0xFFFFFFFFu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    if ((int)(win & 31u) == lane) avail &= ~(1u << (win >> 5));
+    if (lane == j) { my_logit = key_logit(kmax); my_id = (int)win; }
+  }
+  // gates: softmax over the kept logits; entries equal to the largest weigh 1
+  const float lmax = __shfl_sync(0xffffffffu, my_logit, 0);
+  float wgt = 0.f;
+  if (lane < k) wgt = (my_logit == lmax) ? 1.f : expf(my_logit - lmax);
+  float z = wgt;
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  my_gate = lane < k ? wgt / z : 0.f;
+  return __any_sync(0xffffffffu, saw_nan);
+}
+
+// ------------------------------------------------------------- small T
+// One tile slot of a decode step: slot 0 is the shared expert (all T rows,
+// weight 1), slot i >= 1 is block-map tile i-1.  row0 is the slot's first row
+// in the expert-sorted order of the rows (the shared rows follow the P
+// routed ones); tok / gate give each row's token and gate.
+constexpr int kSlotRows = 8;
+struct DecSlot {
+  int expert, row0, rows, pad;
+  int tok[kSlotRows];
+  float gate[kSlotRows];
+};
+constexpr int kMaxSlots = 1 + kSlotRows * kMaxK;  // T <= 8: P <= 64 routed tiles
+
+// Routing of T <= 8 tokens by the first kRouteThreads threads of a CTA, from
+// the logits `lg` ([T][E], shared memory): the slots of the step into
+// `slots` / *nslots (shared memory) and, when `out` is given, the routing
+// outputs (ids, gates, counts, offsets, perm, inv, block map, n_tiles) to
+// global memory.  Counts by counting, positions by counting the earlier pairs
+// of the same expert (stable by pair index), tiles of each expert in
+// ascending order.  Synchronises on named barrier 1 only, so the CTA's other
+// threads may be doing something else.
+__device__ __forceinline__ void small_routing(const float* lg, int T, int E, int k, int BM,
+                                              DecSlot* slots, int* nslots, const RouteArgs* out,
+                                              uint32_t* status) {
+  __shared__ int s_e[kSlotRows * kMaxK];      // expert of pair p = t * k + j
+  __shared__ float s_g[kSlotRows * kMaxK];    // its gate
+  __shared__ int s_perm[kSlotRows * kMaxK];   // pair at sorted position
+  __shared__ int s_scan_tmp[8];
+  __shared__ int s_total;
+  const int P = T * k;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < T) {
+    const int t = warp;
+    float lv[kMaxE / 32];
+#pragma unroll
+    for (int c = 0; c < kMaxE / 32; ++c) {
+      const int e = lane + 32 * c;
+      lv[c] = e < E ? lg[(size_t)t * E + e] : 0.f;
+    }
+    int my_id;
+    float my_gate;
+    const bool nan = warp_topk(lv, E, k, my_id, my_gate);
+    if (nan && lane == 0) set_status(status, LILY_STATUS_NAN_LOGIT);
+    if (lane < k) {
+      s_e[t * k + lane] = my_id;
+      s_g[t * k + lane] = my_gate;
+      if (out) {
+        out->ids[(size_t)t * k + lane] = my_id;
+        out->gates[(size_t)t * k + lane] = my_gate;
+      }
+    }
+  }
+  named_sync(1, kRouteThreads);
+  // counts and offsets: thread e counts its pairs
+  const int e_me = threadIdx.x;  // kRouteThreads == kMaxE
+  int cnt = 0;
+  for (int p = 0; p < P; ++p) cnt += (s_e[p] == e_me);
+  if (e_me >= E) cnt = 0;
+  const int off_me = block_exclusive_scan<true>(cnt, s_scan_tmp);
+  const int ntile = (cnt + BM - 1) / BM;
+  const int toff = block_exclusive_scan<true>(ntile, s_scan_tmp);
+  if (e_me == kMaxE - 1) s_total = toff + ntile;
+  if (out) {
+    if (e_me < E) {
+      out->counts[e_me] = cnt;
+      out->offsets[e_me] = off_me;
+    }
+    if (e_me == 0) out->offsets[E] = P;
+  }
+  named_sync(1, kRouteThreads);
+  // pair p's position: its expert's offset + the earlier pairs of that expert
+  for (int p = threadIdx.x; p < P; p += kRouteThreads) {
+    const int e = s_e[p];
+    int r = 0;
+    for (int q = 0; q < p; ++q) r += (s_e[q] == e);
+    // the scan result of thread e is not visible here; recount the offset
+    int off = 0;
+    for (int q = 0; q < P; ++q) off += (s_e[q] < e);
+    const int pos = off + r;
+    s_perm[pos] = p;
+    if (out) {
+      out->perm[pos] = p;
+      out->inv[p] = pos;
+    }
+  }
+  named_sync(1, kRouteThreads);
+  // slots and block map: thread e writes its tiles; slot 0 = shared expert
+  const int total = s_total;
+  for (int i = 0; i < ntile; ++i) {
+    const int row0 = off_me + i * BM, rows = min(BM, cnt - i * BM);
+    DecSlot& sl = slots[1 + toff + i];
+    const int pr = min(rows, kSlotRows);
+    sl.expert = e_me;
+    sl.row0 = row0;
+    sl.rows = pr;
+    for (int n = 0; n < kSlotRows; ++n) {
+      const int p = n < pr ? s_perm[row0 + n] : 0;
+      sl.tok[n] = n < pr ? p / k : 0;
+      sl.gate[n] = n < pr ? s_g[p] : 0.f;
+    }
+    if (out) {
+      out->block_map[2 * (toff + i)] = e_me;
+      out->block_map[2 * (toff + i) + 1] = row0;
+    }
+  }
+  if (e_me == 0) {
+    *nslots = 1 + total;
+    DecSlot& sl = slots[0];
+    sl.expert = E;
+    sl.row0 = P;
+    sl.rows = T;
+    for (int n = 0; n < kSlotRows; ++n) {
+      sl.tok[n] = n < T ? n : 0;
+      sl.gate[n] = n < T ? 1.f : 0.f;
+    }
+    if (out) *out->n_tiles = total;
+  }
+  if (out)
+    for (int i = total + threadIdx.x; i < out->cap; i += kRouteThreads) {
+      out->block_map[2 * i] = -1;
+      out->block_map[2 * i + 1] = -1;
+    }
+  named_sync(1, kRouteThreads);
+}
+
+}  // namespace lily
