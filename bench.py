@@ -297,10 +297,12 @@ def kernel_work(name, T, d, E, k, F, touched):
         return touched * 2 * mb + T * d * 2, 4 * (P + T) * d * F
     if name in ("down_gemm", "dec_down_combine"):
         return touched * mb + T * d * 4, 2 * (P + T) * d * F
-    if name in ("router_gemm", "router_gemv", "dec_router"):
+    if name in ("router_gemm", "dec_router"):
         return E * d * 4 + T * d * 2 + T * E * 4, 2 * T * d * E
     if name == "route":
         return T * E * 4 + T * k * 8, 0
+    if name == "combine":  # each token's k + 1 fp16 rows in, the fp32 row out
+        return (P + T) * d * 2 + T * d * 4, 0
     return None
 
 

@@ -98,7 +98,7 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t ctrl, hist, x16, xs, w3, part, H, acc, tiles, total;
+  size_t ctrl, hist, x16, xs, w3, part, H, O, tiles, total;
 };
 
 // ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
@@ -116,8 +116,7 @@ Layout layout(const lily_moe_dims& d) {
   L.w3 = off;   off += tc_router ? up(3 * E * D * 2) : 0;
   L.part = off; off += tc_router ? up((size_t)router_splits(d.T, d.d_model) * T * E * 4) : 0;
   L.H = off;    off += up((P + T) * F * 2);
-  L.acc = off;
-  off += up(T * D * 4);  // prefill: fp32 y accumulator
+  L.O = off;    off += up((P + T) * D * 2);  // grouped GEMM path: the down GEMM's rows
   L.tiles = off; off += up((size_t)tile_count(d.T, d.n_experts, d.top_k, d.tile_rows) * 16);
   L.total = off;
   return L;
@@ -269,23 +268,22 @@ GemmArgs gemm_args(const lily_moe_dims& d, const lily_moe_weights* w, const lily
   a.b0 = w->gate_b;
   a.s1 = w->up_s;
   a.b1 = w->up_b;
+  a.inv = r.inv_perm;
   a.H = base + L.H;
-  a.yacc = reinterpret_cast<float*>(base + L.acc);
+  a.O = base + L.O;
   a.tiles = reinterpret_cast<int4*>(base + L.tiles);
   a.status = ws_status(ws);
   return a;
 }
 
-// Routing + grouped GEMMs.  The layer output is accumulated in fp32 into
-// yacc (the workspace accumulator when NULL).
-// The grouped GEMMs (token rows, gate/up + SwiGLU, down + gated combine)
-// from routing already in r.  The layer output is accumulated in fp32 into
-// yacc (the workspace accumulator when NULL).
-int do_experts_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
-                   const lily_moe_routing& r, void* ws, cudaStream_t s, float* yacc = nullptr) {
+// The grouped GEMMs (token rows, gate/up + SwiGLU, down) from routing
+// already in r, then the combine of each token's rows: into y (fp32 or bf16
+// per d.out_dtype), or -- with resid -- added to the fp32 residual with the
+// next layer's RMSNorm into xn (when xn is non-NULL).
+int do_experts(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
+               const lily_moe_routing& r, void* ws, cudaStream_t s, void* y,
+               float* resid = nullptr, void* xn = nullptr, float eps = 0.f) {
   GemmArgs a = gemm_args(d, w, r, ws);
-  if (yacc) a.yacc = yacc;
-  if (!aligned16(a.yacc)) return LILY_ERR_MISALIGNED;
   const Layout L = layout(d);
   uint8_t* base = static_cast<uint8_t*>(ws);
   if (launch_token_rows(a, x, base + L.xs, base + L.x16, s) != cudaSuccess) return LILY_ERR_CUDA;
@@ -296,7 +294,7 @@ int do_experts_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights
   a.s1 = nullptr;
   a.b1 = nullptr;
   if (launch_down(a, w->down_q, s) != cudaSuccess) return LILY_ERR_CUDA;
-  return LILY_OK;
+  return cuda_rc(launch_combine(a, y, d.out_dtype == LILY_DTYPE_F32, resid, xn, eps, s));
 }
 
 // Arguments of the decode GEMV launches (after do_route for T <= 8): the
@@ -328,12 +326,13 @@ DecodeArgs decode_args(const lily_moe_dims& d, const lily_moe_weights* w,
   return a;
 }
 
-// Routing + grouped GEMMs.
-int do_forward_acc(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
-                   const lily_moe_routing& r, void* ws, cudaStream_t s, float* yacc = nullptr) {
+// Routing + grouped GEMMs + combine.
+int do_forward(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
+               const lily_moe_routing& r, void* ws, cudaStream_t s, void* y,
+               float* resid = nullptr, void* xn = nullptr, float eps = 0.f) {
   const int rc = do_route(d, x, nullptr, w, r, ws, s);
   if (rc) return rc;
-  return do_experts_acc(d, x, w, r, ws, s, yacc);
+  return do_experts(d, x, w, r, ws, s, y, resid, xn, eps);
 }
 
 int common_checks(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
@@ -542,13 +541,7 @@ int lily_moe_experts(const lily_moe_dims* dims, const void* x, const lily_moe_we
                      const lily_moe_routing* r, void* y, void* ws, size_t ws_bytes, void* stream) {
   int rc = common_checks(dims, x, w, r, y, ws, ws_bytes, true);
   if (rc) return rc;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (dims->out_dtype == LILY_DTYPE_F32)
-    return do_experts_acc(*dims, x, w, *r, ws, s, static_cast<float*>(y));
-  if ((rc = do_experts_acc(*dims, x, w, *r, ws, s))) return rc;
-  const Layout L = layout(*dims);
-  return cuda_rc(launch_finalize(reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.acc), y,
-                                 (int64_t)dims->T * dims->d_model, s));
+  return do_experts(*dims, x, w, *r, ws, (cudaStream_t)stream, y);
 }
 
 int lily_moe_forward(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
@@ -557,13 +550,7 @@ int lily_moe_forward(const lily_moe_dims* dims, const void* x, const lily_moe_we
   if (rc) return rc;
   const int maxb = route_max_blocks();
   if (maxb > 0 && (dims->T + kRouteTok - 1) / kRouteTok > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
-  cudaStream_t s = (cudaStream_t)stream;
-  if (dims->out_dtype == LILY_DTYPE_F32)  // accumulate straight into the caller's y
-    return do_forward_acc(*dims, x, w, *r, ws, s, static_cast<float*>(y));
-  if ((rc = do_forward_acc(*dims, x, w, *r, ws, s))) return rc;
-  const Layout L = layout(*dims);
-  return cuda_rc(launch_finalize(reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + L.acc), y,
-                                 (int64_t)dims->T * dims->d_model, s));
+  return do_forward(*dims, x, w, *r, ws, (cudaStream_t)stream, y);
 }
 
 int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_weights* w,
@@ -702,8 +689,6 @@ int lily_moe_stack_prefill(const lily_moe_dims* dims, int32_t T_total, int32_t n
   void* lws = base + S.ws;
   lily_moe_routing r = stack_routing(base, S);
   void* xn = base + S.xn;
-  const Layout L = layout(*dims);
-  float* yacc = reinterpret_cast<float*>(static_cast<uint8_t*>(lws) + L.acc);
   const int nchunks = T_total / T;
   for (int c = 0; c < nchunks; ++c) {
     float* xc = x + (size_t)c * T * D;
@@ -715,10 +700,11 @@ int lily_moe_stack_prefill(const lily_moe_dims* dims, int32_t T_total, int32_t n
         return LILY_ERR_CUDA;
       lily_moe_routing rl = r;
       if (layer_logits) rl.logits = layer_logits + ((size_t)l * T_total + (size_t)c * T) * E;
-      if ((rc = do_forward_acc(*dims, xn, &layers[l], rl, lws, s))) return rc;
-      if (launch_stack_boundary(yacc, xc, l + 1 < n_layers ? xn : nullptr, T, D, eps, s) !=
-          cudaSuccess)
-        return LILY_ERR_CUDA;
+      // the layer on bf16(rmsnorm(x)); its combine adds the output to x and
+      // writes the next layer's normalised input
+      if ((rc = do_forward(*dims, xn, &layers[l], rl, lws, s, nullptr, xc,
+                           l + 1 < n_layers ? xn : nullptr, eps)))
+        return rc;
     }
   }
   return LILY_OK;
@@ -828,9 +814,9 @@ int lily_moe_profile_read(double* total_ms, int64_t* launches) {
 }
 
 const char* lily_moe_kernel_name(int kind) {
-  static const char* names[] = {"router_gemm", "router_gemv", "route", "gateup_gemm",
-                                "down_gemm",   "finalize",    "dec_gateup", "dec_down_combine",
-                                "dec_combine", "rmsnorm",     "stack_boundary", "memset_acc",
+  static const char* names[] = {"router_gemm", "dec_router", "route", "gateup_gemm",
+                                "down_gemm",   "combine",    "dec_gateup", "dec_down_combine",
+                                "unused",      "rmsnorm",     "unused", "unused",
                                 "router_prep", "router_reduce", "token_rows"};
   if (kind < 0 || kind >= (int)(sizeof(names) / sizeof(names[0]))) return "unused";
   return names[kind];

@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   volatile int* abort = &fl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nfb = F / kDecUnitRows;
-  const int n_items = (1 + a.cap) * nfb;
+  const int n_items = (1 + min(a.E, T * a.k)) * nfb;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < nstages; ++i) {
@@ -731,8 +731,11 @@ static int num_sms() {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  // at most T*k <= 64 routed experts, each one tile (rows <= T <= BM), plus
+  // the shared expert
+  const int maxslots = 1 + (a.E < a.T * a.k ? a.E : a.T * a.k);
   if (a.T < 1 || a.T > kDecMaxRows || a.d % 128 || a.F % 128 || a.E > kMaxE || a.k > kMaxK ||
-      a.BM < kDecMaxRows || 1 + a.cap > kMaxSlots)
+      a.BM < kDecMaxRows || maxslots > kMaxSlots)
     return cudaErrorInvalidValue;
   CUtensorMap tg, tu, td;
   if (!codes_map(&tg, a.gq, a.d / 2, (a.E + 1) * a.F) ||
@@ -743,7 +746,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   int gst = kGuMaxStages;
   while (gst > 1 && gu_smem(a.T, a.E, a.d, gst).total > kGuSmemBudget) --gst;
   const size_t gsmem = gu_smem(a.T, a.E, a.d, gst).total;
-  const int items = (1 + a.cap) * (a.F / kDecUnitRows);
+  const int items = maxslots * (a.F / kDecUnitRows);
   const int ggrid = items < num_sms() ? items : num_sms();
   cudaError_t err = ensure_smem_attr((const void*)dec_gateup_kernel, gsmem);
   if (err != cudaSuccess) return err;
@@ -753,7 +756,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   // down: one stage per slot up to its budget
   int dst = (int)(kDnStageBudget / dn_stage_bytes(a.F));
-  if (dst > 1 + a.cap) dst = 1 + a.cap;
+  if (dst > maxslots) dst = maxslots;
   if (dst > kDnMaxStages) dst = kDnMaxStages;
   if (dst < 1) dst = 1;
   const size_t dsmem = dn_smem(a.T, a.E, a.F, dst).total;

@@ -39,7 +39,7 @@
 // Persistent: one CTA per SM walks the (tile, slice) work items; warp roles
 // are listed below.  Every wait is bounded (2 s) and sets
 // LILY_STATUS_TIMEOUT when it runs out.
-#include "common.cuh"
+#include "routing.cuh"
 
 namespace lily {
 
@@ -90,15 +90,17 @@ struct GemmLayout {
   static_assert(kNumA >= 2, "tensor memory too small for the A ring");
 };
 
-// Down epilogue staging: per epilogue warp two buffers of 32 token rows x 32
-// output features (fp32), the source of the bulk reductions into y.
-constexpr int kEpiStageFloats = kNumEpiWarps * 2 * 32 * 32;
+// Down epilogue staging: per epilogue warp 32 rows x 32 output features of
+// fp16, rows padded to 40 halves (80 bytes) so that the per-row 16-byte reads
+// of eight consecutive rows hit eight different bank groups.
+constexpr int kEpiRowHalves = 40;
+constexpr int kEpiStageBytes = kNumEpiWarps * 32 * kEpiRowHalves * 2;
 
 __host__ __device__ inline size_t gemm_fixed_bytes(int mats, int BM, int K, int nsb) {
   const int G = K / 64;
   return 1024                                  // alignment slack
          + (size_t)nsb * mats * G * 128 * 4    // scale/bias tables (one per item in flight)
-         + (mats == 1 ? kEpiStageFloats * 4 : 0)  // down: epilogue staging
+         + (mats == 1 ? kEpiStageBytes : 0)  // down: epilogue staging
          + kNumBars * 8                        // mbarriers
          + 16;                                 // abort flag, TMEM address
 }
@@ -299,8 +301,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t* stage_base = smem;
   uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][MATS][G][128] scale|bias<<16
   const int sb_words = MATS * G * 128;                       // one table
-  float* estage = (float*)(sb + nsb * sb_words);             // down: epilogue staging
-  uint64_t* bars = (uint64_t*)(estage + (GATEUP ? 0 : kEpiStageFloats));
+  __half* estage = (__half*)(sb + nsb * sb_words);           // down: epilogue staging
+  uint64_t* bars = (uint64_t*)((uint8_t*)estage + (GATEUP ? 0 : kEpiStageBytes));
   uint64_t* full = bars;                      // [kMaxStages] TMA landed
   uint64_t* empty = bars + kMaxStages;        // [kMaxStages] stage consumed by the MMAs
   uint64_t* afull = bars + 2 * kMaxStages;    // [kMaxA] dequantised A ready in TMEM
@@ -685,10 +687,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
         } else {
-          // Rows of the item (gate already applied in H) into y: each warp
-          // stages its 32 features of up to 32 rows in shared memory, row by
-          // row, and each lane adds one row's 128 bytes into y with one bulk
-          // reduction (the L2 adds a whole line per operation).
+          // Output rows of the item (already weighted: the gate was applied
+          // in H) as fp16 into O, in the same expert-sorted row order as H;
+          // the combine kernel then sums each token's rows.  Each warp stages
+          // its 32 features of up to 32 rows in shared memory, and each lane
+          // stores one row's 64 bytes.
           const int ncol = N - cb < 32 ? N - cb : 32;  // 16 or 32
           uint32_t va[16], vb[16];
           tmem_ld16(tl + cb, va);
@@ -699,23 +702,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
-          float* buf = estage + ((size_t)(q * 2 + (echunk & 1)) * 32 * 32);
-          // this buffer's previous reductions have read their rows
-          bulk_wait_read<1>();
-          __syncwarp();
+          __half* buf = estage + (size_t)q * 32 * kEpiRowHalves;
+          bool range_ok = true;
 #pragma unroll
-          for (int rr = 0; rr < 16; ++rr) buf[rr * 32 + lane] = __uint_as_float(va[rr]);
+          for (int rr = 0; rr < 16; ++rr) {
+            const float v = __uint_as_float(va[rr]);
+            range_ok &= fabsf(v) <= 65504.f;
+            buf[rr * kEpiRowHalves + lane] = __float2half_rn(v);
+          }
           if (ncol == 32) {
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) buf[(16 + rr) * 32 + lane] = __uint_as_float(vb[rr]);
+            for (int rr = 0; rr < 16; ++rr) {
+              const float v = __uint_as_float(vb[rr]);
+              range_ok &= fabsf(v) <= 65504.f;
+              buf[(16 + rr) * kEpiRowHalves + lane] = __float2half_rn(v);
+            }
           }
-          fence_proxy_async_smem();
           __syncwarp();
-          if (lane < ncol && cb + lane < cur.rows)
-            bulk_reduce_add_f32(a.yacc + (size_t)(uint32_t)tokj * a.d + (feat - lane),
-                                smem_u32(buf + lane * 32), 32 * 4);
-          bulk_commit();
-          ++echunk;
+          if (lane < ncol && cb + lane < cur.rows) {
+            const uint4* src = reinterpret_cast<const uint4*>(buf + lane * kEpiRowHalves);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(a.O) +
+                                                  (size_t)(cur.row0 + cb + lane) * a.d +
+                                                  (feat - lane));
+            const uint4 v0 = src[0], v1 = src[1], v2 = src[2], v3 = src[3];
+            dst[0] = v0;
+            dst[1] = v1;
+            dst[2] = v2;
+            dst[3] = v3;
+          }
+          __syncwarp();
+          if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
         }
       }
       cur = nxt;
@@ -725,8 +741,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       have_next = have_nn;
       ++j;
     }
-    // down: this thread's bulk reductions have read shared memory and landed
-    if (!GATEUP) bulk_wait_all();
   }
 
   // ---- teardown: every MMA has finished before TMEM is released
@@ -840,14 +854,6 @@ __global__ void __launch_bounds__(256) token_rows_kernel(const uint4* __restrict
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_wait();  // routing (perm, block map) comes from the predecessor
   pdl_trigger();
-  // the fp32 output accumulator starts at zero (the down GEMM adds into it)
-  {
-    float4* acc4 = reinterpret_cast<float4*>(a.yacc);
-    const int64_t n4 = (int64_t)T * a.d / 4;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
-         i += (int64_t)gridDim.x * blockDim.x)
-      acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   // tile table: {expert, row0, rows, 0}, shared-expert tiles first
   const int nsh = (T + a.BM - 1) / a.BM;
   const int ntab = tile_count(T, a.E, k, a.BM);
@@ -920,28 +926,121 @@ cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
   return launch_gemm<false>(a, q0, q0, b, b, s);
 }
 
-// y = bf16(yacc), 8 elements per thread.
-__global__ void finalize_kernel(const float* __restrict__ yacc, __nv_bfloat16* __restrict__ y,
-                                int64_t n8) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 v0 = __ldcs(reinterpret_cast<const float4*>(yacc) + 2 * i);
-    const float4 v1 = __ldcs(reinterpret_cast<const float4*>(yacc) + 2 * i + 1);
-    __nv_bfloat162 o[4] = {__floats2bfloat162_rn(v0.x, v0.y), __floats2bfloat162_rn(v0.z, v0.w),
-                           __floats2bfloat162_rn(v1.x, v1.y), __floats2bfloat162_rn(v1.z, v1.w)};
-    reinterpret_cast<uint4*>(y)[i] = *reinterpret_cast<const uint4*>(o);
+// Combine: y[t] = sum_j O[inv[t*k + j]] + O[P + t] (the k routed rows of
+// token t in slot order, then its shared-expert row), in fp32 and in that
+// fixed order, so the layer output is the same on every run.  One CTA per
+// token; each thread takes 8 consecutive outputs and issues the loads of all
+// k + 1 rows before adding.  Modes: y fp32, y bf16, or the stacked prefill's
+// boundary: x[t] += y[t] (fp32 residual) and, when xn is given, xn[t] =
+// bf16(x[t] / sqrt(mean(x[t]^2) + eps)) for the next layer.
+constexpr int kCombThreads = 256;
+template <int MODE>  // 0: y fp32, 1: y bf16, 2: residual
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(
+    const __half* __restrict__ O, const int32_t* __restrict__ inv, int k, int P, int d, void* y,
+    float* x, __nv_bfloat16* xn, float eps, uint32_t* status) {
+  __shared__ float s_red[kCombThreads / 32];
+  pdl_wait();  // O comes from the down GEMM
+  pdl_trigger();
+  const int t = blockIdx.x;
+  int rows[kMaxK + 1];
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) {
+    int r = 0;
+    if (j < k) {
+      r = __ldg(inv + (size_t)t * k + j);
+      bad |= r < 0 || r >= P;
+      r = min(max(r, 0), P - 1);
+    }
+    rows[j] = r;
+  }
+  if (bad && threadIdx.x == 0) set_status(status, LILY_STATUS_BAD_TILE);
+  rows[kMaxK] = P + t;
+  const int d8 = d / 8;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < d8; c += kCombThreads) {
+    uint4 v[kMaxK + 1];
+#pragma unroll
+    for (int j = 0; j <= kMaxK; ++j)
+      if (j < k || j == kMaxK)
+        v[j] = __ldcs(reinterpret_cast<const uint4*>(O + (size_t)rows[j] * d) + c);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j <= kMaxK; ++j) {
+      if (j < k || j == kMaxK) {
+        const __half2* h = reinterpret_cast<const __half2*>(&v[j]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(h[e]);
+          acc[2 * e] += f.x;
+          acc[2 * e + 1] += f.y;
+        }
+      }
+    }
+    const size_t o = (size_t)t * d + (size_t)c * 8;
+    if (MODE == 0) {
+      float4* yo = reinterpret_cast<float4*>(static_cast<float*>(y) + o);
+      yo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      yo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else if (MODE == 1) {
+      __nv_bfloat162 b[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) b[e] = __floats2bfloat162_rn(acc[2 * e], acc[2 * e + 1]);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + o) =
+          *reinterpret_cast<const uint4*>(b);
+    } else {
+      float4* xo = reinterpret_cast<float4*>(x + o);
+      float4 a0 = xo[0], a1 = xo[1];
+      a0.x += acc[0]; a0.y += acc[1]; a0.z += acc[2]; a0.w += acc[3];
+      a1.x += acc[4]; a1.y += acc[5]; a1.z += acc[6]; a1.w += acc[7];
+      xo[0] = a0;
+      xo[1] = a1;
+      ss = fmaf(a0.x, a0.x, ss); ss = fmaf(a0.y, a0.y, ss);
+      ss = fmaf(a0.z, a0.z, ss); ss = fmaf(a0.w, a0.w, ss);
+      ss = fmaf(a1.x, a1.x, ss); ss = fmaf(a1.y, a1.y, ss);
+      ss = fmaf(a1.z, a1.z, ss); ss = fmaf(a1.w, a1.w, ss);
+    }
+  }
+  if (MODE == 2 && xn) {
+    ss = warp_sum(ss);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) s_red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombThreads / 32; ++w) tot += s_red[w];
+    const float inv_rms = 1.f / sqrtf(tot / (float)d + eps);
+    for (int c = threadIdx.x; c < d8; c += kCombThreads) {
+      const size_t o = (size_t)t * d + (size_t)c * 8;
+      const float4 a0 = reinterpret_cast<const float4*>(x + o)[0];
+      const float4 a1 = reinterpret_cast<const float4*>(x + o)[1];
+      __nv_bfloat162 b[4] = {__floats2bfloat162_rn(a0.x * inv_rms, a0.y * inv_rms),
+                             __floats2bfloat162_rn(a0.z * inv_rms, a0.w * inv_rms),
+                             __floats2bfloat162_rn(a1.x * inv_rms, a1.y * inv_rms),
+                             __floats2bfloat162_rn(a1.z * inv_rms, a1.w * inv_rms)};
+      *reinterpret_cast<uint4*>(xn + o) = *reinterpret_cast<const uint4*>(b);
+    }
   }
 }
 
-cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s) {
-  const int64_t n8 = n / 8;
-  int blocks = (int)((n8 + 255) / 256);
-  if (blocks > 152 * 8) blocks = 152 * 8;
-  if (blocks < 1) blocks = 1;
+cudaError_t launch_combine(const GemmArgs& a, void* y, bool y_f32, float* x, void* xn, float eps,
+                           cudaStream_t s) {
+  const int P = a.T * a.k;
+  const __half* O = static_cast<const __half*>(a.O);
+  __nv_bfloat16* xnb = static_cast<__nv_bfloat16*>(xn);
   prof_begin(K_FINALIZE, s);
-  finalize_kernel<<<blocks, 256, 0, s>>>(yacc, static_cast<__nv_bfloat16*>(y), n8);
+  cudaError_t err;
+  if (x)
+    err = launch_pdl(combine_kernel<2>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv, a.k, P, a.d,
+                     (void*)nullptr, x, xnb, eps, a.status);
+  else if (y_f32)
+    err = launch_pdl(combine_kernel<0>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv, a.k, P, a.d,
+                     y, (float*)nullptr, (__nv_bfloat16*)nullptr, eps, a.status);
+  else
+    err = launch_pdl(combine_kernel<1>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv, a.k, P, a.d,
+                     y, (float*)nullptr, (__nv_bfloat16*)nullptr, eps, a.status);
   prof_end(K_FINALIZE, s);
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace lily

@@ -14,17 +14,14 @@ namespace lily {
 // Kernel kinds for the optional per-kernel event timing.
 enum KernelKind : int {
   K_ROUTER_GEMM = 0,
-  K_ROUTER_GEMV = 1,
+  K_ROUTER_GEMV = 1,  // the decode router
   K_ROUTE = 2,
   K_GATEUP = 3,
   K_DOWN = 4,
-  K_FINALIZE = 5,
+  K_FINALIZE = 5,     // the combine of each token's output rows
   K_DEC_GATEUP = 6,
   K_DEC_DOWN = 7,
-  K_DEC_COMBINE = 8,  // (fused into K_DEC_DOWN)
   K_RMSNORM = 9,
-  K_STACK_BOUNDARY = 10,
-  K_MEMSET = 11,
   K_ROUTER_PREP = 12,
   K_ROUTER_REDUCE = 13,
   K_TOKEN_ROWS = 14,
@@ -121,8 +118,10 @@ struct GemmArgs {
   const uint16_t* b0;
   const uint16_t* s1;  // up scales (gate/up only)
   const uint16_t* b1;
-  void* H;             // fp16 [P+T][F], 8-element chunks in K-chunk order
-  float* yacc;         // fp32 [T][d]
+  const int32_t* inv;  // inv_perm [P]: the expert-sorted row of pair t*k + j
+  void* H;             // fp16 [P+T][F], 8-element chunks in K-chunk order, rows
+                       // weighted by their gate
+  void* O;             // fp16 [P+T][d] down GEMM output rows (gate applied), same order
   int4* tiles;         // [tile_count(T, E, k, BM)] {expert, row0, rows, 0}: shared-expert
                        // tiles first, then the block map's; rows = 0 marks no tile
   uint32_t* status;
@@ -135,14 +134,18 @@ __host__ __device__ inline int tile_count(int T, int E, int k, int BM) {
 }
 // Token rows for the gate/up GEMM: xs[r] = fp16(x[perm[r] / k]) for the P
 // expert-sorted rows and x16[t] = fp16(x[t]), every 8-element chunk in
-// K-chunk order; the same launch writes the tile table a.tiles and zeroes the
-// fp32 accumulator a.yacc ([T][d], 16-byte aligned).  Then the gate/up GEMM
-// (tensor maps built from the pointers).
+// K-chunk order; the same launch writes the tile table a.tiles.  Then the
+// gate/up GEMM (tensor maps built from the pointers), the down GEMM (output
+// rows into a.O) and the combine of each token's rows.
 cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* x16, cudaStream_t s);
 cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, const uint8_t* gq,
                           const uint8_t* uq, cudaStream_t s);
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s);
-cudaError_t launch_finalize(const float* yacc, void* y, int64_t n, cudaStream_t s);
+// y[t] = sum of token t's rows of O (routed rows in slot order, then the
+// shared row), fp32 (y_f32) or bf16; or, with x non-NULL, x[t] += that sum and
+// xn[t] = bf16(rmsnorm(x[t], eps)) when xn is non-NULL.
+cudaError_t launch_combine(const GemmArgs& a, void* y, bool y_f32, float* x, void* xn, float eps,
+                           cudaStream_t s);
 size_t gemm_smem_bytes(bool gateup, int BM, int K);
 int gemm_stages(bool gateup, int BM, int K);
 
@@ -171,9 +174,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- misc
 cudaError_t launch_rmsnorm(const float* x, void* out, int T, int d, float eps, cudaStream_t s);
-// x += yacc; xn = bf16(rmsnorm(x)) (xn may be NULL)
-cudaError_t launch_stack_boundary(const float* yacc, float* x, void* xn, int T, int d, float eps,
-                                  cudaStream_t s);
+
 
 // Driver entry point for cuTensorMapEncodeTiled (resolved through the runtime).
 CUresult encode_tiled(CUtensorMap* tm, CUtensorMapDataType dt, uint32_t rank, void* base,

@@ -1,5 +1,5 @@
-// misc.cu -- row kernels for the stacked-layer prefill: unit-weight RMSNorm
-// and the residual boundary between two MoE layers.
+// misc.cu -- unit-weight RMSNorm, the pre-norm of the stacked-layer prefill
+// (the residual add and the next layer's norm are fused into the combine).
 //
 // The pages name no normalisation around the MoE block; a bare residual stack
 // x <- x + MoE(x) of SwiGLU experts grows without bound, so the stack uses the
@@ -41,32 +41,10 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_kernel(const float* __res
   rms_row(x + row * d, out + row * d, d, eps, tmp);
 }
 
-// x += yacc (the layer's fp32 output); then (optionally) xn = bf16(rmsnorm(x)).
-__global__ void __launch_bounds__(kRowThreads) stack_boundary_kernel(const float* __restrict__ yacc,
-                                                                     float* __restrict__ x,
-                                                                     __nv_bfloat16* __restrict__ xn,
-                                                                     int d, float eps) {
-  __shared__ float tmp[8];
-  const size_t row = blockIdx.x;
-  float* xr = x + row * d;
-  const float* yr = yacc + row * d;
-  for (int i = threadIdx.x; i < d; i += kRowThreads) xr[i] = xr[i] + yr[i];
-  __syncthreads();
-  if (xn) rms_row(xr, xn + row * d, d, eps, tmp);
-}
-
 cudaError_t launch_rmsnorm(const float* x, void* out, int T, int d, float eps, cudaStream_t s) {
   prof_begin(K_RMSNORM, s);
   rmsnorm_kernel<<<T, kRowThreads, 0, s>>>(x, static_cast<__nv_bfloat16*>(out), d, eps);
   prof_end(K_RMSNORM, s);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_stack_boundary(const float* yacc, float* x, void* xn, int T, int d, float eps,
-                                  cudaStream_t s) {
-  prof_begin(K_STACK_BOUNDARY, s);
-  stack_boundary_kernel<<<T, kRowThreads, 0, s>>>(yacc, x, static_cast<__nv_bfloat16*>(xn), d, eps);
-  prof_end(K_STACK_BOUNDARY, s);
   return cudaGetLastError();
 }
 
