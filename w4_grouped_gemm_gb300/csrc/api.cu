@@ -98,10 +98,11 @@ constexpr size_t kAlign = 256;
 inline size_t up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 struct Layout {
-  size_t ctrl, hist, x16, xs, w3, part, H, O, tiles, total;
+  size_t ctrl, hist, x16, xs, w3, part, H, O, tiles, plan, total;
 };
 
-// ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation
+// ctrl: [0] status, [1] grid-barrier count, [2] grid-barrier generation,
+// [3] decode router CTAs done
 Layout layout(const lily_moe_dims& d) {
   const size_t T = d.T, E = d.n_experts, k = d.top_k, F = d.d_ff, D = d.d_model;
   const size_t P = T * k;
@@ -118,6 +119,7 @@ Layout layout(const lily_moe_dims& d) {
   L.H = off;    off += up((P + T) * F * 2);
   L.O = off;    off += up((P + T) * D * 2);  // grouped GEMM path: the down GEMM's rows
   L.tiles = off; off += up((size_t)tile_count(d.T, d.n_experts, d.top_k, d.tile_rows) * 16);
+  L.plan = off;  off += d.T <= 8 ? up(decode_plan_bytes()) : 0;  // decode: the step's slots
   L.total = off;
   return L;
 }
@@ -206,9 +208,10 @@ RouteArgs route_args(const lily_moe_dims& d, const float* logits_in, const lily_
   return a;
 }
 
-// The decode router (T <= 8): logits, and x in the decode GEMV's fragment
-// order in the x16 / xs regions.  With norm (the stacked decode) x is the
-// fp32 residual and the router scores bf16(rmsnorm(x, eps)).
+// The decode router (T <= 8): logits, x in the decode GEMV's fragment order
+// in the x16 / xs regions, and (its last CTA) the routing outputs and the
+// step's plan.  With norm (the stacked decode) x is the fp32 residual and the
+// router scores bf16(rmsnorm(x, eps)).
 int do_dec_router(const lily_moe_dims& d, const void* x, const lily_moe_weights* w,
                   const lily_moe_routing& r, void* ws, cudaStream_t s, bool norm = false,
                   float eps = 0.f) {
@@ -225,6 +228,9 @@ int do_dec_router(const lily_moe_dims& d, const void* x, const lily_moe_weights*
   da.T = d.T;
   da.d = d.d_model;
   da.E = d.n_experts;
+  da.route = route_args(d, nullptr, r, ws);
+  da.plan = base + L.plan;
+  da.done = reinterpret_cast<uint32_t*>(base + L.ctrl) + 3;
   return cuda_rc(launch_dec_router(da, norm, s));
 }
 
@@ -241,8 +247,7 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
                                        d.n_experts, base + L.w3, part, r.logits, ws_status(ws), s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
     } else {
-      const int rc = do_dec_router(d, x, w, r, ws, s);
-      if (rc) return rc;
+      return do_dec_router(d, x, w, r, ws, s);  // routes in its last CTA
     }
   }
   return cuda_rc(launch_route(route_args(d, logits_in, r, ws), s));
@@ -311,8 +316,7 @@ DecodeArgs decode_args(const lily_moe_dims& d, const lily_moe_weights* w,
   a.F = d.d_ff;
   a.BM = d.tile_rows;
   a.cap = (int)lily_moe_block_map_cap(&d);
-  a.logits = r.logits;
-  a.route = route_args(d, nullptr, r, ws);
+  a.plan = base + L.plan;
   a.gq = w->gate_q; a.gs = w->gate_s; a.gb = w->gate_b;
   a.uq = w->up_q;   a.us = w->up_s;   a.ub = w->up_b;
   a.dq = w->down_q; a.ds = w->down_s; a.db = w->down_b;
@@ -756,9 +760,9 @@ int lily_moe_status(void* ws, void* stream) {
   if (cudaMemcpyAsync(&v, ws_status(ws), 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return LILY_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
-  // clear the bits; after a give-up also the grid-barrier counters (words
-  // 1..2), so that no later call starts from a stale count
-  const size_t clear = (v & LILY_STATUS_TIMEOUT) ? 12 : 4;
+  // clear the bits; after a give-up also the grid-barrier and router-done
+  // counters (words 1..3), so that no later call starts from a stale count
+  const size_t clear = (v & LILY_STATUS_TIMEOUT) ? 16 : 4;
   if (v && cudaMemsetAsync(ws_status(ws), 0, clear, s) != cudaSuccess) return LILY_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LILY_ERR_CUDA;
   return (int)v;

@@ -121,7 +121,9 @@ template <bool F16>
 __device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, float sa, float ba, float sb,
                                           float bb, const uint32_t (&xw)[8], float x0, float x1,
                                           float (&out)[4]) {
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // four independent accumulators (one per k16 step): the four MMAs do not
+  // wait for each other; their sums are added afterwards
+  float part[4][4] = {};
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t pa[4], pb[4];
@@ -130,9 +132,12 @@ __device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, float sa, float ba
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const uint32_t afrag[4] = {pa[2 * m], pb[2 * m], pa[2 * m + 1], pb[2 * m + 1]};
-      mma_16816<F16>(acc, afrag, xw[h * 4 + m * 2], xw[h * 4 + m * 2 + 1]);
+      mma_16816<F16>(part[h * 2 + m], afrag, xw[h * 4 + m * 2], xw[h * 4 + m * 2 + 1]);
     }
   }
+  float acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
   constexpr float off = F16 ? 1024.f : 128.f;  // the code offset of the magic
   out[0] += sa * (acc[0] - off * x0) + ba * x0;
   out[1] += sa * (acc[1] - off * x1) + ba * x1;
@@ -154,12 +159,18 @@ struct DecFlags {
   int abort;
 };
 
-// Logits [T][E] (from the router, complete once this grid may read them)
-// into shared memory, every thread of the CTA loading in parallel.
-__device__ __forceinline__ void load_logits(const float* __restrict__ lg, float* dst, int n) {
-  for (int i = threadIdx.x; i < n / 4; i += blockDim.x)
-    reinterpret_cast<float4*>(dst)[i] = __ldcg(reinterpret_cast<const float4*>(lg) + i);
-  for (int i = (n & ~3) + threadIdx.x; i < n; i += blockDim.x) dst[i] = __ldcg(lg + i);
+// The plan (written by the router launch, complete once this grid may read
+// it) into shared memory: every slot is loaded in parallel with the count,
+// one round trip; returns the count (valid after the next __syncthreads).
+__device__ __forceinline__ int load_plan(const void* plan, DecSlot* slots, int* nslots_s) {
+  const DecPlan* p = static_cast<const DecPlan*>(plan);
+  constexpr int kWords = kMaxSlots * (int)sizeof(DecSlot) / 16;
+  const int4* src = reinterpret_cast<const int4*>(p->slot);
+  for (int i = threadIdx.x; i < kWords; i += blockDim.x)
+    reinterpret_cast<int4*>(slots)[i] = __ldcg(src + i);
+  if (threadIdx.x == 0) *nslots_s = min(max(__ldcg(&p->nslots), 1), kMaxSlots);
+  __syncthreads();
+  return *nslots_s;
 }
 
 // ======================================================= decode router
@@ -291,12 +302,44 @@ __global__ void __launch_bounds__(kDecRouterThreads) dec_router_kernel(const Dec
     const float sum = warp_sum(lo + hi);
     if (lane == 0) a.xsg[u] = sum;
   }
+  // the CTA that finishes last routes: every CTA makes its logits visible and
+  // counts itself done; the last one then sees every logit
+  __shared__ int s_last;
+  __shared__ __align__(16) float s_lg[kDecMaxRows * kMaxE];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < T * E; i += kDecRouterThreads) s_lg[i] = __ldcg(a.logits + i);
+  __syncthreads();
+  DecPlan* plan = static_cast<DecPlan*>(a.plan);
+  small_routing(s_lg, T, E, a.route.k, a.route.BM, plan->slot, &plan->nslots, &a.route,
+                a.route.status);
+  if (threadIdx.x == 0) *a.done = 0;  // back to zero for the next call
+}
+
+size_t decode_plan_bytes() { return sizeof(DecPlan); }
+
+// Shared memory as large as it goes on every SM that runs a decode kernel, so
+// that a CTA of the next kernel in the chain fits beside one of the current
+// kernel (an SM's L1/shared split is fixed while CTAs run on it).
+static void carveout_max(const void* kern) {
+  cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                       (int)cudaSharedmemCarveoutMaxShared);
 }
 
 cudaError_t launch_dec_router(const DecRouterArgs& a, bool norm, cudaStream_t s) {
   if (a.T < 1 || a.T > kDecMaxRows || a.d % 128 || a.d / 16 > 32 * kDecRouterWv || a.E > 256)
     return cudaErrorInvalidValue;
   const int grid = (a.E + kDecRouterEpb - 1) / kDecRouterEpb;
+  static bool attr_set = false;  // (idempotent: races only repeat the call)
+  if (!attr_set) {
+    carveout_max((const void*)dec_router_kernel<true>);
+    carveout_max((const void*)dec_router_kernel<false>);
+    attr_set = true;
+  }
   prof_begin(K_ROUTER_GEMV, s);
   const cudaError_t err =
       norm ? launch_pdl(dec_router_kernel<true>, dim3(grid), dim3(kDecRouterThreads), 0, s, a)
@@ -314,7 +357,7 @@ __host__ __device__ inline DecSmem gu_smem(int T, int E, int d, int nstages) {
   DecSmem m;
   const int G = d / 64;
   uint32_t off = 1024 + (uint32_t)nstages * gu_stage_bytes(d);  // alignment slack + stages
-  m.lg = off;    off += (uint32_t)(T * E * 4 + 15) & ~15u;
+  m.lg = 0;
   m.slots = off; off += (uint32_t)kMaxSlots * sizeof(DecSlot);
   m.xpg = off;   off += (uint32_t)T * G * 128;
   m.xsg = off;   off += (uint32_t)(T * G * 4 + 15) & ~15u;
@@ -327,7 +370,7 @@ __host__ __device__ inline DecSmem gu_smem(int T, int E, int d, int nstages) {
 __host__ __device__ inline DecSmem dn_smem(int T, int E, int F, int nstages) {
   DecSmem m;
   uint32_t off = 1024 + (uint32_t)nstages * dn_stage_bytes(F);
-  m.lg = off;    off += (uint32_t)(T * E * 4 + 15) & ~15u;
+  m.lg = 0;
   m.slots = off; off += (uint32_t)kMaxSlots * sizeof(DecSlot);
   m.xpg = m.xsg = 0;
   m.part = off;  off += kDnTileBytes;
@@ -358,7 +401,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   const uint32_t code_bytes = kDecUnitRows * (d / 2), sc_bytes = kDecUnitRows * G * 2;
   const DecSmem M = gu_smem(T, a.E, d, nstages);
   uint8_t* smem = base;  // stages at the start
-  float* lg_s = (float*)(base + (M.lg - 1024));
   DecSlot* slots = (DecSlot*)(base + (M.slots - 1024));
   uint32_t* xpg_s = (uint32_t*)(base + (M.xpg - 1024));
   float* xsg_s = (float*)(base + (M.xsg - 1024));
@@ -407,18 +449,13 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   const bool early = (int)blockIdx.x < nfb;
   if (early && threadIdx.x == 0) issue(blockIdx.x, a.E, 0);
 
-  pdl_wait();  // logits and x fragments come from the router
+  pdl_wait();  // the plan and x fragments come from the router
   pdl_trigger();
-  load_logits(a.logits, lg_s, T * a.E);
+  const int nslots = load_plan(a.plan, slots, nslots_s);
   for (int i = threadIdx.x; i < T * G * 8; i += kDecThreads)
     reinterpret_cast<uint4*>(xpg_s)[i] = __ldcg(reinterpret_cast<const uint4*>(a.xpg) + i);
   for (int i = threadIdx.x; i < T * G; i += kDecThreads) xsg_s[i] = __ldcg(a.xsg + i);
   __syncthreads();
-  if (threadIdx.x < kRouteThreads)
-    small_routing(lg_s, T, a.E, a.k, a.BM, slots, nslots_s, blockIdx.x == 0 ? &a.route : nullptr,
-                  a.status);
-  __syncthreads();
-  const int nslots = *nslots_s;
 
   if (warp == 0) {
     // ================================================= producer (one lane)
@@ -546,7 +583,6 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   const uint32_t code_bytes = kDecUnitRows * (F / 2), sc_bytes = kDecUnitRows * G * 2;
   const DecSmem M = dn_smem(T, a.E, F, nstages);
   uint8_t* smem = base;
-  float* lg_s = (float*)(base + (M.lg - 1024));
   DecSlot* slots = (DecSlot*)(base + (M.slots - 1024));
   float* ytile = (float*)(base + (M.part - 1024));
   uint64_t* full = (uint64_t*)(base + (M.bars - 1024));
@@ -568,12 +604,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     fence_mbar_init();
     prefetch_tensormap(&tm_d);
   }
-  load_logits(a.logits, lg_s, T * a.E);  // before the wait: see above
+  const int nslots = load_plan(a.plan, slots, nslots_s);  // before the wait: see above
   __syncthreads();
-  if (threadIdx.x < kRouteThreads)
-    small_routing(lg_s, T, a.E, a.k, a.BM, slots, nslots_s, nullptr, a.status);
-  __syncthreads();
-  const int nslots = *nslots_s;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -737,6 +769,12 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
   if (a.T < 1 || a.T > kDecMaxRows || a.d % 128 || a.F % 128 || a.E > kMaxE || a.k > kMaxK ||
       a.BM < kDecMaxRows || maxslots > kMaxSlots)
     return cudaErrorInvalidValue;
+  static bool attr_set = false;  // (idempotent: races only repeat the call)
+  if (!attr_set) {
+    carveout_max((const void*)dec_gateup_kernel);
+    carveout_max((const void*)dec_down_kernel);
+    attr_set = true;
+  }
   CUtensorMap tg, tu, td;
   if (!codes_map(&tg, a.gq, a.d / 2, (a.E + 1) * a.F) ||
       !codes_map(&tu, a.uq, a.d / 2, (a.E + 1) * a.F) ||

@@ -84,6 +84,8 @@ uint64_t route_wait_limit_ns();
 // order (xpg, [T][d/64][32] words) with its 64-group sums (xsg, [T][d/64]).
 // With `norm` x is the fp32 residual [T][d] of a layer stack and the scored
 // rows are bf16(rmsnorm(x, eps)); else x is bf16 [T][d].
+// Its last CTA to finish also routes the tokens: the routing outputs (route)
+// and the step's tile slots (plan: slot count, then the slots) for the GEMVs.
 struct DecRouterArgs {
   const void* x;
   const float* w;   // [E][d]
@@ -93,7 +95,11 @@ struct DecRouterArgs {
   float* xsg;
   float eps;
   int T, d, E;
+  RouteArgs route;
+  void* plan;       // decode plan (decode_plan_bytes())
+  uint32_t* done;   // zero-initialised counter of finished CTAs, returned to zero
 };
+size_t decode_plan_bytes();
 cudaError_t launch_dec_router(const DecRouterArgs& a, bool norm, cudaStream_t s);
 // Router on tensor cores for larger T: W split exactly into three bf16 terms
 // (w_split, [3][E][d]), fp32 partial logits per K-split (partial,
@@ -150,13 +156,11 @@ size_t gemm_smem_bytes(bool gateup, int BM, int K);
 int gemm_stages(bool gateup, int BM, int K);
 
 // ---------------------------------------------------------------- decode
-// The decode GEMVs (T <= 8) route from the router's logits themselves, in
-// each CTA's shared memory; CTA 0 of the gate/up launch also writes the
-// routing outputs (route: ids ... n_tiles; its logits fields are unused).
+// The decode GEMVs (T <= 8) read the step's tile slots from the plan the
+// router launch wrote.
 struct DecodeArgs {
   int T, E, k, d, F, BM, cap;
-  const float* logits;  // [T][E]
-  RouteArgs route;
+  const void* plan;     // the decode plan written by the router launch
   const uint8_t* gq; const uint16_t* gs; const uint16_t* gb;
   const uint8_t* uq; const uint16_t* us; const uint16_t* ub;
   const uint8_t* dq; const uint16_t* ds; const uint16_t* db;

@@ -123,6 +123,13 @@ struct DecSlot {
   float gate[kSlotRows];
 };
 constexpr int kMaxSlots = 1 + kSlotRows * kMaxK;  // T <= 8: P <= 64 routed tiles
+// Decode plan in global memory: the slot count, padded to 16 bytes, then the
+// slots (every DecSlot is 80 bytes, five 16-byte words).
+struct DecPlan {
+  int nslots, pad[3];
+  DecSlot slot[kMaxSlots];
+};
+static_assert(sizeof(DecSlot) == 80 && sizeof(DecPlan) % 16 == 0, "plan layout");
 
 // Routing of T <= 8 tokens by the first kRouteThreads threads of a CTA, from
 // the logits `lg` ([T][E], shared memory): the slots of the step into
