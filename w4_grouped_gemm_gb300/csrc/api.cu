@@ -231,6 +231,13 @@ int do_dec_router(const lily_moe_dims& d, const void* x, const lily_moe_weights*
   da.route = route_args(d, nullptr, r, ws);
   da.plan = base + L.plan;
   da.done = reinterpret_cast<uint32_t*>(base + L.ctrl) + 3;
+  // (routing-only calls may pass no expert weights: then nothing is prefetched)
+  const bool experts = w->gate_q && w->gate_s && w->gate_b && w->up_q && w->up_s && w->up_b &&
+                       w->down_q && w->down_s && w->down_b;
+  da.F = experts ? d.d_ff : 0;
+  da.gq = w->gate_q; da.gs = w->gate_s; da.gb = w->gate_b;
+  da.uq = w->up_q;   da.us = w->up_s;   da.ub = w->up_b;
+  da.dq = w->down_q; da.ds = w->down_s; da.db = w->down_b;
   return cuda_rc(launch_dec_router(da, norm, s));
 }
 

@@ -187,6 +187,24 @@ constexpr int kDecRouterThreads = 256;
 constexpr int kDecRouterEpb = 2;     // experts per CTA
 constexpr int kDecRouterWv = 8;      // float4 of a quarter row per lane: d <= 4096
 
+// Part `part` of `nparts` of expert e's weights (its nine arrays) into L2.
+__device__ __forceinline__ void prefetch_expert(const DecRouterArgs& a, int e, int part,
+                                                int nparts) {
+  const size_t n = (size_t)a.F * a.d;  // weights of one matrix
+  const void* base[9] = {a.gq + e * (n / 2), a.uq + e * (n / 2), a.dq + e * (n / 2),
+                         a.gs + e * (n / 64), a.gb + e * (n / 64), a.us + e * (n / 64),
+                         a.ub + e * (n / 64), a.ds + e * (n / 64), a.db + e * (n / 64)};
+#pragma unroll
+  for (int r = 0; r < 9; ++r) {
+    const size_t bytes = r < 3 ? n / 2 : n / 32;
+    const size_t chunk = ((bytes + nparts - 1) / nparts + 15) & ~(size_t)15;
+    const size_t off = (size_t)part * chunk;
+    if (off < bytes)
+      prefetch_l2(static_cast<const uint8_t*>(base[r]) + off,
+                  (uint32_t)(bytes - off < chunk ? bytes - off : chunk));
+  }
+}
+
 template <bool NORM>
 __global__ void __launch_bounds__(kDecRouterThreads) dec_router_kernel(const DecRouterArgs a) {
   __shared__ float s_part[kDecRouterEpb][4][kDecMaxRows];
@@ -199,6 +217,8 @@ __global__ void __launch_bounds__(kDecRouterThreads) dec_router_kernel(const Dec
   const bool has = e < E;
   const int nq4 = d / 16;  // float4 in a quarter row
   const float4* wq = reinterpret_cast<const float4*>(a.w + (size_t)(has ? e : 0) * d) + qd * nq4;
+  // the shared expert serves every token: its weights head for L2 at once
+  if (a.F > 0 && threadIdx.x == 0) prefetch_expert(a, E, blockIdx.x, gridDim.x);
   float4 wv[kDecRouterWv];
 #pragma unroll
   for (int i = 0; i < kDecRouterWv; ++i) {  // static: before the wait
@@ -318,6 +338,11 @@ __global__ void __launch_bounds__(kDecRouterThreads) dec_router_kernel(const Dec
   small_routing(s_lg, T, E, a.route.k, a.route.BM, plan->slot, &plan->nslots, &a.route,
                 a.route.status);
   if (threadIdx.x == 0) *a.done = 0;  // back to zero for the next call
+  // the routed experts' weights head for L2 now, while the expert GEMVs start
+  constexpr int kParts = 16;
+  const int nrouted = a.F > 0 ? plan->nslots - 1 : 0;
+  for (int i = threadIdx.x; i < nrouted * kParts; i += kDecRouterThreads)
+    prefetch_expert(a, plan->slot[1 + i / kParts].expert, i % kParts, kParts);
 }
 
 size_t decode_plan_bytes() { return sizeof(DecPlan); }

@@ -98,6 +98,13 @@ struct DecRouterArgs {
   RouteArgs route;
   void* plan;       // decode plan (decode_plan_bytes())
   uint32_t* done;   // zero-initialised counter of finished CTAs, returned to zero
+  // the experts' weights ([E+1] experts, d_ff F), prefetched into L2 as soon
+  // as the step's experts are known (the shared expert at the start); F = 0:
+  // no prefetch (expert pointers not given)
+  int F;
+  const uint8_t* gq; const uint16_t* gs; const uint16_t* gb;
+  const uint8_t* uq; const uint16_t* us; const uint16_t* ub;
+  const uint8_t* dq; const uint16_t* ds; const uint16_t* db;
 };
 size_t decode_plan_bytes();
 cudaError_t launch_dec_router(const DecRouterArgs& a, bool norm, cudaStream_t s);

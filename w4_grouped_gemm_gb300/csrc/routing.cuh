@@ -133,20 +133,21 @@ static_assert(sizeof(DecSlot) == 80 && sizeof(DecPlan) % 16 == 0, "plan layout")
 
 // Routing of T <= 8 tokens by the first kRouteThreads threads of a CTA, from
 // the logits `lg` ([T][E], shared memory): the slots of the step into
-// `slots` / *nslots (shared memory) and, when `out` is given, the routing
-// outputs (ids, gates, counts, offsets, perm, inv, block map, n_tiles) to
-// global memory.  Counts by counting, positions by counting the earlier pairs
-// of the same expert (stable by pair index), tiles of each expert in
-// ascending order.  Synchronises on named barrier 1 only, so the CTA's other
-// threads may be doing something else.
+// `slots` / *nslots and, when `out` is given, the routing outputs (ids,
+// gates, counts, offsets, perm, inv, block map, n_tiles) to global memory.
+// With T <= 8 <= BM every touched expert is exactly one tile, so everything
+// follows from counting over the P = T*k <= 64 pairs: pair p's row is
+// #{q : e_q < e_p} + #{q < p : e_q == e_p} (stable by pair index), the first
+// pair of an expert leads it, and its slot is 1 + the number of leaders of
+// smaller experts.  Synchronises on named barrier 1 only (three times).
+// BM (tile rows) is at least 16 > T, so it does not enter.
 __device__ __forceinline__ void small_routing(const float* lg, int T, int E, int k, int BM,
                                               DecSlot* slots, int* nslots, const RouteArgs* out,
                                               uint32_t* status) {
   __shared__ int s_e[kSlotRows * kMaxK];      // expert of pair p = t * k + j
   __shared__ float s_g[kSlotRows * kMaxK];    // its gate
   __shared__ int s_perm[kSlotRows * kMaxK];   // pair at sorted position
-  __shared__ int s_scan_tmp[8];
-  __shared__ int s_total;
+  __shared__ int s_lead[kSlotRows * kMaxK];   // 1 if pair p leads its expert
   const int P = T * k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp < T) {
@@ -171,60 +172,67 @@ __device__ __forceinline__ void small_routing(const float* lg, int T, int E, int
     }
   }
   named_sync(1, kRouteThreads);
-  // counts and offsets: thread e counts its pairs
-  const int e_me = threadIdx.x;  // kRouteThreads == kMaxE
-  int cnt = 0;
-  for (int p = 0; p < P; ++p) cnt += (s_e[p] == e_me);
-  if (e_me >= E) cnt = 0;
-  const int off_me = block_exclusive_scan<true>(cnt, s_scan_tmp);
-  const int ntile = (cnt + BM - 1) / BM;
-  const int toff = block_exclusive_scan<true>(ntile, s_scan_tmp);
-  if (e_me == kMaxE - 1) s_total = toff + ntile;
-  if (out) {
-    if (e_me < E) {
-      out->counts[e_me] = cnt;
-      out->offsets[e_me] = off_me;
-    }
-    if (e_me == 0) out->offsets[E] = P;
-  }
-  named_sync(1, kRouteThreads);
-  // pair p's position: its expert's offset + the earlier pairs of that expert
-  for (int p = threadIdx.x; p < P; p += kRouteThreads) {
+  // pair p: its row, whether it leads its expert (no earlier pair of it),
+  // and its expert's count
+  int p_pos = 0, p_cnt = 0;
+  const int p = threadIdx.x;
+  if (p < P) {
     const int e = s_e[p];
-    int r = 0;
-    for (int q = 0; q < p; ++q) r += (s_e[q] == e);
-    // the scan result of thread e is not visible here; recount the offset
-    int off = 0;
-    for (int q = 0; q < P; ++q) off += (s_e[q] < e);
-    const int pos = off + r;
-    s_perm[pos] = p;
-    if (out) {
-      out->perm[pos] = p;
-      out->inv[p] = pos;
+    int below = 0, before = 0, cnt = 0;
+    for (int q = 0; q < P; ++q) {
+      const int eq = s_e[q];
+      below += eq < e;
+      before += (eq == e) & (q < p);
+      cnt += eq == e;
     }
+    p_pos = below + before;
+    p_cnt = cnt;
+    s_perm[p_pos] = p;
+    s_lead[p] = before == 0;
+    if (out) {
+      out->perm[p_pos] = p;
+      out->inv[p] = p_pos;
+    }
+  }
+  // counts and offsets of every expert
+  if (out && threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int cnt = 0, off = 0;
+    for (int q = 0; q < P; ++q) {
+      cnt += s_e[q] == e;
+      off += s_e[q] < e;
+    }
+    out->counts[e] = cnt;
+    out->offsets[e] = off;
+    if (e == 0) out->offsets[E] = P;
   }
   named_sync(1, kRouteThreads);
-  // slots and block map: thread e writes its tiles; slot 0 = shared expert
-  const int total = s_total;
-  for (int i = 0; i < ntile; ++i) {
-    const int row0 = off_me + i * BM, rows = min(BM, cnt - i * BM);
-    DecSlot& sl = slots[1 + toff + i];
-    const int pr = min(rows, kSlotRows);
-    sl.expert = e_me;
+  // the leader of each expert writes its slot (and block-map tile): slot 1 +
+  // the number of leaders of smaller experts
+  int nlead = 0;
+  for (int q = 0; q < P; ++q) nlead += s_lead[q];
+  if (p < P && s_lead[p]) {
+    int leaders_below = 0;
+    for (int q = 0; q < P; ++q) leaders_below += (s_e[q] < s_e[p]) & s_lead[q];
+    const int p_slot = 1 + leaders_below;
+    DecSlot& sl = slots[p_slot];
+    const int row0 = p_pos;  // a leader is its expert's first row
+    const int rows = min(p_cnt, kSlotRows);
+    sl.expert = s_e[p];
     sl.row0 = row0;
-    sl.rows = pr;
+    sl.rows = rows;
     for (int n = 0; n < kSlotRows; ++n) {
-      const int p = n < pr ? s_perm[row0 + n] : 0;
-      sl.tok[n] = n < pr ? p / k : 0;
-      sl.gate[n] = n < pr ? s_g[p] : 0.f;
+      const int pp = n < rows ? s_perm[row0 + n] : 0;
+      sl.tok[n] = n < rows ? pp / k : 0;
+      sl.gate[n] = n < rows ? s_g[pp] : 0.f;
     }
     if (out) {
-      out->block_map[2 * (toff + i)] = e_me;
-      out->block_map[2 * (toff + i) + 1] = row0;
+      out->block_map[2 * (p_slot - 1)] = s_e[p];
+      out->block_map[2 * (p_slot - 1) + 1] = row0;
     }
   }
-  if (e_me == 0) {
-    *nslots = 1 + total;
+  if (threadIdx.x == 0) {
+    *nslots = 1 + nlead;
     DecSlot& sl = slots[0];
     sl.expert = E;
     sl.row0 = P;
@@ -233,10 +241,10 @@ __device__ __forceinline__ void small_routing(const float* lg, int T, int E, int
       sl.tok[n] = n < T ? n : 0;
       sl.gate[n] = n < T ? 1.f : 0.f;
     }
-    if (out) *out->n_tiles = total;
+    if (out) *out->n_tiles = nlead;
   }
   if (out)
-    for (int i = total + threadIdx.x; i < out->cap; i += kRouteThreads) {
+    for (int i = nlead + threadIdx.x; i < out->cap; i += kRouteThreads) {
       out->block_map[2 * i] = -1;
       out->block_map[2 * i + 1] = -1;
     }
