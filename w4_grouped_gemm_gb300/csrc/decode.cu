@@ -187,21 +187,22 @@ constexpr int kDecRouterThreads = 256;
 constexpr int kDecRouterEpb = 2;     // experts per CTA
 constexpr int kDecRouterWv = 8;      // float4 of a quarter row per lane: d <= 4096
 
-// Part `part` of `nparts` of expert e's weights (its nine arrays) into L2.
+// Part `part` of `nparts` of expert e's weights (its nine arrays) into L2,
+// one bulk prefetch per array (32-bit sizes: one matrix is at most 8 MB).
 __device__ __forceinline__ void prefetch_expert(const DecRouterArgs& a, int e, int part,
                                                 int nparts) {
-  const size_t n = (size_t)a.F * a.d;  // weights of one matrix
-  const void* base[9] = {a.gq + e * (n / 2), a.uq + e * (n / 2), a.dq + e * (n / 2),
-                         a.gs + e * (n / 64), a.gb + e * (n / 64), a.us + e * (n / 64),
-                         a.ub + e * (n / 64), a.ds + e * (n / 64), a.db + e * (n / 64)};
+  const uint32_t n = (uint32_t)a.F * (uint32_t)a.d;  // weights of one matrix
+  const size_t eo = (size_t)e * n;
+  const void* base[9] = {a.gq + eo / 2, a.uq + eo / 2, a.dq + eo / 2,
+                         a.gs + eo / 64, a.gb + eo / 64, a.us + eo / 64,
+                         a.ub + eo / 64, a.ds + eo / 64, a.db + eo / 64};
 #pragma unroll
   for (int r = 0; r < 9; ++r) {
-    const size_t bytes = r < 3 ? n / 2 : n / 32;
-    const size_t chunk = ((bytes + nparts - 1) / nparts + 15) & ~(size_t)15;
-    const size_t off = (size_t)part * chunk;
+    const uint32_t bytes = r < 3 ? n / 2 : n / 32;
+    const uint32_t chunk = ((bytes + (uint32_t)nparts - 1) / (uint32_t)nparts + 15u) & ~15u;
+    const uint32_t off = (uint32_t)part * chunk;
     if (off < bytes)
-      prefetch_l2(static_cast<const uint8_t*>(base[r]) + off,
-                  (uint32_t)(bytes - off < chunk ? bytes - off : chunk));
+      prefetch_l2(static_cast<const uint8_t*>(base[r]) + off, min(chunk, bytes - off));
   }
 }
 
@@ -338,11 +339,6 @@ __global__ void __launch_bounds__(kDecRouterThreads) dec_router_kernel(const Dec
   small_routing(s_lg, T, E, a.route.k, a.route.BM, plan->slot, &plan->nslots, &a.route,
                 a.route.status);
   if (threadIdx.x == 0) *a.done = 0;  // back to zero for the next call
-  // the routed experts' weights head for L2 now, while the expert GEMVs start
-  constexpr int kParts = 16;
-  const int nrouted = a.F > 0 ? plan->nslots - 1 : 0;
-  for (int i = threadIdx.x; i < nrouted * kParts; i += kDecRouterThreads)
-    prefetch_expert(a, plan->slot[1 + i / kParts].expert, i % kParts, kParts);
 }
 
 size_t decode_plan_bytes() { return sizeof(DecPlan); }
@@ -483,20 +479,26 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   __syncthreads();
 
   if (warp == 0) {
-    // ================================================= producer (one lane)
+    // ================================================= producer (warp 0)
+    // this CTA's items with a slot: it = blockIdx.x + u * gridDim.x < nslots * nfb
+    const int valid = nslots * nfb;
+    const int nmine = valid > (int)blockIdx.x ? (valid - (int)blockIdx.x + (int)gridDim.x - 1) /
+                                                    (int)gridDim.x
+                                              : 0;
+    const int first = nmine < nstages ? nmine : nstages;
+    // the first round of the ring: lane u issues item u (in parallel)
+    if (lane < first && !(early && lane == 0)) {
+      const int it = blockIdx.x + lane * gridDim.x;
+      issue(it, slots[it / nfb].expert, lane);
+    }
+    __syncwarp();
     if (lane == 0) {
-      uint32_t u = 0;
-      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const int slot = it / nfb;
-        if (slot >= nslots) break;  // items ascend by slot
+      uint32_t u = first;
+      for (; (int)u < nmine; ++u) {
+        const int it = blockIdx.x + u * gridDim.x;
         const uint32_t st = u % nstages;
-        if (!(early && it == (int)blockIdx.x)) {
-          if (u >= (uint32_t)nstages &&
-              !mbar_wait(smem_u32(&empty[st]), ((u / nstages) - 1) & 1, abort, a.status))
-            break;
-          issue(it, slots[slot].expert, st);
-        }
-        ++u;
+        if (!mbar_wait(smem_u32(&empty[st]), ((u / nstages) - 1) & 1, abort, a.status)) break;
+        issue(it, slots[it / nfb].expert, st);
       }
       if (*abort) {  // let the copies in flight land before the CTA exits
         int never = 0;
@@ -516,7 +518,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     if (slot >= nslots) break;
     const DecSlot& sl = slots[slot];
     const uint32_t st = u % nstages;
-    if (!warp_wait(smem_u32(&full[st]), (u / nstages) & 1, abort, a.status)) break;
+    if (!warp_wait_all(smem_u32(&full[st]), (u / nstages) & 1, abort, a.status)) break;
     // B column gi: slot row gi (zero beyond the slot's rows); accumulator
     // columns 2c, 2c+1 take their rows' group sums
     const int rows = sl.rows;
@@ -562,7 +564,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     // every consumer warp has read the stage and written its partials
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&cons[u & 1]));
-    if (!warp_wait(smem_u32(&cons[u & 1]), (u >> 1) & 1, abort, a.status)) break;
+    if (!warp_wait_all(smem_u32(&cons[u & 1]), (u >> 1) & 1, abort, a.status)) break;
     if (ct == 0) mbar_arrive(smem_u32(&empty[st]));
     if (ct < kDecUnitRows * kDecMaxRows) {
       const int row = ct >> 3, n = ct & 7;
@@ -633,41 +635,36 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   __syncthreads();
 
   if (warp == 0) {
+    // the weights of slot v into stage st
+    auto issue = [&](int v, uint32_t st) {
+      uint8_t* sp = smem + (size_t)st * SB;
+      const uint32_t fb = smem_u32(&full[st]);
+      mbar_arrive_expect_tx(fb, code_bytes + 2 * sc_bytes);
+      const int row0 = slots[v].expert * a.d + f0;
+      for (int b = 0; b < nbox; ++b)
+        tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_d, b * rb, row0, fb);
+      const size_t so = (size_t)row0 * G;
+      bulk_load(smem_u32(sp + code_bytes), a.ds + so, sc_bytes, fb);
+      bulk_load(smem_u32(sp + code_bytes + sc_bytes), a.db + so, sc_bytes, fb);
+    };
+    // the first round of the ring, before the wait: lane v issues slot v
+    const int first = nslots < nstages ? nslots : nstages;
+    if (lane < first) issue(lane, lane);
+    __syncwarp();
+    pdl_wait();
+    pdl_trigger();
     if (lane == 0) {
-      bool waited = false;
-      uint32_t v = 0;
-      for (; (int)v < nslots; ++v) {
+      int v = first;
+      for (; v < nslots; ++v) {
         const uint32_t st = v % nstages;
-        if (v >= (uint32_t)nstages) {
-          if (!waited) {
-            pdl_wait();
-            pdl_trigger();
-            waited = true;
-          }
-          if (!mbar_wait(smem_u32(&empty[st]), ((v / nstages) - 1) & 1, abort, a.status)) break;
-        }
-        uint8_t* sp = smem + (size_t)st * SB;
-        const uint32_t fb = smem_u32(&full[st]);
-        mbar_arrive_expect_tx(fb, code_bytes + 2 * sc_bytes);
-        const int row0 = slots[v].expert * a.d + f0;
-        for (int b = 0; b < nbox; ++b)
-          tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_d, b * rb, row0, fb);
-        const size_t so = (size_t)row0 * G;
-        bulk_load(smem_u32(sp + code_bytes), a.ds + so, sc_bytes, fb);
-        bulk_load(smem_u32(sp + code_bytes + sc_bytes), a.db + so, sc_bytes, fb);
-      }
-      if (!waited) {
-        pdl_wait();
-        pdl_trigger();
+        if (!mbar_wait(smem_u32(&empty[st]), ((v / nstages) - 1) & 1, abort, a.status)) break;
+        issue(v, st);
       }
       if (*abort) {
         int never = 0;
-        for (uint32_t k2 = (v > (uint32_t)nstages ? v - nstages : 0); k2 < v; ++k2)
+        for (int k2 = (v > nstages ? v - nstages : 0); k2 < v; ++k2)
           mbar_wait(smem_u32(&full[k2 % nstages]), (k2 / nstages) & 1, &never, a.status);
       }
-    } else {
-      pdl_wait();
-      pdl_trigger();
     }
     return;
   }
@@ -685,7 +682,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   for (int v = cw; v < nslots; v += kDecConsumers) {
     const DecSlot& sl = slots[v];
     const uint32_t st = v % nstages;
-    if (!warp_wait(smem_u32(&full[st]), (v / nstages) & 1, abort, a.status)) {
+    if (!warp_wait_all(smem_u32(&full[st]), (v / nstages) & 1, abort, a.status)) {
       ok = false;
       break;
     }
@@ -696,18 +693,30 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     const uint8_t* sp = smem + (size_t)st * SB;
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(sp + code_bytes);
     float o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int g0 = 0; g0 < G; g0 += 4) {
-      uint4 hh[4][2];
+    // H fragments of two groups at a time, the next two requested before the
+    // current two are used
+    constexpr int kHc = 2;
+    uint4 hh[kHc][2], hn[kHc][2];
+    auto load_h = [&](int g0, uint4 (&dst)[kHc][2]) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        hh[i][0] = hh[i][1] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < kHc; ++i) {
+        dst[i][0] = dst[i][1] = make_uint4(0, 0, 0, 0);
         if (g0 + i < G && gi < rows) {
-          hh[i][0] = __ldcg(reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64));
-          hh[i][1] = __ldcg(reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64 + 8));
+          dst[i][0] = __ldcg(reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64));
+          dst[i][1] = __ldcg(reinterpret_cast<const uint4*>(hrow + (g0 + i) * 64 + 8));
         }
       }
+    };
+    load_h(0, hn);
+    for (int g0 = 0; g0 < G; g0 += kHc) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kHc; ++i) {
+        hh[i][0] = hn[i][0];
+        hh[i][1] = hn[i][1];
+      }
+      if (g0 + kHc < G) load_h(g0 + kHc, hn);
+#pragma unroll
+      for (int i = 0; i < kHc; ++i) {
         const int g = g0 + i;
         if (g >= G) break;
         const uint32_t xw[8] = {hh[i][0].x, hh[i][0].y, hh[i][0].z, hh[i][0].w,
@@ -749,7 +758,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   if (!ok) return;
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(done));
-  if (!warp_wait(smem_u32(done), 0, abort, a.status)) return;
+  if (!warp_wait_all(smem_u32(done), 0, abort, a.status)) return;
   for (int i = ct; i < T * kDecUnitRows; i += 32 * kDecConsumers) {
     const int t = i / kDecUnitRows, f = i % kDecUnitRows;
     float acc = 0.f;
