@@ -93,11 +93,12 @@ __host__ __device__ __forceinline__ int hpair_pos(int j) {
 __host__ __device__ __forceinline__ int box_bytes(int row_bytes) {
   return row_bytes < 128 ? row_bytes : 128;
 }
-// Shared-memory offset of byte `off` of row r (0..15) of a unit.
-__device__ __forceinline__ uint32_t unit_off(int r, int off, int rb) {
-  const int box = off / rb, b = off % rb;
-  const int phase = rb == 128 ? (r & 7) : ((r >> 1) & 3);
-  return (uint32_t)(box * kDecUnitRows * rb + r * rb + ((((b >> 4) ^ phase)) << 4) + (b & 15));
+// Shared-memory offset of byte `off` of row r (0..15) of a unit whose boxes
+// have rows of 1 << rbs bytes (64 or 128): shifts and masks only.
+__device__ __forceinline__ uint32_t unit_off(int r, int off, int rbs) {
+  const int box = off >> rbs, b = off & ((1 << rbs) - 1);
+  const int phase = rbs == 7 ? (r & 7) : ((r >> 1) & 3);
+  return (uint32_t)(((box * kDecUnitRows + r) << rbs) + ((((b >> 4) ^ phase)) << 4) + (b & 15));
 }
 __host__ __device__ __forceinline__ uint32_t round1k(uint32_t v) { return (v + 1023u) & ~1023u; }
 // Gate/up stage: gate codes, up codes (16 rows x d/2 bytes each), then the
@@ -146,11 +147,11 @@ __device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, float sa, float ba
 }
 
 // Codes of rows gi and gi+8 for this lane's 16 K values of group g.
-__device__ __forceinline__ void unit_codes(const uint8_t* unit, int g, int gi, int c, int rb,
+__device__ __forceinline__ void unit_codes(const uint8_t* unit, int g, int gi, int c, int rbs,
                                            uint2& wa, uint2& wb) {
   const int off = g * 32 + c * 8;
-  wa = *reinterpret_cast<const uint2*>(unit + unit_off(gi, off, rb));
-  wb = *reinterpret_cast<const uint2*>(unit + unit_off(gi + 8, off, rb));
+  wa = *reinterpret_cast<const uint2*>(unit + unit_off(gi, off, rbs));
+  wb = *reinterpret_cast<const uint2*>(unit + unit_off(gi + 8, off, rbs));
 }
 
 
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int T = a.T, d = a.d, F = a.F, G = d / 64;
-  const int rb = box_bytes(d / 2), nbox = (d / 2) / rb;
+  const int rb = box_bytes(d / 2), nbox = (d / 2) / rb, rbs = rb == 128 ? 7 : 6;
   const uint32_t SB = gu_stage_bytes(d);
   const uint32_t code_bytes = kDecUnitRows * (d / 2), sc_bytes = kDecUnitRows * G * 2;
   const DecSmem M = gu_smem(T, a.E, d, nstages);
@@ -538,12 +539,12 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
       const float x0 = 2 * c < rows ? xsg_s[t0 * G + g] : 0.f;
       const float x1 = 2 * c + 1 < rows ? xsg_s[t1 * G + g] : 0.f;
       uint2 wa, wb;
-      unit_codes(sp, g, gi, c, rb, wa, wb);
+      unit_codes(sp, g, gi, c, rbs, wa, wb);
       group_mma<false>(wa, wb, bf16_bits_to_float(sc[gi * G + g]),
                        bf16_bits_to_float(sc[kDecUnitRows * G + gi * G + g]),
                        bf16_bits_to_float(sc[(gi + 8) * G + g]),
                        bf16_bits_to_float(sc[kDecUnitRows * G + (gi + 8) * G + g]), xw, x0, x1, og);
-      unit_codes(sp + code_bytes, g, gi, c, rb, wa, wb);
+      unit_codes(sp + code_bytes, g, gi, c, rbs, wa, wb);
       group_mma<false>(wa, wb, bf16_bits_to_float(sc[2 * kDecUnitRows * G + gi * G + g]),
                        bf16_bits_to_float(sc[3 * kDecUnitRows * G + gi * G + g]),
                        bf16_bits_to_float(sc[2 * kDecUnitRows * G + (gi + 8) * G + g]),
@@ -605,7 +606,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int T = a.T, F = a.F, G = F / 64;
-  const int rb = box_bytes(F / 2), nbox = (F / 2) / rb;
+  const int rb = box_bytes(F / 2), nbox = (F / 2) / rb, rbs = rb == 128 ? 7 : 6;
   const uint32_t SB = dn_stage_bytes(F);
   const uint32_t code_bytes = kDecUnitRows * (F / 2), sc_bytes = kDecUnitRows * G * 2;
   const DecSmem M = dn_smem(T, a.E, F, nstages);
@@ -733,7 +734,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
         const float x0 = __shfl_sync(0xffffffffu, xsum, (2 * c) * 4);
         const float x1 = __shfl_sync(0xffffffffu, xsum, (2 * c + 1) * 4);
         uint2 wa, wb;
-        unit_codes(sp, g, gi, c, rb, wa, wb);
+        unit_codes(sp, g, gi, c, rbs, wa, wb);
         group_mma<true>(wa, wb, bf16_bits_to_float(sc[gi * G + g]),
                         bf16_bits_to_float(sc[kDecUnitRows * G + gi * G + g]),
                         bf16_bits_to_float(sc[(gi + 8) * G + g]),

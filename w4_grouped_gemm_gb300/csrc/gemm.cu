@@ -68,7 +68,8 @@ __host__ __device__ constexpr int groups_per_step(bool /*gateup*/) { return 2; }
 // Tensor memory (512 columns x 128 lanes): accumulator sets first, then the
 // ring of dequantised A tiles (128 rows x 64 fp16 = 32 columns per matrix and
 // group).  A stage holds, per group, a 128-byte-swizzled tile of the token
-// rows (BM x 64 fp16) and the packed codes of each matrix (128 rows x 32 B).
+// rows (BM x 64 fp16), and per matrix the packed codes of the step's groups
+// (128 rows x 64 B, 64-byte swizzle).
 template <bool GATEUP, int BM>
 struct GemmLayout {
   static constexpr int kMats = GATEUP ? 2 : 1;
@@ -387,11 +388,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (elect_one()) {
           mbar_arrive_expect_tx(fb, tx_bytes);
 #pragma unroll
+          // the step's packed codes: one box of 128 rows x (KG * 32) bytes per matrix
+          tma_load_2d(st + BBYTES, &tm_q0, kk * KG * 32, wrow, fb);
+          if (GATEUP) tma_load_2d(st + BBYTES + KG * kPackedBytes, &tm_q1, kk * KG * 32, wrow, fb);
+#pragma unroll
           for (int g = 0; g < KG; ++g) {
             const int grp = kk * KG + g;
-            tma_load_2d(st + BBYTES + g * kPackedBytes, &tm_q0, grp * 32, wrow, fb);
-            if (GATEUP)
-              tma_load_2d(st + BBYTES + (KG + g) * kPackedBytes, &tm_q1, grp * 32, wrow, fb);
             for (int rb = 0; rb < nbox; ++rb)  // the tile's N rows
               tma_load_2d(st + g * L::kBTile + rb * L::kBoxRows * 128, tmb, grp * 64,
                           brow + rb * L::kBoxRows, fb);
@@ -543,19 +545,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ok = false;
           break;
         }
-        // the stage holds the codes with the 32-byte TMA swizzle: half h of
-        // row r sits at 16 * (h ^ sw), which spreads each 8 consecutive
+        // the stage holds a matrix's codes of the step as rows of 64 bytes
+        // (two groups) with the 64-byte TMA swizzle: 16-byte chunk c of row r
+        // sits at 16 * (c ^ ((r >> 1) & 3)), which spreads each 8 consecutive
         // lanes' loads over all eight 16-byte bank groups
-        const int sw = (r >> 2) & 1;
-        const uint8_t* pk0 = stage_base + (size_t)s0 * STAGE + BBYTES +
-                             (size_t)(mat * KG + g) * kPackedBytes + r * 32;
-        const uint8_t* pk1 = pk0 + kPackedBytes;  // gate/up: the step's second group
-        const uint4 lo0 = *reinterpret_cast<const uint4*>(pk0 + 16 * sw);
-        const uint4 hi0 = *reinterpret_cast<const uint4*>(pk0 + 16 * (sw ^ 1));
+        const int ph = (r >> 1) & 3;
+        const uint8_t* pk = stage_base + (size_t)s0 * STAGE + BBYTES +
+                            (size_t)mat * KG * kPackedBytes + r * (KG * 32);
+        const int c0 = 2 * g;  // down: this warp's group of the step
+        const uint4 lo0 = *reinterpret_cast<const uint4*>(pk + 16 * (c0 ^ ph));
+        const uint4 hi0 = *reinterpret_cast<const uint4*>(pk + 16 * ((c0 + 1) ^ ph));
         uint4 lo1 = lo0, hi1 = hi0;
-        if (GATEUP) {
-          lo1 = *reinterpret_cast<const uint4*>(pk1 + 16 * sw);
-          hi1 = *reinterpret_cast<const uint4*>(pk1 + 16 * (sw ^ 1));
+        if (GATEUP) {  // (g = 0) the step's second group
+          lo1 = *reinterpret_cast<const uint4*>(pk + 16 * (2 ^ ph));
+          hi1 = *reinterpret_cast<const uint4*>(pk + 16 * (3 ^ ph));
         }
         const uint32_t sbv0 = sbs[(mat * G + kk * KG + g) * 128 + r];
         const uint32_t sbv1 = GATEUP ? sbs[(mat * G + kk * KG + 1) * 128 + r] : sbv0;
@@ -820,15 +823,17 @@ static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const C
   }
 }
 
-// Packed codes: boxes of 128 rows x 32 bytes with the 32-byte swizzle (the
-// two 16-byte halves of row r swap places when bit 2 of r is set), so that the
-// dequant lanes' 16-byte loads are free of bank conflicts.
+// Packed codes: boxes of 128 rows x 64 bytes (the two quantisation groups of
+// a K-step) with the 64-byte swizzle (the four 16-byte chunks of row r are
+// permuted by XOR with (r >> 1) & 3), so that the dequant lanes' 16-byte
+// loads are free of bank conflicts; one copy per matrix and K-step.
+static_assert(groups_per_step(true) == 2 && groups_per_step(false) == 2, "64-byte code rows");
 static bool packed_map(CUtensorMap* tm, const uint8_t* q, int K, int rows) {
   uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)rows};
   uint64_t strides[1] = {(uint64_t)K / 2};
-  uint32_t box[2] = {32, 128};
+  uint32_t box[2] = {64, 128};
   return encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)q, dims, strides, box,
-                      CU_TENSOR_MAP_SWIZZLE_32B) == CUDA_SUCCESS;
+                      CU_TENSOR_MAP_SWIZZLE_64B) == CUDA_SUCCESS;
 }
 
 // Token rows per TMA box (GemmLayout::kBoxRows).
