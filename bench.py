@@ -347,8 +347,9 @@ class LayerRun:
         shape = synth.LayerShape(T, d, E, k, F)
         self.dims = lily.make_dims(T, d, E, k, F, args.tile_rows)
         # prefill weights are 455 MB a layer; decode touches ~16 MB a layer, so
-        # it rotates >= 16 layers to stay well above the 126 MB L2
-        self.nl = max(args.layers, 16) if self.decode else args.layers
+        # its timed runs rotate >= 16 layers to stay well above the 126 MB L2
+        # (eager runs, used for profiling, take --layers as given)
+        self.nl = max(args.layers, 16) if self.decode and not args.eager else args.layers
         self.layers = []
         for l in range(self.nl):
             inp = synth.make_layer(shape, layer_seed(l, rank), device=dev, zipf_s=wl["zipf"])
