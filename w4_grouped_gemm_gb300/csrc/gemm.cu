@@ -276,7 +276,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     w4_gemm_kernel(const __grid_constant__ CUtensorMap tm_q0,
                    const __grid_constant__ CUtensorMap tm_q1,
                    const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_b2, const GemmArgs a, const int nstages,
+                   const __grid_constant__ CUtensorMap tm_b2,
+                   const __grid_constant__ CUtensorMap tm_bw,
+                   const __grid_constant__ CUtensorMap tm_b2w, const GemmArgs a, const int nstages,
                    const int nsb) {
   using L = GemmLayout<GATEUP, BM>;
   constexpr int MATS = L::kMats;
@@ -340,6 +342,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (GATEUP) prefetch_tensormap(&tm_q1);
     prefetch_tensormap(&tm_b);
     if (GATEUP) prefetch_tensormap(&tm_b2);
+    if (BM > 64) {
+      prefetch_tensormap(&tm_bw);
+      if (GATEUP) prefetch_tensormap(&tm_b2w);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&misc[1]), L::kTmemCols);
@@ -371,10 +377,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int wrow = itm.expert * NOUT + itm.slice * 128;
       // token rows of the item: gate/up reads the expert-sorted copy xs (or,
       // for a shared-expert tile, x16 in token order); down reads H
-      const CUtensorMap* tmb = (GATEUP && itm.shared) ? &tm_b2 : &tm_b;
+      // a tile of more than 64 rows (BM 128) takes one 128-row box per group
+      const bool wide = BM > 64 && N > 64;
+      const CUtensorMap* tmb = (GATEUP && itm.shared) ? (wide ? &tm_b2w : &tm_b2)
+                                                      : (wide ? &tm_bw : &tm_b);
       const int brow = (GATEUP && itm.shared) ? itm.row0 - P : itm.row0;
-      const int nbox = (N + L::kBoxRows - 1) / L::kBoxRows;
-      const uint32_t tx_bytes = KG * (MATS * kPackedBytes + nbox * L::kBoxRows * 128);
+      const int box_rows = wide ? BM : L::kBoxRows;
+      const int nbox = wide ? 1 : (N + L::kBoxRows - 1) / L::kBoxRows;
+      const uint32_t tx_bytes = KG * (MATS * kPackedBytes + nbox * box_rows * 128);
       for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx;
         if (it >= (uint32_t)nstages &&
@@ -395,8 +405,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int g = 0; g < KG; ++g) {
             const int grp = kk * KG + g;
             for (int rb = 0; rb < nbox; ++rb)  // the tile's N rows
-              tma_load_2d(st + g * L::kBTile + rb * L::kBoxRows * 128, tmb, grp * 64,
-                          brow + rb * L::kBoxRows, fb);
+              tma_load_2d(st + g * L::kBTile + rb * box_rows * 128, tmb, grp * 64,
+                          brow + rb * box_rows, fb);
           }
         }
         __syncwarp();
@@ -786,7 +796,8 @@ CUresult encode_tiled(CUtensorMap* tm, CUtensorMapDataType dt, uint32_t rank, vo
 
 template <bool GATEUP, int BM>
 static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, const CUtensorMap& q1,
-                                  const CUtensorMap& b, const CUtensorMap& b2, cudaStream_t s) {
+                                  const CUtensorMap& b, const CUtensorMap& b2,
+                                  const CUtensorMap& bw, const CUtensorMap& b2w, cudaStream_t s) {
   const int K = GATEUP ? a.d : a.F;
   const int NOUT = GATEUP ? a.F : a.d;
   int nstages = 0, nsb = 0;
@@ -806,19 +817,21 @@ static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, cons
     num_sms = 148;
   const int grid = max_items < num_sms ? max_items : num_sms;  // persistent: one CTA per SM
   prof_begin(GATEUP ? K_GATEUP : K_DOWN, s);
-  err = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, s, q0, q1, b, b2, a, nstages, nsb);
+  err = launch_pdl(kern, dim3(grid), dim3(kGemmThreads), smem, s, q0, q1, b, b2, bw, b2w, a, nstages,
+                   nsb);
   prof_end(GATEUP ? K_GATEUP : K_DOWN, s);
   return err;
 }
 
 template <bool GATEUP>
 static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const CUtensorMap& q1,
-                               const CUtensorMap& b, const CUtensorMap& b2, cudaStream_t s) {
+                               const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& bw,
+                               const CUtensorMap& b2w, cudaStream_t s) {
   switch (a.BM) {
-    case 16: return launch_gemm_bm<GATEUP, 16>(a, q0, q1, b, b2, s);
-    case 32: return launch_gemm_bm<GATEUP, 32>(a, q0, q1, b, b2, s);
-    case 64: return launch_gemm_bm<GATEUP, 64>(a, q0, q1, b, b2, s);
-    case 128: return launch_gemm_bm<GATEUP, 128>(a, q0, q1, b, b2, s);
+    case 16: return launch_gemm_bm<GATEUP, 16>(a, q0, q1, b, b2, bw, b2w, s);
+    case 32: return launch_gemm_bm<GATEUP, 32>(a, q0, q1, b, b2, bw, b2w, s);
+    case 64: return launch_gemm_bm<GATEUP, 64>(a, q0, q1, b, b2, bw, b2w, s);
+    case 128: return launch_gemm_bm<GATEUP, 128>(a, q0, q1, b, b2, bw, b2w, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -913,22 +926,24 @@ cudaError_t launch_token_rows(const GemmArgs& a, const void* x, void* xs, void* 
 
 cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, const uint8_t* gq,
                           const uint8_t* uq, cudaStream_t s) {
-  CUtensorMap q0, q1, b, b2;
+  CUtensorMap q0, q1, b, b2, bw, b2w;
   const int P = a.T * a.k;
   if (!packed_map(&q0, gq, a.d, (a.E + 1) * a.F) || !packed_map(&q1, uq, a.d, (a.E + 1) * a.F) ||
       !f16_rows_map(&b, xs, a.d, P, box_rows(a.BM)) ||
-      !f16_rows_map(&b2, x16, a.d, a.T, box_rows(a.BM)))
+      !f16_rows_map(&b2, x16, a.d, a.T, box_rows(a.BM)) ||
+      !f16_rows_map(&bw, xs, a.d, P, a.BM) || !f16_rows_map(&b2w, x16, a.d, a.T, a.BM))
     return cudaErrorInvalidValue;
-  return launch_gemm<true>(a, q0, q1, b, b2, s);
+  return launch_gemm<true>(a, q0, q1, b, b2, bw, b2w, s);
 }
 
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
-  CUtensorMap q0, b;
+  CUtensorMap q0, b, bw;
   const int P = a.T * a.k;
   if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d) ||
-      !f16_rows_map(&b, a.H, a.F, P + a.T, box_rows(a.BM)))
+      !f16_rows_map(&b, a.H, a.F, P + a.T, box_rows(a.BM)) ||
+      !f16_rows_map(&bw, a.H, a.F, P + a.T, a.BM))
     return cudaErrorInvalidValue;
-  return launch_gemm<false>(a, q0, q0, b, b, s);
+  return launch_gemm<false>(a, q0, q0, b, b, bw, bw, s);
 }
 
 // Combine: y[t] = sum_j O[inv[t*k + j]] + O[P + t] (the k routed rows of
