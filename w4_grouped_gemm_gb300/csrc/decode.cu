@@ -174,6 +174,50 @@ __device__ __forceinline__ int load_plan(const void* plan, DecSlot* slots, int* 
   return *nslots_s;
 }
 
+// The slot plan, x in fragment order (nx 16-byte words) and the group sums
+// (nxs floats) into shared memory, with up to four words per thread in flight
+// before their stores (one round trip for the lot instead of one per array).
+__device__ __forceinline__ int load_plan_x(const void* plan, DecSlot* slots, int* nslots_s,
+                                           const uint4* xpg, uint4* xpg_s, int nx,
+                                           const float* xsg, float* xsg_s, int nxs) {
+  const DecPlan* p = static_cast<const DecPlan*>(plan);
+  constexpr int kWords = kMaxSlots * (int)sizeof(DecSlot) / 16;
+  const int4* src = reinterpret_cast<const int4*>(p->slot);
+  const int n = kWords + nx, nt = blockDim.x, tid = threadIdx.x;
+  for (int base = 0; base < n; base += 4 * nt) {
+    int4 v[4];
+    float xs = 0.f;
+    int ns = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * nt + tid;
+      if (i < kWords)
+        v[u] = __ldcg(src + i);
+      else if (i < n)
+        v[u] = __ldcg(reinterpret_cast<const int4*>(xpg) + (i - kWords));
+    }
+    if (base == 0) {
+      if (tid < nxs) xs = __ldcg(xsg + tid);
+      if (tid == 0) ns = __ldcg(&p->nslots);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * nt + tid;
+      if (i < kWords)
+        reinterpret_cast<int4*>(slots)[i] = v[u];
+      else if (i < n)
+        reinterpret_cast<int4*>(xpg_s)[i - kWords] = v[u];
+    }
+    if (base == 0) {
+      if (tid < nxs) xsg_s[tid] = xs;
+      if (tid == 0) *nslots_s = min(max(ns, 1), kMaxSlots);
+    }
+  }
+  for (int i = tid + nt; i < nxs; i += nt) xsg_s[i] = __ldcg(xsg + i);
+  __syncthreads();
+  return *nslots_s;
+}
+
 // ======================================================= decode router
 // Logits of T <= 8 rows: CTA b scores experts 2b and 2b+1, four warps per
 // expert, each over a quarter of d, with its quarter of the weight row
@@ -405,9 +449,9 @@ __host__ __device__ inline DecSmem dn_smem(int T, int E, int F, int nstages) {
 // Work item = (tile slot, 16 rows of F) for both matrices; item i runs on
 // CTA i % grid.  The first item of CTAs 0 .. F/16-1 belongs to the shared
 // expert (slot 0), which needs no routing: its weights are requested before
-// the wait for the router.  Then every CTA loads the logits and x fragments,
-// routes the T <= 8 tokens in its own shared memory (CTA 0 also writes the
-// routing outputs) and streams its items' weights through a ring of stages.
+// the wait for the router.  Then every CTA loads the slot plan (written by
+// the router's last CTA) and the x fragments, and streams its items'
+// weights through a ring of stages, one 3-D copy per matrix and item.
 // Per item each consumer warp takes the groups g = warp, warp + 8, ... of
 // both matrices; the eight partial 16 x 8 results are summed in a fixed order
 // and H = silu(g) * u is written as fp16 in the pair order the down GEMV reads.
@@ -418,7 +462,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int T = a.T, d = a.d, F = a.F, G = d / 64;
-  const int rb = box_bytes(d / 2), nbox = (d / 2) / rb, rbs = rb == 128 ? 7 : 6;
+  const int rb = box_bytes(d / 2), rbs = rb == 128 ? 7 : 6;
   const uint32_t SB = gu_stage_bytes(d);
   const uint32_t code_bytes = kDecUnitRows * (d / 2), sc_bytes = kDecUnitRows * G * 2;
   const DecSmem M = gu_smem(T, a.E, d, nstages);
@@ -457,10 +501,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     const uint32_t fb = smem_u32(&full[st]);
     mbar_arrive_expect_tx(fb, 2 * code_bytes + 4 * sc_bytes);
     const int row0 = expert * F + (it % nfb) * kDecUnitRows;
-    for (int b = 0; b < nbox; ++b) {
-      tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_g, b * rb, row0, fb);
-      tma_load_2d(smem_u32(sp + code_bytes + b * kDecUnitRows * rb), &tm_u, b * rb, row0, fb);
-    }
+    tma_load_3d(smem_u32(sp), &tm_g, 0, row0, 0, fb);
+    tma_load_3d(smem_u32(sp + code_bytes), &tm_u, 0, row0, 0, fb);
     const size_t so = (size_t)row0 * G;
     bulk_load(smem_u32(sp + 2 * code_bytes), a.gs + so, sc_bytes, fb);
     bulk_load(smem_u32(sp + 2 * code_bytes + sc_bytes), a.gb + so, sc_bytes, fb);
@@ -473,11 +515,8 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
 
   pdl_wait();  // the plan and x fragments come from the router
   pdl_trigger();
-  const int nslots = load_plan(a.plan, slots, nslots_s);
-  for (int i = threadIdx.x; i < T * G * 8; i += kDecThreads)
-    reinterpret_cast<uint4*>(xpg_s)[i] = __ldcg(reinterpret_cast<const uint4*>(a.xpg) + i);
-  for (int i = threadIdx.x; i < T * G; i += kDecThreads) xsg_s[i] = __ldcg(a.xsg + i);
-  __syncthreads();
+  const int nslots = load_plan_x(a.plan, slots, nslots_s, reinterpret_cast<const uint4*>(a.xpg),
+                                 reinterpret_cast<uint4*>(xpg_s), T * G * 8, a.xsg, xsg_s, T * G);
 
   if (warp == 0) {
     // ================================================= producer (warp 0)
@@ -606,7 +645,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const int T = a.T, F = a.F, G = F / 64;
-  const int rb = box_bytes(F / 2), nbox = (F / 2) / rb, rbs = rb == 128 ? 7 : 6;
+  const int rb = box_bytes(F / 2), rbs = rb == 128 ? 7 : 6;
   const uint32_t SB = dn_stage_bytes(F);
   const uint32_t code_bytes = kDecUnitRows * (F / 2), sc_bytes = kDecUnitRows * G * 2;
   const DecSmem M = dn_smem(T, a.E, F, nstages);
@@ -642,8 +681,7 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
       const uint32_t fb = smem_u32(&full[st]);
       mbar_arrive_expect_tx(fb, code_bytes + 2 * sc_bytes);
       const int row0 = slots[v].expert * a.d + f0;
-      for (int b = 0; b < nbox; ++b)
-        tma_load_2d(smem_u32(sp + b * kDecUnitRows * rb), &tm_d, b * rb, row0, fb);
+      tma_load_3d(smem_u32(sp), &tm_d, 0, row0, 0, fb);
       const size_t so = (size_t)row0 * G;
       bulk_load(smem_u32(sp + code_bytes), a.ds + so, sc_bytes, fb);
       bulk_load(smem_u32(sp + code_bytes + sc_bytes), a.db + so, sc_bytes, fb);
@@ -776,12 +814,17 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
 }
 
 // ---------------------------------------------------------------- host side
+// Packed codes of 16-row units as one copy: the rows of a unit cut into
+// chunks of rb bytes (the swizzle span), chunk-major in shared memory (chunk
+// b's 16 rows at b * 16 * rb), i.e. the layout of one 16 x rb box per chunk,
+// with the same swizzle phase (row index mod 8), from a single 3-D copy:
+// dimensions (byte within the chunk, row, chunk) with strides (row_bytes, rb).
 static bool codes_map(CUtensorMap* tm, const uint8_t* q, int row_bytes, int rows) {
   const int rb = box_bytes(row_bytes);
-  uint64_t dims[2] = {(uint64_t)row_bytes, (uint64_t)rows};
-  uint64_t strides[1] = {(uint64_t)row_bytes};
-  uint32_t box[2] = {(uint32_t)rb, (uint32_t)kDecUnitRows};
-  return encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)q, dims, strides, box,
+  uint64_t dims[3] = {(uint64_t)rb, (uint64_t)rows, (uint64_t)(row_bytes / rb)};
+  uint64_t strides[2] = {(uint64_t)row_bytes, (uint64_t)rb};
+  uint32_t box[3] = {(uint32_t)rb, (uint32_t)kDecUnitRows, (uint32_t)(row_bytes / rb)};
+  return encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)q, dims, strides, box,
                       rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) ==
          CUDA_SUCCESS;
 }

@@ -3,35 +3,40 @@
 // The expert GEMMs take about 90% of prefill time (page "Revolutionizing Local
 // AI Inference on Apple Silicon", section "Enhanced Tile and Scan
 // Operations").  Weights stay 4-bit in HBM; each CTA streams one 128-row slice
-// of one expert's packed codes with TMA, rebuilds it as fp16 one K-step at a
-// time in tensor memory (w = scale*q + bias), and feeds tcgen05
-// MMAs that accumulate in FP32 in tensor memory, so the expanded weights never
-// reach HBM (page "Lily Beats MLX-LM 1.35x on Decode: Perplexity's Rust+Metal
-// Engine for Apple Silicon", section "Prefill: fusing dequantisation and
-// keeping routing GPU-resident").
+// of packed codes with TMA, rebuilds it as fp16 one K-step at a time in tensor
+// memory (w = scale*q + bias), and feeds tcgen05 MMAs that accumulate in FP32
+// in tensor memory, so the expanded weights never reach HBM (page "Lily Beats
+// MLX-LM 1.35x on Decode: Perplexity's Rust+Metal Engine for Apple Silicon",
+// section "Prefill: fusing dequantisation and keeping routing GPU-resident").
 //
 // Operand roles (weights as the M=128 operand, token rows as N):
-//   A = dequantised weight slice, 128 output features x 64 K per group, fp16,
-//       in tensor memory (lane = feature, two K elements per 32-bit column),
-//       written by the dequant warps with tcgen05.st
+//   A = dequantised weight slice, 128 rows x 64 K per group, fp16, in tensor
+//       memory (lane = weight row, two K elements per 32-bit column), written
+//       by the dequant warps with tcgen05.st.  Gate/up: an item covers 64
+//       features of both matrices; the 32 rows of TMEM lane quadrant q are
+//       the gate rows of features 16q..16q+15, then the up rows of the same
+//       features, so one MMA computes both projections of a feature, an item
+//       needs one accumulator of N columns (two items' accumulators and a
+//       deep A ring fit in tensor memory), and each epilogue warp finds the
+//       gate and up outputs of its features in its own quadrant.  Down: 128
+//       output features.
 //   B = token rows of one block-map tile (<= BM rows) x 64 K, fp16, K-major,
-//       128-byte swizzle, brought by TMA in boxes of up to 64 rows: gate/up
-//       reads xs,
-//       the fp16 rows of x in expert-sorted order written once per layer by
-//       token_rows_kernel (one pass instead of a TMA gather per K-step);
-//       down reads rows of H
+//       128-byte swizzle, brought by TMA in boxes of up to 64 rows (one
+//       128-row box when a BM 128 tile holds more than 64 rows): gate/up
+//       reads xs, the fp16 rows of x in expert-sorted order written once per
+//       layer by token_rows_kernel (one pass instead of a TMA gather per
+//       K-step); down reads rows of H
 //   D = 128 x N fp32 in TMEM
 // Operand precision: fp16 rather than the pages' bf16.  Rounding the
 // rebuilt weights and H to bf16 alone puts the layer outside max|err| <= 2e-2
 // of rms on these weight distributions; fp16 is 8x finer, runs at the same
 // kind::f16 tensor rate, and holds x, the group scales and biases exactly in
 // [2^-17, 65504] (values beyond 65504 set LILY_STATUS_F16_RANGE).
-// Epilogues: gate/up writes H = w * silu(g) * u (fp16) in expert-sorted row
-// order, w the row's routing gate (1 for shared-expert rows), so the down
-// GEMM's output rows come out already weighted; down stages each row's 128
-// outputs of a slice in shared memory and adds them into the fp32
-// token-order accumulator with bulk reductions (cp.reduce.async.bulk), one
-// 128-byte line per operation.
+// Epilogues: gate/up writes H = silu(g) * u (fp16) in expert-sorted row
+// order; down writes its output rows as fp16 rows O (same order), staged
+// through shared memory so that each lane stores 64 contiguous bytes of one
+// row, and combine_kernel then sums each token's k + 1 rows, weighted by the
+// routing gates, in a fixed order (the same bits on every run).
 // K order: the rebuilt weights come out of the nibble extraction with each
 // 8-element K chunk in the order (0,4,1,5,2,6,3,7); the K operands x16 and H
 // are stored in that same order, so no shuffle is needed.
@@ -46,18 +51,21 @@ namespace lily {
 // Warp roles.  Warp 0: TMA producer.  Warp 1: TMEM owner + MMA issuer (one
 // thread).  Warps 2..9: dequant (one 128-row weight slice per K-step), which
 // write the rebuilt weights straight into tensor memory (tcgen05.st): each
-// warp owns the TMEM lane quadrant warp % 4, i.e. weight rows 32*(warp%4)..+31.
-// Warps 10..13: epilogue (TMEM -> global), overlapped with the next item's
-// main loop through double-buffered accumulators; the epilogue warps also
-// fill the next item's scale/bias table ahead of the dequant warps.
+// warp owns the TMEM lane quadrant warp % 4, i.e. weight rows 32*(warp%4)..+31;
+// warps 2..5 rebuild both quantisation groups of the even K-steps (of the
+// CTA's running step count), 6..9 those of the odd ones, so two steps are
+// rebuilt at once and each step is published by one set of four warps.  Warps 10..13: epilogue (TMEM -> global), overlapped with the next
+// item's main loop through double-buffered accumulators; the epilogue warps
+// also fill the next item's scale/bias table ahead of the dequant warps
+// (gate/up; the down dequant lanes fill their own rows).
 constexpr int kNumDequantWarps = 8;
 constexpr int kNumEpiWarps = 4;
 constexpr int kEpiWarp0 = 2 + kNumDequantWarps;
 constexpr int kGemmThreads = 32 * (2 + kNumDequantWarps + kNumEpiWarps);  // 448
 constexpr int kMaxStages = 12;
 constexpr int kPackedBytes = 128 * 32;  // 128 rows x 64 4-bit codes
-constexpr int kMaxA = 4;                // dequantised-A ring depth (TMEM)
-constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 9;
+constexpr int kMaxA = 8;                // dequantised-A ring depth in K-steps (TMEM)
+constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 4 + 4 + 1;
 
 // Quantisation groups (64 K each) per K-step, two in both GEMMs: the fixed
 // per-step hand-offs of every warp role (the producer's expect-tx and copies,
@@ -65,28 +73,28 @@ constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 9;
 // store wait and arrival) are paid once per 128 K.
 __host__ __device__ constexpr int groups_per_step(bool /*gateup*/) { return 2; }
 
-// Tensor memory (512 columns x 128 lanes): accumulator sets first, then the
-// ring of dequantised A tiles (128 rows x 64 fp16 = 32 columns per matrix and
-// group).  A stage holds, per group, a 128-byte-swizzled tile of the token
-// rows (BM x 64 fp16), and per matrix the packed codes of the step's groups
-// (128 rows x 64 B, 64-byte swizzle).
+// Tensor memory (512 columns x 128 lanes): two accumulator sets of N <= BM
+// columns, then the ring of dequantised A tiles (128 rows x 128 fp16 = 64
+// columns per K-step).  A stage holds, per group, a 128-byte-swizzled tile of
+// the token rows (BM x 64 fp16), and the packed codes of the step's 128
+// weight rows (128 rows x 64 B, 64-byte swizzle; gate/up: the 64 gate rows of
+// the slice, then its 64 up rows).
 template <bool GATEUP, int BM>
 struct GemmLayout {
-  static constexpr int kMats = GATEUP ? 2 : 1;
   static constexpr int kGroups = groups_per_step(GATEUP);
   static constexpr int kBTile = BM * 128;  // token rows of one group
   // token rows per TMA box: fewer, taller boxes per step (the rows past an
   // item's last are other tiles' rows or zero fill, never stored)
   static constexpr int kBoxRows = BM < 64 ? BM : 64;
   static constexpr int kBBytes = kGroups * kBTile;
-  static constexpr int kStage = kBBytes + kMats * kGroups * kPackedBytes;
-  static constexpr int kACols = 32 * kGroups;  // one matrix's A tile
-  static constexpr int kAccCols = GATEUP ? 2 * BM : BM;  // one accumulator set
-  static constexpr int kNumAcc = (GATEUP ? BM <= 64 : BM <= 128) ? 2 : 1;
+  static constexpr int kStage = kBBytes + kGroups * kPackedBytes;
+  static constexpr int kOutRows = GATEUP ? 64 : 128;  // output features per item (and matrix)
+  static constexpr int kACols = 32 * kGroups;          // A tile of one K-step
+  static constexpr int kAccCols = BM;                  // one accumulator set
+  static constexpr int kNumAcc = 2;
   static constexpr int kAOff = kNumAcc * kAccCols;
-  static constexpr int kNumA = (512 - kAOff) / (kMats * kACols) < kMaxA
-                                   ? (512 - kAOff) / (kMats * kACols)
-                                   : kMaxA;
+  static constexpr int kNumA =
+      (512 - kAOff) / kACols < kMaxA ? (512 - kAOff) / kACols : kMaxA;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kNumA >= 2, "tensor memory too small for the A ring");
 };
@@ -97,27 +105,35 @@ struct GemmLayout {
 constexpr int kEpiRowHalves = 40;
 constexpr int kEpiStageBytes = kNumEpiWarps * 32 * kEpiRowHalves * 2;
 
-__host__ __device__ inline size_t gemm_fixed_bytes(int mats, int BM, int K, int nsb) {
+// Gate/up: weight row r of an item (= TMEM lane r) is row code_row(r) of the
+// step's code tile (64 gate rows, then 64 up rows): matrix (r >> 4) & 1 and
+// feature 16 * (r >> 5) + (r & 15) of the item's 64.
+__host__ __device__ constexpr int gu_matrix(int r) { return (r >> 4) & 1; }
+__host__ __device__ constexpr int gu_feature(int r) { return 16 * (r >> 5) + (r & 15); }
+__host__ __device__ constexpr int gu_code_row(int r) { return 64 * gu_matrix(r) + gu_feature(r); }
+
+__host__ __device__ inline size_t gemm_fixed_bytes(bool gateup, int BM, int K, int nsb) {
   const int G = K / 64;
-  return 1024                                  // alignment slack
-         + (size_t)nsb * mats * G * 128 * 4    // scale/bias tables (one per item in flight)
-         + (mats == 1 ? kEpiStageBytes : 0)  // down: epilogue staging
-         + kNumBars * 8                        // mbarriers
-         + 16;                                 // abort flag, TMEM address
+  return 1024                                    // alignment slack
+         + (size_t)nsb * G * 128 * 4             // scale/bias tables (one per item in flight)
+         + (gateup ? 0 : kEpiStageBytes)          // down: epilogue staging
+         + kNumBars * 8                          // mbarriers
+         + 16;                                   // abort flag, TMEM address
 }
 
 size_t gemm_stage_bytes(bool gateup, int BM) {
   const int kg = groups_per_step(gateup);
-  return (size_t)kg * ((size_t)BM * 128 + (gateup ? 2 : 1) * kPackedBytes);
+  return (size_t)kg * ((size_t)BM * 128 + kPackedBytes);
 }
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
 
-// Pipeline depth and scale-table buffering that fit in shared memory: two
-// scale tables (the next item's is filled while the current one is in use)
-// when that still leaves >= 3 stages, else one table.
+// Pipeline depth and scale-table buffering that fit in shared memory.
+// Gate/up: two scale tables (the next item's is filled while the current one
+// is in use) when that still leaves >= 3 stages, else one table.  Down: two
+// tables always, one per dequant warp set.
 static int stages_for(bool gateup, int BM, int K, int nsb) {
-  const size_t fixed = gemm_fixed_bytes(gateup ? 2 : 1, BM, K, nsb);
+  const size_t fixed = gemm_fixed_bytes(gateup, BM, K, nsb);
   if (fixed >= kSmemLimit) return 0;
   int s = (int)((kSmemLimit - fixed) / gemm_stage_bytes(gateup, BM));
   return s > kMaxStages ? kMaxStages : s;
@@ -125,13 +141,13 @@ static int stages_for(bool gateup, int BM, int K, int nsb) {
 
 void gemm_config(bool gateup, int BM, int K, int* stages, int* nsb) {
   const int s2 = stages_for(gateup, BM, K, 2);
-  if (s2 >= 3) {
+  if (s2 >= 3 || (!gateup && s2 >= 2)) {  // down: one table per dequant warp set
     *stages = s2;
     *nsb = 2;
     return;
   }
   const int s1 = stages_for(gateup, BM, K, 1);
-  *stages = s1 >= 2 ? s1 : 0;
+  *stages = (gateup && s1 >= 2) ? s1 : 0;
   *nsb = 1;
 }
 
@@ -144,7 +160,7 @@ int gemm_stages(bool gateup, int BM, int K) {
 size_t gemm_smem_bytes(bool gateup, int BM, int K) {
   int s, n;
   gemm_config(gateup, BM, K, &s, &n);
-  return gemm_fixed_bytes(gateup ? 2 : 1, BM, K, n) + (size_t)s * gemm_stage_bytes(gateup, BM);
+  return gemm_fixed_bytes(gateup, BM, K, n) + (size_t)s * gemm_stage_bytes(gateup, BM);
 }
 
 // Position in a ring of n slots: slot index and the parity of its use count
@@ -159,10 +175,11 @@ struct Ring {
   }
 };
 
-// One work item = one block-map tile (or shared-expert tile) x one 128-row
-// slice of the weight matrix.  Items are numbered tile-major so the slices of
-// one tile, and the tiles of one expert, run at the same time and share the
-// expert's weights and token rows through L2.  Shared-expert tiles come first.
+// One work item = one block-map tile (or shared-expert tile) x one slice of
+// output features (gate/up: 64 features of both matrices; down: 128).  Items
+// are numbered tile-major so the slices of one tile, and the tiles of one
+// expert, run at the same time and share the expert's weights and token rows
+// through L2.  Shared-expert tiles come first.
 struct Item {
   int expert, row0, rows, slice;
   bool shared;
@@ -181,51 +198,44 @@ __device__ __forceinline__ bool item_from(int4 t, int w, int nslices, int nsh, I
   it.rows = t.z;
   return t.z > 0;
 }
-template <int BM>
-__device__ __forceinline__ bool get_item(const GemmArgs& a, int w, int nslices, int nsh, int P,
-                                         Item& it) {
-  return item_from(load_tile(a, w, nslices), w, nslices, nsh, it);
-}
 
 // Advance w (stepping by gridDim.x) to the next valid item; false at the end.
-template <int BM>
 __device__ __forceinline__ bool next_item(const GemmArgs& a, int& w, int n_items, int nslices,
-                                          int nsh, int P, Item& it) {
+                                          int nsh, Item& it) {
   for (; w < n_items; w += gridDim.x)
-    if (get_item<BM>(a, w, nslices, nsh, P, it)) return true;
+    if (item_from(load_tile(a, w, nslices), w, nslices, nsh, it)) return true;
   return false;
 }
 
-// Scale/bias table of one item: sb[mat][g][r] = (fp16 scale | fp16 bias << 16)
-// for the item's 128 weight rows r and every group g.  Filled by the epilogue
-// threads, thread r owning row r: 16-byte loads of 8 scales and the 8
-// matching biases, one f16x2 conversion and one 4-byte store per group.
-template <int MATS>
-__device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint32_t* sbw) {
+// One scale-table word: fp16(scale) | fp16(bias) << 16 from bf16 bit patterns.
+__device__ __forceinline__ uint32_t sb_word(uint16_t sc, uint16_t bi) {
+  return (uint32_t)bf16_to_f16_bits(sc) | ((uint32_t)bf16_to_f16_bits(bi) << 16);
+}
+
+// Scale/bias table of one gate/up item: sb[g][r] = (fp16 scale | fp16 bias <<
+// 16) of weight row r (see gu_code_row) and every group g.
+// Filled by the epilogue threads, thread r owning row r (`row` = its matrix
+// row, `sp`/`bp` = its matrix's scales and biases): 16-byte loads of 8 scales
+// and the 8 matching biases (two such pairs in flight), one f16x2 conversion
+// and one 4-byte store per group.
+__device__ void scale_fill(const uint16_t* sp, const uint16_t* bp, size_t row, int G, int r,
+                           uint32_t* sbw) {
   if ((G & 7) == 0) {
-    const int per = G / 8;
-    const int npair = MATS * per;  // (matrix, 8-group chunk) pairs
-    for (int base = 0; base < npair; base += 4) {
-      uint4 vs[4], vb[4];
+    const int nch = G / 8;
+    for (int base = 0; base < nch; base += 2) {
+      uint4 vs[2], vb[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int q = base + j;
-        if (q < npair) {
-          const int mat = q / per, ch = q % per;
-          const uint16_t* sp = (mat == 0 ? a.s0 : a.s1) + row * G + ch * 8;
-          const uint16_t* bp = (mat == 0 ? a.b0 : a.b1) + row * G + ch * 8;
-          vs[j] = __ldg(reinterpret_cast<const uint4*>(sp));
-          vb[j] = __ldg(reinterpret_cast<const uint4*>(bp));
+      for (int j = 0; j < 2; ++j)
+        if (base + j < nch) {
+          vs[j] = __ldg(reinterpret_cast<const uint4*>(sp + row * G) + base + j);
+          vb[j] = __ldg(reinterpret_cast<const uint4*>(bp + row * G) + base + j);
         }
-      }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int q = base + j;
-        if (q < npair) {
-          const int mat = q / per, ch = q % per;
+      for (int j = 0; j < 2; ++j)
+        if (base + j < nch) {
           const uint32_t ws[4] = {vs[j].x, vs[j].y, vs[j].z, vs[j].w};
           const uint32_t wb[4] = {vb[j].x, vb[j].y, vb[j].z, vb[j].w};
-          uint32_t* dst = sbw + (size_t)(mat * G + ch * 8) * 128 + r;
+          uint32_t* dst = sbw + (size_t)((base + j) * 8) * 128 + r;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {  // groups 2u (low halves) and 2u+1 (high halves)
             const __half2 lo = __floats2half2_rn(__uint_as_float(ws[u] << 16),
@@ -236,38 +246,11 @@ __device__ void scale_fill(const GemmArgs& a, size_t row, int G, int r, uint32_t
             dst[(2 * u + 1) * 128] = *reinterpret_cast<const uint32_t*>(&hi);
           }
         }
-      }
     }
   } else {
-    for (int q = 0; q < MATS * G; ++q) {
-      const int mat = q / G, g = q % G;
-      const uint16_t* sp = mat == 0 ? a.s0 : a.s1;
-      const uint16_t* bp = mat == 0 ? a.b0 : a.b1;
-      sbw[(size_t)(mat * G + g) * 128 + r] =
-          (uint32_t)bf16_to_f16_bits(__ldg(sp + row * G + g)) |
-          ((uint32_t)bf16_to_f16_bits(__ldg(bp + row * G + g)) << 16);
-    }
+    for (int g = 0; g < G; ++g)
+      sbw[(size_t)g * 128 + r] = sb_word(__ldg(sp + row * G + g), __ldg(bp + row * G + g));
   }
-}
-
-// Lane l's row (cb + l of the item, clamped to its last row): the token it
-// belongs to and its gate weight (1 for shared-expert rows).
-__device__ __forceinline__ void row_token_gate(const GemmArgs& a, const Item& it, int cb, int lane,
-                                               int P, int& tok, float& g) {
-  const int rj = it.row0 + min(cb + lane, it.rows - 1);
-  if (it.shared) {
-    tok = rj - P;
-    g = 1.f;
-  } else {
-    const int p = min(max(__ldg(a.perm + rj), 0), P - 1);  // out-of-range entries were flagged
-    tok = p / a.k;
-    g = __ldg(a.gates + p);
-  }
-}
-
-// One scale-table word: fp16(scale) | fp16(bias) << 16 from bf16 bit patterns.
-__device__ __forceinline__ uint32_t sb_word(uint16_t sc, uint16_t bi) {
-  return (uint32_t)bf16_to_f16_bits(sc) | ((uint32_t)bf16_to_f16_bits(bi) << 16);
 }
 
 // Persistent kernel: one CTA per SM loops over the work items.
@@ -281,17 +264,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    const __grid_constant__ CUtensorMap tm_b2w, const GemmArgs a, const int nstages,
                    const int nsb) {
   using L = GemmLayout<GATEUP, BM>;
-  constexpr int MATS = L::kMats;
   constexpr int BBYTES = L::kBBytes;
   constexpr int STAGE = L::kStage;
   constexpr int NACC = L::kNumAcc;
+  constexpr int NA = L::kNumA;
 
   const int K = GATEUP ? a.d : a.F;     // reduction length
   const int NOUT = GATEUP ? a.F : a.d;  // output features of each matrix
   constexpr int KG = L::kGroups;
   const int G = K / 64;                 // quantisation groups
   const int NST = G / KG;               // K-steps per item
-  const int nslices = NOUT / 128;
+  const int nslices = NOUT / L::kOutRows;
   const int P = a.T * a.k;
   const int nsh = (a.T + BM - 1) / BM;
   const int cap = (P + BM - 1) / BM + min(a.E, P);
@@ -302,13 +285,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
-  uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][MATS][G][128] scale|bias<<16
-  const int sb_words = MATS * G * 128;                       // one table
-  __half* estage = (__half*)(sb + nsb * sb_words);           // down: epilogue staging
-  uint64_t* bars = (uint64_t*)((uint8_t*)estage + (GATEUP ? 0 : kEpiStageBytes));
+  uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][G][128] scale|bias<<16
+  const int sb_words = G * 128;                              // one table
+  uint8_t* estage = (uint8_t*)(sb + nsb * sb_words);         // epilogue staging
+  uint64_t* bars = (uint64_t*)(estage + (GATEUP ? 0 : kEpiStageBytes));
   uint64_t* full = bars;                      // [kMaxStages] TMA landed
-  uint64_t* empty = bars + kMaxStages;        // [kMaxStages] stage consumed by the MMAs
-  uint64_t* afull = bars + 2 * kMaxStages;    // [kMaxA] dequantised A ready in TMEM
+  uint64_t* empty = full + kMaxStages;        // [kMaxStages] stage consumed by the MMAs
+  uint64_t* afull = empty + kMaxStages;       // [kMaxA] dequantised A ready in TMEM
   uint64_t* aempty = afull + kMaxA;           // [kMaxA] A consumed by the MMAs
   uint64_t* accfull = aempty + kMaxA;         // [2] accumulator set final
   uint64_t* accempty = accfull + 2;           // [2] accumulator set drained by the epilogue
@@ -326,7 +309,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < kMaxA; ++b) {
-      mbar_init(smem_u32(&afull[b]), kNumDequantWarps);
+      mbar_init(smem_u32(&afull[b]), kNumDequantWarps / 2);
       mbar_init(smem_u32(&aempty[b]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -374,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         continue;
       }
       const int N = (itm.rows + 15) & ~15;
-      const int wrow = itm.expert * NOUT + itm.slice * 128;
+      const int wrow = itm.expert * NOUT + itm.slice * L::kOutRows;
       // token rows of the item: gate/up reads the expert-sorted copy xs (or,
       // for a shared-expert tile, x16 in token order); down reads H
       // a tile of more than 64 rows (BM 128) takes one 128-row box per group
@@ -384,7 +367,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int brow = (GATEUP && itm.shared) ? itm.row0 - P : itm.row0;
       const int box_rows = wide ? BM : L::kBoxRows;
       const int nbox = wide ? 1 : (N + L::kBoxRows - 1) / L::kBoxRows;
-      const uint32_t tx_bytes = KG * (MATS * kPackedBytes + nbox * box_rows * 128);
+      const uint32_t tx_bytes = KG * (kPackedBytes + nbox * box_rows * 128);
       for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx;
         if (it >= (uint32_t)nstages &&
@@ -397,10 +380,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t st = smem_u32(stage_base + (size_t)s * STAGE);
         if (elect_one()) {
           mbar_arrive_expect_tx(fb, tx_bytes);
-#pragma unroll
-          // the step's packed codes: one box of 128 rows x (KG * 32) bytes per matrix
+          // the step's packed codes, 128 rows x (KG * 32) bytes: gate/up
+          // takes the slice's 64 gate rows, then the same features' up rows
           tma_load_2d(st + BBYTES, &tm_q0, kk * KG * 32, wrow, fb);
-          if (GATEUP) tma_load_2d(st + BBYTES + KG * kPackedBytes, &tm_q1, kk * KG * 32, wrow, fb);
+          if (GATEUP) tma_load_2d(st + BBYTES + 64 * KG * 32, &tm_q1, kk * KG * 32, wrow, fb);
 #pragma unroll
           for (int g = 0; g < KG; ++g) {
             const int grp = kk * KG + g;
@@ -426,6 +409,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // barrier, so a full A buffer implies that the stage's token rows landed.
     uint32_t it = 0, titem = 0;
     Ring rs;  // stage ring position of step it
+    Ring ra;  // A ring position of step it
     bool ok = true;
     int4 tnext = (int)blockIdx.x < n_items ? load_tile(a, blockIdx.x, nslices) : make_int4(0, 0, 0, 0);
     for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
@@ -441,26 +425,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       tc_fence_after();
       const uint32_t dacc = tmem + ab * L::kAccCols;
-      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
-        const int s = rs.idx, b = it % L::kNumA;
-        if (!warp_wait_all(smem_u32(&afull[b]), (it / L::kNumA) & 1, abort, a.status)) {
+      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages), ra.next(NA)) {
+        const int s = rs.idx, b = ra.idx;
+        if (!warp_wait_all(smem_u32(&afull[b]), ra.ph, abort, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t sbase = smem_u32(stage_base + (size_t)s * STAGE);
+        const uint32_t at = tmem + L::kAOff + b * L::kACols;  // A tile in TMEM
         if (elect_one()) {
 #pragma unroll
-          for (int m = 0; m < MATS; ++m) {
-            const uint32_t at = tmem + L::kAOff + (b * MATS + m) * L::kACols;  // A tile in TMEM
+          for (int g = 0; g < KG; ++g) {
+            const uint64_t bdesc = sdesc_sw128(sbase + g * L::kBTile);
 #pragma unroll
-            for (int g = 0; g < KG; ++g) {
-              const uint64_t bdesc = sdesc_sw128(sbase + g * L::kBTile);
-#pragma unroll
-              for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
-                mma_f16_ts(dacc + m * BM, at + g * 32 + k16 * 8, bdesc + 2 * k16, idesc,
-                           (kk | g | k16) != 0);
-            }
+            for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
+              mma_f16_ts(dacc, at + g * 32 + k16 * 8, bdesc + 2 * k16, idesc,
+                         (kk | g | k16) != 0);
           }
           mma_commit(smem_u32(&empty[s]));
           mma_commit(smem_u32(&aempty[b]));
@@ -475,22 +456,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ================================================= dequant
-    // gate/up: warps 2..5 rebuild the gate slice, 6..9 the up slice, both
-    // groups of each K-step; down: warps 2..5 take the first group of each
-    // K-step, 6..9 the second.  One weight row per lane.
+    // Warps 2..5 rebuild the K-steps with an even running index it, 6..9
+    // those with an odd one (both groups each).  One weight row per lane.
     const int q = warp & 3;
     const int r = q * 32 + lane;          // weight row within the slice = TMEM lane
-    const int hsel = (warp - 2) >> 2;
-    const int mat = GATEUP ? hsel : 0;
-    const int g = GATEUP ? 0 : hsel;      // group within the K-step
+    const uint32_t par = (uint32_t)(warp - 2) >> 2;  // parity of this warp's steps
+    const int crow = GATEUP ? gu_code_row(r) : r;  // its row of the step's code tile
     const uint32_t tlane = (uint32_t)(q * 32) << 16;
     uint32_t it = 0, j = 0;
     Ring rs;  // stage ring position of step it
+    Ring ra;  // A ring position of step it
     bool ok = true;
     // down: each lane fills its own row's table entries (the groups of its
-    // parity g) in table slot 0, which only it reads; the raw bf16 scales and
-    // biases of the next item are loaded one item ahead, as 16-byte chunks,
-    // when G is 8 or 16 (else read one by one at the item's start)
+    // own K-steps) in its warp set's table slot (par), which only it reads;
+    // the raw bf16 scales and biases of the next item are loaded one item
+    // ahead, as 16-byte chunks, when G is 8 or 16 (else read one by one at
+    // the item's start)
     constexpr int kPfChunks = 2;  // 8-group chunks held in registers
     uint4 pfs[kPfChunks], pfb[kPfChunks];
     int pf_w = -1;                // work item whose scales pfs/pfb hold
@@ -509,24 +490,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       pf_w = wn;
     };
-    auto down_fill = [&](int w, const Item& itm) {
-      uint32_t* dst = sb;  // slot 0, entries [group][row]
+    // groups 2kk, 2kk+1 (K-step kk of an item starting at running step it0)
+    // belong to this warp when (it0 + kk) has its parity
+    auto down_fill = [&](int w, const Item& itm, uint32_t it0) {
+      uint32_t* dst = sb + par * sb_words;  // this warp set's slot, entries [group][row]
       if (pf_w == w) {
 #pragma unroll
         for (int c = 0; c < kPfChunks; ++c)
           if (c * 8 < G) {
-            // groups c*8 + 2u + g sit in word u, half g, of each chunk
+            // groups c*8 + 2u and c*8 + 2u + 1 (K-step 4c + u) sit in the
+            // two halves of word u of each chunk
             const uint32_t ws[4] = {pfs[c].x, pfs[c].y, pfs[c].z, pfs[c].w};
             const uint32_t wb[4] = {pfb[c].x, pfb[c].y, pfb[c].z, pfb[c].w};
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              dst[(c * 8 + 2 * u + g) * 128 + r] =
-                  sb_word((uint16_t)(ws[u] >> (16 * g)), (uint16_t)(wb[u] >> (16 * g)));
+              if (((it0 + (uint32_t)u) & 1u) == par) {
+                dst[(c * 8 + 2 * u) * 128 + r] = sb_word((uint16_t)ws[u], (uint16_t)wb[u]);
+                dst[(c * 8 + 2 * u + 1) * 128 + r] =
+                    sb_word((uint16_t)(ws[u] >> 16), (uint16_t)(wb[u] >> 16));
+              }
           }
       } else {
         const size_t row = sb_row(itm.expert, itm.slice);
-        for (int grp = g; grp < G; grp += 2)
-          dst[grp * 128 + r] = sb_word(__ldg(a.s0 + row * G + grp), __ldg(a.b0 + row * G + grp));
+        for (int grp = 0; grp < G; ++grp)
+          if (((it0 + (uint32_t)(grp >> 1)) & 1u) == par)
+            dst[grp * 128 + r] =
+                sb_word(__ldg(a.s0 + row * G + grp), __ldg(a.b0 + row * G + grp));
       }
     };
     int4 tnext = (int)blockIdx.x < n_items ? load_tile(a, blockIdx.x, nslices) : make_int4(0, 0, 0, 0);
@@ -535,63 +524,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (w + (int)gridDim.x < n_items) tnext = load_tile(a, w + gridDim.x, nslices);
       Item itm;
       if (!item_from(tcur, w, nslices, nsh, itm)) continue;
-      const int slot = GATEUP ? j % nsb : 0;
+      const int slot = GATEUP ? j % nsb : (int)par;
       if (GATEUP) {
         if (!warp_wait(smem_u32(&sbfull[slot]), (j / nsb) & 1, abort, a.status)) break;
       } else {
-        down_fill(w, itm);
+        down_fill(w, itm, it);
         if (w + (int)gridDim.x < n_items) down_prefetch(w + gridDim.x, tnext);
       }
       const uint32_t* sbs = sb + slot * sb_words;
-      // Per K-step a gate/up warp rebuilds both groups of its matrix (their
-      // loads, arithmetic and tensor-memory stores interleave, and one store
-      // wait and one arrival cover both); a down warp rebuilds its group.
-      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
-        const int s0 = rs.idx, b0 = it % L::kNumA;
-        // the stage's TMA landed and the A buffer was consumed
-        if (!warp_wait_all2(smem_u32(&full[s0]), rs.ph, smem_u32(&aempty[b0]),
-                            ((it / L::kNumA) + 1) & 1, it >= (uint32_t)L::kNumA, abort,
-                            a.status)) {
+      for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages), ra.next(NA)) {
+        if ((it & 1u) != par) continue;  // the other warp set's step
+        const int s0 = rs.idx, b0 = ra.idx;
+        // the stage's TMA landed and the A buffer was consumed; the warp
+        // sleeps in the wait (it issues nothing while the epilogue warps,
+        // which share its SM sub-partition, drain the accumulators)
+        if (!warp_wait_all2_blocking(smem_u32(&full[s0]), rs.ph, smem_u32(&aempty[b0]),
+                                     ra.ph ^ 1u, it >= (uint32_t)NA, abort, a.status)) {
           ok = false;
           break;
         }
-        // the stage holds a matrix's codes of the step as rows of 64 bytes
-        // (two groups) with the 64-byte TMA swizzle: 16-byte chunk c of row r
-        // sits at 16 * (c ^ ((r >> 1) & 3)), which spreads each 8 consecutive
-        // lanes' loads over all eight 16-byte bank groups
-        const int ph = (r >> 1) & 3;
-        const uint8_t* pk = stage_base + (size_t)s0 * STAGE + BBYTES +
-                            (size_t)mat * KG * kPackedBytes + r * (KG * 32);
-        const int c0 = 2 * g;  // down: this warp's group of the step
-        const uint4 lo0 = *reinterpret_cast<const uint4*>(pk + 16 * (c0 ^ ph));
-        const uint4 hi0 = *reinterpret_cast<const uint4*>(pk + 16 * ((c0 + 1) ^ ph));
-        uint4 lo1 = lo0, hi1 = hi0;
-        if (GATEUP) {  // (g = 0) the step's second group
-          lo1 = *reinterpret_cast<const uint4*>(pk + 16 * (2 ^ ph));
-          hi1 = *reinterpret_cast<const uint4*>(pk + 16 * (3 ^ ph));
-        }
-        const uint32_t sbv0 = sbs[(mat * G + kk * KG + g) * 128 + r];
-        const uint32_t sbv1 = GATEUP ? sbs[(mat * G + kk * KG + 1) * 128 + r] : sbv0;
+        // the stage holds the step's codes as rows of 64 bytes (two groups)
+        // with the 64-byte TMA swizzle: 16-byte chunk c of row R sits at
+        // 16 * (c ^ ((R >> 1) & 3)), which spreads each 8 consecutive lanes'
+        // loads (8 consecutive code rows) over all eight 16-byte bank groups
+        const int ph = (crow >> 1) & 3;
+        const uint8_t* pk = stage_base + (size_t)s0 * STAGE + BBYTES + crow * (KG * 32);
+        const uint4 lo0 = *reinterpret_cast<const uint4*>(pk + 16 * (0 ^ ph));
+        const uint4 hi0 = *reinterpret_cast<const uint4*>(pk + 16 * (1 ^ ph));
+        const uint4 lo1 = *reinterpret_cast<const uint4*>(pk + 16 * (2 ^ ph));
+        const uint4 hi1 = *reinterpret_cast<const uint4*>(pk + 16 * (3 ^ ph));
+        const uint32_t sbv0 = sbs[(kk * KG) * 128 + r], sbv1 = sbs[(kk * KG + 1) * 128 + r];
         const uint32_t s20 = prmt(sbv0, sbv0, 0x1010u), b20 = prmt(sbv0, sbv0, 0x3232u);
         const uint32_t s21 = prmt(sbv1, sbv1, 0x1010u), b21 = prmt(sbv1, sbv1, 0x3232u);
         const uint32_t wd0[8] = {lo0.x, lo0.y, lo0.z, lo0.w, hi0.x, hi0.y, hi0.z, hi0.w};
         const uint32_t wd1[8] = {lo1.x, lo1.y, lo1.z, lo1.w, hi1.x, hi1.y, hi1.z, hi1.w};
         uint32_t o0[32], o1[32];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
+        for (int jj = 0; jj < 8; ++jj) {  // the two groups' arithmetic interleaved
           uint32_t t4[4], u4[4];
           dequant8(wd0[jj], s20, b20, t4);
-          if (GATEUP) dequant8(wd1[jj], s21, b21, u4);
+          dequant8(wd1[jj], s21, b21, u4);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             o0[4 * jj + e] = t4[e];
-            o1[4 * jj + e] = GATEUP ? u4[e] : 0u;
+            o1[4 * jj + e] = u4[e];
           }
         }
-        const uint32_t acol =
-            tmem + tlane + L::kAOff + (b0 * MATS + mat) * L::kACols + g * 32;
+        const uint32_t acol = tmem + tlane + L::kAOff + b0 * L::kACols;
         tmem_st32(acol, o0);
-        if (GATEUP) tmem_st32(acol + 32, o1);
+        tmem_st32(acol + 32, o1);
         // the stores must be complete before the MMA issuer is told: wait,
         // order them before the arrive, then one arrive per warp and step
         tmem_st_wait();
@@ -606,27 +587,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // ================================================= epilogue
-    // Per item j: (1) fill the scale table of item j+1 for the dequant warps,
-    // (2) for short items (down), start loading item j+2's table into
-    // registers, (3) drain item j's accumulators to global memory.
+    // Per item j: (1) gate/up: fill the scale table of item j+1 for the
+    // dequant warps, (2) drain item j's accumulators to global memory.
     const int q = warp & 3;  // TMEM lane quadrant of this warp
     const int r = threadIdx.x - 32 * kEpiWarp0;
     auto slot_ptr = [&](int slot) { return sb + (size_t)slot * sb_words; };
-    auto row_of = [&](const Item& it) {
-      return (size_t)it.expert * NOUT + (size_t)it.slice * 128 + r;
+    // gate/up: thread r fills the table entries of weight row r
+    auto fill = [&](const Item& it, int slot) {
+      const size_t row = (size_t)it.expert * NOUT + (size_t)it.slice * 64 + gu_feature(r);
+      if (gu_matrix(r) == 0)
+        scale_fill(a.s0, a.b0, row, G, r, slot_ptr(slot));
+      else
+        scale_fill(a.s1, a.b1, row, G, r, slot_ptr(slot));
     };
     int w = blockIdx.x;
     Item cur, nxt, nn;
-    bool have = next_item<BM>(a, w, n_items, nslices, nsh, P, cur);
+    bool have = next_item(a, w, n_items, nslices, nsh, cur);
     if (GATEUP && have) {
-      scale_fill<MATS>(a, row_of(cur), G, r, slot_ptr(0));
+      fill(cur, 0);
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sbfull[0]));
     }
     int wn = w + gridDim.x;
-    bool have_next = have && next_item<BM>(a, wn, n_items, nslices, nsh, P, nxt);
+    bool have_next = have && next_item(a, wn, n_items, nslices, nsh, nxt);
     uint32_t j = 0;
-    uint32_t echunk = 0;  // down: staged row chunks (alternating buffers)
     while (have) {
       if (GATEUP && have_next) {
         const uint32_t jn = j + 1;
@@ -634,78 +618,74 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (jn >= (uint32_t)nsb &&
             !warp_wait(smem_u32(&sbempty[slot]), ((jn / nsb) + 1) & 1, abort, a.status))
           break;
-        scale_fill<MATS>(a, row_of(nxt), G, r, slot_ptr(slot));
+        fill(nxt, slot);
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sbfull[slot]));
       }
       int wnn = wn + gridDim.x;
-      const bool have_nn = have_next && next_item<BM>(a, wnn, n_items, nslices, nsh, P, nn);
+      const bool have_nn = have_next && next_item(a, wnn, n_items, nslices, nsh, nn);
 
       const int N = (cur.rows + 15) & ~15;
       const int ab = j % NACC;
-      // the first 32 rows' tokens and gate weights, looked up before the
-      // accumulator wait so that the dependent loads overlap it
-      int tok0 = 0;
-      float gate0 = 0.f;
-      row_token_gate(a, cur, 0, lane, P, tok0, gate0);
       if (!warp_wait(smem_u32(&accfull[ab]), (j / NACC) & 1, abort, a.status)) break;
       tc_fence_after();
-      const int feat = cur.slice * 128 + q * 32 + lane;
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + ab * L::kAccCols;
+      bool range_ok = true;
       for (int cb = 0; cb < N; cb += 32) {
         const bool last = cb + 32 >= N;
-        int tokj = tok0;
-        float gj = gate0;
-        if (cb > 0) row_token_gate(a, cur, cb, lane, P, tokj, gj);
+        const int ncol = N - cb < 32 ? N - cb : 32;  // 16 or 32
         if (GATEUP) {
-          uint32_t gr[32], ur[32];
-          tmem_ld32(tl + cb, gr);
-          tmem_ld32(tl + BM + cb, ur);
+          // Lanes 0..15 of warp q hold the gate outputs g of features
+          // 16q..16q+15 of the slice, lanes 16..31 the up outputs u of the
+          // same features (32 rows each).  Per step lanes 0..15 compute H of
+          // rows cb + rr and lanes 16..31 of rows cb + 16 + rr, each fetching
+          // the other half's value of its row with one shuffle.
+          uint32_t v[32];
+          tmem_ld32(tl + cb, v);
           tmem_ld_wait();
           if (last) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
-          bool range_ok = true;
+          const bool hi = lane >= 16;
+          const int feat = cur.slice * 64 + gu_feature(q * 32 + lane);
           // H holds each 8-feature chunk in K-chunk order (it is the down
           // GEMM's K operand against weights rebuilt in that order), so
           // features e and e + 4 sit side by side: lanes with e < 4 store the
-          // pair of column jj,
-          // lanes with e >= 4 that of column jj + 1, one 4-byte store each
+          // pair of row rr, lanes with e >= 4 that of row rr + 1, one 4-byte
+          // store each
           const bool up4 = (lane & 4) != 0;
-          __half2* Hp = reinterpret_cast<__half2*>(
-              static_cast<__half*>(a.H) + ((feat & ~7) | ((feat & 3) << 1)));
+          __half2* Hp = reinterpret_cast<__half2*>(static_cast<__half*>(a.H) +
+                                                   ((feat & ~7) | ((feat & 3) << 1)));
+          const int rb0 = cb + (hi ? 16 : 0);
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 2) {
-            if (cb + jj >= N) break;  // (warp-uniform; N is a multiple of 16)
+          for (int rr = 0; rr < 16; rr += 2) {
             float hv[2];
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-              const float gv = __uint_as_float(gr[jj + t]), uv = __uint_as_float(ur[jj + t]);
-              // gate * silu(g) * u with the fast reciprocal: its few-ulp fp32
-              // error is far below the fp16 rounding of H; g -> -inf gives 0
-              // as it should.  The row's gate weight is applied here, so the
-              // down GEMM's rows come out already weighted.
-              const float gate = __shfl_sync(0xffffffffu, gj, jj + t);
-              hv[t] = __fdividef(gate * gv * uv, 1.f + __expf(-gv));
+              const uint32_t send = hi ? v[rr + t] : v[rr + t + 16];
+              const float other = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
+              const float own = __uint_as_float(hi ? v[rr + t + 16] : v[rr + t]);
+              const float gv = hi ? other : own, uv = hi ? own : other;
+              // silu(g) * u with the fast reciprocal: its few-ulp fp32 error
+              // is far below the fp16 rounding of H; g -> -inf gives 0
+              hv[t] = __fdividef(gv, 1.f + __expf(-gv)) * uv;
             }
             const float recv = __shfl_xor_sync(0xffffffffu, up4 ? hv[0] : hv[1], 4);
-            const float lo = up4 ? recv : hv[0], hi = up4 ? hv[1] : recv;
-            const int n = cb + jj + (up4 ? 1 : 0);
+            const float lo = up4 ? recv : hv[0], hi2 = up4 ? hv[1] : recv;
+            const int n = rb0 + rr + (up4 ? 1 : 0);
             if (n < cur.rows) {
-              range_ok &= fabsf(lo) <= 65504.f && fabsf(hi) <= 65504.f;
-              Hp[(size_t)(cur.row0 + n) * (a.F / 2)] = __floats2half2_rn(lo, hi);
+              range_ok &= fabsf(lo) <= 65504.f && fabsf(hi2) <= 65504.f;
+              Hp[(size_t)(cur.row0 + n) * (a.F / 2)] = __floats2half2_rn(lo, hi2);
             }
           }
-          if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
         } else {
-          // Output rows of the item (already weighted: the gate was applied
-          // in H) as fp16 into O, in the same expert-sorted row order as H;
-          // the combine kernel then sums each token's rows.  Each warp stages
-          // its 32 features of up to 32 rows in shared memory, and each lane
-          // stores one row's 64 bytes.
-          const int ncol = N - cb < 32 ? N - cb : 32;  // 16 or 32
+          // Output rows of the item as fp16 into O, in the same
+          // expert-sorted row order as H; the combine kernel then sums each
+          // token's rows.  Each warp stages its 32 features of up to 32 rows
+          // in shared memory, and each lane stores one row's 64 bytes.
+          const int feat = cur.slice * 128 + q * 32 + lane;
           uint32_t va[16], vb[16];
           tmem_ld16(tl + cb, va);
           if (ncol == 32) tmem_ld16(tl + cb + 16, vb);
@@ -715,8 +695,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
-          __half* buf = estage + (size_t)q * 32 * kEpiRowHalves;
-          bool range_ok = true;
+          __half* buf = reinterpret_cast<__half*>(estage) + (size_t)q * 32 * kEpiRowHalves;
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) {
             const float v = __uint_as_float(va[rr]);
@@ -744,9 +723,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             dst[3] = v3;
           }
           __syncwarp();
-          if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
         }
       }
+      if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
       cur = nxt;
       have = have_next;
       nxt = nn;
@@ -810,7 +789,7 @@ static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, cons
   const int P = a.T * a.k;
   const int cap = (P + BM - 1) / BM + (a.E < P ? a.E : P);
   const int nsh = (a.T + BM - 1) / BM;
-  const int max_items = (nsh + cap) * (NOUT / 128);
+  const int max_items = (nsh + cap) * (NOUT / GemmLayout<GATEUP, BM>::kOutRows);
   int num_sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -836,15 +815,16 @@ static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const C
   }
 }
 
-// Packed codes: boxes of 128 rows x 64 bytes (the two quantisation groups of
-// a K-step) with the 64-byte swizzle (the four 16-byte chunks of row r are
-// permuted by XOR with (r >> 1) & 3), so that the dequant lanes' 16-byte
-// loads are free of bank conflicts; one copy per matrix and K-step.
+// Packed codes: boxes of box_rows rows x 64 bytes (the two quantisation
+// groups of a K-step) with the 64-byte swizzle (the four 16-byte chunks of
+// row r are permuted by XOR with (r >> 1) & 3), so that the dequant lanes'
+// 16-byte loads are free of bank conflicts: per K-step one 128-row copy
+// (down), or 64 rows of the gate matrix and 64 of the up matrix (gate/up).
 static_assert(groups_per_step(true) == 2 && groups_per_step(false) == 2, "64-byte code rows");
-static bool packed_map(CUtensorMap* tm, const uint8_t* q, int K, int rows) {
+static bool packed_map(CUtensorMap* tm, const uint8_t* q, int K, int rows, int box_rows) {
   uint64_t dims[2] = {(uint64_t)K / 2, (uint64_t)rows};
   uint64_t strides[1] = {(uint64_t)K / 2};
-  uint32_t box[2] = {64, 128};
+  uint32_t box[2] = {64, (uint32_t)box_rows};
   return encode_tiled(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, (void*)q, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_64B) == CUDA_SUCCESS;
 }
@@ -928,7 +908,8 @@ cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, co
                           const uint8_t* uq, cudaStream_t s) {
   CUtensorMap q0, q1, b, b2, bw, b2w;
   const int P = a.T * a.k;
-  if (!packed_map(&q0, gq, a.d, (a.E + 1) * a.F) || !packed_map(&q1, uq, a.d, (a.E + 1) * a.F) ||
+  if (!packed_map(&q0, gq, a.d, (a.E + 1) * a.F, 64) ||
+      !packed_map(&q1, uq, a.d, (a.E + 1) * a.F, 64) ||
       !f16_rows_map(&b, xs, a.d, P, box_rows(a.BM)) ||
       !f16_rows_map(&b2, x16, a.d, a.T, box_rows(a.BM)) ||
       !f16_rows_map(&bw, xs, a.d, P, a.BM) || !f16_rows_map(&b2w, x16, a.d, a.T, a.BM))
@@ -939,16 +920,17 @@ cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, co
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
   CUtensorMap q0, b, bw;
   const int P = a.T * a.k;
-  if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d) ||
+  if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d, 128) ||
       !f16_rows_map(&b, a.H, a.F, P + a.T, box_rows(a.BM)) ||
       !f16_rows_map(&bw, a.H, a.F, P + a.T, a.BM))
     return cudaErrorInvalidValue;
   return launch_gemm<false>(a, q0, q0, b, b, bw, bw, s);
 }
 
-// Combine: y[t] = sum_j O[inv[t*k + j]] + O[P + t] (the k routed rows of
-// token t in slot order, then its shared-expert row), in fp32 and in that
-// fixed order, so the layer output is the same on every run.  One CTA per
+// Combine: y[t] = sum_j gate[t][j] * O[inv[t*k + j]] + O[P + t] (the k
+// routed rows of token t in slot order, weighted by their routing gates, then
+// its shared-expert row), in fp32 and in that fixed order, so the layer
+// output is the same on every run.  One CTA per
 // token; each thread takes 8 consecutive outputs and issues the loads of all
 // k + 1 rows before adding.  Modes: y fp32, y bf16, or the stacked prefill's
 // boundary: x[t] += y[t] (fp32 residual) and, when xn is given, xn[t] =
@@ -956,24 +938,29 @@ cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
 constexpr int kCombThreads = 256;
 template <int MODE>  // 0: y fp32, 1: y bf16, 2: residual
 __global__ void __launch_bounds__(kCombThreads) combine_kernel(
-    const __half* __restrict__ O, const int32_t* __restrict__ inv, int k, int P, int d, void* y,
-    float* x, __nv_bfloat16* xn, float eps, uint32_t* status) {
+    const __half* __restrict__ O, const int32_t* __restrict__ inv,
+    const float* __restrict__ gates, int k, int P, int d, void* y, float* x, __nv_bfloat16* xn,
+    float eps, uint32_t* status) {
   __shared__ float s_red[kCombThreads / 32];
   pdl_wait();  // O comes from the down GEMM
   pdl_trigger();
   const int t = blockIdx.x;
   int rows[kMaxK + 1];
+  float gw[kMaxK + 1];
   bool bad = false;
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
     int r = 0;
+    gw[j] = 0.f;
     if (j < k) {
       r = __ldg(inv + (size_t)t * k + j);
+      gw[j] = __ldg(gates + (size_t)t * k + j);
       bad |= r < 0 || r >= P;
       r = min(max(r, 0), P - 1);
     }
     rows[j] = r;
   }
+  gw[kMaxK] = 1.f;  // the shared expert
   if (bad && threadIdx.x == 0) set_status(status, LILY_STATUS_BAD_TILE);
   rows[kMaxK] = P + t;
   const int d8 = d / 8;
@@ -992,8 +979,8 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 f = __half22float2(h[e]);
-          acc[2 * e] += f.x;
-          acc[2 * e + 1] += f.y;
+          acc[2 * e] = fmaf(gw[j], f.x, acc[2 * e]);
+          acc[2 * e + 1] = fmaf(gw[j], f.y, acc[2 * e + 1]);
         }
       }
     }
@@ -1051,14 +1038,14 @@ cudaError_t launch_combine(const GemmArgs& a, void* y, bool y_f32, float* x, voi
   prof_begin(K_FINALIZE, s);
   cudaError_t err;
   if (x)
-    err = launch_pdl(combine_kernel<2>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv, a.k, P, a.d,
-                     (void*)nullptr, x, xnb, eps, a.status);
+    err = launch_pdl(combine_kernel<2>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv,
+                     a.gates, a.k, P, a.d, (void*)nullptr, x, xnb, eps, a.status);
   else if (y_f32)
-    err = launch_pdl(combine_kernel<0>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv, a.k, P, a.d,
-                     y, (float*)nullptr, (__nv_bfloat16*)nullptr, eps, a.status);
+    err = launch_pdl(combine_kernel<0>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv,
+                     a.gates, a.k, P, a.d, y, (float*)nullptr, (__nv_bfloat16*)nullptr, eps, a.status);
   else
-    err = launch_pdl(combine_kernel<1>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv, a.k, P, a.d,
-                     y, (float*)nullptr, (__nv_bfloat16*)nullptr, eps, a.status);
+    err = launch_pdl(combine_kernel<1>, dim3(a.T), dim3(kCombThreads), 0, s, O, a.inv,
+                     a.gates, a.k, P, a.d, y, (float*)nullptr, (__nv_bfloat16*)nullptr, eps, a.status);
   prof_end(K_FINALIZE, s);
   return err;
 }
