@@ -61,12 +61,28 @@ DEFAULT_WORKLOAD = "prefill512"
 
 # ncu DRAM traffic (read + write bytes per launch) of the dominant kernel, keyed
 # by workload and by a hash of the kernel's source files: a changed kernel
-# reports null until it is profiled again.
-KERNEL_SOURCES = ["w4_grouped_gemm_gb300/csrc/gemm.cu", "w4_grouped_gemm_gb300/csrc/common.cuh"]
-NCU_TRAFFIC = {  # {(workload, kernel, source_hash): bytes}
-    # ncu dram__bytes_{read,write}.sum, w4_gemm_kernel<1, 64>, prefill512 layer:
-    # 322.20 MB read + 6.06 MB written
-    ("prefill512", "gateup_gemm", "fe4c349ddb1b7603"): 328253440,
+# reports null until it is profiled again.  KERNEL_SOURCES lists the sources
+# each kernel family is built from.
+KERNEL_SOURCES = {
+    "gemm": ["w4_grouped_gemm_gb300/csrc/gemm.cu", "w4_grouped_gemm_gb300/csrc/common.cuh"],
+    "decode": ["w4_grouped_gemm_gb300/csrc/decode.cu", "w4_grouped_gemm_gb300/csrc/common.cuh",
+               "w4_grouped_gemm_gb300/csrc/routing.cuh"],
+}
+
+
+def kernel_family(name: str) -> str:
+    return "decode" if name.startswith("dec_") else "gemm"
+
+
+NCU_TRAFFIC = {  # {(workload, kernel, source_hash): bytes per launch}
+    # ncu dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel,
+    # from the launch list of `bench.py --workload W --eager --steps 3
+    # --warmup 3 --layers 1 --no-cpu-baseline --no-e2e` (mean over launches)
+    ("prefill512", "gateup_gemm", "08b3bcad7d45cf2f"): 325687888,  # 322.20 + 3.49 MB
+    ("prefill2048_zipf", "gateup_gemm", "08b3bcad7d45cf2f"): 227902528,  # 210.14 + 17.77 MB
+    ("prefill8192", "gateup_gemm", "08b3bcad7d45cf2f"): 670281872,  # 605.28 + 65.00 MB
+    ("decode1", "dec_router", "21fef2fc61a94cfa"): 3929200,  # 3.93 MB read
+    ("decode1", "dec_gateup", "21fef2fc61a94cfa"): 10657312,  # 10.66 MB read
 }
 
 
@@ -295,7 +311,7 @@ def kernel_work(name, T, d, E, k, F, touched):
     P = T * k
     if name in ("gateup_gemm", "dec_gateup"):
         return touched * 2 * mb + T * d * 2, 4 * (P + T) * d * F
-    if name in ("down_gemm", "dec_down_combine"):
+    if name in ("down_gemm", "dec_down"):
         return touched * mb + T * d * 4, 2 * (P + T) * d * F
     if name in ("router_gemm", "dec_router"):
         return E * d * 4 + T * d * 2 + T * E * 4, 2 * T * d * E
@@ -713,8 +729,8 @@ def run_lily(args, world, rank, local):
         if work:
             roofline = roofline_of(dom, kernels[dom]["us_per_launch"] * 1e-6, work, hbm, tf_burst,
                                    peak_src)
-            roofline["traffic"] = NCU_TRAFFIC.get((args.workload, dom,
-                                                   source_hash(KERNEL_SOURCES)))
+            roofline["traffic"] = NCU_TRAFFIC.get(
+                (args.workload, dom, source_hash(KERNEL_SOURCES[kernel_family(dom)])))
     launches = int(round(sum(v["launches"] for v in prof.values()) / prof_steps * args.steps))
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
 

@@ -57,9 +57,9 @@ extern "C" {
 #define LILY_STATUS_BAD_TILE 0x4u        /* a block-map entry was out of range */
 #define LILY_STATUS_F16_RANGE 0x8u       /* a value above 65504, the fp16 range
                                             of the tensor-core operands and the
-                                            intermediate rows: |x|, |gate*silu(g)*u|
-                                            (decode |silu(g)*u|) or a gated output
-                                            row value of the grouped GEMM path   */
+                                            intermediate rows: |x|, |silu(g)*u|,
+                                            or an expert output row value of the
+                                            grouped GEMM path                   */
 
 /* ------------------------------------------------------------------ shapes
  * T          tokens (rows) of this call; 1 <= T <= 16384 (decode: 1..8)
@@ -152,9 +152,10 @@ int lily_moe_route(const lily_moe_dims* dims, const void* x, const float* logits
 
 /* The whole layer for prefill-sized T: routing as in lily_moe_route, then the
  * gate/up grouped GEMM (fused 4-bit dequant + SwiGLU) and the down grouped GEMM
- * (fused dequant; each output row, already weighted by its gate, is stored
- * in expert-sorted order), then the combine of each token's k + 1 rows in a
- * fixed order back into token order, so y is the same bits on every run.
+ * (fused dequant; each expert output row is stored as fp16 in expert-sorted
+ * order), then the combine of each token's k + 1 rows, weighted by their
+ * routing gates, in a fixed order back into token order, so y is the same
+ * bits on every run.
  *   x  bf16 [T][d] device in; y [T][d] device out, fp32 or bf16 per
  *   dims->out_dtype. */
 int lily_moe_forward(const lily_moe_dims* dims, const void* x,

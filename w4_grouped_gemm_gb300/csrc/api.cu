@@ -826,7 +826,7 @@ int lily_moe_profile_read(double* total_ms, int64_t* launches) {
 
 const char* lily_moe_kernel_name(int kind) {
   static const char* names[] = {"router_gemm", "dec_router", "route", "gateup_gemm",
-                                "down_gemm",   "combine",    "dec_gateup", "dec_down_combine",
+                                "down_gemm",   "combine",    "dec_gateup", "dec_down",
                                 "unused",      "rmsnorm",     "unused", "unused",
                                 "router_prep", "router_reduce", "token_rows"};
   if (kind < 0 || kind >= (int)(sizeof(names) / sizeof(names[0]))) return "unused";
