@@ -73,6 +73,11 @@ constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 4 + 4 + 1;
 // store wait and arrival) are paid once per 128 K.
 __host__ __device__ constexpr int groups_per_step(bool /*gateup*/) { return 2; }
 
+// 128-row weight sub-slices per work item (see GemmLayout::kSub).
+__host__ __device__ constexpr int sub_slices(bool gateup, int BM) {
+  return (gateup && BM <= 64) ? 2 : 1;
+}
+
 // Tensor memory (512 columns x 128 lanes): two accumulator sets of N <= BM
 // columns, then the ring of dequantised A tiles (128 rows x 128 fp16 = 64
 // columns per K-step).  A stage holds, per group, a 128-byte-swizzled tile of
@@ -87,16 +92,22 @@ struct GemmLayout {
   // item's last are other tiles' rows or zero fill, never stored)
   static constexpr int kBoxRows = BM < 64 ? BM : 64;
   static constexpr int kBBytes = kGroups * kBTile;
-  static constexpr int kStage = kBBytes + kGroups * kPackedBytes;
-  static constexpr int kOutRows = GATEUP ? 64 : 128;  // output features per item (and matrix)
-  static constexpr int kACols = 32 * kGroups;          // A tile of one K-step
-  static constexpr int kAccCols = BM;                  // one accumulator set
+  // 128-row sub-slices per item: gate/up tiles of at most 64 rows take two
+  // (128 features of both matrices, 16 MMAs per K-step), so the per-step
+  // hand-offs are paid once per 128 features; BM 128 takes one, which leaves
+  // room for two accumulator sets and a 4-step A ring
+  static constexpr int kSub = (GATEUP && BM <= 64) ? 2 : 1;
+  static constexpr int kStage = kBBytes + kSub * kGroups * kPackedBytes;
+  static constexpr int kOutRows = GATEUP ? 64 * kSub : 128;  // output features per item
+  static constexpr int kACols = 32 * kGroups * kSub;          // A tiles of one K-step
+  static constexpr int kAccCols = BM * kSub;                  // one accumulator set
   static constexpr int kNumAcc = 2;
   static constexpr int kAOff = kNumAcc * kAccCols;
   static constexpr int kNumA =
       (512 - kAOff) / kACols < kMaxA ? (512 - kAOff) / kACols : kMaxA;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kNumA >= 2, "tensor memory too small for the A ring");
+  static_assert(kSub == sub_slices(GATEUP, BM), "sub-slices");
 };
 
 // Down epilogue staging: per epilogue warp 32 rows x 32 output features of
@@ -115,7 +126,7 @@ __host__ __device__ constexpr int gu_code_row(int r) { return 64 * gu_matrix(r) 
 __host__ __device__ inline size_t gemm_fixed_bytes(bool gateup, int BM, int K, int nsb) {
   const int G = K / 64;
   return 1024                                    // alignment slack
-         + (size_t)nsb * G * 128 * 4             // scale/bias tables (one per item in flight)
+         + (size_t)nsb * G * 128 * sub_slices(gateup, BM) * 4  // scale/bias tables
          + (gateup ? 0 : kEpiStageBytes)          // down: epilogue staging
          + kNumBars * 8                          // mbarriers
          + 16;                                   // abort flag, TMEM address
@@ -123,7 +134,7 @@ __host__ __device__ inline size_t gemm_fixed_bytes(bool gateup, int BM, int K, i
 
 size_t gemm_stage_bytes(bool gateup, int BM) {
   const int kg = groups_per_step(gateup);
-  return (size_t)kg * ((size_t)BM * 128 + kPackedBytes);
+  return (size_t)kg * ((size_t)BM * 128 + (size_t)sub_slices(gateup, BM) * kPackedBytes);
 }
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
@@ -213,13 +224,14 @@ __device__ __forceinline__ uint32_t sb_word(uint16_t sc, uint16_t bi) {
 }
 
 // Scale/bias table of one gate/up item: sb[g][r] = (fp16 scale | fp16 bias <<
-// 16) of weight row r (see gu_code_row) and every group g.
-// Filled by the epilogue threads, thread r owning row r (`row` = its matrix
-// row, `sp`/`bp` = its matrix's scales and biases): 16-byte loads of 8 scales
-// and the 8 matching biases (two such pairs in flight), one f16x2 conversion
-// and one 4-byte store per group.
+// 16) of weight row r (128 rows per sub-slice, see gu_code_row) and every
+// group g; `ld` words per group.  Filled by the epilogue threads, thread r
+// owning rows r (+ 128 per further sub-slice) (`row` = its matrix row,
+// `sp`/`bp` = its matrix's scales and biases): 16-byte loads of 8 scales and
+// the 8 matching biases (two such pairs in flight), one f16x2 conversion and
+// one 4-byte store per group.
 __device__ void scale_fill(const uint16_t* sp, const uint16_t* bp, size_t row, int G, int r,
-                           uint32_t* sbw) {
+                           int ld, uint32_t* sbw) {
   if ((G & 7) == 0) {
     const int nch = G / 8;
     for (int base = 0; base < nch; base += 2) {
@@ -235,21 +247,21 @@ __device__ void scale_fill(const uint16_t* sp, const uint16_t* bp, size_t row, i
         if (base + j < nch) {
           const uint32_t ws[4] = {vs[j].x, vs[j].y, vs[j].z, vs[j].w};
           const uint32_t wb[4] = {vb[j].x, vb[j].y, vb[j].z, vb[j].w};
-          uint32_t* dst = sbw + (size_t)((base + j) * 8) * 128 + r;
+          uint32_t* dst = sbw + (size_t)((base + j) * 8) * ld + r;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {  // groups 2u (low halves) and 2u+1 (high halves)
             const __half2 lo = __floats2half2_rn(__uint_as_float(ws[u] << 16),
                                                  __uint_as_float(wb[u] << 16));
             const __half2 hi = __floats2half2_rn(__uint_as_float(ws[u] & 0xFFFF0000u),
                                                  __uint_as_float(wb[u] & 0xFFFF0000u));
-            dst[(2 * u) * 128] = *reinterpret_cast<const uint32_t*>(&lo);
-            dst[(2 * u + 1) * 128] = *reinterpret_cast<const uint32_t*>(&hi);
+            dst[(2 * u) * ld] = *reinterpret_cast<const uint32_t*>(&lo);
+            dst[(2 * u + 1) * ld] = *reinterpret_cast<const uint32_t*>(&hi);
           }
         }
     }
   } else {
     for (int g = 0; g < G; ++g)
-      sbw[(size_t)g * 128 + r] = sb_word(__ldg(sp + row * G + g), __ldg(bp + row * G + g));
+      sbw[(size_t)g * ld + r] = sb_word(__ldg(sp + row * G + g), __ldg(bp + row * G + g));
   }
 }
 
@@ -268,6 +280,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int STAGE = L::kStage;
   constexpr int NACC = L::kNumAcc;
   constexpr int NA = L::kNumA;
+  constexpr int SUB = L::kSub;
 
   const int K = GATEUP ? a.d : a.F;     // reduction length
   const int NOUT = GATEUP ? a.F : a.d;  // output features of each matrix
@@ -285,8 +298,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t* stage_base = smem;
-  uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][G][128] scale|bias<<16
-  const int sb_words = G * 128;                              // one table
+  uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][G][128*SUB] scale|bias<<16
+  const int sb_words = G * 128 * SUB;                        // one table
   uint8_t* estage = (uint8_t*)(sb + nsb * sb_words);         // epilogue staging
   uint64_t* bars = (uint64_t*)(estage + (GATEUP ? 0 : kEpiStageBytes));
   uint64_t* full = bars;                      // [kMaxStages] TMA landed
@@ -309,7 +322,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int b = 0; b < kMaxA; ++b) {
-      mbar_init(smem_u32(&afull[b]), kNumDequantWarps / 2);
+      // one warp set per K-step (SUB 1) or all eight warps (SUB 2)
+      mbar_init(smem_u32(&afull[b]), SUB == 1 ? kNumDequantWarps / 2 : kNumDequantWarps);
       mbar_init(smem_u32(&aempty[b]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -367,7 +381,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int brow = (GATEUP && itm.shared) ? itm.row0 - P : itm.row0;
       const int box_rows = wide ? BM : L::kBoxRows;
       const int nbox = wide ? 1 : (N + L::kBoxRows - 1) / L::kBoxRows;
-      const uint32_t tx_bytes = KG * (kPackedBytes + nbox * box_rows * 128);
+      const uint32_t tx_bytes = KG * (SUB * kPackedBytes + nbox * box_rows * 128);
       for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages)) {
         const int s = rs.idx;
         if (it >= (uint32_t)nstages &&
@@ -382,8 +396,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(fb, tx_bytes);
           // the step's packed codes, 128 rows x (KG * 32) bytes: gate/up
           // takes the slice's 64 gate rows, then the same features' up rows
-          tma_load_2d(st + BBYTES, &tm_q0, kk * KG * 32, wrow, fb);
-          if (GATEUP) tma_load_2d(st + BBYTES + 64 * KG * 32, &tm_q1, kk * KG * 32, wrow, fb);
+#pragma unroll
+          for (int j = 0; j < SUB; ++j) {  // sub-slice j: its code tile of 128 rows
+            const uint32_t ct = st + BBYTES + j * KG * kPackedBytes;
+            tma_load_2d(ct, &tm_q0, kk * KG * 32, wrow + 64 * j, fb);
+            if (GATEUP) tma_load_2d(ct + 64 * KG * 32, &tm_q1, kk * KG * 32, wrow + 64 * j, fb);
+          }
 #pragma unroll
           for (int g = 0; g < KG; ++g) {
             const int grp = kk * KG + g;
@@ -439,9 +457,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int g = 0; g < KG; ++g) {
             const uint64_t bdesc = sdesc_sw128(sbase + g * L::kBTile);
 #pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
-              mma_f16_ts(dacc, at + g * 32 + k16 * 8, bdesc + 2 * k16, idesc,
-                         (kk | g | k16) != 0);
+            for (int j = 0; j < SUB; ++j)  // sub-slice j: its A tile and accumulator
+#pragma unroll
+              for (int k16 = 0; k16 < 4; ++k16)  // +32 B along K = +2 in the descriptor
+                mma_f16_ts(dacc + j * BM, at + j * 32 * KG + g * 32 + k16 * 8, bdesc + 2 * k16,
+                           idesc, (kk | g | k16) != 0);
           }
           mma_commit(smem_u32(&empty[s]));
           mma_commit(smem_u32(&aempty[b]));
@@ -456,11 +476,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp < kEpiWarp0) {
     // ================================================= dequant
-    // Warps 2..5 rebuild the K-steps with an even running index it, 6..9
-    // those with an odd one (both groups each).  One weight row per lane.
+    // One sub-slice (SUB 1): warps 2..5 rebuild the K-steps with an even
+    // running index it, 6..9 those with an odd one (both groups each).  Two
+    // sub-slices (SUB 2): warps 2..5 rebuild sub-slice 0 of every step, 6..9
+    // sub-slice 1.  One weight row per lane.
     const int q = warp & 3;
     const int r = q * 32 + lane;          // weight row within the slice = TMEM lane
-    const uint32_t par = (uint32_t)(warp - 2) >> 2;  // parity of this warp's steps
+    const uint32_t par = (uint32_t)(warp - 2) >> 2;  // step parity (SUB 1) / sub-slice (SUB 2)
+    const int jsub = SUB == 2 ? (int)par : 0;
     const int crow = GATEUP ? gu_code_row(r) : r;  // its row of the step's code tile
     const uint32_t tlane = (uint32_t)(q * 32) << 16;
     uint32_t it = 0, j = 0;
@@ -533,7 +556,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       const uint32_t* sbs = sb + slot * sb_words;
       for (int kk = 0; kk < NST; ++kk, ++it, rs.next(nstages), ra.next(NA)) {
-        if ((it & 1u) != par) continue;  // the other warp set's step
+        if (SUB == 1 && (it & 1u) != par) continue;  // the other warp set's step
         const int s0 = rs.idx, b0 = ra.idx;
         // the stage's TMA landed and the A buffer was consumed; the warp
         // sleeps in the wait (it issues nothing while the epilogue warps,
@@ -548,12 +571,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // 16 * (c ^ ((R >> 1) & 3)), which spreads each 8 consecutive lanes'
         // loads (8 consecutive code rows) over all eight 16-byte bank groups
         const int ph = (crow >> 1) & 3;
-        const uint8_t* pk = stage_base + (size_t)s0 * STAGE + BBYTES + crow * (KG * 32);
+        const uint8_t* pk = stage_base + (size_t)s0 * STAGE + BBYTES +
+                            jsub * KG * kPackedBytes + crow * (KG * 32);
         const uint4 lo0 = *reinterpret_cast<const uint4*>(pk + 16 * (0 ^ ph));
         const uint4 hi0 = *reinterpret_cast<const uint4*>(pk + 16 * (1 ^ ph));
         const uint4 lo1 = *reinterpret_cast<const uint4*>(pk + 16 * (2 ^ ph));
         const uint4 hi1 = *reinterpret_cast<const uint4*>(pk + 16 * (3 ^ ph));
-        const uint32_t sbv0 = sbs[(kk * KG) * 128 + r], sbv1 = sbs[(kk * KG + 1) * 128 + r];
+        const int tr = jsub * 128 + r;  // table row
+        const uint32_t sbv0 = sbs[(kk * KG) * (128 * SUB) + tr];
+        const uint32_t sbv1 = sbs[(kk * KG + 1) * (128 * SUB) + tr];
         const uint32_t s20 = prmt(sbv0, sbv0, 0x1010u), b20 = prmt(sbv0, sbv0, 0x3232u);
         const uint32_t s21 = prmt(sbv1, sbv1, 0x1010u), b21 = prmt(sbv1, sbv1, 0x3232u);
         const uint32_t wd0[8] = {lo0.x, lo0.y, lo0.z, lo0.w, hi0.x, hi0.y, hi0.z, hi0.w};
@@ -570,7 +596,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             o1[4 * jj + e] = u4[e];
           }
         }
-        const uint32_t acol = tmem + tlane + L::kAOff + b0 * L::kACols;
+        const uint32_t acol = tmem + tlane + L::kAOff + b0 * L::kACols + jsub * 32 * KG;
         tmem_st32(acol, o0);
         tmem_st32(acol + 32, o1);
         // the stores must be complete before the MMA issuer is told: wait,
@@ -594,11 +620,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     auto slot_ptr = [&](int slot) { return sb + (size_t)slot * sb_words; };
     // gate/up: thread r fills the table entries of weight row r
     auto fill = [&](const Item& it, int slot) {
-      const size_t row = (size_t)it.expert * NOUT + (size_t)it.slice * 64 + gu_feature(r);
-      if (gu_matrix(r) == 0)
-        scale_fill(a.s0, a.b0, row, G, r, slot_ptr(slot));
-      else
-        scale_fill(a.s1, a.b1, row, G, r, slot_ptr(slot));
+#pragma unroll
+      for (int j = 0; j < SUB; ++j) {  // sub-slice j: table rows 128 j + r
+        const size_t row = (size_t)it.expert * NOUT + (size_t)it.slice * L::kOutRows + 64 * j +
+                           gu_feature(r);
+        if (gu_matrix(r) == 0)
+          scale_fill(a.s0, a.b0, row, G, 128 * j + r, 128 * SUB, slot_ptr(slot));
+        else
+          scale_fill(a.s1, a.b1, row, G, 128 * j + r, 128 * SUB, slot_ptr(slot));
+      }
     };
     int w = blockIdx.x;
     Item cur, nxt, nn;
@@ -631,8 +661,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + ab * L::kAccCols;
       bool range_ok = true;
-      for (int cb = 0; cb < N; cb += 32) {
-        const bool last = cb + 32 >= N;
+      // 32-row chunks of each sub-slice's accumulator (columns js * BM + cb)
+      const int nch = (N + 31) / 32;
+      for (int ci = 0; ci < SUB * nch; ++ci) {
+        const int js = SUB == 1 ? 0 : ci / nch, cb = 32 * (SUB == 1 ? ci : ci % nch);
+        const bool last = ci == SUB * nch - 1;
         const int ncol = N - cb < 32 ? N - cb : 32;  // 16 or 32
         if (GATEUP) {
           // Lanes 0..15 of warp q hold the gate outputs g of features
@@ -641,7 +674,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // rows cb + rr and lanes 16..31 of rows cb + 16 + rr, each fetching
           // the other half's value of its row with one shuffle.
           uint32_t v[32];
-          tmem_ld32(tl + cb, v);
+          tmem_ld32(tl + js * BM + cb, v);
           tmem_ld_wait();
           if (last) {
             tc_fence_before();
@@ -649,7 +682,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
           const bool hi = lane >= 16;
-          const int feat = cur.slice * 64 + gu_feature(q * 32 + lane);
+          const int feat = cur.slice * L::kOutRows + 64 * js + gu_feature(q * 32 + lane);
           // H holds each 8-feature chunk in K-chunk order (it is the down
           // GEMM's K operand against weights rebuilt in that order), so
           // features e and e + 4 sit side by side: lanes with e < 4 store the
