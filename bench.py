@@ -369,8 +369,10 @@ class LayerRun:
         self.layers = []
         for l in range(self.nl):
             inp = synth.make_layer(shape, layer_seed(l, rank), device=dev, zipf_s=wl["zipf"])
-            self.layers.append((inp["x"], lily.LayerWeights(inp["router_w"], inp["router_b"],
-                                                            inp["experts"])))
+            w = lily.LayerWeights(inp["router_w"], inp["router_b"], inp["experts"])
+            if T > 8:  # weights are static: their router split is made once, at load
+                w.split_router()
+            self.layers.append((inp["x"], w))
         self.r = lily.RoutingBuffers(self.dims, dev)
         self.ws = lily.alloc_workspace(lily.lily_moe_workspace_bytes(self.dims), dev)
         self.y = torch.empty(T, d, dtype=lily.out_torch_dtype(self.dims), device=dev)
@@ -441,7 +443,7 @@ class StackPrefillRun:
         for l in range(self.nlay):
             wr, br = synth.make_router(E, d, layer_seed(l, rank) + 1, dev)
             ex = synth.make_experts(E, d, F, layer_seed(l, rank) + 2, dev)
-            self.weights.append(lily.LayerWeights(wr, br, ex))
+            self.weights.append(lily.LayerWeights(wr, br, ex).split_router())
         g = torch.Generator(device=dev)
         g.manual_seed(layer_seed(0, rank))
         self.x0 = torch.randn(self.T_total, d, generator=g, device=dev, dtype=torch.float32)
@@ -805,6 +807,8 @@ class Ablation:
         self.inp = synth.make_layer(shape, seed, device=dev, zipf_s=zipf)
         self.x = self.inp["x"]
         self.w = lily.LayerWeights(self.inp["router_w"], self.inp["router_b"], self.inp["experts"])
+        if T > 8:
+            self.w.split_router()
         self.r = lily.RoutingBuffers(self.dims, dev)
         self.ws = lily.alloc_workspace(lily.lily_moe_workspace_bytes(self.dims), dev)
         self.y_ref = torch.empty(T, d, dtype=torch.float32, device=dev)

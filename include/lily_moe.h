@@ -87,6 +87,12 @@ typedef struct {
  *   gate_s, gate_b, up_s, up_b  bf16 [E+1][F][d/64]  scale / bias per group
  *   down_q    uint8 [E+1][d][F/2]
  *   down_s, down_b  bf16 [E+1][d][F/64]
+ *   router_w_split  optional bf16 [3][E][d], 16-byte aligned: router_w split
+ *              exactly into three bf16 terms (hi + mid + lo == w) by
+ *              lily_moe_router_split.  The router (T > 8) runs on tensor cores
+ *              against this split; given here it is made once per set of
+ *              weights, else every call splits router_w into the workspace.
+ *              The logits are the same bits either way.
  */
 typedef struct {
   const float* router_w;
@@ -100,6 +106,7 @@ typedef struct {
   const uint8_t* down_q;
   const uint16_t* down_s;
   const uint16_t* down_b;
+  const void* router_w_split;  // optional, see lily_moe_router_split; NULL = split per call
 } lily_moe_weights;
 
 /* Routing outputs, caller-owned device buffers (P = T*k pairs, pair p = t*k+j).
@@ -234,6 +241,19 @@ int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x
 /* Turn the end-to-end graph cache on (enable != 0, the default) or off; either
  * way every cached graph is destroyed.  Returns the previous setting (0/1). */
 int lily_moe_host_graphs(int enable);
+
+/* The exact three-term bf16 split of a router weight matrix (see
+ * lily_moe_weights.router_w_split), written to `split` on `stream`.
+ *   router_w  fp32 [n_experts][d_model] device, 16-byte aligned
+ *   split     device, lily_moe_router_split_bytes(n_experts, d_model) bytes,
+ *             16-byte aligned, caller-owned
+ * Weights are static between calls, so a caller splits once after loading
+ * them (as it packs the 4-bit codes).  Errors: LILY_ERR_INVALID_ARG,
+ * LILY_ERR_UNSUPPORTED_SHAPE (d_model not a multiple of 128 in [128, 4096],
+ * n_experts > 256), LILY_ERR_MISALIGNED, LILY_ERR_CUDA. */
+size_t lily_moe_router_split_bytes(int32_t n_experts, int32_t d_model);
+int lily_moe_router_split(const float* router_w, int32_t n_experts, int32_t d_model,
+                          void* split, void* stream);
 
 /* Unit-weight RMSNorm, out = bf16(x / sqrt(mean(x^2) + eps)), x fp32 [T][d],
  * out bf16 [T][d].  The pre-norm of the stacked-layer prefill. */

@@ -161,3 +161,22 @@ def test_static_decode_refuses_rows_before_size(L):
     big = lily.make_dims(8, 4096, 256, 8, 4096, 128)
     assert L.lily_moe_decode_static(ctypes.byref(big), 256, ctypes.byref(w), ctypes.byref(r),
                                     256, None) == lily.LILY_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_router_split_arguments(L):
+    """The one-time router split reports its size and checks its arguments
+    before any CUDA call; a misaligned split in the weights is refused."""
+    assert L.lily_moe_router_split_bytes(256, 2048) == 3 * 256 * 2048 * 2
+    assert L.lily_moe_router_split_bytes(0, 2048) == 0
+    assert L.lily_moe_router_split(None, 256, 2048, 256, None) == lily.LILY_ERR_INVALID_ARG
+    assert L.lily_moe_router_split(256, 256, 2048, None, None) == lily.LILY_ERR_INVALID_ARG
+    assert L.lily_moe_router_split(256, 257, 2048, 256, None) == lily.LILY_ERR_INVALID_ARG
+    assert L.lily_moe_router_split(256, 256, 2000, 256, None) == lily.LILY_ERR_UNSUPPORTED_SHAPE
+    assert L.lily_moe_router_split(264, 256, 2048, 256, None) == lily.LILY_ERR_MISALIGNED
+    assert L.lily_moe_router_split(256, 256, 2048, 264, None) == lily.LILY_ERR_MISALIGNED
+    d = lily.make_dims(64, 512, 32, 4, 128, 32)
+    wt = _lib.Weights(*([256] * 11))
+    wt.router_w_split = 264
+    rt = _lib.Routing(*([256] * 9))
+    assert L.lily_moe_forward(ctypes.byref(d), 16, ctypes.byref(wt), ctypes.byref(rt), 16, 16,
+                              1 << 40, None) == lily.LILY_ERR_MISALIGNED

@@ -37,6 +37,7 @@ EXPORTS = (
     "lily_moe_decode_static",
     "lily_moe_forward_host", "lily_moe_host_graphs",
     "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_decode",
+    "lily_moe_router_split_bytes", "lily_moe_router_split",
     "lily_moe_stack_workspace_bytes",
     "lily_moe_status", "lily_moe_set_route_wait_ns", "lily_moe_strerror", "lily_moe_profile_enable", "lily_moe_profile_read",
     "lily_moe_kernel_name", "lily_moe_version",
@@ -62,7 +63,7 @@ class Dims(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "router_w", "router_bias", "gate_q", "gate_s", "gate_b", "up_q", "up_s", "up_b",
-        "down_q", "down_s", "down_b")]
+        "down_q", "down_s", "down_b", "router_w_split")]
 
 
 class Routing(ctypes.Structure):
@@ -97,6 +98,8 @@ def lib():
             "lily_moe_forward_host": (I, [DP, P, P, WP, RP, P, P, P, SZ, P]),
             "lily_moe_host_graphs": (I, [I]),
             "lily_moe_rmsnorm": (I, [ctypes.c_int32, ctypes.c_int32, P, ctypes.c_float, P, P]),
+            "lily_moe_router_split_bytes": (SZ, [ctypes.c_int32, ctypes.c_int32]),
+            "lily_moe_router_split": (I, [P, ctypes.c_int32, ctypes.c_int32, P, P]),
             "lily_moe_stack_prefill": (I, [DP, ctypes.c_int32, ctypes.c_int32, WP, P,
                                            ctypes.c_float, P, P, P, SZ, P]),
             "lily_moe_stack_decode": (I, [DP, ctypes.c_int32, WP, P, ctypes.c_float, P, P, P,
@@ -184,17 +187,30 @@ def _cached_view(owner, refs: tuple, struct):
 
 @dataclass
 class LayerWeights:
-    """torch tensors of one layer; .c is the ctypes view (keeps the tensors alive)."""
+    """torch tensors of one layer; .c is the ctypes view (keeps the tensors alive).
+    router_split: the router weights' three-term bf16 split made once by
+    lily_moe_router_split (or None: the library splits on every call)."""
     router_w: torch.Tensor
     router_b: torch.Tensor | None
     experts: dict
+    router_split: torch.Tensor | None = None
 
     @property
     def c(self) -> Weights:
         e = self.experts
         refs = (self.router_w, self.router_b, e["gate_q"], e["gate_s"], e["gate_b"], e["up_q"],
-                e["up_s"], e["up_b"], e["down_q"], e["down_s"], e["down_b"])
+                e["up_s"], e["up_b"], e["down_q"], e["down_s"], e["down_b"], self.router_split)
         return _cached_view(self, refs, Weights)
+
+    def split_router(self, stream=None) -> "LayerWeights":
+        """Make the router weights' split once (lily_moe_router_split); later
+        calls with these weights skip the per-call split."""
+        E, d = self.router_w.shape
+        n = lib().lily_moe_router_split_bytes(E, d)
+        buf = torch.empty(n // 2, dtype=torch.bfloat16, device=self.router_w.device)
+        lily_moe_router_split(self.router_w, buf, stream)
+        self.router_split = buf
+        return self
 
 
 class RoutingBuffers:
@@ -272,6 +288,12 @@ def lily_moe_host_graphs(enable: bool) -> bool:
     """Turn the end-to-end call's graph cache on or off (dropping cached
     graphs); returns the previous setting."""
     return bool(lib().lily_moe_host_graphs(1 if enable else 0))
+
+
+def lily_moe_router_split(router_w, split, stream=None):
+    E, d = router_w.shape
+    _check(lib().lily_moe_router_split(_ptr(router_w), E, d, _ptr(split), _stream(stream)),
+           "lily_moe_router_split")
 
 
 def lily_moe_rmsnorm(x, out, eps=1e-6, stream=None):

@@ -157,7 +157,8 @@ int check_weights(const lily_moe_weights* w, bool need_router, bool need_experts
   if (!w) return LILY_ERR_INVALID_ARG;
   if (need_router) {
     if (!w->router_w) return LILY_ERR_INVALID_ARG;
-    if (!aligned16(w->router_w) || (w->router_bias && !aligned16(w->router_bias)))
+    if (!aligned16(w->router_w) || (w->router_bias && !aligned16(w->router_bias)) ||
+        (w->router_w_split && !aligned16(w->router_w_split)))
       return LILY_ERR_MISALIGNED;
   }
   if (need_experts) {
@@ -251,7 +252,8 @@ int do_route(const lily_moe_dims& d, const void* x, const float* logits_in,
     if (d.T > 8) {
       float* part = reinterpret_cast<float*>(base + L.part);
       cudaError_t e = launch_router_tc(x, w->router_w, w->router_bias, d.T, d.d_model,
-                                       d.n_experts, base + L.w3, part, r.logits, ws_status(ws), s);
+                                       d.n_experts, base + L.w3, w->router_w_split, part,
+                                       r.logits, ws_status(ws), s);
       if (e != cudaSuccess) return LILY_ERR_CUDA;
     } else {
       return do_dec_router(d, x, w, r, ws, s);  // routes in its last CTA
@@ -622,6 +624,21 @@ int lily_moe_host_graphs(int enable) {
   g_hg.clear();
   g_hg_on = enable != 0;
   return was;
+}
+
+size_t lily_moe_router_split_bytes(int32_t n_experts, int32_t d_model) {
+  if (n_experts < 1 || d_model < 1) return 0;
+  return (size_t)3 * n_experts * d_model * 2;
+}
+
+int lily_moe_router_split(const float* router_w, int32_t n_experts, int32_t d_model, void* split,
+                          void* stream) {
+  if (!router_w || !split || n_experts < 1 || n_experts > 256) return LILY_ERR_INVALID_ARG;
+  if (d_model % 128 || d_model < 128 || d_model > 4096) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(router_w) || !aligned16(split)) return LILY_ERR_MISALIGNED;
+  int rc = check_arch();
+  if (rc) return rc;
+  return cuda_rc(launch_router_split(router_w, n_experts, d_model, split, (cudaStream_t)stream));
 }
 
 int lily_moe_rmsnorm(int32_t T, int32_t d, const float* x, float eps, void* out, void* stream) {

@@ -113,9 +113,11 @@ cudaError_t launch_dec_router(const DecRouterArgs& a, bool norm, cudaStream_t s)
 // [router_splits(T,d)][T][E]) summed in order into logits (+ bias).
 int router_splits(int T, int d);
 size_t router_tc_smem(int E);
+// w_presplit: the same split made ahead by launch_router_split, or NULL.
 cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, int T, int d,
-                             int E, void* w_split, float* partial, float* logits, uint32_t* status,
-                             cudaStream_t s);
+                             int E, void* w_split, const void* w_presplit, float* partial,
+                             float* logits, uint32_t* status, cudaStream_t s);
+cudaError_t launch_router_split(const float* w, int E, int d, void* w_split, cudaStream_t s);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 int route_max_blocks();  // co-resident blocks of the routing kernel (0 = unknown)
 

@@ -233,9 +233,23 @@ __global__ void __launch_bounds__(256) router_reduce_kernel(const float* __restr
   }
 }
 
+cudaError_t launch_router_split(const float* w, int E, int d, void* w_split, cudaStream_t s) {
+  const int64_t n_w = (int64_t)E * d;
+  int pblocks = (int)((n_w / 4 + 255) / 256);
+  if (pblocks > 152 * 8) pblocks = 152 * 8;
+  prof_begin(K_ROUTER_PREP, s);
+  const cudaError_t err = launch_pdl(router_prep_kernel, dim3(pblocks), dim3(256), 0, s, w,
+                                     static_cast<__nv_bfloat16*>(w_split), n_w);
+  prof_end(K_ROUTER_PREP, s);
+  return err;
+}
+
 cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, int T, int d,
-                             int E, void* w_split, float* partial, float* logits, uint32_t* status,
-                             cudaStream_t s) {
+                             int E, void* w_split, const void* w_presplit, float* partial,
+                             float* logits, uint32_t* status, cudaStream_t s) {
+  // a split made once ahead (weights do not change between calls) replaces
+  // the per-call split into the workspace
+  void* wsp = w_presplit ? const_cast<void*>(w_presplit) : w_split;
   const int NE = router_ne(E);
   CUtensorMap tm_x, tm_w;
   {
@@ -250,18 +264,15 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
     uint64_t dims[2] = {(uint64_t)d, (uint64_t)3 * E};
     uint64_t strides[1] = {(uint64_t)d * 2};
     uint32_t box[2] = {64, (uint32_t)NE};
-    if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_split, dims, strides, box,
+    if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wsp, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const int64_t n_w = (int64_t)E * d;
-  int pblocks = (int)((n_w / 4 + 255) / 256);
-  if (pblocks > 152 * 8) pblocks = 152 * 8;
-  prof_begin(K_ROUTER_PREP, s);
-  cudaError_t err = launch_pdl(router_prep_kernel, dim3(pblocks), dim3(256), 0, s, w,
-                               static_cast<__nv_bfloat16*>(w_split), n_w);
-  prof_end(K_ROUTER_PREP, s);
-  if (err != cudaSuccess) return err;
+  cudaError_t err = cudaSuccess;
+  if (!w_presplit) {
+    err = launch_router_split(w, E, d, w_split, s);
+    if (err != cudaSuccess) return err;
+  }
   const size_t smem = router_tc_smem(E);
   err = ensure_smem_attr((const void*)router_tc_kernel, smem);
   if (err != cudaSuccess) return err;
