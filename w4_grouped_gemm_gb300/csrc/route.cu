@@ -372,19 +372,21 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
         if (tl < ntok && lane + 32 * c < E) a.logits_dst[(size_t)(t0 + tl) * E + lane + 32 * c] = lv[i][c];
     }
   }
+  // the warp's tokens' selections interleaved (tokens past the end select
+  // from zeros and are not stored)
+  int my_id[kWarpTok];
+  float my_gate[kWarpTok];
+  const uint32_t nan_mask = warp_topk_multi<kWarpTok>(lv, E, k, my_id, my_gate);
 #pragma unroll
   for (int i = 0; i < kWarpTok; ++i) {
     const int tl = warp * kWarpTok + i;
     if (tl >= ntok) break;
     const int t = t0 + tl;
-    int my_id;
-    float my_gate;
-    if (warp_topk(lv[i], E, k, my_id, my_gate) && lane == 0)
-      set_status(a.status, LILY_STATUS_NAN_LOGIT);
+    if (((nan_mask >> i) & 1u) && lane == 0) set_status(a.status, LILY_STATUS_NAN_LOGIT);
     if (lane < k) {
-      a.ids[(size_t)t * k + lane] = my_id;
-      a.gates[(size_t)t * k + lane] = my_gate;
-      s_ids[tl * k + lane] = my_id;
+      a.ids[(size_t)t * k + lane] = my_id[i];
+      a.gates[(size_t)t * k + lane] = my_gate[i];
+      s_ids[tl * k + lane] = my_id[i];
     }
   }
   // ---- phase 2: block histogram and stable local rank of each pair (one

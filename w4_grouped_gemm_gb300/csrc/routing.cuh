@@ -111,6 +111,76 @@ __device__ __forceinline__ bool warp_topk(const float (&lv)[kMaxE / 32], int E, 
   return __any_sync(0xffffffffu, saw_nan);
 }
 
+// warp_topk for NT tokens at once (lv[i] the logits of token i, as above):
+// the same selection, with the NT tokens' rounds interleaved so that their
+// reduction latencies overlap.  Returns a bit mask of the tokens with a NaN
+// logit.
+template <int NT>
+__device__ __forceinline__ uint32_t warp_topk_multi(const float (&lv)[NT][kMaxE / 32], int E,
+                                                    int k, int (&my_id)[NT],
+                                                    float (&my_gate)[NT]) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[NT][kMaxE / 32];
+  uint32_t avail[NT];
+  uint32_t nan_mask = 0;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    avail[i] = 0;
+    bool saw_nan = false;
+#pragma unroll
+    for (int c = 0; c < kMaxE / 32; ++c) {
+      const int e = lane + 32 * c;
+      key[i][c] = 0;
+      if (e < E) {
+        saw_nan |= (lv[i][c] != lv[i][c]);
+        key[i][c] = logit_key(lv[i][c]);
+        avail[i] |= 1u << c;
+      }
+    }
+    if (__any_sync(0xffffffffu, saw_nan)) nan_mask |= 1u << i;
+  }
+  float my_logit[NT];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    my_logit[i] = 0.f;
+    my_id[i] = 0;
+  }
+  for (int j = 0; j < k; ++j) {
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      // lane-local best: largest key, lowest id on ties (c ascending = id ascending)
+      uint32_t bk = 0;
+      int bc = -1;
+#pragma unroll
+      for (int c = 0; c < kMaxE / 32; ++c)
+        if ((avail[i] >> c) & 1u)
+          if (bc < 0 || key[i][c] > bk) {
+            bk = key[i][c];
+            bc = c;
+          }
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, bc >= 0 ? bk : 0u);
+      const uint32_t cand = (bc >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bc) : 0xFFFFFFFFu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      if ((int)(win & 31u) == lane) avail[i] &= ~(1u << (win >> 5));
+      if (lane == j) {
+        my_logit[i] = key_logit(kmax);
+        my_id[i] = (int)win;
+      }
+    }
+  }
+  // gates: softmax over the kept logits; entries equal to the largest weigh 1
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const float lmax = __shfl_sync(0xffffffffu, my_logit[i], 0);
+    float wgt = 0.f;
+    if (lane < k) wgt = (my_logit[i] == lmax) ? 1.f : expf(my_logit[i] - lmax);
+    float z = wgt;
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    my_gate[i] = lane < k ? wgt / z : 0.f;
+  }
+  return nan_mask;
+}
+
 // ------------------------------------------------------------- small T
 // One tile slot of a decode step: slot 0 is the shared expert (all T rows,
 // weight 1), slot i >= 1 is block-map tile i-1.  row0 is the slot's first row
