@@ -106,7 +106,7 @@ struct Layout {
 Layout layout(const lily_moe_dims& d) {
   const size_t T = d.T, E = d.n_experts, k = d.top_k, F = d.d_ff, D = d.d_model;
   const size_t P = T * k;
-  const size_t nblk = (T + kRouteTok - 1) / kRouteTok;
+  const size_t nblk = (size_t)route_blocks((int)T);
   Layout L;
   size_t off = 0;
   L.ctrl = off; off += up(256);
@@ -546,7 +546,7 @@ int lily_moe_route(const lily_moe_dims* dims, const void* x, const float* logits
   if ((rc = check_ws(dims, ws, ws_bytes))) return rc;
   if ((rc = check_arch())) return rc;
   const int maxb = route_max_blocks();
-  if (maxb > 0 && (dims->T + kRouteTok - 1) / kRouteTok > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (maxb > 0 && route_blocks(dims->T) > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
   return do_route(*dims, x, logits_in, w, *r, ws, (cudaStream_t)stream);
 }
 
@@ -562,7 +562,7 @@ int lily_moe_forward(const lily_moe_dims* dims, const void* x, const lily_moe_we
   int rc = common_checks(dims, x, w, r, y, ws, ws_bytes, true);
   if (rc) return rc;
   const int maxb = route_max_blocks();
-  if (maxb > 0 && (dims->T + kRouteTok - 1) / kRouteTok > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
+  if (maxb > 0 && route_blocks(dims->T) > maxb) return LILY_ERR_UNSUPPORTED_SHAPE;
   return do_forward(*dims, x, w, *r, ws, (cudaStream_t)stream, y);
 }
 

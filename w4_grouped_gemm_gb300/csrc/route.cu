@@ -332,10 +332,12 @@ __device__ bool grid_barrier(uint32_t* bar, uint32_t nblocks, uint32_t* status,
   return s_ok != 0;
 }
 
-// Routing of tokens [blk * kRouteTok, ...) as block blk of nblk (the body of
-// route_kernel; also run by the last block of the small-T router launch with
-// blk = 0, nblk = 1).  Needs kRouteThreads threads.
+// Routing of tokens [blk * 8 * WT, ...) as block blk of nblk (the body of
+// route_kernel; WT tokens per warp).  Needs kRouteThreads threads.
+template <int WT>  // tokens per warp
 __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk) {
+  constexpr int kBlkTok = 8 * WT;  // tokens per block
+  static_assert(kBlkTok <= kRouteTok, "shared arrays hold kRouteTok tokens");
   __shared__ int s_ids[kRouteTok * kMaxK];
   __shared__ int s_rank[kRouteTok * kMaxK];
   __shared__ int s_cnt[kMaxE];
@@ -345,12 +347,12 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
 
   const int T = a.T, E = a.E, k = a.k;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blk * kRouteTok;
-  const int ntok = min(kRouteTok, T - t0);
+  const int t0 = blk * kBlkTok;
+  const int ntok = min(kBlkTok, T - t0);
   const int npair = ntok * k;
 
   // ---- phase 1: top-k + gates, one warp per token (4 tokens per warp)
-  constexpr int kWarpTok = kRouteTok / 8;
+  constexpr int kWarpTok = WT;
   // logits of this warp's tokens (lane holds experts lane + 32c), all loads
   // of the warp issued together
   float lv[kWarpTok][kMaxE / 32];
@@ -484,10 +486,11 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
   }
 }
 
+template <int WT>
 __global__ void __launch_bounds__(kRouteThreads, 4) route_kernel(RouteArgs a) {
   pdl_wait();  // the logits come from the predecessor
   pdl_trigger();
-  route_body(a, blockIdx.x, gridDim.x);
+  route_body<WT>(a, blockIdx.x, gridDim.x);
 }
 
 int route_max_blocks() {
@@ -496,22 +499,28 @@ int route_max_blocks() {
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
   if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, route_kernel, kRouteThreads, 0) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, route_kernel<4>, kRouteThreads, 0) !=
       cudaSuccess)
     return 0;
   if (dev >= 0 && dev < 64) cached[dev] = nsm * per;
   return nsm * per;
 }
 
-cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
-  const int nblk = (a.T + kRouteTok - 1) / kRouteTok;
+template <int WT>
+static cudaError_t launch_route_wt(const RouteArgs& a, cudaStream_t s) {
+  const int nblk = (a.T + 8 * WT - 1) / (8 * WT);
   RouteArgs args = a;
   void* params[] = {&args};
-  prof_begin(K_ROUTE, s);
   // one block needs no co-residency guarantee: a plain launch is cheaper
-  cudaError_t err = nblk == 1 ? launch_pdl(route_kernel, dim3(1), dim3(kRouteThreads), 0, s, args)
-                              : cudaLaunchCooperativeKernel((const void*)route_kernel, dim3(nblk),
-                                                            dim3(kRouteThreads), params, 0, s);
+  return nblk == 1 ? launch_pdl(route_kernel<WT>, dim3(1), dim3(kRouteThreads), 0, s, args)
+                   : cudaLaunchCooperativeKernel((const void*)route_kernel<WT>, dim3(nblk),
+                                                 dim3(kRouteThreads), params, 0, s);
+}
+
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
+  prof_begin(K_ROUTE, s);
+  const cudaError_t err =
+      route_tok(a.T) == 16 ? launch_route_wt<2>(a, s) : launch_route_wt<4>(a, s);
   prof_end(K_ROUTE, s);
   return err;
 }
