@@ -39,10 +39,10 @@ void prof_end(int kind, cudaStream_t s);
 
 // Tokens handled by one block of the routing kernel.
 constexpr int kRouteTok = 32;  // tokens per routing block, at most
-// Tokens per routing block: 16 (two per warp) up to T = 512, where the
+// Tokens per routing block: 16 (two per warp) up to T = 2048, where the
 // block-parallel top-k is the routing kernel's longest phase and SMs are
 // idle, else 32 (more blocks would lengthen the histogram sums).
-__host__ __device__ inline int route_tok(int T) { return T <= 512 ? 16 : 32; }
+__host__ __device__ inline int route_tok(int T) { return T <= 2048 ? 16 : 32; }
 __host__ __device__ inline int route_blocks(int T) { return (T + route_tok(T) - 1) / route_tok(T); }
 constexpr int kRouteThreads = 256;
 

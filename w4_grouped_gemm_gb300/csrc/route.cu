@@ -430,7 +430,7 @@ __device__ __forceinline__ void route_body(const RouteArgs& a, int blk, int nblk
     for (int e = threadIdx.x; e < kMaxE; e += kRouteThreads) {
       int cnt = 0, before = 0;
       if (e < E) {
-#pragma unroll 8
+#pragma unroll 16
         for (int b = 0; b < nblk; ++b) {
           int h = __ldcg(&a.hist[(size_t)b * E + e]);
           cnt += h;
