@@ -917,7 +917,17 @@ __global__ void __launch_bounds__(256) token_rows_kernel(const uint4* __restrict
     }
     const uint4* src = x + (size_t)tok * d8;
     uint4* dst = row < P ? xs + (size_t)row * d8 : x16 + (size_t)(row - P) * d8;
-    for (int c = lane; c < d8; c += 32) dst[c] = bf8_to_h8_kchunk(__ldg(src + c), ok);
+    // up to eight loads of the row in flight per lane before the stores
+    constexpr int kU = 8;
+    for (int c0 = lane; c0 < d8; c0 += 32 * kU) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (c0 + 32 * u < d8) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+        if (c0 + 32 * u < d8) dst[c0 + 32 * u] = bf8_to_h8_kchunk(v[u], ok);
+    }
   }
   if (!ok) set_status(status, LILY_STATUS_F16_RANGE);
 }
