@@ -460,7 +460,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
                       const __grid_constant__ CUtensorMap tm_u, const DecodeArgs a,
                       const int nstages) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so
+  // the compiler keeps the accesses in the shared window (not generic)
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int T = a.T, d = a.d, F = a.F, G = d / 64;
   const int rb = box_bytes(d / 2), rbs = rb == 128 ? 7 : 6;
   const uint32_t SB = gu_stage_bytes(d);
@@ -643,7 +645,9 @@ __global__ void __launch_bounds__(kDecThreads, kDecMinBlocks)
     dec_down_kernel(const __grid_constant__ CUtensorMap tm_d, const DecodeArgs a,
                     const int nstages) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so
+  // the compiler keeps the accesses in the shared window (not generic)
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int T = a.T, F = a.F, G = F / 64;
   const int rb = box_bytes(F / 2), rbs = rb == 128 ? 7 : 6;
   const uint32_t SB = dn_stage_bytes(F);

@@ -296,7 +296,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   // ---- shared memory carve-up
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so
+  // the compiler keeps the accesses in the shared window (not generic)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* stage_base = smem;
   uint32_t* sb = (uint32_t*)(smem + (size_t)nstages * STAGE);  // [nsb][G][128*SUB] scale|bias<<16
   const int sb_words = G * 128 * SUB;                        // one table

@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      int T, int d, int E, int NE, float* __restrict__ partial, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // aligned up to 1024 bytes by pointer arithmetic on the shared array, so
+  // the compiler keeps the accesses in the shared window (not generic)
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int ABYTES = 128 * 128, STAGE = ABYTES + NE * 128;
   uint64_t* full = (uint64_t*)(smem + kRtStages * STAGE);
   uint64_t* empty = full + kRtStages;
