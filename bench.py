@@ -78,11 +78,11 @@ NCU_TRAFFIC = {  # {(workload, kernel, source_hash): bytes per launch}
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel,
     # from the launch list of `bench.py --workload W --eager --steps 3
     # --warmup 3 --layers 1 --no-cpu-baseline --no-e2e` (mean over launches)
-    ("prefill512", "gateup_gemm", "5fe1f7f30f4ea538"): 325326096,  # 322.24 + 3.09 MB
-    ("prefill2048_zipf", "gateup_gemm", "5fe1f7f30f4ea538"): 227837568,  # 210.14 + 17.70 MB
-    ("prefill8192", "gateup_gemm", "5fe1f7f30f4ea538"): 670289376,  # 605.29 + 65.00 MB
-    ("decode1", "dec_router", "802e9bed095d3d43"): 3929440,  # 3.93 MB read
-    ("decode1", "dec_gateup", "802e9bed095d3d43"): 10657344,  # 10.66 MB read
+    ("prefill512", "gateup_gemm", "038835181a10f4f7"): 325321424,  # 322.24 + 3.08 MB
+    ("prefill2048_zipf", "gateup_gemm", "038835181a10f4f7"): 227774416,  # 210.14 + 17.63 MB
+    ("prefill8192", "gateup_gemm", "038835181a10f4f7"): 670235824,  # 605.31 + 64.92 MB
+    ("decode1", "dec_router", "1e4732c2b0694c6c"): 3929168,  # 3.93 MB read
+    ("decode1", "dec_gateup", "1e4732c2b0694c6c"): 10655856,  # 10.66 MB read
 }
 
 
