@@ -368,16 +368,19 @@ __global__ void __launch_bounds__(kDecRouterThreads) dec_router_kernel(const Dec
     const float sum = warp_sum(lo + hi);
     if (lane == 0) a.xsg[u] = sum;
   }
-  // the CTA that finishes last routes: every CTA makes its logits visible and
-  // counts itself done; the last one then sees every logit
+  // the CTA that finishes last routes: every CTA counts itself done with one
+  // acquire-release add (after the CTA barrier, so it orders every write of
+  // the CTA before it, and the last CTA's reads of the logits after it)
   __shared__ int s_last;
   __shared__ __align__(16) float s_lg[kDecMaxRows * kMaxE];
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(a.done, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.done) : "memory");
+    s_last = old == gridDim.x - 1;
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   for (int i = threadIdx.x; i < T * E; i += kDecRouterThreads) s_lg[i] = __ldcg(a.logits + i);
   __syncthreads();
   DecPlan* plan = static_cast<DecPlan*>(a.plan);
