@@ -81,8 +81,8 @@ NCU_TRAFFIC = {  # {(workload, kernel, source_hash): bytes per launch}
     ("prefill512", "gateup_gemm", "038835181a10f4f7"): 325321424,  # 322.24 + 3.08 MB
     ("prefill2048_zipf", "gateup_gemm", "038835181a10f4f7"): 227774416,  # 210.14 + 17.63 MB
     ("prefill8192", "gateup_gemm", "038835181a10f4f7"): 670235824,  # 605.31 + 64.92 MB
-    ("decode1", "dec_router", "1e4732c2b0694c6c"): 3929168,  # 3.93 MB read
-    ("decode1", "dec_gateup", "1e4732c2b0694c6c"): 10655856,  # 10.66 MB read
+    ("decode1", "dec_router", "549388bb5c81e12a"): 3928672,  # 3.93 MB read
+    ("decode1", "dec_gateup", "549388bb5c81e12a"): 10657264,  # 10.66 MB read
 }
 
 
