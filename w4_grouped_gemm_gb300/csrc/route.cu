@@ -66,14 +66,25 @@ int router_splits(int T, int d) {
 }
 
 static int router_ne(int E) { return (E + 15) & ~15; }
-
-size_t router_tc_smem(int E) {
-  return 1024 + (size_t)kRtStages * (128 * 128 + router_ne(E) * 128) + 16 * 8 + 16;
+// Experts per CTA: all of them, or -- while twice the CTAs still fit on the
+// SMs at once, from 128 experts on in multiples of 32 -- half of them, two
+// CTAs per token tile and split: twice the SMs pulling the split weights
+// through, each half the bytes per step.  (With the grid already filling the
+// SMs, a second wave measured slower: T = 2048 and 8192.)
+static int router_nec(int E, int ctas, int sms) {
+  const int NE = router_ne(E);
+  return (NE >= 128 && NE % 32 == 0 && 2 * ctas <= sms) ? NE / 2 : NE;
 }
+
+static size_t router_tc_smem_nec(int NEc) {
+  return 1024 + (size_t)kRtStages * (128 * 128 + NEc * 128) + 16 * 8 + 16;
+}
+size_t router_tc_smem(int E) { return router_tc_smem_nec(router_ne(E)); }
 
 __global__ void __launch_bounds__(kRtThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                      int T, int d, int E, int NE, float* __restrict__ partial, uint32_t* status) {
+  // NE: experts of this CTA (a multiple of 16), from expert n0 = blockIdx.z * NE
   extern __shared__ uint8_t smem_raw[];
   // aligned up to 1024 bytes by pointer arithmetic on the shared array, so
   // the compiler keeps the accesses in the shared window (not generic)
@@ -85,7 +96,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   int* misc = (int*)(accfull + 1);
   volatile int* abort = misc;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * 128, split = blockIdx.y, S = gridDim.y;
+  const int m0 = blockIdx.x * 128, split = blockIdx.y, S = gridDim.y, n0 = blockIdx.z * NE;
   const int KB = d / 64, KS = 3 * KB;
   const int ks0 = split * KS / S, nk = (split + 1) * KS / S - ks0;
   uint32_t tcols = 32;
@@ -126,7 +137,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         uint8_t* sp = smem + (size_t)st * STAGE;
         mbar_arrive_expect_tx(fb, (uint32_t)STAGE);
         tma_load_2d(smem_u32(sp), &tm_x, kb * 64, m0, fb);
-        tma_load_2d(smem_u32(sp + ABYTES), &tm_w, kb * 64, term * E, fb);
+        tma_load_2d(smem_u32(sp + ABYTES), &tm_w, kb * 64, term * E + n0, fb);
       }
       if (*abort) {  // let copies still in flight land before exit
         int never = 0;
@@ -162,13 +173,13 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       tc_fence_after();
       const int q = warp & 3;
       const int t = m0 + q * 32 + lane;
-      float* dst = partial + ((size_t)split * T + t) * E;
+      float* dst = partial + ((size_t)split * T + t) * E + n0;
       for (int cb = 0; cb < NE; cb += 32) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + cb, v);
         tmem_ld_wait();
         if (t < T) {
-          if ((E & 3) == 0 && cb + 32 <= E) {
+          if ((E & 3) == 0 && cb + 32 <= NE && n0 + cb + 32 <= E) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
               *reinterpret_cast<float4*>(dst + cb + j) =
@@ -177,7 +188,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (cb + j < E) dst[cb + j] = __uint_as_float(v[j]);
+              if (cb + j < NE && n0 + cb + j < E) dst[cb + j] = __uint_as_float(v[j]);
           }
         }
       }
@@ -252,7 +263,12 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
   // a split made once ahead (weights do not change between calls) replaces
   // the per-call split into the workspace
   void* wsp = w_presplit ? const_cast<void*>(w_presplit) : w_split;
-  const int NE = router_ne(E);
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 0;
+  const int ctas = ((T + 127) / 128) * router_splits(T, d);
+  const int NEc = router_nec(E, ctas, sms), nN = router_ne(E) / NEc;
   CUtensorMap tm_x, tm_w;
   {
     uint64_t dims[2] = {(uint64_t)d, (uint64_t)T};
@@ -265,7 +281,7 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
   {
     uint64_t dims[2] = {(uint64_t)d, (uint64_t)3 * E};
     uint64_t strides[1] = {(uint64_t)d * 2};
-    uint32_t box[2] = {64, (uint32_t)NE};
+    uint32_t box[2] = {64, (uint32_t)NEc};
     if (encode_tiled(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wsp, dims, strides, box,
                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -275,12 +291,12 @@ cudaError_t launch_router_tc(const void* x, const float* w, const float* bias, i
     err = launch_router_split(w, E, d, w_split, s);
     if (err != cudaSuccess) return err;
   }
-  const size_t smem = router_tc_smem(E);
+  const size_t smem = router_tc_smem_nec(NEc);
   err = ensure_smem_attr((const void*)router_tc_kernel, smem);
   if (err != cudaSuccess) return err;
-  dim3 grid((T + 127) / 128, router_splits(T, d));
+  dim3 grid((T + 127) / 128, router_splits(T, d), nN);
   prof_begin(K_ROUTER_GEMM, s);
-  err = launch_pdl(router_tc_kernel, grid, dim3(kRtThreads), smem, s, tm_x, tm_w, T, d, E, NE,
+  err = launch_pdl(router_tc_kernel, grid, dim3(kRtThreads), smem, s, tm_x, tm_w, T, d, E, NEc,
                    partial, status);
   prof_end(K_ROUTER_GEMM, s);
   if (err != cudaSuccess) return err;
