@@ -42,6 +42,8 @@ def test_small_layer_all_tile_rows(oracle_lib, bm):
     (synth.LayerShape(130, 384, 24, 5, 256), 64),     # 2 F slices, 3 d slices
     (synth.LayerShape(9, 512, 32, 4, 128), 32),       # smallest prefill T
     (synth.LayerShape(257, 128, 8, 8, 128), 128),     # E == k: every expert chosen
+    (synth.LayerShape(150, 256, 8, 2, 4096), 128),    # largest F: a 3-stage down ring
+    (synth.LayerShape(70, 4096, 4, 2, 128), 64),      # largest d: one gate/up scale table
 ])
 def test_ragged_layers(oracle_lib, shape, bm):
     _check_forward(Layer(shape, seed=shape.T * 7, tile_rows=bm))

@@ -279,7 +279,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr int BBYTES = L::kBBytes;
   constexpr int STAGE = L::kStage;
   constexpr int NACC = L::kNumAcc;
-  constexpr int NA = L::kNumA;
+  // A buffers in use: at most the stage count.  A dequant warp at step it
+  // knows only that the MMAs of step it - NA have finished; its parity wait
+  // on the stage of step it is sound only if the stage's previous use (step
+  // it - nstages) has landed, i.e. if nstages >= NA.
+  const int NA = L::kNumA < nstages ? L::kNumA : nstages;
   constexpr int SUB = L::kSub;
 
   const int K = GATEUP ? a.d : a.F;     // reduction length
