@@ -547,10 +547,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 sb_word(__ldg(a.s0 + row * G + grp), __ldg(a.b0 + row * G + grp));
       }
     };
+    // table entries two items ahead: the next item's entry (for the scale
+    // prefetch below) was requested one item earlier, not just now
+    const int g1 = (int)gridDim.x;
     int4 tnext = (int)blockIdx.x < n_items ? load_tile(a, blockIdx.x, nslices) : make_int4(0, 0, 0, 0);
-    for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+    int4 tnext2 = (int)blockIdx.x + g1 < n_items ? load_tile(a, blockIdx.x + g1, nslices)
+                                                 : make_int4(0, 0, 0, 0);
+    for (int w = blockIdx.x; ok && w < n_items; w += g1) {
       const int4 tcur = tnext;
-      if (w + (int)gridDim.x < n_items) tnext = load_tile(a, w + gridDim.x, nslices);
+      tnext = tnext2;  // item w + g1
+      if (w + 2 * g1 < n_items) tnext2 = load_tile(a, w + 2 * g1, nslices);
       Item itm;
       if (!item_from(tcur, w, nslices, nsh, itm)) continue;
       const int slot = GATEUP ? j % nsb : (int)par;
@@ -646,6 +652,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     int wn = w + gridDim.x;
     bool have_next = have && next_item(a, wn, n_items, nslices, nsh, nxt);
+    // table entry of the item after next, requested one item ahead so that
+    // its load is not waited for at the item boundary
+    int4 tpre = (have_next && wn + (int)gridDim.x < n_items)
+                    ? load_tile(a, wn + gridDim.x, nslices)
+                    : make_int4(0, 0, 0, 0);
     uint32_t j = 0;
     while (have) {
       if (GATEUP && have_next) {
@@ -659,7 +670,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&sbfull[slot]));
       }
       int wnn = wn + gridDim.x;
-      const bool have_nn = have_next && next_item(a, wnn, n_items, nslices, nsh, nn);
+      bool have_nn = false;
+      if (have_next && wnn < n_items) {
+        have_nn = item_from(tpre, wnn, nslices, nsh, nn);
+        if (!have_nn) {  // an empty tile: scan on (rare)
+          wnn += gridDim.x;
+          have_nn = next_item(a, wnn, n_items, nslices, nsh, nn);
+        }
+      }
+      if (have_nn && wnn + (int)gridDim.x < n_items) tpre = load_tile(a, wnn + gridDim.x, nslices);
 
       const int N = (cur.rows + 15) & ~15;
       const int ab = j % NACC;
