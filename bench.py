@@ -404,19 +404,56 @@ class LayerRun:
         nbytes = self.touched() * 3 * expert_matrix_bytes(d, F) + E * d * 4 + T * d * (2 + 4)
         return nbytes, layer_flops(T, d, E, wl["k"], F), self.nl
 
-    # end to end: host x in, the layer through the host-buffer entry point, host y out
+    # end to end: host x in, the layer through the host-buffer entry point, host y
+    # out, every step.  Prefill keeps two calls in flight on two streams (each
+    # with its own staging, routing buffers, workspace and host output), so one
+    # call's copies overlap the other's kernels; its kernels fill the GPU, so
+    # the kernels of the two calls still run one after the other.  Decode runs
+    # one synchronous call at a time: two T = 1 layers in flight would share
+    # the GPU as a batch of two, a different workload.
     def e2e_prepare(self):
         T, d = self.wl["T"], self.wl["d"]
         self.xh = [self.layers[l][0].cpu().pin_memory() for l in range(self.nl)]
-        self.yh = torch.empty(T, d, dtype=self.y.dtype).pin_memory()
-        self.xd = torch.empty(T, d, dtype=torch.bfloat16, device=self.dev)
+        nsets = 1 if self.decode else 2
+        self.e2e_sets = []
+        for j in range(nsets):
+            first = j == 0
+            self.e2e_sets.append({
+                "r": self.r if first else self.lily.RoutingBuffers(self.dims, self.dev),
+                "ws": self.ws if first else self.lily.alloc_workspace(
+                    self.lily.lily_moe_workspace_bytes(self.dims), self.dev),
+                "y": self.y if first else torch.empty_like(self.y),
+                "xd": torch.empty(T, d, dtype=torch.bfloat16, device=self.dev),
+                "yh": torch.empty(T, d, dtype=self.y.dtype).pin_memory(),
+                "stream": None if self.decode else torch.cuda.Stream(device=self.dev),
+                "busy": False})
+        # every (layer, buffer set) pair is called once before timing (its
+        # first call runs eagerly and captures the graph later calls replay)
+        self.e2e_warm = max(3, self.nl * nsets)
         self.h2d = T * d * 2
         self.d2h = T * d * self.y.element_size()
 
     def e2e_step(self, i):
-        self.lily.lily_moe_forward_host(self.dims, self.xh[i % self.nl], self.xd,
-                                        self.layers[i % self.nl][1], self.r, self.y, self.yh,
-                                        self.ws, None)
+        b = self.e2e_sets[i % len(self.e2e_sets)]
+        x, w = self.xh[i % self.nl], self.layers[i % self.nl][1]
+        if b["stream"] is None:
+            self.lily.lily_moe_forward_host(self.dims, x, b["xd"], w, b["r"], b["y"], b["yh"],
+                                            b["ws"], None)
+            return
+        if b["busy"]:
+            b["stream"].synchronize()  # this set's previous call has finished
+        self.lily.lily_moe_forward_host_async(self.dims, x, b["xd"], w, b["r"], b["y"], b["yh"],
+                                              b["ws"], b["stream"])
+        b["busy"] = True
+
+    def e2e_drain(self):
+        for b in self.e2e_sets:
+            if b["stream"] is not None and b["busy"]:
+                b["stream"].synchronize()
+                b["busy"] = False
+        for b in self.e2e_sets:
+            if self.lily.lily_moe_status(b["ws"]):
+                raise RuntimeError("device status bits set in the end-to-end leg")
 
     def config(self):
         c = {"l2": f"inputs larger than L2: {self.nl} layers of weights rotated per step",
@@ -694,13 +731,17 @@ def run_lily(args, world, rank, local):
     run.e2e_prepare()
     e2e_steps = 3 if args.no_e2e else max(3, min(args.steps, 5 if wl["kind"] == "stack_prefill"
                                                   else 200))
-    for i in range(3):
+    for i in range(getattr(run, "e2e_warm", 3)):
         run.e2e_step(i)
+    if hasattr(run, "e2e_drain"):
+        run.e2e_drain()
     if world > 1:
         torch.distributed.barrier()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         run.e2e_step(i)
+    if hasattr(run, "e2e_drain"):
+        run.e2e_drain()  # the last calls' results are in host memory
     e2e_s = time.perf_counter() - t0
     e2e_s = max_over_ranks(e2e_s, world, dev)
 

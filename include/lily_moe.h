@@ -238,6 +238,20 @@ int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x
                           void* y_dev, void* y_host, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/* lily_moe_forward_host without the final wait: once the argument set's
+ * graph is cached (page-locked host buffers, second and later calls), the
+ * call only queues the copy-layer-copy graph on `stream` and returns; y_host
+ * holds the result once `stream` has been synchronised.  Until then none of
+ * x_host, x_dev, y_dev, y_host, the routing buffers or the workspace may be
+ * reused or freed.  A first call (or a call while profiling is on, or with a
+ * pageable host buffer) runs as lily_moe_forward_host does, synchronously.
+ * Calls on different streams with disjoint buffers overlap one call's copies
+ * with another's kernels.  Same arguments and errors as lily_moe_forward_host. */
+int lily_moe_forward_host_async(const lily_moe_dims* dims, const void* x_host, void* x_dev,
+                                const lily_moe_weights* weights, lily_moe_routing* routing,
+                                void* y_dev, void* y_host, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /* Turn the end-to-end graph cache on (enable != 0, the default) or off; either
  * way every cached graph is destroyed.  Returns the previous setting (0/1). */
 int lily_moe_host_graphs(int enable);

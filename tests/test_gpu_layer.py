@@ -176,6 +176,48 @@ def test_forward_host_entry(oracle_lib):
     assert torch.equal(yh, ydev.cpu())
 
 
+def test_forward_host_async_two_streams(oracle_lib):
+    """Two host-buffer calls in flight on two streams, each with its own
+    staging, routing buffers, workspace and host buffers: once a stream is
+    synchronised its host output equals the device entry point's result for
+    that call's input (each set's first call runs eagerly, later ones replay
+    its graph), and a set is refilled only after its stream has finished."""
+    T, d = 64, 512
+    L = Layer(synth.LayerShape(T, d, 32, 4, 128), seed=4400, tile_rows=32)
+    g = torch.Generator().manual_seed(4401)
+    xs = [(torch.randn(T, d, generator=g) * (1.0 + c)).to(torch.bfloat16) for c in range(6)]
+    refs = []
+    for x in xs:  # device entry point, before the sets share L's buffers
+        L.x.copy_(x)
+        refs.append(L.forward().cpu().clone())
+    lily.lily_moe_host_graphs(True)
+    dev = L.x.device
+    sets = []
+    for j in range(2):
+        sets.append({
+            "r": L.r if j == 0 else lily.RoutingBuffers(L.dims, dev),
+            "ws": L.ws if j == 0 else lily.alloc_workspace(lily.lily_moe_workspace_bytes(L.dims),
+                                                           dev),
+            "xh": torch.empty(T, d, dtype=torch.bfloat16).pin_memory(),
+            "yh": torch.empty(T, d, dtype=L.y.dtype).pin_memory(),
+            "xd": torch.empty_like(L.x), "yd": torch.empty_like(L.y),
+            "s": torch.cuda.Stream(device=dev), "call": None})
+    for c, x in enumerate(xs):
+        b = sets[c % 2]
+        b["s"].synchronize()
+        if b["call"] is not None:
+            assert torch.equal(b["yh"], refs[b["call"]]), f"call {b['call']}"
+        b["xh"].copy_(x)
+        b["yh"].fill_(float("nan"))
+        lily.lily_moe_forward_host_async(L.dims, b["xh"], b["xd"], L.w, b["r"], b["yd"], b["yh"],
+                                         b["ws"], b["s"])
+        b["call"] = c
+    for b in sets:
+        b["s"].synchronize()
+        assert torch.equal(b["yh"], refs[b["call"]]), f"call {b['call']}"
+        assert lily.lily_moe_status(b["ws"]) == 0
+
+
 @pytest.mark.parametrize("T", [64, 5])
 @pytest.mark.parametrize("pinned", [True, False])
 def test_forward_host_graph_cache(oracle_lib, T, pinned):

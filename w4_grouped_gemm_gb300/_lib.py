@@ -35,7 +35,7 @@ EXPORTS = (
     "lily_moe_workspace_bytes", "lily_moe_block_map_cap", "lily_moe_check_dims",
     "lily_moe_route", "lily_moe_forward", "lily_moe_experts", "lily_moe_decode",
     "lily_moe_decode_static",
-    "lily_moe_forward_host", "lily_moe_host_graphs",
+    "lily_moe_forward_host", "lily_moe_forward_host_async", "lily_moe_host_graphs",
     "lily_moe_rmsnorm", "lily_moe_stack_prefill", "lily_moe_stack_decode",
     "lily_moe_router_split_bytes", "lily_moe_router_split",
     "lily_moe_stack_workspace_bytes",
@@ -96,6 +96,7 @@ def lib():
             "lily_moe_decode": (I, [DP, P, WP, RP, P, P, SZ, P]),
             "lily_moe_decode_static": (I, [DP, P, WP, RP, P, P]),
             "lily_moe_forward_host": (I, [DP, P, P, WP, RP, P, P, P, SZ, P]),
+            "lily_moe_forward_host_async": (I, [DP, P, P, WP, RP, P, P, P, SZ, P]),
             "lily_moe_host_graphs": (I, [I]),
             "lily_moe_rmsnorm": (I, [ctypes.c_int32, ctypes.c_int32, P, ctypes.c_float, P, P]),
             "lily_moe_router_split_bytes": (SZ, [ctypes.c_int32, ctypes.c_int32]),
@@ -282,6 +283,17 @@ def lily_moe_forward_host(dims, x_host, x_dev, weights: LayerWeights, routing: R
                                      _ptr(y_dev), _ptr(y_host), _ptr(ws), ws.numel(),
                                      _stream(stream))
     _check(rc, "lily_moe_forward_host")
+
+
+def lily_moe_forward_host_async(dims, x_host, x_dev, weights: LayerWeights,
+                                routing: RoutingBuffers, y_dev, y_host, ws, stream=None):
+    """lily_moe_forward_host without the final wait (see the header): the
+    result is in y_host once `stream` has been synchronised."""
+    rc = lib().lily_moe_forward_host_async(ctypes.byref(dims), _ptr(x_host), _ptr(x_dev),
+                                           ctypes.byref(weights.c), ctypes.byref(routing.c),
+                                           _ptr(y_dev), _ptr(y_host), _ptr(ws), ws.numel(),
+                                           _stream(stream))
+    _check(rc, "lily_moe_forward_host_async")
 
 
 def lily_moe_host_graphs(enable: bool) -> bool:

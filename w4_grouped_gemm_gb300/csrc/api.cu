@@ -577,9 +577,11 @@ int lily_moe_decode(const lily_moe_dims* dims, const void* x, const lily_moe_wei
   return cuda_rc(launch_decode(decode_args(*dims, w, *r, ws, y, nullptr), s));
 }
 
-int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x_dev,
-                          const lily_moe_weights* w, lily_moe_routing* r, void* y_dev,
-                          void* y_host, void* ws, size_t ws_bytes, void* stream) {
+// The host-buffer step; `sync`: wait for it before returning (a replayed
+// graph is otherwise left running on the stream).
+static int forward_host(const lily_moe_dims* dims, const void* x_host, void* x_dev,
+                        const lily_moe_weights* w, lily_moe_routing* r, void* y_dev, void* y_host,
+                        void* ws, size_t ws_bytes, void* stream, bool sync) {
   if (!dims || !x_host || !y_host) return LILY_ERR_INVALID_ARG;
   int rc = common_checks(dims, x_dev, w, r, y_dev, ws, ws_bytes, true);
   if (rc) return rc;
@@ -608,12 +610,24 @@ int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x
       }
     }
     if (launched < 0) return LILY_ERR_CUDA;
-    if (launched > 0) return cuda_rc(cudaStreamSynchronize(s));
+    if (launched > 0) return sync ? cuda_rc(cudaStreamSynchronize(s)) : LILY_OK;
   }
   if ((rc = host_step(h, s))) return rc;
   if ((rc = cuda_rc(cudaStreamSynchronize(s)))) return rc;
   if (graphable) host_graph_capture(h, key);
   return LILY_OK;
+}
+
+int lily_moe_forward_host(const lily_moe_dims* dims, const void* x_host, void* x_dev,
+                          const lily_moe_weights* w, lily_moe_routing* r, void* y_dev,
+                          void* y_host, void* ws, size_t ws_bytes, void* stream) {
+  return forward_host(dims, x_host, x_dev, w, r, y_dev, y_host, ws, ws_bytes, stream, true);
+}
+
+int lily_moe_forward_host_async(const lily_moe_dims* dims, const void* x_host, void* x_dev,
+                                const lily_moe_weights* w, lily_moe_routing* r, void* y_dev,
+                                void* y_host, void* ws, size_t ws_bytes, void* stream) {
+  return forward_host(dims, x_host, x_dev, w, r, y_dev, y_host, ws, ws_bytes, stream, false);
 }
 
 int lily_moe_host_graphs(int enable) {
