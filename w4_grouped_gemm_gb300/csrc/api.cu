@@ -513,7 +513,8 @@ int lily_moe_check_dims(const lily_moe_dims* d) {
     return LILY_ERR_UNSUPPORTED_SHAPE;
   if (d->tile_rows != 16 && d->tile_rows != 32 && d->tile_rows != 64 && d->tile_rows != 128)
     return LILY_ERR_UNSUPPORTED_SHAPE;
-  if (gemm_stages(true, d->tile_rows, d->d_model) < 2 || gemm_stages(false, d->tile_rows, d->d_ff) < 2)
+  if (gemm_stages(true, d->tile_rows, d->d_model, d->d_ff) < 2 ||
+      gemm_stages(false, d->tile_rows, d->d_ff, d->d_model) < 2)
     return LILY_ERR_UNSUPPORTED_SHAPE;
   return LILY_OK;
 }

@@ -73,9 +73,11 @@ constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxA + 4 + 4 + 1;
 // store wait and arrival) are paid once per 128 K.
 __host__ __device__ constexpr int groups_per_step(bool /*gateup*/) { return 2; }
 
-// 128-row weight sub-slices per work item (see GemmLayout::kSub).
-__host__ __device__ constexpr int sub_slices(bool gateup, int BM) {
-  return (gateup && BM <= 64) ? 2 : 1;
+// 128-row weight sub-slices per work item (see GemmLayout::kSub): two at BM
+// <= 64 (gate/up always; down when its d output features split into items of
+// 256), else one.  nout: output features of each matrix (gate/up F, down d).
+__host__ __device__ constexpr int sub_slices(bool gateup, int BM, int nout) {
+  return BM > 64 ? 1 : (gateup || nout % 256 == 0) ? 2 : 1;
 }
 
 // Tensor memory (512 columns x 128 lanes): two accumulator sets of N <= BM
@@ -84,7 +86,7 @@ __host__ __device__ constexpr int sub_slices(bool gateup, int BM) {
 // the token rows (BM x 64 fp16), and the packed codes of the step's 128
 // weight rows (128 rows x 64 B, 64-byte swizzle; gate/up: the 64 gate rows of
 // the slice, then its 64 up rows).
-template <bool GATEUP, int BM>
+template <bool GATEUP, int BM, int SUB>
 struct GemmLayout {
   static constexpr int kGroups = groups_per_step(GATEUP);
   static constexpr int kBTile = BM * 128;  // token rows of one group
@@ -92,13 +94,14 @@ struct GemmLayout {
   // item's last are other tiles' rows or zero fill, never stored)
   static constexpr int kBoxRows = BM < 64 ? BM : 64;
   static constexpr int kBBytes = kGroups * kBTile;
-  // 128-row sub-slices per item: gate/up tiles of at most 64 rows take two
-  // (128 features of both matrices, 16 MMAs per K-step), so the per-step
-  // hand-offs are paid once per 128 features; BM 128 takes one, which leaves
-  // room for two accumulator sets and a 4-step A ring
-  static constexpr int kSub = (GATEUP && BM <= 64) ? 2 : 1;
+  // 128-row sub-slices per item: tiles of at most 64 rows take two (gate/up:
+  // 128 features of both matrices; down: 256 output features; 16 MMAs per
+  // K-step), so the per-step hand-offs are paid once per two sub-slices and a
+  // down item's token rows serve twice the features; BM 128 takes one, which
+  // leaves room for two accumulator sets and a 4-step A ring
+  static constexpr int kSub = SUB;
   static constexpr int kStage = kBBytes + kSub * kGroups * kPackedBytes;
-  static constexpr int kOutRows = GATEUP ? 64 * kSub : 128;  // output features per item
+  static constexpr int kOutRows = (GATEUP ? 64 : 128) * kSub;  // output features per item
   static constexpr int kACols = 32 * kGroups * kSub;          // A tiles of one K-step
   static constexpr int kAccCols = BM * kSub;                  // one accumulator set
   static constexpr int kNumAcc = 2;
@@ -107,7 +110,7 @@ struct GemmLayout {
       (512 - kAOff) / kACols < kMaxA ? (512 - kAOff) / kACols : kMaxA;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kNumA >= 2, "tensor memory too small for the A ring");
-  static_assert(kSub == sub_slices(GATEUP, BM), "sub-slices");
+  static_assert(SUB == 1 || (SUB == 2 && BM <= 64), "sub-slices");
 };
 
 // Down epilogue staging: per epilogue warp 32 rows x 32 output features of
@@ -123,18 +126,18 @@ __host__ __device__ constexpr int gu_matrix(int r) { return (r >> 4) & 1; }
 __host__ __device__ constexpr int gu_feature(int r) { return 16 * (r >> 5) + (r & 15); }
 __host__ __device__ constexpr int gu_code_row(int r) { return 64 * gu_matrix(r) + gu_feature(r); }
 
-__host__ __device__ inline size_t gemm_fixed_bytes(bool gateup, int BM, int K, int nsb) {
+__host__ __device__ inline size_t gemm_fixed_bytes(bool gateup, int BM, int K, int nsb, int sub) {
   const int G = K / 64;
   return 1024                                    // alignment slack
-         + (size_t)nsb * G * 128 * sub_slices(gateup, BM) * 4  // scale/bias tables
+         + (size_t)nsb * G * 128 * sub * 4       // scale/bias tables
          + (gateup ? 0 : kEpiStageBytes)          // down: epilogue staging
          + kNumBars * 8                          // mbarriers
          + 16;                                   // abort flag, TMEM address
 }
 
-size_t gemm_stage_bytes(bool gateup, int BM) {
+size_t gemm_stage_bytes(bool gateup, int BM, int sub) {
   const int kg = groups_per_step(gateup);
-  return (size_t)kg * ((size_t)BM * 128 + (size_t)sub_slices(gateup, BM) * kPackedBytes);
+  return (size_t)kg * ((size_t)BM * 128 + (size_t)sub * kPackedBytes);
 }
 
 constexpr size_t kSmemLimit = 232448;  // 227 KB per block
@@ -143,35 +146,35 @@ constexpr size_t kSmemLimit = 232448;  // 227 KB per block
 // Gate/up: two scale tables (the next item's is filled while the current one
 // is in use) when that still leaves >= 3 stages, else one table.  Down: two
 // tables always, one per dequant warp set.
-static int stages_for(bool gateup, int BM, int K, int nsb) {
-  const size_t fixed = gemm_fixed_bytes(gateup, BM, K, nsb);
+static int stages_for(bool gateup, int BM, int K, int nsb, int sub) {
+  const size_t fixed = gemm_fixed_bytes(gateup, BM, K, nsb, sub);
   if (fixed >= kSmemLimit) return 0;
-  int s = (int)((kSmemLimit - fixed) / gemm_stage_bytes(gateup, BM));
+  int s = (int)((kSmemLimit - fixed) / gemm_stage_bytes(gateup, BM, sub));
   return s > kMaxStages ? kMaxStages : s;
 }
 
-void gemm_config(bool gateup, int BM, int K, int* stages, int* nsb) {
-  const int s2 = stages_for(gateup, BM, K, 2);
+void gemm_config(bool gateup, int BM, int K, int sub, int* stages, int* nsb) {
+  const int s2 = stages_for(gateup, BM, K, 2, sub);
   if (s2 >= 3 || (!gateup && s2 >= 2)) {  // down: one table per dequant warp set
     *stages = s2;
     *nsb = 2;
     return;
   }
-  const int s1 = stages_for(gateup, BM, K, 1);
+  const int s1 = stages_for(gateup, BM, K, 1, sub);
   *stages = (gateup && s1 >= 2) ? s1 : 0;
   *nsb = 1;
 }
 
-int gemm_stages(bool gateup, int BM, int K) {
+int gemm_stages(bool gateup, int BM, int K, int nout) {
   int s, n;
-  gemm_config(gateup, BM, K, &s, &n);
+  gemm_config(gateup, BM, K, sub_slices(gateup, BM, nout), &s, &n);
   return s;
 }
 
-size_t gemm_smem_bytes(bool gateup, int BM, int K) {
+size_t gemm_smem_bytes(bool gateup, int BM, int K, int sub) {
   int s, n;
-  gemm_config(gateup, BM, K, &s, &n);
-  return gemm_fixed_bytes(gateup, BM, K, n) + (size_t)s * gemm_stage_bytes(gateup, BM);
+  gemm_config(gateup, BM, K, sub, &s, &n);
+  return gemm_fixed_bytes(gateup, BM, K, n, sub) + (size_t)s * gemm_stage_bytes(gateup, BM, sub);
 }
 
 // Position in a ring of n slots: slot index and the parity of its use count
@@ -266,7 +269,7 @@ __device__ void scale_fill(const uint16_t* sp, const uint16_t* bp, size_t row, i
 }
 
 // Persistent kernel: one CTA per SM loops over the work items.
-template <bool GATEUP, int BM>
+template <bool GATEUP, int BM, int SUB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     w4_gemm_kernel(const __grid_constant__ CUtensorMap tm_q0,
                    const __grid_constant__ CUtensorMap tm_q1,
@@ -275,7 +278,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    const __grid_constant__ CUtensorMap tm_bw,
                    const __grid_constant__ CUtensorMap tm_b2w, const GemmArgs a, const int nstages,
                    const int nsb) {
-  using L = GemmLayout<GATEUP, BM>;
+  using L = GemmLayout<GATEUP, BM, SUB>;
   constexpr int BBYTES = L::kBBytes;
   constexpr int STAGE = L::kStage;
   constexpr int NACC = L::kNumAcc;
@@ -284,7 +287,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // on the stage of step it is sound only if the stage's previous use (step
   // it - nstages) has landed, i.e. if nstages >= NA.
   const int NA = L::kNumA < nstages ? L::kNumA : nstages;
-  constexpr int SUB = L::kSub;
 
   const int K = GATEUP ? a.d : a.F;     // reduction length
   const int NOUT = GATEUP ? a.F : a.d;  // output features of each matrix
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int j = 0; j < SUB; ++j) {  // sub-slice j: its code tile of 128 rows
             const uint32_t ct = st + BBYTES + j * KG * kPackedBytes;
-            tma_load_2d(ct, &tm_q0, kk * KG * 32, wrow + 64 * j, fb);
+            tma_load_2d(ct, &tm_q0, kk * KG * 32, wrow + (GATEUP ? 64 : 128) * j, fb);
             if (GATEUP) tma_load_2d(ct + 64 * KG * 32, &tm_q1, kk * KG * 32, wrow + 64 * j, fb);
           }
 #pragma unroll
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint4 pfs[kPfChunks], pfb[kPfChunks];
     int pf_w = -1;                // work item whose scales pfs/pfb hold
     auto sb_row = [&](int expert, int slice) {
-      return (size_t)expert * NOUT + (size_t)slice * 128 + r;
+      return (size_t)expert * NOUT + (size_t)slice * L::kOutRows + jsub * 128 + r;
     };
     auto down_prefetch = [&](int wn, int4 t) {
       // 16-byte chunks of 8 groups: whole chunks only (G a multiple of 8)
@@ -522,7 +524,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // groups 2kk, 2kk+1 (K-step kk of an item starting at running step it0)
     // belong to this warp when (it0 + kk) has its parity
     auto down_fill = [&](int w, const Item& itm, uint32_t it0) {
-      uint32_t* dst = sb + par * sb_words;  // this warp set's slot, entries [group][row]
+      // this warp set's slot, entries [group][table row jsub * 128 + r]
+      uint32_t* dst = sb + par * sb_words + jsub * 128;
       if (pf_w == w) {
 #pragma unroll
         for (int c = 0; c < kPfChunks; ++c)
@@ -533,17 +536,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t wb[4] = {pfb[c].x, pfb[c].y, pfb[c].z, pfb[c].w};
 #pragma unroll
             for (int u = 0; u < 4; ++u)
-              if (((it0 + (uint32_t)u) & 1u) == par) {
-                dst[(c * 8 + 2 * u) * 128 + r] = sb_word((uint16_t)ws[u], (uint16_t)wb[u]);
-                dst[(c * 8 + 2 * u + 1) * 128 + r] =
+              if (SUB == 2 || ((it0 + (uint32_t)u) & 1u) == par) {
+                dst[(c * 8 + 2 * u) * (128 * SUB) + r] = sb_word((uint16_t)ws[u], (uint16_t)wb[u]);
+                dst[(c * 8 + 2 * u + 1) * (128 * SUB) + r] =
                     sb_word((uint16_t)(ws[u] >> 16), (uint16_t)(wb[u] >> 16));
               }
           }
       } else {
         const size_t row = sb_row(itm.expert, itm.slice);
         for (int grp = 0; grp < G; ++grp)
-          if (((it0 + (uint32_t)(grp >> 1)) & 1u) == par)
-            dst[grp * 128 + r] =
+          if (SUB == 2 || ((it0 + (uint32_t)(grp >> 1)) & 1u) == par)
+            dst[grp * (128 * SUB) + r] =
                 sb_word(__ldg(a.s0 + row * G + grp), __ldg(a.b0 + row * G + grp));
       }
     };
@@ -743,10 +746,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // expert-sorted row order as H; the combine kernel then sums each
           // token's rows.  Each warp stages its 32 features of up to 32 rows
           // in shared memory, and each lane stores one row's 64 bytes.
-          const int feat = cur.slice * 128 + q * 32 + lane;
+          const int feat = cur.slice * L::kOutRows + js * 128 + q * 32 + lane;
           uint32_t va[16], vb[16];
-          tmem_ld16(tl + cb, va);
-          if (ncol == 32) tmem_ld16(tl + cb + 16, vb);
+          tmem_ld16(tl + js * BM + cb, va);
+          if (ncol == 32) tmem_ld16(tl + js * BM + cb + 16, vb);
           tmem_ld_wait();
           if (last) {
             tc_fence_before();
@@ -831,23 +834,23 @@ CUresult encode_tiled(CUtensorMap* tm, CUtensorMapDataType dt, uint32_t rank, vo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-template <bool GATEUP, int BM>
+template <bool GATEUP, int BM, int SUB>
 static cudaError_t launch_gemm_bm(const GemmArgs& a, const CUtensorMap& q0, const CUtensorMap& q1,
                                   const CUtensorMap& b, const CUtensorMap& b2,
                                   const CUtensorMap& bw, const CUtensorMap& b2w, cudaStream_t s) {
   const int K = GATEUP ? a.d : a.F;
   const int NOUT = GATEUP ? a.F : a.d;
   int nstages = 0, nsb = 0;
-  gemm_config(GATEUP, BM, K, &nstages, &nsb);
+  gemm_config(GATEUP, BM, K, SUB, &nstages, &nsb);
   if (nstages < 2) return cudaErrorInvalidValue;
-  const size_t smem = gemm_smem_bytes(GATEUP, BM, K);
-  auto kern = w4_gemm_kernel<GATEUP, BM>;
+  const size_t smem = gemm_smem_bytes(GATEUP, BM, K, SUB);
+  auto kern = w4_gemm_kernel<GATEUP, BM, SUB>;
   cudaError_t err = ensure_smem_attr((const void*)kern, smem);
   if (err != cudaSuccess) return err;
   const int P = a.T * a.k;
   const int cap = (P + BM - 1) / BM + (a.E < P ? a.E : P);
   const int nsh = (a.T + BM - 1) / BM;
-  const int max_items = (nsh + cap) * (NOUT / GemmLayout<GATEUP, BM>::kOutRows);
+  const int max_items = (nsh + cap) * (NOUT / GemmLayout<GATEUP, BM, SUB>::kOutRows);
   int num_sms = 0, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -864,11 +867,23 @@ template <bool GATEUP>
 static cudaError_t launch_gemm(const GemmArgs& a, const CUtensorMap& q0, const CUtensorMap& q1,
                                const CUtensorMap& b, const CUtensorMap& b2, const CUtensorMap& bw,
                                const CUtensorMap& b2w, cudaStream_t s) {
+  // gate/up: two sub-slices at BM <= 64; down: two when d splits into
+  // 256-feature items, else one
+  const bool two = sub_slices(GATEUP, a.BM, GATEUP ? a.F : a.d) == 2;
   switch (a.BM) {
-    case 16: return launch_gemm_bm<GATEUP, 16>(a, q0, q1, b, b2, bw, b2w, s);
-    case 32: return launch_gemm_bm<GATEUP, 32>(a, q0, q1, b, b2, bw, b2w, s);
-    case 64: return launch_gemm_bm<GATEUP, 64>(a, q0, q1, b, b2, bw, b2w, s);
-    case 128: return launch_gemm_bm<GATEUP, 128>(a, q0, q1, b, b2, bw, b2w, s);
+#define LILY_GEMM_BM(BMV)                                                   \
+  case BMV:                                                                 \
+    if constexpr (GATEUP) {                                                 \
+      return launch_gemm_bm<GATEUP, BMV, 2>(a, q0, q1, b, b2, bw, b2w, s);  \
+    } else {                                                                \
+      return two ? launch_gemm_bm<GATEUP, BMV, 2>(a, q0, q1, b, b2, bw, b2w, s) \
+                 : launch_gemm_bm<GATEUP, BMV, 1>(a, q0, q1, b, b2, bw, b2w, s); \
+    }
+    LILY_GEMM_BM(16)
+    LILY_GEMM_BM(32)
+    LILY_GEMM_BM(64)
+#undef LILY_GEMM_BM
+    case 128: return launch_gemm_bm<GATEUP, 128, 1>(a, q0, q1, b, b2, bw, b2w, s);
     default: return cudaErrorInvalidValue;
   }
 }

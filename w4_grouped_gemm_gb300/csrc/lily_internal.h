@@ -166,8 +166,9 @@ cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s);
 // xn[t] = bf16(rmsnorm(x[t], eps)) when xn is non-NULL.
 cudaError_t launch_combine(const GemmArgs& a, void* y, bool y_f32, float* x, void* xn, float eps,
                            cudaStream_t s);
-size_t gemm_smem_bytes(bool gateup, int BM, int K);
-int gemm_stages(bool gateup, int BM, int K);
+size_t gemm_smem_bytes(bool gateup, int BM, int K, int sub);
+// Pipeline stages of a grouped GEMM (nout: its output features per matrix).
+int gemm_stages(bool gateup, int BM, int K, int nout);
 
 // ---------------------------------------------------------------- decode
 // The decode GEMVs (T <= 8) read the step's tile slots from the plan the
