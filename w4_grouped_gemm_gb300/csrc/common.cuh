@@ -238,6 +238,26 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
       "l"(tm), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// Shared memory -> global through a 2-D tensor map (bulk group of this
+// thread), and the waits on this thread's bulk groups: until their reads of
+// shared memory are done (the buffer may be rewritten), or fully written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int32_t c0, int32_t c1,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tm),
+      "r"(c0), "r"(c1), "r"(src)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int32_t c0,
                                             int32_t c1, int32_t c2, uint32_t bar) {
   asm volatile(

@@ -118,6 +118,10 @@ struct GemmLayout {
 // of eight consecutive rows hit eight different bank groups.
 constexpr int kEpiRowHalves = 40;
 constexpr int kEpiStageBytes = kNumEpiWarps * 32 * kEpiRowHalves * 2;
+// At BM 128 the rows are packed (32 halves), the layout of a 32 x 32 box of
+// O, so a full chunk leaves by one tensor store (partial chunks by the lanes).
+template <int BM>
+__host__ __device__ constexpr int epi_row_halves() { return BM == 128 ? 32 : kEpiRowHalves; }
 
 // Gate/up: weight row r of an item (= TMEM lane r) is row code_row(r) of the
 // step's code tile (64 gate rows, then 64 up rows): matrix (r >> 4) & 1 and
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     misc[0] = 0;
     fence_mbar_init();
     prefetch_tensormap(&tm_q0);
-    if (GATEUP) prefetch_tensormap(&tm_q1);
+    prefetch_tensormap(&tm_q1);  // gate/up: up codes; down: the output rows
     prefetch_tensormap(&tm_b);
     if (GATEUP) prefetch_tensormap(&tm_b2);
     if (BM > 64) {
@@ -745,7 +749,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // Output rows of the item as fp16 into O, in the same
           // expert-sorted row order as H; the combine kernel then sums each
           // token's rows.  Each warp stages its 32 features of up to 32 rows
-          // in shared memory, and each lane stores one row's 64 bytes.
+          // in shared memory; at BM 128 a chunk of 32 rows leaves as one
+          // tensor store (tm_q1 is then O's map), else each lane stores one
+          // row's 64 bytes.
+          constexpr int RH = epi_row_halves<BM>();
           const int feat = cur.slice * L::kOutRows + js * 128 + q * 32 + lane;
           uint32_t va[16], vb[16];
           tmem_ld16(tl + js * BM + cb, va);
@@ -757,33 +764,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
           }
           __half* buf = reinterpret_cast<__half*>(estage) + (size_t)q * 32 * kEpiRowHalves;
+          if (BM == 128) {  // the previous chunk's tensor store has read the buffer
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+          }
 #pragma unroll
           for (int rr = 0; rr < 16; ++rr) {
             const float v = __uint_as_float(va[rr]);
             range_ok &= fabsf(v) <= 65504.f;
-            buf[rr * kEpiRowHalves + lane] = __float2half_rn(v);
+            buf[rr * RH + lane] = __float2half_rn(v);
           }
           if (ncol == 32) {
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
               const float v = __uint_as_float(vb[rr]);
               range_ok &= fabsf(v) <= 65504.f;
-              buf[(16 + rr) * kEpiRowHalves + lane] = __float2half_rn(v);
+              buf[(16 + rr) * RH + lane] = __float2half_rn(v);
             }
           }
-          __syncwarp();
-          if (lane < ncol && cb + lane < cur.rows) {
-            const uint4* src = reinterpret_cast<const uint4*>(buf + lane * kEpiRowHalves);
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(a.O) +
-                                                  (size_t)(cur.row0 + cb + lane) * a.d +
-                                                  (feat - lane));
-            const uint4 v0 = src[0], v1 = src[1], v2 = src[2], v3 = src[3];
-            dst[0] = v0;
-            dst[1] = v1;
-            dst[2] = v2;
-            dst[3] = v3;
+          if (BM == 128 && ncol == 32 && cb + 32 <= cur.rows) {
+            fence_proxy_async_shared();  // the stores above, to the tensor store
+            __syncwarp();
+            if (lane == 0) tma_store_2d(&tm_q1, feat - lane, cur.row0 + cb, smem_u32(buf));
+          } else {
+            __syncwarp();
+            if (lane < ncol && cb + lane < cur.rows) {
+              const uint4* src = reinterpret_cast<const uint4*>(buf + lane * RH);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__half*>(a.O) +
+                                                    (size_t)(cur.row0 + cb + lane) * a.d +
+                                                    (feat - lane));
+              const uint4 v0 = src[0], v1 = src[1], v2 = src[2], v3 = src[3];
+              dst[0] = v0;
+              dst[1] = v1;
+              dst[2] = v2;
+              dst[3] = v3;
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       if (!range_ok) set_status(a.status, LILY_STATUS_F16_RANGE);
@@ -794,6 +811,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       have_next = have_nn;
       ++j;
     }
+    if (!GATEUP && BM == 128 && lane == 0) bulk_wait_all();  // O fully written
   }
 
   // ---- teardown: every MMA has finished before TMEM is released
@@ -1001,13 +1019,20 @@ cudaError_t launch_gateup(const GemmArgs& a, const void* xs, const void* x16, co
 }
 
 cudaError_t launch_down(const GemmArgs& a, const uint8_t* dq, cudaStream_t s) {
-  CUtensorMap q0, b, bw;
+  CUtensorMap q0, b, bw, o;
   const int P = a.T * a.k;
+  // o: the output rows O, 32 x 32 boxes without swizzle (the epilogue's
+  // staging layout at BM 128), for the tensor stores of full chunks
+  uint64_t odims[2] = {(uint64_t)a.d, (uint64_t)(P + a.T)};
+  uint64_t ostrides[1] = {(uint64_t)a.d * 2};
+  uint32_t obox[2] = {32, 32};
   if (!packed_map(&q0, dq, a.F, (a.E + 1) * a.d, 128) ||
       !f16_rows_map(&b, a.H, a.F, P + a.T, box_rows(a.BM)) ||
-      !f16_rows_map(&bw, a.H, a.F, P + a.T, a.BM))
+      !f16_rows_map(&bw, a.H, a.F, P + a.T, a.BM) ||
+      encode_tiled(&o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a.O, odims, ostrides, obox,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  return launch_gemm<false>(a, q0, q0, b, b, bw, bw, s);
+  return launch_gemm<false>(a, q0, o, b, b, bw, bw, s);
 }
 
 // Combine: y[t] = sum_j gate[t][j] * O[inv[t*k + j]] + O[P + t] (the k
