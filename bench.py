@@ -78,9 +78,9 @@ NCU_TRAFFIC = {  # {(workload, kernel, source_hash): bytes per launch}
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of the dominant kernel,
     # from the launch list of `bench.py --workload W --eager --steps 3
     # --warmup 3 --layers 1 --no-cpu-baseline --no-e2e` (mean over launches)
-    ("prefill512", "gateup_gemm", "6d30299c4ae2ec46"): 325353152,  # 322.24 + 3.11 MB
-    ("prefill2048_zipf", "gateup_gemm", "6d30299c4ae2ec46"): 227761664,  # 210.14 + 17.63 MB
-    ("prefill8192", "gateup_gemm", "6d30299c4ae2ec46"): 670280752,  # 605.32 + 64.96 MB
+    ("prefill512", "gateup_gemm", "4fbc732c9698cc88"): 325353168,  # 322.25 + 3.11 MB
+    ("prefill2048_zipf", "gateup_gemm", "4fbc732c9698cc88"): 227830656,  # 210.14 + 17.69 MB
+    ("prefill8192", "gateup_gemm", "4fbc732c9698cc88"): 670299472,  # 605.30 + 65.00 MB
     ("decode1", "dec_router", "549388bb5c81e12a"): 3928672,  # 3.93 MB read
     ("decode1", "dec_gateup", "549388bb5c81e12a"): 10657264,  # 10.66 MB read
 }
